@@ -1,0 +1,248 @@
+"""CPU oracle for attention over a block-quantized KV cache.
+
+TEST INFRASTRUCTURE ONLY.  This package wraps ``kvq_oracle.c`` (plain C99,
+fp32 block codecs written from their formulas, fp64 softmax attention) with
+ctypes and numpy.  It shares no code with the CUDA library and must never be
+imported by it: only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` use it.
+
+Every function follows a definition stated in ``kvq_oracle.c``'s header:
+the f16 / q8_0 / q4_0 block formats (sizes from the "Codecs" table of the
+buun-llama-cpp listing), the cache layout of the library's public header, and
+the plain softmax-attention definition evaluated in fp64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libkvq_oracle.so")
+
+F16, Q8_0, Q4_0 = 0, 1, 2
+SIDE_K, SIDE_V = 0, 1
+D = 128
+UNIT_TOKENS = 16
+ROW_BYTES = {F16: 256, Q8_0: 136, Q4_0: 72}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/libkvq_oracle.so`` with gcc."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        u8p = ctypes.POINTER(ctypes.c_uint8)
+        u16p = ctypes.POINTER(ctypes.c_uint16)
+        f64p = ctypes.POINTER(ctypes.c_double)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        lib.kvqo_half_to_float.argtypes = [ctypes.c_uint16]
+        lib.kvqo_half_to_float.restype = ctypes.c_float
+        lib.kvqo_float_to_half_rn.argtypes = [ctypes.c_float]
+        lib.kvqo_float_to_half_rn.restype = ctypes.c_uint16
+        lib.kvqo_encode_rows.argtypes = [ctypes.c_int, ctypes.c_int64, u16p, u8p]
+        lib.kvqo_decode_rows.argtypes = [ctypes.c_int, ctypes.c_int64, u8p, f64p]
+        lib.kvqo_unit_offset.argtypes = [ctypes.c_int] * 4
+        lib.kvqo_append_side.argtypes = [ctypes.c_int, ctypes.c_int, u8p, ctypes.c_int,
+                                         ctypes.c_int, ctypes.c_int, i32p, i32p, ctypes.c_int,
+                                         u16p]
+        lib.kvqo_dequant_stream.argtypes = [ctypes.c_int, ctypes.c_int, u8p, ctypes.c_int,
+                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int64, f64p]
+        lib.kvqo_attend_rows.argtypes = [ctypes.c_int, u16p, ctypes.c_int64, f64p, f64p, i64p,
+                                         ctypes.c_double, f64p, f64p]
+        lib.kvqo_decode_layer.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, u16p,
+                                          ctypes.c_double, u8p, f64p, f64p]
+        lib.kvqo_prefill_chunk.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int64, ctypes.c_int, u16p, ctypes.c_double,
+                                           u8p, f64p, f64p]
+        lib.kvqo_num_threads.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray, ctype):
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be C-contiguous"
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def _as_half_bits(x) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.float16:
+        return np.ascontiguousarray(x).view(np.uint16)
+    if x.dtype == np.uint16:
+        return np.ascontiguousarray(x)
+    raise TypeError(f"expected float16 (or its uint16 bits), got {x.dtype}")
+
+
+def num_threads() -> int:
+    return int(_load().kvqo_num_threads())
+
+
+# --------------------------------------------------------------------------- fp16
+
+def half_to_float(bits: int) -> float:
+    return float(_load().kvqo_half_to_float(int(bits)))
+
+
+def float_to_half_bits(x: float) -> int:
+    return int(_load().kvqo_float_to_half_rn(float(np.float32(x))))
+
+
+# --------------------------------------------------------------------------- codecs
+
+def encode_rows(codec: int, x) -> np.ndarray:
+    """fp16 [n, 128] -> canonical row bytes uint8 [n, row_bytes]."""
+    xb = _as_half_bits(x).reshape(-1, D)
+    out = np.zeros((xb.shape[0], ROW_BYTES[codec]), np.uint8)
+    rc = _load().kvqo_encode_rows(codec, xb.shape[0], _ptr(xb, ctypes.c_uint16),
+                                  _ptr(out, ctypes.c_uint8))
+    if rc:
+        raise ValueError(f"oracle encode failed ({rc}): non-finite input?")
+    return out
+
+
+def decode_rows(codec: int, rows: np.ndarray) -> np.ndarray:
+    """canonical row bytes [n, row_bytes] -> fp64 [n, 128]."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint8).reshape(-1, ROW_BYTES[codec])
+    out = np.zeros((rows.shape[0], D), np.float64)
+    _load().kvqo_decode_rows(codec, rows.shape[0], _ptr(rows, ctypes.c_uint8),
+                             _ptr(out, ctypes.c_double))
+    return out
+
+
+def unit_offset(codec: int, side: int, r: int, cb: int) -> int:
+    return int(_load().kvqo_unit_offset(codec, side, r, cb))
+
+
+def unit_offset_table(codec: int, side: int) -> np.ndarray:
+    """int32 [16, row_bytes]: unit byte offset of canonical byte cb of row r."""
+    rb = ROW_BYTES[codec]
+    lib = _load()
+    return np.array([[lib.kvqo_unit_offset(codec, side, r, cb) for cb in range(rb)]
+                     for r in range(UNIT_TOKENS)], np.int32)
+
+
+# --------------------------------------------------------------------------- cache
+
+def cache_bytes(codec: int, n_seqs: int, n_kv: int, capacity: int) -> int:
+    return n_seqs * n_kv * capacity * ROW_BYTES[codec]
+
+
+def append_side(codec: int, side: int, cache: np.ndarray, n_seqs: int, n_kv: int,
+                capacity: int, seq_lens, n_new, x_new) -> None:
+    """Quantize-on-append into ``cache`` (uint8, modified in place).
+
+    ``x_new``: fp16 [n_seqs, max_new, n_kv, 128]; row i < n_new[s] goes to
+    position seq_lens[s] + i.  ``seq_lens`` is not modified.
+    """
+    assert cache.dtype == np.uint8 and cache.flags["C_CONTIGUOUS"]
+    xb = _as_half_bits(x_new)
+    max_new = xb.shape[1]
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    nn = np.ascontiguousarray(n_new, np.int32)
+    rc = _load().kvqo_append_side(codec, side, _ptr(cache, ctypes.c_uint8), n_seqs, n_kv,
+                                  capacity, _ptr(sl, ctypes.c_int32), _ptr(nn, ctypes.c_int32),
+                                  max_new, _ptr(xb, ctypes.c_uint16))
+    if rc:
+        raise ValueError(f"oracle append failed ({rc})")
+
+
+def dequant_stream(codec: int, side: int, cache: np.ndarray, n_kv: int, capacity: int,
+                   seq: int, kvh: int, n_tokens: int) -> np.ndarray:
+    out = np.zeros((n_tokens, D), np.float64)
+    rc = _load().kvqo_dequant_stream(codec, side, _ptr(cache, ctypes.c_uint8), n_kv, capacity,
+                                     seq, kvh, n_tokens, _ptr(out, ctypes.c_double))
+    if rc:
+        raise ValueError("oracle dequant failed")
+    return out
+
+
+# --------------------------------------------------------------------------- attention
+
+def attend_rows(q, K: np.ndarray, V: np.ndarray, limit, scale: float):
+    """q fp16 [n, 128]; K, V fp64 [T, 128]; row r attends keys < limit[r]."""
+    qb = _as_half_bits(q).reshape(-1, D)
+    K = np.ascontiguousarray(K, np.float64)
+    V = np.ascontiguousarray(V, np.float64)
+    lim = np.ascontiguousarray(np.broadcast_to(np.asarray(limit, np.int64), (qb.shape[0],)))
+    out = np.zeros((qb.shape[0], D), np.float64)
+    lse = np.zeros(qb.shape[0], np.float64)
+    rc = _load().kvqo_attend_rows(qb.shape[0], _ptr(qb, ctypes.c_uint16), K.shape[0],
+                                  _ptr(K, ctypes.c_double), _ptr(V, ctypes.c_double),
+                                  _ptr(lim, ctypes.c_int64), float(scale),
+                                  _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc:
+        raise MemoryError("oracle attend failed")
+    return out, lse
+
+
+def decode_layer(codec_k: int, codec_v: int, cache_k: np.ndarray, cache_v: np.ndarray,
+                 n_seqs: int, n_kv: int, n_q: int, capacity: int, seq_lens, q, scale: float,
+                 sel=None):
+    """Decode attention of one layer; ``sel`` (bool [n_seqs, n_kv]) limits the groups."""
+    qb = _as_half_bits(q).reshape(n_seqs, n_q, D)
+    sl = np.ascontiguousarray(seq_lens, np.int32)
+    out = np.full((n_seqs, n_q, D), np.nan)
+    lse = np.full((n_seqs, n_q), np.nan)
+    selp = None
+    if sel is not None:
+        s8 = np.ascontiguousarray(np.asarray(sel, bool).reshape(n_seqs, n_kv), np.uint8)
+        selp = _ptr(s8, ctypes.c_uint8)
+    rc = _load().kvqo_decode_layer(codec_k, codec_v, _ptr(cache_k, ctypes.c_uint8),
+                                   _ptr(cache_v, ctypes.c_uint8), n_seqs, n_kv, n_q, capacity,
+                                   _ptr(sl, ctypes.c_int32), _ptr(qb, ctypes.c_uint16),
+                                   float(scale), selp, _ptr(out, ctypes.c_double),
+                                   _ptr(lse, ctypes.c_double))
+    if rc:
+        raise ValueError(f"oracle decode failed ({rc})")
+    return out, lse
+
+
+def prefill_chunk(codec_k: int, codec_v: int, cache_k: np.ndarray, cache_v: np.ndarray,
+                  n_kv: int, n_q: int, capacity: int, seq: int, q_start: int, q, scale: float,
+                  rows=None):
+    """Causal chunk attention; q fp16 [n_tok, n_q, 128]; ``rows`` limits query rows."""
+    qb = _as_half_bits(q)
+    n_tok = qb.shape[0]
+    qb = qb.reshape(n_tok, n_q, D)
+    out = np.full((n_tok, n_q, D), np.nan)
+    lse = np.full((n_tok, n_q), np.nan)
+    selp = None
+    if rows is not None:
+        s8 = np.zeros(n_tok, np.uint8)
+        s8[np.asarray(rows)] = 1
+        selp = _ptr(s8, ctypes.c_uint8)
+    rc = _load().kvqo_prefill_chunk(codec_k, codec_v, _ptr(cache_k, ctypes.c_uint8),
+                                    _ptr(cache_v, ctypes.c_uint8), n_kv, n_q, capacity, seq,
+                                    q_start, n_tok, _ptr(qb, ctypes.c_uint16), float(scale), selp,
+                                    _ptr(out, ctypes.c_double), _ptr(lse, ctypes.c_double))
+    if rc:
+        raise ValueError(f"oracle prefill failed ({rc})")
+    return out, lse

@@ -1,0 +1,583 @@
+/*
+ * kvq_oracle.c -- plain, slow CPU oracle for attention over a block-quantized
+ * KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product library links, includes or
+ * calls this file; it shares no code, header, table or constant generator
+ * with the CUDA path.  Only the tests, the smoke check and the benchmark's CPU
+ * baseline use it.
+ *
+ * What it computes, and where each piece comes from:
+ *
+ *  - Block codecs f16 / q8_0 / q4_0 ("Codecs" table of the buun-llama-cpp
+ *    listing: f16 16.0, q8_0 8.5 and q4_0 4.5 bits per value, i.e. 32-value
+ *    blocks of a 2-byte fp16 scale plus 32 int8 or 16 packed nibble bytes).
+ *    The encoders are the written fp32 formulas this library defines:
+ *      q8_0: amax = max|x|; d = amax / 127 (fp32 RN division);
+ *            q = round-half-away-from-zero(x / d) (fp32 RN division), 0 if d == 0;
+ *            stored d16 = fp16_RN(d).
+ *      q4_0: m = the signed x of largest |x| (lowest index wins ties);
+ *            d = m / -8 (fp32 RN); t = x / d (0 if d == 0); u = t + 8.5 (fp32 RN);
+ *            q = min(15, trunc(u)); byte j = q[j] | q[j+16] << 4; stored fp16_RN(d).
+ *    Decoding is exact: x^ = d16 * q (q8_0), d16 * (q - 8) (q4_0).
+ *  - The per-(layer, side) codec choice of the classic F16 -> Q8_0 -> Q4_0
+ *    ladder ("VBR -- Variable Bit-Rate KV Cache" section of the same listing)
+ *    is just the codec argument of every call below.
+ *  - Softmax attention, the plain definition, in fp64 over the dequantized
+ *    cache: s_t = scale * q . k^_t over the attended keys, p = softmax(s),
+ *    o = sum_t p_t v^_t, lse = max s + log sum exp(s - max s).  Decode attends
+ *    every cached key; a prefill chunk attends causally (query at absolute
+ *    position P sees keys 0..P), after the chunk's own keys were appended
+ *    (the ubatch discussion of the serverAppConfigs commit log).
+ *  - The cache byte layout, written from its specification (the library's
+ *    public header documents the same layout): the cache of one layer and
+ *    side is [seq][kv_head][capacity/16 units][unit bytes]; a unit holds 16
+ *    consecutive tokens; every canonical row byte (the row's blocks laid end
+ *    to end) has exactly one place in the unit, given by kvqo_unit_offset.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define KVQO_D 128
+#define KVQO_UNIT_TOKENS 16
+
+enum { KVQO_F16 = 0, KVQO_Q8_0 = 1, KVQO_Q4_0 = 2 };
+enum { KVQO_SIDE_K = 0, KVQO_SIDE_V = 1 };
+
+/* ------------------------------------------------------------------------ */
+/* IEEE binary16 <-> binary32, written out bit by bit.                       */
+/* ------------------------------------------------------------------------ */
+
+float kvqo_half_to_float(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) & 1u;
+    int exp = (h >> 10) & 0x1f;
+    uint32_t man = h & 0x3ffu;
+    float mag;
+    if (exp == 0) {
+        /* zero or subnormal: man * 2^-24, exact in fp32 */
+        mag = ldexpf((float)man, -24);
+    } else if (exp == 31) {
+        mag = man ? NAN : INFINITY;
+    } else {
+        mag = ldexpf((float)(man | 0x400u), exp - 25);
+    }
+    return sign ? -mag : mag;
+}
+
+double kvqo_half_to_double(uint16_t h) { return (double)kvqo_half_to_float(h); }
+
+/* Round an fp32 value to the nearest binary16, ties to even; values beyond the
+ * largest finite half become infinity, tiny values become subnormals or zero. */
+uint16_t kvqo_float_to_half_rn(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    uint32_t fexp = (bits >> 23) & 0xffu;
+    uint32_t fman = bits & 0x7fffffu;
+    if (fexp == 0xff) /* inf / nan */
+        return (uint16_t)(sign | 0x7c00u | (fman ? 0x200u : 0u));
+    if (fexp == 0 && fman == 0)
+        return sign;
+    /* value = 1.fman * 2^(fexp-127) (fp32 subnormals are far below half range) */
+    int e = (int)fexp - 127;
+    if (e > 15)
+        return (uint16_t)(sign | 0x7c00u);
+    uint32_t sig = fman | 0x800000u; /* 24-bit significand, value = sig * 2^(e-23) */
+    int shift;                       /* right shift turning sig into a half mantissa */
+    int hexp;
+    if (e >= -14) {                  /* normal half: 11-bit significand */
+        shift = 13;
+        hexp = e + 15;
+    } else {                         /* subnormal half: units of 2^-24 */
+        shift = 13 + (-14 - e);
+        hexp = 0;
+        if (shift > 25)              /* below half of the smallest subnormal */
+            return sign;
+    }
+    uint32_t kept = sig >> shift;
+    uint32_t rem = sig & ((1u << shift) - 1u);
+    uint32_t half = 1u << (shift - 1);
+    if (rem > half || (rem == half && (kept & 1u)))
+        kept += 1;
+    uint32_t out;
+    if (hexp == 0) {
+        out = kept; /* may carry into the smallest normal, which is then exact */
+    } else {
+        /* kept holds 1.mmmmmmmmmm (11 bits), maybe carried to 2^11 */
+        if (kept >= 0x800u) {
+            kept >>= 1;
+            hexp += 1;
+        }
+        if (hexp >= 31)
+            return (uint16_t)(sign | 0x7c00u);
+        out = ((uint32_t)hexp << 10) | (kept & 0x3ffu);
+    }
+    return (uint16_t)(sign | out);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Block codecs (canonical byte form: fp16 scale little-endian, then quants). */
+/* ------------------------------------------------------------------------ */
+
+static int kvqo_all_finite(const float *x, int n)
+{
+    for (int j = 0; j < n; ++j)
+        if (!isfinite(x[j]))
+            return 0;
+    return 1;
+}
+
+/* q8_0: 34 bytes = d16 (2) + 32 x int8. Returns 0, or -1 for non-finite input. */
+int kvqo_q8_0_encode_block(const uint16_t *x16, uint8_t *out)
+{
+    float x[32];
+    for (int j = 0; j < 32; ++j)
+        x[j] = kvqo_half_to_float(x16[j]);
+    if (!kvqo_all_finite(x, 32))
+        return -1;
+    float amax = 0.0f;
+    for (int j = 0; j < 32; ++j) {
+        float a = fabsf(x[j]);
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / 127.0f;
+    uint16_t d16 = kvqo_float_to_half_rn(d);
+    out[0] = (uint8_t)(d16 & 0xffu);
+    out[1] = (uint8_t)(d16 >> 8);
+    for (int j = 0; j < 32; ++j) {
+        int q = 0;
+        if (d != 0.0f) {
+            float t = x[j] / d;
+            q = (int)roundf(t); /* C roundf: halfway cases away from zero */
+        }
+        out[2 + j] = (uint8_t)(int8_t)q;
+    }
+    return 0;
+}
+
+/* q4_0: 18 bytes = d16 (2) + 16 bytes, byte j = q[j] | q[j+16] << 4. */
+int kvqo_q4_0_encode_block(const uint16_t *x16, uint8_t *out)
+{
+    float x[32];
+    for (int j = 0; j < 32; ++j)
+        x[j] = kvqo_half_to_float(x16[j]);
+    if (!kvqo_all_finite(x, 32))
+        return -1;
+    int jmax = 0;
+    float amax = fabsf(x[0]);
+    for (int j = 1; j < 32; ++j) {
+        float a = fabsf(x[j]);
+        if (a > amax) { /* strict: the lowest index keeps a tie */
+            amax = a;
+            jmax = j;
+        }
+    }
+    float m = x[jmax];
+    float d = m / -8.0f;
+    uint16_t d16 = kvqo_float_to_half_rn(d);
+    out[0] = (uint8_t)(d16 & 0xffu);
+    out[1] = (uint8_t)(d16 >> 8);
+    int q[32];
+    for (int j = 0; j < 32; ++j) {
+        float t = (d != 0.0f) ? x[j] / d : 0.0f;
+        float u = t + 8.5f;
+        int v = (int)u; /* truncation toward zero; u >= 0.5 here */
+        q[j] = v > 15 ? 15 : v;
+    }
+    for (int j = 0; j < 16; ++j)
+        out[2 + j] = (uint8_t)((q[j] & 0xf) | ((q[j + 16] & 0xf) << 4));
+    return 0;
+}
+
+void kvqo_q8_0_decode_block(const uint8_t *in, double *out)
+{
+    uint16_t d16 = (uint16_t)(in[0] | (in[1] << 8));
+    double d = kvqo_half_to_double(d16);
+    for (int j = 0; j < 32; ++j)
+        out[j] = d * (double)(int8_t)in[2 + j];
+}
+
+void kvqo_q4_0_decode_block(const uint8_t *in, double *out)
+{
+    uint16_t d16 = (uint16_t)(in[0] | (in[1] << 8));
+    double d = kvqo_half_to_double(d16);
+    for (int j = 0; j < 16; ++j) {
+        out[j] = d * (double)((int)(in[2 + j] & 0xf) - 8);
+        out[j + 16] = d * (double)((int)(in[2 + j] >> 4) - 8);
+    }
+}
+
+/* Canonical row bytes for head_dim 128: the row's four blocks end to end. */
+int kvqo_row_bytes(int codec)
+{
+    switch (codec) {
+    case KVQO_F16: return 2 * KVQO_D;
+    case KVQO_Q8_0: return 4 * 34;
+    case KVQO_Q4_0: return 4 * 18;
+    default: return -1;
+    }
+}
+
+int kvqo_unit_bytes(int codec)
+{
+    int rb = kvqo_row_bytes(codec);
+    return rb < 0 ? -1 : rb * KVQO_UNIT_TOKENS;
+}
+
+/* Encode n rows of 128 fp16 values into canonical row bytes. */
+int kvqo_encode_rows(int codec, int64_t n, const uint16_t *x, uint8_t *out)
+{
+    int rb = kvqo_row_bytes(codec);
+    if (rb < 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint16_t *xr = x + i * KVQO_D;
+        uint8_t *o = out + i * rb;
+        if (codec == KVQO_F16) {
+            for (int d = 0; d < KVQO_D; ++d) {
+                o[2 * d] = (uint8_t)(xr[d] & 0xffu);
+                o[2 * d + 1] = (uint8_t)(xr[d] >> 8);
+            }
+        } else {
+            for (int b = 0; b < 4; ++b) {
+                int rc = codec == KVQO_Q8_0 ? kvqo_q8_0_encode_block(xr + 32 * b, o + 34 * b)
+                                            : kvqo_q4_0_encode_block(xr + 32 * b, o + 18 * b);
+                if (rc)
+                    return rc;
+            }
+        }
+    }
+    return 0;
+}
+
+/* Decode n canonical rows into fp64 values. */
+int kvqo_decode_rows(int codec, int64_t n, const uint8_t *in, double *out)
+{
+    int rb = kvqo_row_bytes(codec);
+    if (rb < 0)
+        return -1;
+    for (int64_t i = 0; i < n; ++i) {
+        const uint8_t *r = in + i * rb;
+        double *o = out + i * KVQO_D;
+        if (codec == KVQO_F16) {
+            for (int d = 0; d < KVQO_D; ++d)
+                o[d] = kvqo_half_to_double((uint16_t)(r[2 * d] | (r[2 * d + 1] << 8)));
+        } else if (codec == KVQO_Q8_0) {
+            for (int b = 0; b < 4; ++b)
+                kvqo_q8_0_decode_block(r + 34 * b, o + 32 * b);
+        } else {
+            for (int b = 0; b < 4; ++b)
+                kvqo_q4_0_decode_block(r + 18 * b, o + 32 * b);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Cache layout: where canonical row byte cb of token row r (0..15) of a unit */
+/* lives inside the unit.  K-side and V-side units differ.                   */
+/* ------------------------------------------------------------------------ */
+
+int kvqo_unit_offset(int codec, int side, int r, int cb)
+{
+    if (r < 0 || r >= KVQO_UNIT_TOKENS || cb < 0 || cb >= kvqo_row_bytes(codec))
+        return -1;
+    int g = r & 7, rh = r >> 3;              /* K side: row = g + 8 * rh */
+    int tig = (r & 7) >> 1, par = r & 1;     /* V side: row = 2 * tig + par + 8 * rh */
+    if (codec == KVQO_F16) {
+        int d = cb >> 1, k = cb & 1;
+        if (side == KVQO_SIDE_K) {
+            int b = d >> 5, h = (d >> 4) & 1, w = (d >> 2) & 3, i = d & 3;
+            return (2 * b + rh) * 512 + (4 * g + w) * 16 + h * 8 + i * 2 + k;
+        } else {
+            int mt = d >> 4, gq = (d & 15) >> 1, sub = d & 1;
+            return mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + sub * 2 + par) * 2 + k;
+        }
+    }
+    if (codec == KVQO_Q8_0) {
+        int b = cb / 34, o = cb % 34;
+        if (o < 2) { /* scale byte o of block b */
+            if (side == KVQO_SIDE_K)
+                return 2048 + g * 16 + rh * 8 + b * 2 + o;
+            return 2048 + tig * 32 + b * 8 + rh * 4 + par * 2 + o;
+        }
+        int e = o - 2, d = 32 * b + e;
+        if (side == KVQO_SIDE_K) {
+            int h = e >> 4, w = (e >> 2) & 3, i = e & 3;
+            return b * 512 + (4 * g + w) * 16 + (2 * rh + h) * 4 + i;
+        } else {
+            int mt = d >> 4, gq = (d & 15) >> 1, sub = d & 1;
+            return (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2 + sub;
+        }
+    }
+    if (codec == KVQO_Q4_0) {
+        int b = cb / 18, o = cb % 18;
+        if (o < 2) {
+            if (side == KVQO_SIDE_K)
+                return 1024 + g * 16 + rh * 8 + b * 2 + o;
+            return 1024 + tig * 32 + b * 8 + rh * 4 + par * 2 + o;
+        }
+        int jc = o - 2; /* canonical packed byte 0..15 of block b */
+        if (side == KVQO_SIDE_K) {
+            int w = jc >> 2, i = jc & 3;
+            return (b >> 1) * 512 + (4 * g + w) * 16 + ((b & 1) * 2 + rh) * 4 + i;
+        } else {
+            int mt = 2 * b + (jc >> 3), gq = jc & 7;
+            return (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
+        }
+    }
+    return -1;
+}
+
+static uint8_t *kvqo_stream(uint8_t *cache, int codec, int n_kv, int capacity, int seq, int kvh)
+{
+    int64_t ub = kvqo_unit_bytes(codec);
+    int64_t units = capacity / KVQO_UNIT_TOKENS;
+    return cache + ((int64_t)seq * n_kv + kvh) * units * ub;
+}
+
+/* Scatter one canonical row into token position pos of a (seq, kv_head) stream. */
+static void kvqo_put_row(uint8_t *stream, int codec, int side, int64_t pos, const uint8_t *row)
+{
+    int rb = kvqo_row_bytes(codec);
+    uint8_t *unit = stream + (pos / KVQO_UNIT_TOKENS) * kvqo_unit_bytes(codec);
+    int r = (int)(pos % KVQO_UNIT_TOKENS);
+    for (int cb = 0; cb < rb; ++cb)
+        unit[kvqo_unit_offset(codec, side, r, cb)] = row[cb];
+}
+
+static void kvqo_get_row(const uint8_t *stream, int codec, int side, int64_t pos, uint8_t *row)
+{
+    int rb = kvqo_row_bytes(codec);
+    const uint8_t *unit = stream + (pos / KVQO_UNIT_TOKENS) * kvqo_unit_bytes(codec);
+    int r = (int)(pos % KVQO_UNIT_TOKENS);
+    for (int cb = 0; cb < rb; ++cb)
+        row[cb] = unit[kvqo_unit_offset(codec, side, r, cb)];
+}
+
+/* Quantize-on-append for one side of one layer.
+ * x_new: fp16 [n_seqs][max_new][n_kv][128]; row i < n_new[s] of sequence s
+ * goes to token position seq_lens[s] + i.  Lengths are not updated here.
+ * Returns 0, -1 on bad arguments or capacity overflow, -2 on non-finite input. */
+int kvqo_append_side(int codec, int side, uint8_t *cache, int n_seqs, int n_kv, int capacity,
+                     const int32_t *seq_lens, const int32_t *n_new, int max_new,
+                     const uint16_t *x_new)
+{
+    int rb = kvqo_row_bytes(codec);
+    if (rb < 0 || capacity % KVQO_UNIT_TOKENS)
+        return -1;
+    uint8_t row[256];
+    for (int s = 0; s < n_seqs; ++s) {
+        if (n_new[s] < 0 || n_new[s] > max_new || seq_lens[s] < 0 ||
+            (int64_t)seq_lens[s] + n_new[s] > capacity)
+            return -1;
+        for (int i = 0; i < n_new[s]; ++i)
+            for (int h = 0; h < n_kv; ++h) {
+                const uint16_t *x = x_new + (((int64_t)s * max_new + i) * n_kv + h) * KVQO_D;
+                if (kvqo_encode_rows(codec, 1, x, row))
+                    return -2;
+                kvqo_put_row(kvqo_stream(cache, codec, n_kv, capacity, s, h), codec, side,
+                             (int64_t)seq_lens[s] + i, row);
+            }
+    }
+    return 0;
+}
+
+/* Read tokens [0, n_tokens) of one (seq, kv_head) stream back as fp64 [n][128]. */
+int kvqo_dequant_stream(int codec, int side, const uint8_t *cache, int n_kv, int capacity,
+                        int seq, int kvh, int64_t n_tokens, double *out)
+{
+    int rb = kvqo_row_bytes(codec);
+    if (rb < 0 || n_tokens > capacity)
+        return -1;
+    uint8_t row[256];
+    const uint8_t *st = kvqo_stream((uint8_t *)cache, codec, n_kv, capacity, seq, kvh);
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        kvqo_get_row(st, codec, side, t, row);
+        kvqo_decode_rows(codec, 1, row, out + t * KVQO_D);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Softmax attention in fp64 (the plain definition).                         */
+/* ------------------------------------------------------------------------ */
+
+/* One query row against keys 0..n_keys-1. out: 128 doubles; *lse written. */
+static void kvqo_attend_one(const uint16_t *q16, const double *K, const double *V, int64_t n_keys,
+                            double scale, double *s_buf, double *out, double *lse)
+{
+    double q[KVQO_D];
+    for (int d = 0; d < KVQO_D; ++d)
+        q[d] = kvqo_half_to_double(q16[d]);
+    for (int d = 0; d < KVQO_D; ++d)
+        out[d] = 0.0;
+    if (n_keys <= 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    double m = -INFINITY;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        const double *k = K + t * KVQO_D;
+        double s = 0.0;
+        for (int d = 0; d < KVQO_D; ++d)
+            s += q[d] * k[d];
+        s *= scale;
+        s_buf[t] = s;
+        if (s > m)
+            m = s;
+    }
+    double z = 0.0;
+    for (int64_t t = 0; t < n_keys; ++t) {
+        double p = exp(s_buf[t] - m);
+        z += p;
+        const double *v = V + t * KVQO_D;
+        for (int d = 0; d < KVQO_D; ++d)
+            out[d] += p * v[d];
+    }
+    for (int d = 0; d < KVQO_D; ++d)
+        out[d] /= z;
+    *lse = m + log(z);
+}
+
+/* n_rows query rows (fp16 [n_rows][128]) against one key/value set
+ * (fp64 [T][128]); row r attends keys 0..limit[r]-1.  OpenMP over rows when
+ * compiled with it; each row is computed independently in fixed order. */
+int kvqo_attend_rows(int n_rows, const uint16_t *q, int64_t T, const double *K, const double *V,
+                     const int64_t *limit, double scale, double *out, double *lse)
+{
+    int bad = 0;
+#pragma omp parallel
+    {
+        double *s_buf = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+#pragma omp for schedule(dynamic, 1)
+        for (int r = 0; r < n_rows; ++r) {
+            if (!s_buf) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
+            }
+            int64_t L = limit[r] < T ? limit[r] : T;
+            kvqo_attend_one(q + (int64_t)r * KVQO_D, K, V, L, scale, s_buf,
+                            out + (int64_t)r * KVQO_D, lse + r);
+        }
+        free(s_buf);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Decode attention of one layer for a subset of (seq, kv_head) groups.
+ * q: fp16 [n_seqs][n_q][128]; out fp64 [n_seqs][n_q][128]; lse fp64 [n_seqs][n_q].
+ * Only groups with sel[seq * n_kv + kvh] != 0 are computed (sel may be NULL
+ * for all).  Query head h reads kv head h / (n_q / n_kv). */
+int kvqo_decode_layer(int codec_k, int codec_v, const uint8_t *cache_k, const uint8_t *cache_v,
+                      int n_seqs, int n_kv, int n_q, int capacity, const int32_t *seq_lens,
+                      const uint16_t *q, double scale, const uint8_t *sel, double *out,
+                      double *lse)
+{
+    if (n_kv <= 0 || n_q % n_kv)
+        return -1;
+    int G = n_q / n_kv;
+    for (int s = 0; s < n_seqs; ++s)
+        for (int h = 0; h < n_kv; ++h) {
+            if (sel && !sel[s * n_kv + h])
+                continue;
+            int64_t T = seq_lens[s];
+            if (T < 0 || T > capacity)
+                return -1;
+            double *K = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
+            double *V = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
+            int64_t *lim = (int64_t *)malloc(sizeof(int64_t) * (size_t)G);
+            if (!K || !V || !lim) {
+                free(K); free(V); free(lim);
+                return -1;
+            }
+            kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, s, h, T, K);
+            kvqo_dequant_stream(codec_v, KVQO_SIDE_V, cache_v, n_kv, capacity, s, h, T, V);
+            for (int j = 0; j < G; ++j)
+                lim[j] = T;
+            int64_t row0 = (int64_t)s * n_q + (int64_t)h * G;
+            int rc = kvqo_attend_rows(G, q + row0 * KVQO_D, T, K, V, lim, scale,
+                                      out + row0 * KVQO_D, lse + row0);
+            free(K); free(V); free(lim);
+            if (rc)
+                return rc;
+        }
+    return 0;
+}
+
+/* Causal attention of one prefill chunk of sequence `seq`: query i (absolute
+ * position q_start + i) of head h attends keys 0..q_start+i.  The chunk's keys
+ * must already be in the cache.  q: fp16 [n_tok][n_q][128]; out fp64
+ * [n_tok][n_q][128]; lse [n_tok][n_q].  Only query rows with row_sel[i] != 0
+ * are computed when row_sel is given. */
+int kvqo_prefill_chunk(int codec_k, int codec_v, const uint8_t *cache_k, const uint8_t *cache_v,
+                       int n_kv, int n_q, int capacity, int seq, int64_t q_start, int n_tok,
+                       const uint16_t *q, double scale, const uint8_t *row_sel, double *out,
+                       double *lse)
+{
+    if (n_kv <= 0 || n_q % n_kv)
+        return -1;
+    int G = n_q / n_kv;
+    int64_t T = q_start + n_tok;
+    if (T > capacity || q_start < 0)
+        return -1;
+    double *K = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
+    double *V = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
+    uint16_t *qg = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)n_tok * G * KVQO_D);
+    int64_t *lim = (int64_t *)malloc(sizeof(int64_t) * (size_t)n_tok * G);
+    double *og = (double *)malloc(sizeof(double) * (size_t)n_tok * G * KVQO_D);
+    double *lg = (double *)malloc(sizeof(double) * (size_t)n_tok * G);
+    int rc = 0;
+    if (!K || !V || !qg || !lim || !og || !lg) {
+        rc = -1;
+        goto done;
+    }
+    for (int h = 0; h < n_kv && !rc; ++h) {
+        kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, seq, h, T, K);
+        kvqo_dequant_stream(codec_v, KVQO_SIDE_V, cache_v, n_kv, capacity, seq, h, T, V);
+        int nr = 0;
+        for (int i = 0; i < n_tok; ++i) {
+            if (row_sel && !row_sel[i])
+                continue;
+            for (int j = 0; j < G; ++j) {
+                memcpy(qg + (int64_t)nr * KVQO_D, q + ((int64_t)i * n_q + h * G + j) * KVQO_D,
+                       sizeof(uint16_t) * KVQO_D);
+                lim[nr] = q_start + i + 1;
+                ++nr;
+            }
+        }
+        rc = kvqo_attend_rows(nr, qg, T, K, V, lim, scale, og, lg);
+        nr = 0;
+        for (int i = 0; i < n_tok && !rc; ++i) {
+            if (row_sel && !row_sel[i])
+                continue;
+            for (int j = 0; j < G; ++j) {
+                int64_t dst = (int64_t)i * n_q + h * G + j;
+                memcpy(out + dst * KVQO_D, og + (int64_t)nr * KVQO_D, sizeof(double) * KVQO_D);
+                lse[dst] = lg[nr];
+                ++nr;
+            }
+        }
+    }
+done:
+    free(K); free(V); free(qg); free(lim); free(og); free(lg);
+    return rc;
+}
+
+int kvqo_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,395 @@
+"""Pins for the CPU oracle: checks against what the pages and mathematics fix.
+
+These tests never touch the CUDA library.  Each pin is chosen so that a
+plausible slip in the oracle (a wrong rounding mode, a dropped scale, a
+transposed layout, a wrong softmax normaliser or an off-by-one key limit)
+fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- fp16 helpers
+
+def test_half_to_float_exhaustive_matches_numpy():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([oracle.half_to_float(int(b)) for b in bits], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_float_to_half_matches_numpy_round_to_nearest_even():
+    rng = np.random.default_rng(11)
+    vals = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(20000) * 1e-5).astype(np.float32),   # subnormal half range
+        (rng.standard_normal(5000) * 3e4).astype(np.float32),     # near overflow
+        np.array([65504, 65519.996, 65520, -65520, 2.0 ** -24, 2.0 ** -25, 3 * 2.0 ** -26,
+                  2.0 ** -14, 2.0 ** -14 * (1 - 2.0 ** -12), 0.0, -0.0, 1e-30, -1e-30,
+                  1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, np.inf, -np.inf], np.float32),
+    ])
+    # halfway points between adjacent halves exercise ties-to-even
+    h = rng.integers(0, 0x7bff, 5000).astype(np.uint16)
+    lo = h.view(np.float16).astype(np.float64)
+    hi = (h + 1).view(np.float16).astype(np.float64)
+    vals = np.concatenate([vals, ((lo + hi) / 2).astype(np.float32)])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.float_to_half_bits(float(v)) for v in vals], np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- sizes (pages)
+
+def test_row_bytes_follow_the_codec_table():
+    g = _golden("codec_sizes.json")
+    for name, codec in (("f16", oracle.F16), ("q8_0", oracle.Q8_0), ("q4_0", oracle.Q4_0)):
+        bpv = g["bits_per_value"][name]
+        assert oracle.ROW_BYTES[codec] * 8 == bpv * g["head_dim"]
+        x = np.zeros((1, 128), np.float16)
+        assert oracle.encode_rows(codec, x).shape == (1, g["derived"]["row_bytes"][name])
+
+
+def test_kv_bytes_per_token_worked_examples():
+    g = _golden("kv_bytes_per_token.json")
+    L, H = g["geometry"]["layers"], g["geometry"]["kv_heads"]
+    per_tok = lambda ck, cv: L * H * (oracle.ROW_BYTES[ck] + oracle.ROW_BYTES[cv])
+    assert per_tok(oracle.F16, oracle.Q8_0) / 1024 == g["kib_per_token"]["k_f16_v_q8_0"]
+    assert per_tok(oracle.F16, oracle.F16) / 1024 == g["kib_per_token"]["k_f16_v_f16"]
+    ex = g["slots_example"]
+    gib = ex["slots"] * ex["tokens_per_slot"] * per_tok(oracle.F16, oracle.Q8_0) / 2 ** 30
+    assert round(gib, 1) == ex["gib_rounded_1dp"]
+
+
+# ---------------------------------------------------------------- codecs: hand-derived blocks
+
+@pytest.mark.parametrize("fixture,codec", [("q8_0_blocks.json", oracle.Q8_0),
+                                            ("q4_0_blocks.json", oracle.Q4_0)])
+def test_hand_derived_blocks(fixture, codec):
+    for case in _golden(fixture)["cases"]:
+        x = np.array(case["x"], np.float16)
+        row = np.tile(x, 4)[None, :]          # the same block four times along head_dim
+        got = oracle.encode_rows(codec, row)[0]
+        bb = 34 if codec == oracle.Q8_0 else 18
+        d16 = int(case["d16_hex"], 16)
+        q = np.array(case["q"], np.int64)
+        if codec == oracle.Q8_0:
+            want = np.concatenate([[d16 & 0xff, d16 >> 8], q.astype(np.int8).view(np.uint8)])
+        else:
+            want = np.concatenate([[d16 & 0xff, d16 >> 8], q[:16] | (q[16:] << 4)])
+        for b in range(4):
+            assert np.array_equal(got[b * bb:(b + 1) * bb], want.astype(np.uint8)), case["name"]
+
+
+def _random_blocks(rng, n):
+    kinds = [
+        lambda: rng.standard_normal(32),
+        lambda: rng.standard_normal(32) * 1e-4,            # small scales, subnormal d16
+        lambda: rng.standard_normal(32) * 300,
+        lambda: np.where(rng.random(32) < 0.1, rng.standard_normal(32) * 8, rng.standard_normal(32)),
+        lambda: rng.integers(-3, 4, 32).astype(np.float64),  # many ties in |x|
+    ]
+    return np.stack([kinds[i % len(kinds)]() for i in range(n)]).astype(np.float16)
+
+
+def test_q8_0_properties_nearest_integer_and_error_bound():
+    rng = np.random.default_rng(5)
+    x16 = _random_blocks(rng, 4000)
+    rows = oracle.encode_rows(oracle.Q8_0, x16.reshape(-1, 128)).reshape(-1, 34)
+    x = x16.astype(np.float64)
+    d16 = rows[:, :2].copy().view(np.uint16)[:, 0].view(np.float16).astype(np.float64)
+    q = rows[:, 2:].view(np.int8).astype(np.float64)
+    amax = np.abs(x).max(1)
+    d = (amax.astype(np.float32) / np.float32(127)).astype(np.float64)
+    # the stored scale is the fp16 rounding of amax/127 (within half an fp16 ulp)
+    assert np.all(np.abs(d16 - amax / 127) <= np.maximum(np.abs(amax / 127) * 2 ** -11, 2 ** -25) + 1e-12)
+    nz = d > 0
+    t = x[nz] / d[nz, None]
+    # q is a nearest integer of x/d (fp32 division adds at most one fp32 ulp)
+    assert np.all(np.abs(t - q[nz]) <= 0.5 + 1e-5)
+    assert np.all(np.abs(q) <= 127)
+    # ties go away from zero: wherever |x/d| is (very nearly) k + 1/2, |q| = k + 1
+    frac = np.abs(t) - np.floor(np.abs(t))
+    tie = np.abs(frac - 0.5) < 1e-9
+    assert np.all(np.abs(q[nz][tie]) == np.floor(np.abs(t[tie])) + 1)
+    # reconstruction error: |x - d16 q| <= d/2 + |q| |d - d16| (+ rounding slack)
+    err = np.abs(x - d16[:, None] * q)
+    bound = d[:, None] / 2 + np.abs(q) * np.abs(d - d16)[:, None] + 1e-6 * amax[:, None] + 1e-12
+    assert np.all(err <= bound)
+    assert np.all(q[~nz] == 0)
+
+
+def test_q4_0_properties():
+    rng = np.random.default_rng(6)
+    x16 = _random_blocks(rng, 4000)
+    rows = oracle.encode_rows(oracle.Q4_0, x16.reshape(-1, 128)).reshape(-1, 18)
+    x = x16.astype(np.float64)
+    d16 = rows[:, :2].copy().view(np.uint16)[:, 0].view(np.float16).astype(np.float64)
+    nib = np.concatenate([rows[:, 2:] & 0xf, rows[:, 2:] >> 4], axis=1).astype(np.float64)
+    jmax = np.argmax(np.abs(x), axis=1)               # numpy argmax: first occurrence
+    m = x[np.arange(len(x)), jmax]
+    d = (m.astype(np.float32) / np.float32(-8)).astype(np.float64)
+    assert np.all(np.abs(d16 - m / -8) <= np.maximum(np.abs(m / 8) * 2 ** -11, 2 ** -25) + 1e-12)
+    # the element holding the block maximum always encodes to nibble 0 (x^ = -8 d = m)
+    assert np.all(nib[np.arange(len(x)), jmax][d != 0] == 0)
+    nz = d != 0
+    t = x[nz] / d[nz, None]
+    unclamped = t + 8.5 < 16
+    # q - 8 = floor(t + 1/2) where not clamped: a nearest integer, ties upward
+    assert np.all(np.abs(t - (nib[nz] - 8))[unclamped] <= 0.5 + 1e-5)
+    assert np.all(nib[nz][~unclamped] == 15)
+    assert np.all(nib[~nz] == 8)
+    err = np.abs(x - d16[:, None] * (nib - 8))[nz]
+    bound = (np.abs(d[nz, None]) / 2 + np.abs(nib[nz] - 8) * np.abs(d - d16)[nz, None]
+             + 1e-6 * np.abs(m[nz, None]) + 1e-12)
+    assert np.all(err[unclamped] <= bound[unclamped])
+    # clamped values (x/d > 7.5: opposite sign, within d/2 of |m|) err by at most |d|
+    cbound = np.broadcast_to(np.abs(d[nz, None]) + np.abs(d - d16)[nz, None] * 8
+                             + 1e-6 * np.abs(m[nz, None]), err.shape)
+    assert np.all(err[~unclamped] <= cbound[~unclamped])
+
+
+def _fl32(r: Fraction) -> Fraction:
+    """Nearest binary32 to a rational (ties to even), by exact arithmetic."""
+    if r == 0:
+        return Fraction(0)
+    s = -1 if r < 0 else 1
+    a = abs(r)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, -126)
+    ulp = Fraction(2) ** (e - 23)
+    k = a / ulp
+    fl = math.floor(k)
+    rem = k - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return s * fl * ulp
+
+
+def test_q8_0_exact_rational_rounding_on_sampled_blocks():
+    """The two fp32 divisions of the formula, redone in exact rational arithmetic."""
+    rng = np.random.default_rng(8)
+    x16 = _random_blocks(rng, 60)
+    rows = oracle.encode_rows(oracle.Q8_0, x16.reshape(-1, 128)).reshape(-1, 34)
+    for blk, row in zip(x16, rows):
+        xs = [Fraction(float(v)) for v in blk.astype(np.float64)]
+        amax = max(abs(v) for v in xs)
+        d = _fl32(amax / 127)
+        for j, xv in enumerate(xs):
+            if d == 0:
+                want = 0
+            else:
+                t = _fl32(xv / d)
+                want = int(math.floor(abs(t) + Fraction(1, 2))) * (1 if t >= 0 else -1)
+            assert int(np.int8(row[2 + j].astype(np.int8))) == want
+
+
+# ---------------------------------------------------------------- cache layout
+
+@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("side", [oracle.SIDE_K, oracle.SIDE_V])
+def test_unit_layout_is_a_bijection(codec, side):
+    tab = oracle.unit_offset_table(codec, side)
+    ub = 16 * oracle.ROW_BYTES[codec]
+    assert tab.min() == 0 and tab.max() == ub - 1
+    assert np.array_equal(np.sort(tab.ravel()), np.arange(ub))
+
+
+@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0])
+def test_append_then_dequant_round_trip_in_pieces(codec):
+    rng = np.random.default_rng(3)
+    n_seqs, n_kv, cap = 2, 3, 64
+    x = rng.standard_normal((n_seqs, 40, n_kv, 128)).astype(np.float16)
+    for side in (oracle.SIDE_K, oracle.SIDE_V):
+        cache_a = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, cap), np.uint8)
+        cache_b = np.zeros_like(cache_a)
+        lens = np.array([0, 5], np.int32)
+        # one append of all rows versus three ragged appends
+        oracle.append_side(codec, side, cache_a, n_seqs, n_kv, cap, lens, [40, 33], x)
+        pos = lens.copy()
+        for piece in ([7, 1], [16, 17], [17, 15]):
+            piece = np.array(piece, np.int32)
+            xs = np.zeros((n_seqs, int(piece.max()), n_kv, 128), np.float16)
+            for s in range(n_seqs):
+                off = int(pos[s] - lens[s])
+                xs[s, :piece[s]] = x[s, off:off + piece[s]]
+            oracle.append_side(codec, side, cache_b, n_seqs, n_kv, cap, pos, piece, xs)
+            pos += piece
+        assert np.array_equal(cache_a, cache_b)
+        for s, n in ((0, 40), (1, 33)):
+            for h in range(n_kv):
+                got = oracle.dequant_stream(codec, side, cache_a, n_kv, cap, s, h, lens[s] + n)
+                want = oracle.decode_rows(codec, oracle.encode_rows(codec, x[s, :n, h]))
+                assert np.array_equal(got[lens[s]:], want)
+                if codec == oracle.F16:
+                    assert np.array_equal(got[lens[s]:], x[s, :n, h].astype(np.float64))
+
+
+def test_append_rejects_capacity_overflow():
+    cache = np.zeros(oracle.cache_bytes(oracle.Q8_0, 1, 1, 16), np.uint8)
+    x = np.zeros((1, 4, 1, 128), np.float16)
+    with pytest.raises(ValueError):
+        oracle.append_side(oracle.Q8_0, 0, cache, 1, 1, 16, [14], [4], x)
+
+
+# ---------------------------------------------------------------- attention
+
+def _softmax_attn_numpy(q, K, V, scale):
+    s = (q.astype(np.float64) @ K.T) * scale
+    m = s.max(axis=-1, keepdims=True)
+    p = np.exp(s - m)
+    z = p.sum(axis=-1, keepdims=True)
+    return (p / z) @ V, (m + np.log(z))[..., 0]
+
+
+def test_zero_query_gives_mean_of_values():
+    rng = np.random.default_rng(1)
+    T = 37
+    K = rng.standard_normal((T, 128))
+    V = rng.standard_normal((T, 128))
+    q = np.zeros((3, 128), np.float16)
+    out, lse = oracle.attend_rows(q, K, V, T, 1 / math.sqrt(128))
+    assert np.allclose(out, V.mean(0), rtol=0, atol=1e-12)
+    assert np.allclose(lse, math.log(T), atol=1e-12)
+
+
+def test_dominant_score_selects_one_value_row():
+    rng = np.random.default_rng(2)
+    T, star = 50, 17
+    q = np.zeros((1, 128), np.float16)
+    q[0, 0] = 1.0
+    K = rng.standard_normal((T, 128)) * 0.01
+    K[star, 0] = 100.0 * math.sqrt(128)      # score 100 above every other key
+    V = rng.standard_normal((T, 128))
+    out, _ = oracle.attend_rows(q, K, V, T, 1 / math.sqrt(128))
+    assert np.allclose(out[0], V[star], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_brute_force_four_token_contexts(seed):
+    rng = np.random.default_rng(100 + seed)
+    q = rng.standard_normal((5, 128)).astype(np.float16)
+    K = rng.standard_normal((4, 128)).astype(np.float16).astype(np.float64)
+    V = rng.standard_normal((4, 128)).astype(np.float16).astype(np.float64)
+    scale = 1 / math.sqrt(128)
+    out, lse = oracle.attend_rows(q, K, V, 4, scale)
+    ref_o, ref_l = _softmax_attn_numpy(q, K, V, scale)
+    assert np.allclose(out, ref_o, rtol=0, atol=1e-13)
+    assert np.allclose(lse, ref_l, rtol=0, atol=1e-13)
+    # each prefix length against explicit per-token sums
+    for L in range(1, 5):
+        o, l = oracle.attend_rows(q[:1], K, V, L, scale)
+        s = [float(np.dot(q[0].astype(np.float64), K[t])) * scale for t in range(L)]
+        w = [math.exp(v - max(s)) for v in s]
+        ref = sum(wi * V[t] for t, wi in enumerate(w)) / sum(w)
+        assert np.allclose(o[0], ref, rtol=0, atol=1e-13)
+        assert abs(l[0] - (max(s) + math.log(sum(w)))) < 1e-13
+
+
+def test_f16_codec_attention_matches_torch_float64():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(4)
+    T = 29
+    q = rng.standard_normal((4, 128)).astype(np.float16)
+    kv16 = rng.standard_normal((2, T, 128)).astype(np.float16)
+    K, V = kv16.astype(np.float64)
+    out, _ = oracle.attend_rows(q, K, V, T, 0.0883883)
+    qt = torch.from_numpy(q.astype(np.float64))
+    p = torch.softmax(qt @ torch.from_numpy(K).T * 0.0883883, dim=-1)
+    ref = (p @ torch.from_numpy(V)).numpy()
+    assert np.allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_lse_merge_of_split_keys_equals_unsplit():
+    rng = np.random.default_rng(9)
+    T = 301
+    q = rng.standard_normal((2, 128)).astype(np.float16)
+    K = rng.standard_normal((T, 128))
+    V = rng.standard_normal((T, 128))
+    scale = 1 / math.sqrt(128)
+    full_o, full_l = oracle.attend_rows(q, K, V, T, scale)
+    cuts = [0, 64, 65, 200, T]
+    parts = [oracle.attend_rows(q, K[a:b], V[a:b], b - a, scale) for a, b in zip(cuts, cuts[1:])]
+    L = np.stack([p[1] for p in parts])
+    M = L.max(0)
+    w = np.exp(L - M)
+    merged = sum(wi[:, None] * p[0] for wi, p in zip(w, parts)) / w.sum(0)[:, None]
+    assert np.allclose(merged, full_o, rtol=0, atol=1e-12)
+    assert np.allclose(M + np.log(w.sum(0)), full_l, rtol=0, atol=1e-12)
+
+
+def test_empty_context_gives_zero_and_minus_inf():
+    q = np.ones((1, 128), np.float16)
+    out, lse = oracle.attend_rows(q, np.zeros((0, 128)), np.zeros((0, 128)), 0, 1.0)
+    assert np.all(out == 0) and np.isneginf(lse[0])
+
+
+def _fill_layer(rng, ck, cv, n_seqs, n_kv, cap, lens):
+    caches = []
+    xs = []
+    for codec, side in ((ck, oracle.SIDE_K), (cv, oracle.SIDE_V)):
+        c = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, cap), np.uint8)
+        x = rng.standard_normal((n_seqs, max(lens), n_kv, 128)).astype(np.float16)
+        oracle.append_side(codec, side, c, n_seqs, n_kv, cap, [0] * n_seqs, lens, x)
+        caches.append(c)
+        xs.append(x)
+    return caches, xs
+
+
+def test_decode_layer_gqa_mapping_and_ragged_lengths():
+    rng = np.random.default_rng(12)
+    n_seqs, n_kv, n_q, cap = 3, 2, 6, 48
+    lens = [5, 33, 1]
+    ck, cv = oracle.Q8_0, oracle.Q4_0
+    (cache_k, cache_v), (xk, xv) = _fill_layer(rng, ck, cv, n_seqs, n_kv, cap, lens)
+    q = rng.standard_normal((n_seqs, n_q, 128)).astype(np.float16)
+    out, lse = oracle.decode_layer(ck, cv, cache_k, cache_v, n_seqs, n_kv, n_q, cap, lens, q, 0.1)
+    G = n_q // n_kv
+    for s in range(n_seqs):
+        for h in range(n_q):
+            kv = h // G
+            K = oracle.decode_rows(ck, oracle.encode_rows(ck, xk[s, :lens[s], kv]))
+            V = oracle.decode_rows(cv, oracle.encode_rows(cv, xv[s, :lens[s], kv]))
+            ro, rl = _softmax_attn_numpy(q[s, h][None], K, V, 0.1)
+            assert np.allclose(out[s, h], ro[0], rtol=0, atol=1e-12)
+            assert abs(lse[s, h] - rl[0]) < 1e-12
+
+
+def test_prefill_chunk_is_causal_over_cached_plus_new_keys():
+    rng = np.random.default_rng(13)
+    n_kv, n_q, cap, cached, n_tok = 2, 4, 64, 20, 9
+    ck = cv = oracle.Q8_0
+    (cache_k, cache_v), (xk, xv) = _fill_layer(rng, ck, cv, 1, n_kv, cap, [cached + n_tok])
+    q = rng.standard_normal((n_tok, n_q, 128)).astype(np.float16)
+    out, lse = oracle.prefill_chunk(ck, cv, cache_k, cache_v, n_kv, n_q, cap, 0, cached, q, 0.125)
+    for i in range(n_tok):
+        for h in range(n_q):
+            kv = h // (n_q // n_kv)
+            L = cached + i + 1
+            K = oracle.decode_rows(ck, oracle.encode_rows(ck, xk[0, :L, kv]))
+            V = oracle.decode_rows(cv, oracle.encode_rows(cv, xv[0, :L, kv]))
+            ro, rl = _softmax_attn_numpy(q[i, h][None], K, V, 0.125)
+            assert np.allclose(out[i, h], ro[0], rtol=0, atol=1e-12)
+    sub_o, _ = oracle.prefill_chunk(ck, cv, cache_k, cache_v, n_kv, n_q, cap, 0, cached, q, 0.125,
+                                    rows=[0, 8])
+    assert np.array_equal(sub_o[[0, 8]], out[[0, 8]]) and np.isnan(sub_o[1]).all()
