@@ -1,0 +1,150 @@
+"""attention_quantized_kv_gb300: attention over a block-quantized KV cache on GB300.
+
+A thin Python layer over libkvq's C ABI (include/kvq.h).  PyTorch provides
+device memory and streams; every step of the path (quantize-on-append,
+split-K decode attention with its log-sum-exp merge, chunked-prefill
+attention) runs in the library's sm_103a kernels.  The functions below only
+marshal arguments: they take torch tensors, pass their device pointers and
+raise ``KVQError`` on a non-zero status.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+
+import torch
+
+from . import _abi
+from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN,
+                   KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT, kvq_layer)
+
+__all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "CODEC_NAMES", "KVQError", "KVLayer",
+           "kv_append_quantize", "attn_decode_workspace", "attn_decode",
+           "attn_prefill_workspace", "attn_prefill_chunk", "kvq_row_bytes", "kvq_cache_bytes",
+           "default_scale"]
+
+CODEC_NAMES = {KVQ_F16: "f16", KVQ_Q8_0: "q8_0", KVQ_Q4_0: "q4_0"}
+HEAD_DIM = 128
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        msg = _abi.load().kvq_status_str(status).decode()
+        super().__init__(f"{where}: {msg} (status {status})")
+        self.status = status
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise KVQError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else int(t.data_ptr())
+
+
+def default_scale(head_dim: int = HEAD_DIM) -> float:
+    return 1.0 / math.sqrt(head_dim)
+
+
+def kvq_row_bytes(codec: int, head_dim: int = HEAD_DIM) -> int:
+    return int(_abi.load().kvq_row_bytes(codec, head_dim))
+
+
+def kvq_cache_bytes(codec: int, n_seqs: int, n_kv_heads: int, capacity: int,
+                    head_dim: int = HEAD_DIM) -> int:
+    return int(_abi.load().kvq_cache_bytes(codec, n_seqs, n_kv_heads, capacity, head_dim))
+
+
+class KVLayer:
+    """One layer's cache: torch-owned device buffers plus the C descriptor.
+
+    ``k_cache``/``v_cache`` are uint8 tensors in the layout of include/kvq.h,
+    ``seq_lens`` int32 [n_seqs] and ``err`` one int32 error word.
+    """
+
+    def __init__(self, n_seqs: int, n_kv_heads: int, n_q_heads: int, capacity: int,
+                 codec_k: int, codec_v: int, device="cuda", head_dim: int = HEAD_DIM,
+                 k_cache=None, v_cache=None):
+        self.n_seqs, self.n_kv_heads, self.n_q_heads = n_seqs, n_kv_heads, n_q_heads
+        self.capacity, self.codec_k, self.codec_v, self.head_dim = (capacity, codec_k, codec_v,
+                                                                    head_dim)
+        kb = kvq_cache_bytes(codec_k, n_seqs, n_kv_heads, capacity, head_dim)
+        vb = kvq_cache_bytes(codec_v, n_seqs, n_kv_heads, capacity, head_dim)
+        if kb < 0 or vb < 0:
+            raise ValueError("invalid cache geometry (capacity must be a multiple of 256, "
+                             "head_dim 128, codecs f16/q8_0/q4_0)")
+        self.k_cache = k_cache if k_cache is not None else torch.empty(kb, dtype=torch.uint8,
+                                                                        device=device)
+        self.v_cache = v_cache if v_cache is not None else torch.empty(vb, dtype=torch.uint8,
+                                                                        device=device)
+        assert self.k_cache.numel() == kb and self.v_cache.numel() == vb
+        self.seq_lens = torch.zeros(n_seqs, dtype=torch.int32, device=device)
+        self.err = torch.zeros(1, dtype=torch.int32, device=device)
+        self._desc = None
+
+    def desc(self) -> kvq_layer:
+        d = kvq_layer()
+        d.n_seqs, d.n_kv_heads, d.n_q_heads = self.n_seqs, self.n_kv_heads, self.n_q_heads
+        d.head_dim, d.capacity = self.head_dim, self.capacity
+        d.codec_k, d.codec_v, d.reserved = self.codec_k, self.codec_v, 0
+        d.k_cache, d.v_cache = _ptr(self.k_cache), _ptr(self.v_cache)
+        d.seq_lens, d.err = _ptr(self.seq_lens), _ptr(self.err)
+        self._desc = d
+        return d
+
+
+def kv_append_quantize(layer: KVLayer, k_new, v_new, n_new, update_lens: bool = True,
+                       stream=None) -> None:
+    """k_new, v_new: fp16 [n_seqs, max_new, n_kv, 128]; n_new: int32 [n_seqs] (device)."""
+    assert k_new.dtype == torch.float16 and v_new.dtype == torch.float16
+    assert k_new.is_contiguous() and v_new.is_contiguous() and n_new.dtype == torch.int32
+    max_new = int(k_new.shape[1])
+    d = layer.desc()
+    _check(_abi.load().kv_append_quantize(ctypes.byref(d), _ptr(k_new), _ptr(v_new),
+                                          _ptr(n_new), max_new, int(bool(update_lens)),
+                                          _stream_ptr(stream)), "kv_append_quantize")
+
+
+def attn_decode_workspace(layer: KVLayer, max_len: int) -> int:
+    n = ctypes.c_size_t(0)
+    d = layer.desc()
+    _check(_abi.load().attn_decode_workspace(ctypes.byref(d), int(max_len), ctypes.byref(n)),
+           "attn_decode_workspace")
+    return int(n.value)
+
+
+def attn_decode(layer: KVLayer, q, scale: float, out, lse, max_len: int, workspace,
+                stream=None) -> None:
+    """q, out: fp16 [n_seqs, n_q, 128]; lse: fp32 [n_seqs, n_q] or None."""
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous()
+    d = layer.desc()
+    _check(_abi.load().attn_decode(ctypes.byref(d), _ptr(q), float(scale), _ptr(out), _ptr(lse),
+                                   int(max_len), _ptr(workspace), int(workspace.numel() *
+                                                                      workspace.element_size()),
+                                   _stream_ptr(stream)), "attn_decode")
+
+
+def attn_prefill_workspace(layer: KVLayer, q_start: int, n_q_tok: int) -> int:
+    n = ctypes.c_size_t(0)
+    d = layer.desc()
+    _check(_abi.load().attn_prefill_workspace(ctypes.byref(d), int(q_start), int(n_q_tok),
+                                              ctypes.byref(n)), "attn_prefill_workspace")
+    return int(n.value)
+
+
+def attn_prefill_chunk(layer: KVLayer, seq: int, q_start: int, q, scale: float, out, lse,
+                       workspace, stream=None) -> None:
+    """q, out: fp16 [n_q_tok, n_q, 128]; lse: fp32 [n_q_tok, n_q] or None."""
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous()
+    d = layer.desc()
+    _check(_abi.load().attn_prefill_chunk(ctypes.byref(d), int(seq), int(q_start),
+                                          int(q.shape[0]), _ptr(q), float(scale), _ptr(out),
+                                          _ptr(lse), _ptr(workspace),
+                                          int(workspace.numel() * workspace.element_size()),
+                                          _stream_ptr(stream)), "attn_prefill_chunk")

@@ -1,0 +1,150 @@
+// kvq_api.cu -- the C ABI of libkvq (include/kvq.h): argument validation on
+// the host, launch planning, and dispatch to the kernels.  Nothing here
+// allocates, frees or synchronizes device memory.
+#include <cuda_runtime.h>
+
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+#include "kvq_launch.h"
+
+namespace {
+
+constexpr int kHeadDim = 128;
+
+bool valid_codec(int c) { return c == KVQ_F16 || c == KVQ_Q8_0 || c == KVQ_Q4_0; }
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_layer(const kvq_layer *L) {
+  if (!L) return KVQ_EINVAL;
+  if (L->head_dim != kHeadDim) return KVQ_EUNSUPPORTED;
+  if (!valid_codec(L->codec_k) || !valid_codec(L->codec_v)) return KVQ_EUNSUPPORTED;
+  if (L->n_seqs <= 0 || L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->capacity <= 0 ||
+      L->reserved != 0)
+    return KVQ_EINVAL;
+  if (L->n_q_heads % L->n_kv_heads != 0) return KVQ_EINVAL;
+  if (!L->k_cache || !L->v_cache || !L->seq_lens) return KVQ_EINVAL;
+  if (L->capacity % 256 != 0) return KVQ_EALIGN;
+  if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16) || !aligned(L->seq_lens, 4) ||
+      (L->err && !aligned(L->err, 4)))
+    return KVQ_EALIGN;
+  // every byte offset must fit in int64 (it always does for int32 geometry)
+  return KVQ_OK;
+}
+
+int device_sms() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kvq_status_str(int status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_EINVAL: return "KVQ_EINVAL: invalid argument";
+    case KVQ_EUNSUPPORTED: return "KVQ_EUNSUPPORTED: head_dim or codec not supported";
+    case KVQ_ECAPACITY: return "KVQ_ECAPACITY: position past the cache capacity";
+    case KVQ_EALIGN: return "KVQ_EALIGN: misaligned pointer or capacity not a multiple of 256";
+    case KVQ_EWORKSPACE: return "KVQ_EWORKSPACE: workspace missing or too small";
+    case KVQ_ECUDA: return "KVQ_ECUDA: CUDA runtime error";
+    default: return "KVQ: unknown status";
+  }
+}
+
+int64_t kvq_row_bytes(int codec, int32_t head_dim) {
+  if (head_dim != kHeadDim || !valid_codec(codec)) return -1;
+  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : 72;
+}
+
+int64_t kvq_cache_bytes(int codec, int32_t n_seqs, int32_t n_kv_heads, int32_t capacity,
+                        int32_t head_dim) {
+  const int64_t rb = kvq_row_bytes(codec, head_dim);
+  if (rb < 0 || n_seqs <= 0 || n_kv_heads <= 0 || capacity <= 0 || capacity % 256 != 0)
+    return -1;
+  return rb * n_seqs * n_kv_heads * static_cast<int64_t>(capacity);
+}
+
+int kv_append_quantize(const kvq_layer *layer, const void *k_new, const void *v_new,
+                       const int32_t *n_new, int32_t max_new, int32_t update_lens,
+                       void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (max_new < 0 || !n_new) return KVQ_EINVAL;
+  if (max_new > layer->capacity) return KVQ_ECAPACITY;
+  if (max_new > 0 && (!k_new || !v_new)) return KVQ_EINVAL;
+  if (!aligned(k_new, 8) || !aligned(v_new, 8) || !aligned(n_new, 4)) return KVQ_EALIGN;
+  const cudaError_t e = kvq::launch_append(*layer, k_new, v_new, n_new, max_new, update_lens,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!bytes || max_len <= 0) return KVQ_EINVAL;
+  if (max_len > layer->capacity) return KVQ_ECAPACITY;
+  const int sms = device_sms();
+  if (sms <= 0) return KVQ_ECUDA;
+  *bytes = static_cast<size_t>(kvq::plan_decode(*layer, max_len, sms).ws_bytes);
+  return KVQ_OK;
+}
+
+int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
+                int32_t max_len, void *workspace, size_t ws_bytes, void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!q || !out || max_len <= 0) return KVQ_EINVAL;
+  if (max_len > layer->capacity) return KVQ_ECAPACITY;
+  if (!aligned(q, 8) || !aligned(out, 8) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;
+  if (!workspace) return KVQ_EWORKSPACE;
+  if (!aligned(workspace, 16)) return KVQ_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return KVQ_ECUDA;
+  const kvq::DecodePlan pl = kvq::plan_decode(*layer, max_len, sms);
+  if (ws_bytes < static_cast<size_t>(pl.ws_bytes)) return KVQ_EWORKSPACE;
+  const cudaError_t e = kvq::launch_decode(*layer, pl, q, scale, out, lse, max_len, workspace,
+                                           static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int32_t n_q_tok,
+                           size_t *bytes) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!bytes || q_start < 0 || n_q_tok <= 0) return KVQ_EINVAL;
+  if (static_cast<int64_t>(q_start) + n_q_tok > layer->capacity) return KVQ_ECAPACITY;
+  *bytes = static_cast<size_t>(kvq::plan_prefill(*layer, q_start, n_q_tok).ws_bytes);
+  return KVQ_OK;
+}
+
+int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int32_t n_q_tok,
+                       const void *q, float scale, void *out, float *lse, void *workspace,
+                       size_t ws_bytes, void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!q || !out || q_start < 0 || n_q_tok <= 0 || seq < 0 || seq >= layer->n_seqs)
+    return KVQ_EINVAL;
+  if (static_cast<int64_t>(q_start) + n_q_tok > layer->capacity) return KVQ_ECAPACITY;
+  if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;
+  if (!workspace) return KVQ_EWORKSPACE;
+  if (!aligned(workspace, 16)) return KVQ_EALIGN;
+  const kvq::PrefillPlan pl = kvq::plan_prefill(*layer, q_start, n_q_tok);
+  if (ws_bytes < static_cast<size_t>(pl.ws_bytes)) return KVQ_EWORKSPACE;
+  const cudaError_t e = kvq::launch_prefill(*layer, pl, seq, q_start, n_q_tok, q, scale, out, lse,
+                                            workspace, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,168 @@
+// kvq_device.cuh -- device helpers shared by the libkvq kernels (sm_103a).
+//
+// Warp-level tensor-core MMA (m16n8k16, fp16 in, fp32 accumulate), fragment
+// transposes, exact small-integer -> fp16 conversions, mbarrier-tracked bulk
+// async copies with bounded waits, and the unit geometry of the cache layout
+// documented in include/kvq.h.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int kD = 128;          // head_dim
+constexpr int kUnitTokens = 16;  // tokens per layout unit
+
+__host__ __device__ constexpr int row_bytes(int codec) {
+  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : 72;
+}
+__host__ __device__ constexpr int unit_bytes(int codec) { return kUnitTokens * row_bytes(codec); }
+// Byte offset of the scale area inside a unit (q8_0 / q4_0 only).
+__host__ __device__ constexpr int unit_scale_offset(int codec) {
+  return codec == KVQ_Q8_0 ? 2048 : 1024;
+}
+
+// ---------------------------------------------------------------- tensor-core MMA
+
+// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulators.
+// a[0]=(row g, k 2t..2t+1) a[1]=(row g+8, k 2t..) a[2]=(row g, k 2t+8..) a[3]=(row g+8, k 2t+8..)
+// b[0]=(k 2t..2t+1, col g) b[1]=(k 2t+8.., col g); c/d: [0..1]=(row g, col 2t..) [2..3]=(row g+8)
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Transpose an 8x8 fp16 matrix held as one m8n8 fragment per warp.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t lop3_and_xor(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;  // (a & b) ^ c
+  asm("lop3.b32 %0, %1, %2, %3, 0x6a;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;  // (a & b) | c
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t hsub2_bits(uint32_t a, uint32_t b) {
+  __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+  return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Signed bytes 0 and 2 of w as an exact fp16 pair (byte 0 in the low half).
+// Each byte is biased to x+128 and placed in the mantissa of 1024, giving
+// 1152 + x exactly; subtracting 1152 leaves x.
+__device__ __forceinline__ uint32_t s8_pair_02(uint32_t w) {
+  return hsub2_bits(lop3_and_xor(w, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+}
+// Signed bytes 1 and 3.
+__device__ __forceinline__ uint32_t s8_pair_13(uint32_t w) {
+  return hsub2_bits(lop3_and_xor(w >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
+}
+// Nibbles at bit 4k and 16+4k of (w) as the exact fp16 pair (n - 8):
+// the nibble lands in the mantissa of 1024; subtracting 1032 leaves n - 8.
+__device__ __forceinline__ uint32_t u4_pair_minus8(uint32_t w) {
+  return hsub2_bits(lop3_and_or(w, 0x000f000fu, 0x64006400u), 0x64086408u);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk async copy global -> shared, completion counted on an mbarrier.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32_t bytes,
+                                              uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;\n" : "=l"(t));
+  return t;
+}
+
+// Wait for the given phase of an mbarrier, giving up after ~limit_ns.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase,
+                                                  uint64_t limit_ns = 1000000000ull) {
+  if (mbar_try_wait(bar, phase)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, phase)) return true;
+    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Plain shared-memory vector load: ordered after the memory-clobbering waits.
+__device__ __forceinline__ uint4 lds128(const void *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+__device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+}  // namespace kvq

@@ -1,0 +1,41 @@
+// kvq_launch.h -- internal launch entry points shared between the C ABI
+// translation unit and the kernel translation units of libkvq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_new,
+                          const int32_t *n_new, int max_new, int update_lens,
+                          cudaStream_t stream);
+
+struct DecodePlan {
+  int n_hgroups = 1;     // groups of up to 8 query heads per kv head
+  int split_tokens = 0;  // tokens per split (multiple of 16)
+  int n_splits = 1;      // splits per stream
+  int64_t ws_o_bytes = 0;
+  int64_t ws_bytes = 0;
+};
+
+DecodePlan plan_decode(const kvq_layer &L, int max_len, int num_sms);
+cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *q, float scale,
+                          void *out, float *lse, int max_len, void *workspace,
+                          cudaStream_t stream);
+
+struct PrefillPlan {
+  int64_t kv_tokens = 0;     // keys attended by the chunk: q_start + n_q_tok
+  int64_t kv_tokens_pad = 0; // rounded up to the attention tile
+  int64_t ws_k_bytes = 0;    // fp16 K staging [n_kv][kv_tokens_pad][128]
+  int64_t ws_bytes = 0;
+};
+
+PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok);
+cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, int q_start,
+                           int n_q_tok, const void *q, float scale, void *out, float *lse,
+                           void *workspace, cudaStream_t stream);
+
+}  // namespace kvq

@@ -1,0 +1,532 @@
+"""Benchmark of quantized-KV attention on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+for the default workload (32 query / 8 KV heads, 32768 cached q4_0 keys with
+outlier channels) that is: quantize-append one new K/V token, then decode
+attention of all 32 query heads over the 32769 keys.  The cache is built
+(untimed) through the same append kernel.  Inputs are resident in HBM when the
+timed region starts; L2 is flushed (a 2 x L2-size write) before every timed
+step.  Timing: CUDA events on the launching stream around each step, W
+warm-up steps, K timed steps, barrier + synchronize on both sides, max over
+ranks.  ``value`` is the whole-job effective bandwidth: algorithmic bytes
+(every attended K/V row read once, q read, out written, the appended rows
+read and written) divided by the step time.
+
+Also reported: ``e2e`` (the same metric through the C ABI with pinned host
+buffers: per step the H2D copy of q and the new K/V rows, the kernels, and the
+D2H copy of the output), ``roofline`` for the decode kernels, the SM clock
+record of the timed region, and ``cpu_baseline``: the fp64 C oracle timed on
+this host's cores on a bounded sample of the same workload.
+
+``--impl reference`` times that oracle alone (the reference arm) on the same
+workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized-KV attention: effective HBM GB/s, % of peak, µs per layer-step"
+DEFAULT_WORKLOAD = "append_decode_q4_ctx32k"
+ROW = {0: 256, 1: 136, 2: 72}
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def step_work(w):
+    """(bytes, flops, decode_bytes_per_layer list) of one step of workload w."""
+    lens = w.final_lens()
+    total_b, total_f, per_layer = 0, 0, []
+    for ck, cv in w.codecs:
+        app = w.n_seqs * w.append_new * w.n_kv * (2 * 256 + ROW[ck] + ROW[cv])
+        if w.kind == "decode":
+            kv = sum(lens) * w.n_kv * (ROW[ck] + ROW[cv])
+            qo = 2 * w.n_seqs * w.n_q * 256
+            fl = sum(lens) * w.n_q * 4 * 128
+        else:
+            n_tok, q0 = w.append_new, w.lens[0]
+            kv = (q0 + n_tok) * w.n_kv * (ROW[ck] + ROW[cv])
+            qo = 2 * n_tok * w.n_q * 256
+            fl = sum(q0 + i + 1 for i in range(n_tok)) * w.n_q * 4 * 128
+        per_layer.append(kv + qo)
+        total_b += kv + qo + app
+        total_f += fl
+    return total_b, total_f, per_layer
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+class OursArm:
+    def __init__(self, w, device):
+        import torch
+        import attention_quantized_kv_gb300 as kvq
+        from attention_quantized_kv_gb300 import workloads as wl
+        self.torch, self.kvq, self.wl, self.w, self.dev = torch, kvq, wl, w, device
+        self.scale = 1.0 / math.sqrt(128)
+        self.layers, self.ws, self.q, self.kn, self.vn = [], [], [], [], []
+        self.max_len = max(w.final_lens())
+        self.init_lens = torch.tensor(w.lens, dtype=torch.int32, device=device)
+        n_tok = w.append_new if w.kind == "prefill" else 1
+        for l, (ck, cv) in enumerate(w.codecs):
+            L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device)
+            self._fill(L, l)
+            self.layers.append(L)
+            qq = wl.queries(w, l, n_tok, device)
+            if w.kind == "decode":
+                self.q.append(qq[:, 0].contiguous())
+                nb = kvq.attn_decode_workspace(L, self.max_len)
+            else:
+                self.q.append(qq[0].contiguous())
+                nb = kvq.attn_prefill_workspace(L, w.lens[0], w.append_new)
+            self.ws.append(torch.empty(nb, dtype=torch.uint8, device=device))
+            if w.append_new:
+                ks = torch.stack([wl.kv_rows(w, l, 0, s, w.lens[s], w.append_new, device)
+                                  for s in range(w.n_seqs)])
+                vs = torch.stack([wl.kv_rows(w, l, 1, s, w.lens[s], w.append_new, device)
+                                  for s in range(w.n_seqs)])
+                self.kn.append(ks.contiguous())
+                self.vn.append(vs.contiguous())
+        self.n_new = torch.full((w.n_seqs,), w.append_new, dtype=torch.int32, device=device)
+        self.out = [torch.empty_like(q) for q in self.q]
+        self.lse = [torch.empty(q.shape[:2], dtype=torch.float32, device=device) for q in self.q]
+        torch.cuda.synchronize()
+
+    def _fill(self, L, l, chunk=8192):
+        torch, wl, w = self.torch, self.wl, self.w
+        for start in range(0, max(w.lens), chunk):
+            n = [max(0, min(chunk, ln - start)) for ln in w.lens]
+            mx = max(n)
+            k = torch.zeros((w.n_seqs, mx, w.n_kv, 128), dtype=torch.float16, device=self.dev)
+            v = torch.zeros_like(k)
+            for s in range(w.n_seqs):
+                if n[s]:
+                    k[s, :n[s]] = wl.kv_rows(w, l, 0, s, start, n[s], self.dev)
+                    v[s, :n[s]] = wl.kv_rows(w, l, 1, s, start, n[s], self.dev)
+            self.kvq.kv_append_quantize(L, k, v, torch.tensor(n, dtype=torch.int32,
+                                                              device=self.dev))
+
+    def reset(self):
+        for L in self.layers:
+            L.seq_lens.copy_(self.init_lens)
+
+    def launches_per_step(self):
+        per_layer = (2 if self.w.append_new else 0) + 2
+        return per_layer * len(self.layers)
+
+    def step(self, ev=None, q=None, kn=None, vn=None):
+        """One pass of the hot path; ev: list collecting (start, end) events of
+        the attention call of each layer."""
+        kvq, w = self.kvq, self.w
+        torch = self.torch
+        for l, L in enumerate(self.layers):
+            if w.append_new:
+                kvq.kv_append_quantize(L, (kn or self.kn)[l], (vn or self.vn)[l], self.n_new)
+            if ev is not None:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+            if w.kind == "decode":
+                kvq.attn_decode(L, (q or self.q)[l], self.scale, self.out[l], self.lse[l],
+                                self.max_len, self.ws[l])
+            else:
+                kvq.attn_prefill_chunk(L, 0, w.lens[0], (q or self.q)[l], self.scale,
+                                       self.out[l], self.lse[l], self.ws[l])
+            if ev is not None:
+                b.record()
+                ev.append((a, b, l))
+
+    def layer_errs(self):
+        return [int(L.err.item()) for L in self.layers]
+
+
+def _flush_l2(torch, buf):
+    buf.zero_()
+
+
+def _traffic_for(workload):
+    """dram bytes per launch of the decode/prefill kernels from a committed ncu
+    summary, if it was taken on the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != _kernel_source_hash(e.get("kernel", "decode")):
+        return None
+    return e.get("bytes_per_launch")
+
+
+def _kernel_source_hash(kind):
+    names = {"decode": ["decode.cu", "kvq_device.cuh"],
+             "prefill": ["prefill.cu", "kvq_device.cuh"]}[kind]
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "attention_quantized_kv_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def run_ours(args, w, rank, world, dist):
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    arm = OursArm(w, dev)
+    bytes_step, flops_step, per_layer_bytes = step_work(w)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    for _ in range(args.warmup):
+        _flush_l2(torch, flush)
+        arm.reset()
+        arm.step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler(local)
+    clk.start()
+    starts, ends, ev = [], [], []
+    for _ in range(args.steps):
+        _flush_l2(torch, flush)
+        arm.reset()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        arm.step(ev)
+        b.record()
+        starts.append(a)
+        ends.append(b)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = float(sum(step_ms))
+    attn_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    attn_bytes = sum(per_layer_bytes[l] for _, _, l in ev)
+    errs = arm.layer_errs()
+
+    # e2e: through the C ABI with pinned host buffers, copies inside the timed region
+    h_q = [q.cpu().pin_memory() for q in arm.q]
+    h_k = [k.cpu().pin_memory() for k in arm.kn]
+    h_v = [v.cpu().pin_memory() for v in arm.vn]
+    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in arm.out]
+    d_q = [torch.empty_like(q) for q in arm.q]
+    d_k = [torch.empty_like(k) for k in arm.kn]
+    d_v = [torch.empty_like(v) for v in arm.vn]
+    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    e2e_ms = []
+    for it in range(args.warmup + args.steps):
+        _flush_l2(torch, flush)
+        arm.reset()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for x, y in zip(d_q + d_k + d_v, h_q + h_k + h_v):
+            x.copy_(y, non_blocking=True)
+        arm.step(None, d_q, d_k or None, d_v or None)
+        for x, y in zip(h_out, arm.out):
+            x.copy_(y, non_blocking=True)
+        b.record()
+        b.synchronize()
+        if it >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_total = float(sum(e2e_ms))
+
+    if dist:
+        t = torch.tensor([total_ms, e2e_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total = float(t[0]), float(t[1])
+    if rank != 0:
+        return None
+
+    hbm, tf, peak_kind = _peaks()
+    ms_step = total_ms / args.steps
+    value = world * bytes_step * args.steps / (total_ms * 1e-3) / 1e9
+    achieved_attn = attn_bytes / (sum(attn_ms) * 1e-3) / 1e9
+    n_layers = w.n_layers
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "us_per_layer_step": round(ms_step * 1e3 / n_layers, 3),
+        "pct_of_hbm_peak": round(100 * value / world / hbm, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 in / fp32 accumulate over q8_0/q4_0/f16 KV",
+        "data": "synthetic (seeded N(0,1) fp16 draws, cache built by the append kernel)",
+        "config": {"workload": w.name, "description": w.description, "n_seqs": w.n_seqs,
+                   "n_q_heads": w.n_q, "n_kv_heads": w.n_kv, "head_dim": 128,
+                   "context": w.final_lens() if w.n_seqs <= 2 else
+                   {"sum": sum(w.final_lens()), "min": min(w.final_lens()),
+                    "max": max(w.final_lens())},
+                   "layers": n_layers,
+                   "codecs": [[["f16", "q8_0", "q4_0"][c] for c in p] for p in w.codecs],
+                   "l2": "flushed before every timed step (2 x L2 write)",
+                   "parallelism": f"replicas x{world}"},
+        "bytes_per_step": bytes_step,
+        "flops_per_step": flops_step,
+        "e2e": {"value": round(world * bytes_step * args.steps / (e2e_total * 1e-3) / 1e9, 2),
+                "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_total / args.steps, 5)},
+        "gpu_launches": arm.launches_per_step() * args.steps,
+        "clocks": clocks,
+        "device_errors": errs,
+    }
+    if w.kind == "decode":
+        line["roofline"] = {"bound": "hbm", "kernel": "attn_decode (split + merge kernels)",
+                            "achieved": round(achieved_attn, 2), "peak": hbm,
+                            "peak_kind": peak_kind, "unit": "GB/s",
+                            "frac": round(achieved_attn / hbm, 4),
+                            "traffic": _traffic_for(w.name)}
+    else:
+        fl = flops_step / n_layers
+        tfs = fl / (np.mean(attn_ms) * 1e-3) / 1e12
+        line["roofline"] = {"bound": "tensor", "kernel": "attn_prefill_chunk",
+                            "achieved": round(tfs, 2), "peak": tf, "peak_kind": peak_kind,
+                            "unit": "TFLOP/s", "frac": round(tfs / tf, 4),
+                            "traffic": _traffic_for(w.name)}
+    return line
+
+
+# ------------------------------------------------------------------ the oracle (CPU)
+
+class OracleArm:
+    """The fp64 C oracle over a bounded sample of the workload on host cores."""
+
+    def __init__(self, w, budget_groups=None):
+        import torch
+        import oracle
+        from attention_quantized_kv_gb300 import workloads as wl
+        self.w, self.oracle, self.scale = w, oracle, 1.0 / math.sqrt(128)
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        G = w.n_q // w.n_kv
+        # sample: (layer, seq, kv head) groups, in order, until the sample's
+        # attended keys reach ~40M x rows (a few seconds of fp64 work per step)
+        groups, budget = [], 0
+        cap_rows = 2e7 if w.kind == "decode" else 0
+        for l in range(w.n_layers):
+            for s in range(w.n_seqs):
+                for h in range(w.n_kv):
+                    if groups and budget > cap_rows:
+                        break
+                    groups.append((l, s, h))
+                    budget += w.final_lens()[s] * G
+        self.groups = groups
+        self.caches, self.q, self.new = [], [], []
+        for l, s, h in groups:
+            ck, cv = w.codecs[l]
+            cs = []
+            for side, codec in ((0, ck), (1, cv)):
+                rows = wl.kv_rows(w, l, side, s, 0, w.lens[s], dev)[:, h].cpu().numpy()
+                c = np.zeros(oracle.cache_bytes(codec, 1, 1, w.capacity), np.uint8)
+                oracle.append_side(codec, side, c, 1, 1, w.capacity, [0], [w.lens[s]],
+                                   rows.reshape(1, -1, 1, 128))
+                new = (wl.kv_rows(w, l, side, s, w.lens[s], w.append_new, dev)[:, h].cpu().numpy()
+                       if w.append_new else None)
+                cs.append((c, new))
+            self.caches.append(cs)
+            n_tok = w.append_new if w.kind == "prefill" else 1
+            qq = wl.queries(w, l, n_tok, dev)[s].cpu().numpy()  # [n_tok, n_q, 128]
+            self.q.append(qq[:, h * G:(h + 1) * G])
+        # prefill: a fixed sample of query rows
+        self.rows = None
+        if w.kind == "prefill":
+            self.rows = [0, 1, w.append_new // 2, w.append_new - 1]
+        self.sample_desc = (f"{len(groups)} of {w.n_layers * w.n_seqs * w.n_kv} "
+                            f"(layer, seq, kv head) groups"
+                            + (f", {len(self.rows)} of {w.append_new} query rows"
+                               if self.rows else ""))
+
+    def sample_bytes(self):
+        w = self.w
+        tot = 0
+        G = w.n_q // w.n_kv
+        for (l, s, h) in self.groups:
+            ck, cv = w.codecs[l]
+            T = w.final_lens()[s]
+            app = w.append_new * (2 * 256 + ROW[ck] + ROW[cv])
+            if w.kind == "decode":
+                tot += T * (ROW[ck] + ROW[cv]) + 2 * G * 256 + app
+            else:
+                frac = len(self.rows) / w.append_new
+                tot += frac * (T * (ROW[ck] + ROW[cv]) + 2 * w.append_new * G * 256) + app
+        return tot
+
+    def step(self):
+        w, o = self.w, self.oracle
+        G = w.n_q // w.n_kv
+        for (l, s, h), cs, q in zip(self.groups, self.caches, self.q):
+            ck, cv = w.codecs[l]
+            (kc, kn), (vc, vn) = cs
+            kc, vc = kc.copy(), vc.copy()
+            if w.append_new:
+                o.append_side(ck, 0, kc, 1, 1, w.capacity, [w.lens[s]], [w.append_new],
+                              kn.reshape(1, -1, 1, 128))
+                o.append_side(cv, 1, vc, 1, 1, w.capacity, [w.lens[s]], [w.append_new],
+                              vn.reshape(1, -1, 1, 128))
+            if w.kind == "decode":
+                o.decode_layer(ck, cv, kc, vc, 1, 1, G, w.capacity, [w.final_lens()[s]],
+                               np.ascontiguousarray(q[0]), self.scale)
+            else:
+                o.prefill_chunk(ck, cv, kc, vc, 1, G, w.capacity, 0, w.lens[0],
+                                np.ascontiguousarray(q), self.scale, rows=self.rows)
+
+
+def time_oracle(w, steps, warmup, min_seconds=0.0):
+    import oracle
+    arm = OracleArm(w)
+    for _ in range(warmup):
+        arm.step()
+    t0 = time.perf_counter()
+    n = 0
+    while n < steps or (time.perf_counter() - t0) < min_seconds:
+        arm.step()
+        n += 1
+        if min_seconds and n >= steps and time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    gbs = arm.sample_bytes() * n / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": f"{arm.sample_desc}; {n} steps in {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+        tdist.init_process_group("nccl")
+        dist = tdist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from attention_quantized_kv_gb300 import workloads as wl
+    w = wl.get(args.workload)
+
+    if args.impl == "reference":
+        if rank == 0:
+            r = time_oracle(w, args.steps, args.warmup)
+            line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world,
+                    "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                    "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, fp32 codec",
+                    "data": "synthetic", "impl": "reference",
+                    "config": {"workload": w.name, "description": w.description},
+                    "cpu_baseline": r,
+                    "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    line = run_ours(args, w, rank, world, dist)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = time_oracle(w, 1, 0, min_seconds=10.0)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

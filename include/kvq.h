@@ -1,0 +1,186 @@
+/*
+ * kvq.h -- C ABI of libkvq: attention over a block-quantized KV cache on one
+ * GB300 (sm_103a).
+ *
+ * Operations (all asynchronous on the caller's CUDA stream):
+ *   kv_append_quantize   quantize new K/V rows into the cache (f16 / q8_0 / q4_0)
+ *   attn_decode          split-K decode attention over every cached key
+ *   attn_prefill_chunk   causal attention of one prefill chunk (ubatch)
+ *
+ * Sources.  The codecs and their sizes follow the "Codecs" table of the
+ * buun-llama-cpp listing (f16 16.0, q8_0 8.5, q4_0 4.5 bits per value); the
+ * per-(layer, side) codec choice follows its "VBR -- Variable Bit-Rate KV
+ * Cache" section (the classic F16 -> Q8_0 -> Q4_0 ladder, K and V typed
+ * independently, flash attention mandatory); the asymmetric K=f16 / V=q8_0
+ * contract, the ubatch-sized prefill chunks and the 256-aligned per-slot
+ * pools follow the serverAppConfigs commit log (frank_small_unit.bats
+ * commit).  Softmax attention is the plain definition: o = softmax(scale *
+ * q K^T) V over the attended keys, K and V dequantized.
+ *
+ * Ownership.  The caller allocates every buffer (cache, lengths, inputs,
+ * outputs, workspace) in device memory and keeps it alive until the work on
+ * the stream has finished.  The library never allocates, frees or
+ * synchronizes; it keeps no state between calls besides cached device
+ * attributes.
+ *
+ * Errors.  Every entry point validates its arguments on the host before any
+ * launch and returns a kvq_status; it never aborts.  Conditions that only the
+ * device can see (a length that passes capacity, a wait that timed out) set
+ * bits in the optional device word kvq_layer.err (KVQ_DEVERR_*) and the
+ * affected rows are skipped.
+ *
+ * ------------------------------------------------------------------------
+ * Block codecs (head_dim 128 = four 32-value blocks per row):
+ *   f16  : 128 fp16 values.                              256 bytes / row
+ *   q8_0 : per block fp16 d16 + 32 int8 q.               136 bytes / row
+ *          amax = max|x| (fp32); d = amax / 127 (fp32, IEEE RN division);
+ *          q = round-half-away-from-zero(x / d) (IEEE RN division), or 0 when
+ *          d == 0; d16 = fp16_RN(d).  x^ = d16 * q.
+ *   q4_0 : per block fp16 d16 + 16 bytes of nibbles.      72 bytes / row
+ *          m = the signed x with the largest |x| (lowest index wins ties);
+ *          d = m / -8 (fp32 RN); t = x / d (fp32 RN; 0 when d == 0);
+ *          u = t + 8.5 (fp32 RN); q = min(15, trunc(u));
+ *          canonical byte j = q[j] | q[j+16] << 4; d16 = fp16_RN(d).
+ *          x^ = d16 * (q - 8).
+ *   The canonical row is the row's four blocks end to end (d16 little-endian
+ *   before each block's quants).
+ *
+ * Cache layout (one layer, one side):
+ *   [n_seqs][n_kv_heads][capacity / 16 units][unit_bytes]
+ *   A unit holds 16 consecutive tokens (unit_bytes = 16 * row bytes: 4096,
+ *   2176, 1152).  Inside a unit, canonical byte cb of token row r (0..15) is
+ *   placed as follows (all integer arithmetic; g = r & 7, rh = r >> 3,
+ *   tig = (r & 7) >> 1, par = r & 1):
+ *   K side
+ *     f16  value d, byte k:  b=d>>5, h=(d>>4)&1, w=(d>>2)&3, i=d&3
+ *          -> (2b+rh)*512 + (4g+w)*16 + h*8 + i*2 + k
+ *     q8_0 quant of dim 32b+e: h=e>>4, w=(e>>2)&3, i=e&3
+ *          -> b*512 + (4g+w)*16 + (2rh+h)*4 + i
+ *          scale byte k of block b -> 2048 + g*16 + rh*8 + b*2 + k
+ *     q4_0 canonical byte jc (0..15) of block b: w=jc>>2, i=jc&3
+ *          -> (b>>1)*512 + (4g+w)*16 + ((b&1)*2+rh)*4 + i
+ *          scale byte k of block b -> 1024 + g*16 + rh*8 + b*2 + k
+ *   V side
+ *     f16  value d, byte k:  mt=d>>4, gq=(d&15)>>1, s=d&1
+ *          -> mt*512 + (4gq+tig)*16 + (rh*4+s*2+par)*2 + k
+ *     q8_0 quant of dim d: mt=d>>4, gq=(d&15)>>1, s=d&1
+ *          -> (mt>>1)*512 + (4gq+tig)*16 + ((mt&1)*2+rh)*4 + par*2 + s
+ *          scale byte k of block b -> 2048 + tig*32 + b*8 + rh*4 + par*2 + k
+ *     q4_0 canonical byte jc of block b: mt=2b+(jc>>3), gq=jc&7
+ *          -> (mt>>2)*512 + (4gq+tig)*16 + (mt&3)*4 + par*2 + rh
+ *          scale byte k of block b -> 1024 + tig*32 + b*8 + rh*4 + par*2 + k
+ *   The layout stores exactly the canonical bytes (8.5 / 4.5 / 16 bits per
+ *   value); it only orders them so that each thread of the decode kernel
+ *   reads its tensor-core operand fragments with aligned 16-byte loads.
+ * ------------------------------------------------------------------------
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Codec of one (layer, side) cache tensor. */
+typedef enum { KVQ_F16 = 0, KVQ_Q8_0 = 1, KVQ_Q4_0 = 2 } kvq_codec;
+
+/* Host-side status returned by every entry point. */
+typedef enum {
+    KVQ_OK = 0,
+    KVQ_EINVAL = 1,       /* null pointer, non-positive size, bad index, n_q % n_kv != 0 */
+    KVQ_EUNSUPPORTED = 2, /* head_dim != 128 or unknown codec */
+    KVQ_ECAPACITY = 3,    /* a host-known position passes capacity */
+    KVQ_EALIGN = 4,       /* capacity not a multiple of 256, or a misaligned pointer */
+    KVQ_EWORKSPACE = 5,   /* workspace null or smaller than the *_workspace query says */
+    KVQ_ECUDA = 6         /* a CUDA runtime call or a launch failed */
+} kvq_status;
+
+/* Bits OR-ed into *kvq_layer.err by the device (the word is never cleared). */
+#define KVQ_DEVERR_CAPACITY 1 /* append: seq_lens[s] + n_new[s] > capacity; rows skipped */
+#define KVQ_DEVERR_MAXLEN 2   /* decode: seq_lens[s] > max_len; keys past max_len ignored */
+#define KVQ_DEVERR_TIMEOUT 4  /* a bounded wait on an async copy gave up */
+#define KVQ_DEVERR_SEQLEN 8   /* prefill: seq_lens[seq] < q_start + n_q_tok */
+
+/* One layer's cache.  All pointers are device pointers owned by the caller.
+ * k_cache / v_cache: kvq_cache_bytes() bytes each, 16-byte aligned, in the
+ * layout above.  seq_lens: int32[n_seqs], the number of valid tokens of each
+ * sequence.  err: optional int32 error word (NULL to skip). */
+typedef struct kvq_layer {
+    int32_t n_seqs;
+    int32_t n_kv_heads;
+    int32_t n_q_heads;  /* multiple of n_kv_heads; head h reads kv head h / (n_q/n_kv) */
+    int32_t head_dim;   /* must be 128 */
+    int32_t capacity;   /* tokens per (seq, kv head) stream; multiple of 256 */
+    int32_t codec_k;    /* kvq_codec of the K side */
+    int32_t codec_v;    /* kvq_codec of the V side */
+    int32_t reserved;   /* must be 0 */
+    void *k_cache;
+    void *v_cache;
+    int32_t *seq_lens;
+    int32_t *err;
+} kvq_layer;
+
+/* Human-readable name of a status code (static string). */
+KVQ_API const char *kvq_status_str(int status);
+
+/* Bytes of one canonical row (256 / 136 / 72 for head_dim 128), or -1. */
+KVQ_API int64_t kvq_row_bytes(int codec, int32_t head_dim);
+
+/* Bytes of one side's cache for the given geometry, or -1 on bad arguments. */
+KVQ_API int64_t kvq_cache_bytes(int codec, int32_t n_seqs, int32_t n_kv_heads, int32_t capacity,
+                        int32_t head_dim);
+
+/* Quantize-on-append (block codecs above).
+ * k_new, v_new: fp16 [n_seqs][max_new][n_kv_heads][128], 8-byte aligned.
+ * n_new: device int32[n_seqs], rows to append per sequence (0..max_new).
+ * Row i < n_new[s] of sequence s is encoded with the side's codec and written
+ * at token position seq_lens[s] + i.  When update_lens != 0, seq_lens[s] +=
+ * n_new[s] afterwards (stream-ordered).  Positions past capacity set
+ * KVQ_DEVERR_CAPACITY and are skipped. */
+KVQ_API int kv_append_quantize(const kvq_layer *layer, const void *k_new, const void *v_new,
+                       const int32_t *n_new, int32_t max_new, int32_t update_lens,
+                       void *stream);
+
+/* Workspace bytes that attn_decode needs for this layer and max_len. */
+KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes);
+
+/* Decode attention: every query head of every sequence attends all
+ * seq_lens[s] cached keys (split-K over the token axis, log-sum-exp merge).
+ * q: fp16 [n_seqs][n_q_heads][128] (8-byte aligned); out: fp16
+ * [n_seqs][n_q_heads][128]; lse: optional fp32 [n_seqs][n_q_heads] natural-log
+ * sum-exp of the scaled scores (NULL to skip).  max_len bounds every
+ * seq_lens[s] (1..capacity).  workspace: device, 16-byte aligned, at least
+ * attn_decode_workspace() bytes.  A sequence of length 0 gives out = 0 and
+ * lse = -inf. */
+KVQ_API int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
+                int32_t max_len, void *workspace, size_t ws_bytes, void *stream);
+
+/* Workspace bytes that attn_prefill_chunk needs for a chunk ending at
+ * q_start + n_q_tok. */
+KVQ_API int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int32_t n_q_tok,
+                           size_t *bytes);
+
+/* Causal attention of one prefill chunk of sequence `seq`: query i (absolute
+ * position q_start + i) of head h attends keys 0 .. q_start + i of kv head
+ * h / (n_q/n_kv).  The chunk's own keys must already be appended.
+ * q: fp16 [n_q_tok][n_q_heads][128]; out: fp16 [n_q_tok][n_q_heads][128];
+ * lse: optional fp32 [n_q_tok][n_q_heads].  workspace: device, 16-byte
+ * aligned, at least attn_prefill_workspace() bytes. */
+KVQ_API int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int32_t n_q_tok,
+                       const void *q, float scale, void *out, float *lse, void *workspace,
+                       size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

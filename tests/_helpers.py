@@ -1,0 +1,61 @@
+"""Shared helpers of the GPU tests: fill caches through the CUDA append path
+and build the matching oracle caches from the same seeded draws."""
+import math
+
+import numpy as np
+import torch
+
+import attention_quantized_kv_gb300 as kvq
+from attention_quantized_kv_gb300 import workloads as wl
+
+import oracle
+
+ROW = {0: 256, 1: 136, 2: 72}
+
+
+def gpu_layer(w, layer_idx, device="cuda", chunk=4096, lens=None):
+    """A KVLayer of workload w filled through kv_append_quantize (zero-initialised)."""
+    ck, cv = w.codecs[layer_idx]
+    L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device,
+                    k_cache=torch.zeros(kvq.kvq_cache_bytes(ck, w.n_seqs, w.n_kv, w.capacity),
+                                        dtype=torch.uint8, device=device),
+                    v_cache=torch.zeros(kvq.kvq_cache_bytes(cv, w.n_seqs, w.n_kv, w.capacity),
+                                        dtype=torch.uint8, device=device))
+    lens = w.lens if lens is None else lens
+    for start in range(0, max(lens), chunk):
+        n = [max(0, min(chunk, ln - start)) for ln in lens]
+        mx = max(n)
+        k_new = torch.zeros((w.n_seqs, mx, w.n_kv, 128), dtype=torch.float16, device=device)
+        v_new = torch.zeros_like(k_new)
+        for s in range(w.n_seqs):
+            if n[s]:
+                k_new[s, :n[s]] = wl.kv_rows(w, layer_idx, 0, s, start, n[s], device)
+                v_new[s, :n[s]] = wl.kv_rows(w, layer_idx, 1, s, start, n[s], device)
+        kvq.kv_append_quantize(L, k_new, v_new, torch.tensor(n, dtype=torch.int32, device=device))
+    return L
+
+
+def oracle_stream(w, layer_idx, seq, kvh, n_tokens, device="cuda"):
+    """Oracle caches (K side, V side) of ONE (seq, kv head) stream as a 1x1 layer."""
+    ck, cv = w.codecs[layer_idx]
+    cap = w.capacity
+    out = []
+    for side, codec in ((0, ck), (1, cv)):
+        rows = wl.kv_rows(w, layer_idx, side, seq, 0, n_tokens, device)[:, kvh]
+        x = rows.cpu().numpy().reshape(1, n_tokens, 1, 128)
+        c = np.zeros(oracle.cache_bytes(codec, 1, 1, cap), np.uint8)
+        oracle.append_side(codec, side, c, 1, 1, cap, [0], [n_tokens], x)
+        out.append(c)
+    return out
+
+
+def gpu_stream_bytes(L, side, seq, kvh):
+    cache = L.k_cache if side == 0 else L.v_cache
+    codec = L.codec_k if side == 0 else L.codec_v
+    n = L.capacity * ROW[codec]
+    s0 = (seq * L.n_kv_heads + kvh) * n
+    return cache[s0:s0 + n].cpu().numpy()
+
+
+def tol(vmax):
+    return 2e-3 * vmax

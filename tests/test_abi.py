@@ -1,0 +1,112 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+the header declares, and rejects bad arguments on the host (no launches)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_quantized_kv_gb300 import build, _abi
+    build.build()
+    return _abi.load()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"^KVQ_API\s+[\w\s\*]*?\b(\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_binding_exports():
+    from attention_quantized_kv_gb300 import _abi
+    assert _declared_functions() == sorted(_abi.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    import subprocess
+    from attention_quantized_kv_gb300 import _abi
+    out = subprocess.run(["nm", "-D", "--defined-only", _abi.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l}
+    for name in _declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+    # nothing else leaks out of the library's own code
+    assert exported == set(_declared_functions())
+
+
+def test_row_and_cache_bytes(lib):
+    assert [lib.kvq_row_bytes(c, 128) for c in (0, 1, 2)] == [256, 136, 72]
+    assert lib.kvq_row_bytes(1, 64) == -1 and lib.kvq_row_bytes(7, 128) == -1
+    assert lib.kvq_cache_bytes(1, 2, 4, 512, 128) == 2 * 4 * 512 * 136
+    assert lib.kvq_cache_bytes(2, 1, 1, 300, 128) == -1       # not a multiple of 256
+    assert lib.kvq_status_str(4).decode().startswith("KVQ_EALIGN")
+
+
+def _layer(**kw):
+    from attention_quantized_kv_gb300._abi import kvq_layer
+    d = kvq_layer()
+    vals = dict(n_seqs=1, n_kv_heads=2, n_q_heads=8, head_dim=128, capacity=4096, codec_k=1,
+                codec_v=1, reserved=0, k_cache=0x100000, v_cache=0x200000, seq_lens=0x300000,
+                err=0)
+    vals.update(kw)
+    for k, v in vals.items():
+        setattr(d, k, v)
+    return d
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=64), 2), (dict(codec_k=5), 2), (dict(n_q_heads=7), 1),
+    (dict(capacity=1000), 4), (dict(k_cache=0x100008), 4), (dict(seq_lens=0), 1),
+    (dict(n_seqs=0), 1), (dict(reserved=1), 1),
+])
+def test_layer_validation(lib, kw, status):
+    d = _layer(**kw)
+    n = ctypes.c_size_t(0)
+    assert lib.attn_decode(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 16, 0x600000,
+                           1 << 20, None) == status
+    assert lib.kv_append_quantize(ctypes.byref(d), 0x400000, 0x500000, 0x600000, 1, 1,
+                                  None) == status
+    assert lib.attn_prefill_workspace(ctypes.byref(d), 0, 16, ctypes.byref(n)) == status
+
+
+def test_call_argument_validation(lib):
+    d = _layer()
+    assert lib.attn_decode(None, 0x400000, 0.1, 0x500000, None, 16, 0x600000, 1, None) == 1
+    assert lib.attn_decode(ctypes.byref(d), None, 0.1, 0x500000, None, 16, 0x600000, 1, None) == 1
+    assert lib.attn_decode(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 0, 0x600000, 1, None) == 1
+    assert lib.attn_decode(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 5000, 0x600000, 1,
+                           None) == 3
+    assert lib.attn_decode(ctypes.byref(d), 0x400002, 0.1, 0x500000, None, 16, 0x600000, 1,
+                           None) == 4
+    assert lib.attn_decode(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 16, None, 1, None) == 5
+    assert lib.kv_append_quantize(ctypes.byref(d), 0x400000, 0x500000, None, 1, 1, None) == 1
+    assert lib.kv_append_quantize(ctypes.byref(d), 0x400000, 0x500000, 0x600000, 5000, 1,
+                                  None) == 3
+    assert lib.attn_prefill_chunk(ctypes.byref(d), 1, 0, 16, 0x400000, 0.1, 0x500000, None,
+                                  0x600000, 1 << 30, None) == 1      # seq out of range
+    assert lib.attn_prefill_chunk(ctypes.byref(d), 0, 4090, 16, 0x400000, 0.1, 0x500000, None,
+                                  0x600000, 1 << 30, None) == 3
+    n = ctypes.c_size_t(0)
+    assert lib.attn_prefill_workspace(ctypes.byref(d), 0, 2048, ctypes.byref(n)) == 0
+    assert n.value > 0
+    assert lib.attn_prefill_chunk(ctypes.byref(d), 0, 0, 2048, 0x400000, 0.1, 0x500000, None,
+                                  0x600000, n.value - 1, None) == 5
+
+
+def test_oracle_and_library_share_no_code():
+    """The oracle is independent of the CUDA path: neither includes nor imports the other."""
+    csrc = os.path.join(ROOT, "attention_quantized_kv_gb300", "csrc")
+    for f in os.listdir(csrc):
+        txt = open(os.path.join(csrc, f)).read()
+        assert "kvq_oracle" not in txt and "oracle" not in txt.lower(), f
+    for f in os.listdir(os.path.join(ROOT, "attention_quantized_kv_gb300")):
+        if f.endswith(".py"):
+            txt = open(os.path.join(ROOT, "attention_quantized_kv_gb300", f)).read()
+            assert "import oracle" not in txt and "from oracle" not in txt, f
+    otxt = open(os.path.join(ROOT, "oracle", "kvq_oracle.c")).read()
+    assert "#include \"" not in otxt and "kvq.h" not in otxt
