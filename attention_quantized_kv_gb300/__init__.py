@@ -87,16 +87,19 @@ class KVLayer:
         self.seq_lens = torch.zeros(n_seqs, dtype=torch.int32, device=device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         self._desc = None
+        self._desc_key = None
 
     def desc(self) -> kvq_layer:
-        d = kvq_layer()
-        d.n_seqs, d.n_kv_heads, d.n_q_heads = self.n_seqs, self.n_kv_heads, self.n_q_heads
-        d.head_dim, d.capacity = self.head_dim, self.capacity
-        d.codec_k, d.codec_v, d.reserved = self.codec_k, self.codec_v, 0
-        d.k_cache, d.v_cache = _ptr(self.k_cache), _ptr(self.v_cache)
-        d.seq_lens, d.err = _ptr(self.seq_lens), _ptr(self.err)
-        self._desc = d
-        return d
+        """The C descriptor (rebuilt only when a buffer was replaced)."""
+        key = (_ptr(self.k_cache), _ptr(self.v_cache), _ptr(self.seq_lens), _ptr(self.err))
+        if self._desc is None or self._desc_key != key:
+            d = kvq_layer()
+            d.n_seqs, d.n_kv_heads, d.n_q_heads = self.n_seqs, self.n_kv_heads, self.n_q_heads
+            d.head_dim, d.capacity = self.head_dim, self.capacity
+            d.codec_k, d.codec_v, d.reserved = self.codec_k, self.codec_v, 0
+            d.k_cache, d.v_cache, d.seq_lens, d.err = key
+            self._desc, self._desc_key = d, key
+        return self._desc
 
 
 def kv_append_quantize(layer: KVLayer, k_new, v_new, n_new, update_lens: bool = True,
@@ -112,6 +115,7 @@ def kv_append_quantize(layer: KVLayer, k_new, v_new, n_new, update_lens: bool = 
 
 
 def attn_decode_workspace(layer: KVLayer, max_len: int) -> int:
+    """Bytes of decode workspace; allocate it zero-filled (torch.zeros)."""
     n = ctypes.c_size_t(0)
     d = layer.desc()
     _check(_abi.load().attn_decode_workspace(ctypes.byref(d), int(max_len), ctypes.byref(n)),

@@ -4,26 +4,36 @@
 // over all cached keys, with K and V dequantized from f16 / q8_0 / q4_0 blocks
 // (the codecs of the "Codecs" table of the buun-llama-cpp listing; the K and
 // V sides are typed independently, as in its VBR section's per-(layer, side)
-// ladder).  The token axis is cut into splits; each split produces a partial
+// ladder).  Work is cut along the token axis; each piece produces a partial
 // (running max m, running sum l, unnormalised o) and a second kernel merges
-// the partials with the log-sum-exp identity.
+// the partials of each (sequence, head) with the log-sum-exp identity: the
+// last CTA to finish a stream (an atomic ticket, no waiting) merges its
+// partials and writes the output rows.
 //
-// Design (one CTA = 4 warps = one split of one (sequence, kv head, group of
-// up to 8 query heads)):
-//  * Each warp owns a ring of shared-memory stages; lane 0 streams 16-token
-//    units of K and V into it with 1-D bulk async copies (TMA engine) tracked
-//    by mbarriers, so that many KB per SM are in flight without registers.
+// Work partition.  A "stream" is one (sequence, kv head, group of up to 8
+// query heads); its keys are 16-token units.  All units of all streams are
+// laid end to end and the grid (about two CTAs per SM, all resident) takes
+// equal contiguous slices, so ragged lengths cost no imbalance.  A CTA's slice
+// crosses at most a few stream boundaries; at each one its warps merge their
+// partials and the CTA writes one partial for that stream.
+//
+// Inside a CTA (8 warps):
+//  * A ring of shared-memory stages, one 16-token unit of K and V per stage,
+//    filled with 1-D bulk async copies (TMA engine) on mbarriers.  Unit k
+//    goes to stage k % NS and is consumed by warp k % 8 (NS is a multiple of
+//    8, so every stage has one owner warp); after consuming unit k the owner
+//    refills the stage with unit k + NS, so ~80 KB per CTA stay in flight.
 //  * The cache layout (include/kvq.h) stores each unit so that every thread
 //    fetches exactly its tensor-core operand bytes with aligned 16-byte
-//    shared loads (conflict-free: a warp reads 512 contiguous bytes).
+//    shared loads (a warp reads 512 contiguous bytes: conflict-free).
 //  * Quants become exact fp16 integers in registers (bias-and-subtract on
 //    the fp16 mantissa).  S = K Q^T runs on mma.sync m16n8k16 with the 16
-//    tokens of a unit as M and the query heads of the group as N.  Per-block
-//    scales are factored out of the 32-value sums (two MMAs per block into a
-//    fresh accumulator, then s += d * partial), so dequantization is exact.
-//  * Online softmax in the log2 domain, per head, with xor-shuffle maxima;
-//    P is transposed in registers (movmatrix) into the B operand of O^T = V^T
-//    P^T, whose M is 16 head dims; the V block scale is folded into P.
+//    tokens as M and the query heads of the group as N.  Block scales are
+//    factored out of the 32-value sums (two MMAs per block into a fresh
+//    accumulator, then s += d * partial), so K dequantization is exact.
+//  * Online softmax in the log2 domain per head with xor-shuffle maxima; P is
+//    transposed in registers (movmatrix) into the B operand of O^T = V^T P^T
+//    (M = 16 head dims); the V block scale is folded into P.
 #include <cuda_runtime.h>
 
 #include <math.h>
@@ -34,18 +44,24 @@
 namespace kvq {
 namespace {
 
-constexpr int kDecodeWarps = 4;
-constexpr int kWarpSmemBudget = 24576;
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRingBytes = 84 * 1024;
+constexpr int kMaxSeqs = kDecodeMaxSeqs;
+constexpr int kRedFloats = 36;  // per lane: o[8][4], m0, m1, l0, l1
 
 struct DecodeParams {
   const uint8_t *k_cache;
   const uint8_t *v_cache;
   const int32_t *seq_lens;
   const __half *q;
-  float *part_o;   // [n_seqs][n_q][n_splits][128]
-  float2 *part_ml; // [n_seqs][n_q][n_splits]: (max in log2 units, sum)
+  float *part_o;    // [slots][8][128]
+  float2 *part_ml;  // [slots][8]: (max in log2 units, sum)
+  int32_t *tickets; // [streams] arrival counters (zero between calls)
+  __half *out;      // [n_seqs][n_q][128]
+  float *lse;       // [n_seqs][n_q] or null
   int32_t *err;
-  int n_seqs, n_kv, n_q, G, n_hgroups, capacity, max_len, split_tokens, n_splits;
+  int n_seqs, n_kv, n_q, G, n_hg, capacity, max_len;
   float scale_log2;
 };
 
@@ -54,11 +70,18 @@ struct DecodeCfg {
   static constexpr int UK = unit_bytes(CK);
   static constexpr int UV = unit_bytes(CV);
   static constexpr int STAGE = UK + UV;
-  static constexpr int NS_RAW = kWarpSmemBudget / STAGE;
-  static constexpr int NS = NS_RAW < 2 ? 2 : (NS_RAW > 8 ? 8 : NS_RAW);
-  static constexpr int WARP_SMEM = NS * STAGE;
-  static constexpr int SMEM = kDecodeWarps * WARP_SMEM;
-  static_assert(SMEM >= kDecodeWarps * (8 * 128 + 16) * 4, "reduction area must fit");
+  // Stage s always belongs to warp s % kWarps (NS is a multiple of kWarps):
+  // the warp that consumes unit k also refills its stage with unit k + NS
+  // and is the only waiter on that stage's mbarrier, so phase waits are
+  // strictly sequential per barrier.
+  static constexpr int NS_RAW = kRingBytes / STAGE / kWarps * kWarps;
+  static constexpr int NS = NS_RAW > 32 ? 32 : (NS_RAW < kWarps ? kWarps : NS_RAW);
+  static constexpr int RING = NS * STAGE;
+  static constexpr int RED = 4 * 32 * kRedFloats * 4;  // tree-merge slots
+  static constexpr int SMEM = RING + RED;
+  static_assert(NS % kWarps == 0, "stage ownership needs NS % warps == 0");
+  // Two units per warp step when each warp owns at least four stages.
+  static constexpr bool PAIR = NS / kWarps >= 4;
 };
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
@@ -75,7 +98,7 @@ __device__ __forceinline__ int v_dim(int mt, int mrow) {
   return 16 * mt + 2 * (mrow & 7) + (mrow >> 3);
 }
 
-// S (16 tokens x 8 heads) of one unit, already multiplied by scale*log2(e).
+// S (16 tokens x 8 heads) of one unit, multiplied by scale*log2(e).
 template <int CK>
 __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const uint32_t (&qb)[8][2],
                                             float scale_log2, float (&s)[4]) {
@@ -106,10 +129,11 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
       } else {
         const uint4 w = lds128(ku + (b >> 1) * 512 + lane * 16);
         const uint32_t W0 = (b & 1) ? w.z : w.x, W1 = (b & 1) ? w.w : w.y;
-        const uint32_t a0[4] = {u4_pair_minus8(W0), u4_pair_minus8(W1), u4_pair_minus8(W0 >> 8),
-                                u4_pair_minus8(W1 >> 8)};
-        const uint32_t a1[4] = {u4_pair_minus8(W0 >> 4), u4_pair_minus8(W1 >> 4),
-                                u4_pair_minus8(W0 >> 12), u4_pair_minus8(W1 >> 12)};
+        const uint32_t X0 = W0 >> 8, X1 = W1 >> 8;
+        const uint32_t a0[4] = {u4_pair_minus8(W0), u4_pair_minus8(W1), u4_pair_minus8(X0),
+                                u4_pair_minus8(X1)};
+        const uint32_t a1[4] = {u4_pair_minus8_hi(W0), u4_pair_minus8_hi(W1),
+                                u4_pair_minus8_hi(X0), u4_pair_minus8_hi(X1)};
         mma16816(sb, a0, qb[2 * b][0], qb[2 * b][1]);
         mma16816(sb, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
       }
@@ -126,13 +150,14 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
 }
 
 // O^T (128 dims x 8 heads) += V^T (dims x 16 tokens) * P^T (16 tokens x heads).
-template <int CV>
+// FULL: all 16 tokens of the unit are valid (no masking needed).
+template <int CV, bool FULL>
 __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0, uint32_t B1,
                                         int nvalid, float (&o)[8][4]) {
   const int tig = lane & 3;
-  // token validity masks for the halves this thread holds: (t0,t1)=(2tig,2tig+1), (t2,t3)=+8
+  // token validity of the halves this thread holds: (2tig, 2tig+1) and (+8, +9)
   uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
-  if (nvalid < 16) {
+  if (!FULL) {
     m01 = (2 * tig < nvalid ? 0x0000ffffu : 0u) | (2 * tig + 1 < nvalid ? 0xffff0000u : 0u);
     m23 = (2 * tig + 8 < nvalid ? 0x0000ffffu : 0u) | (2 * tig + 9 < nvalid ? 0xffff0000u : 0u);
   }
@@ -140,23 +165,34 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
       const uint4 r = lds128(vu + mt * 512 + lane * 16);
-      const uint32_t a[4] = {r.x & m01, r.y & m01, r.z & m23, r.w & m23};
+      uint32_t a[4] = {r.x, r.y, r.z, r.w};
+      if (!FULL) { a[0] &= m01; a[1] &= m01; a[2] &= m23; a[3] &= m23; }
       mma16816(o[mt], a, B0, B1);
     }
   } else {
     const uint4 s01 = lds128(vu + unit_scale_offset(CV) + tig * 32);
     const uint4 s23 = lds128(vu + unit_scale_offset(CV) + tig * 32 + 16);
-    const uint32_t dp01[4] = {s01.x & m01, s01.z & m01, s23.x & m01, s23.z & m01};
-    const uint32_t dp23[4] = {s01.y & m23, s01.w & m23, s23.y & m23, s23.w & m23};
+    uint32_t dp01[4] = {s01.x, s01.z, s23.x, s23.z};
+    uint32_t dp23[4] = {s01.y, s01.w, s23.y, s23.w};
+    if (!FULL) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) { dp01[b] &= m01; dp23[b] &= m23; }
+    }
+    // P^T with the V block scale folded in, one pair of B registers per block
+    uint32_t bp0[4], bp1[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      bp0[b] = hmul2_bits(B0, dp01[b]);
+      bp1[b] = hmul2_bits(B1, dp23[b]);
+    }
     if (CV == KVQ_Q8_0) {
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint32_t bp0 = hmul2_bits(B0, dp01[b]), bp1 = hmul2_bits(B1, dp23[b]);
         const uint4 w = lds128(vu + b * 512 + lane * 16);
         const uint32_t a0[4] = {s8_pair_02(w.x), s8_pair_13(w.x), s8_pair_02(w.y), s8_pair_13(w.y)};
         const uint32_t a1[4] = {s8_pair_02(w.z), s8_pair_13(w.z), s8_pair_02(w.w), s8_pair_13(w.w)};
-        mma16816(o[2 * b], a0, bp0, bp1);
-        mma16816(o[2 * b + 1], a1, bp0, bp1);
+        mma16816(o[2 * b], a0, bp0[b], bp1[b]);
+        mma16816(o[2 * b + 1], a1, bp0[b], bp1[b]);
       }
     } else {
 #pragma unroll
@@ -166,254 +202,483 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           const int mt = 4 * jv + qq, b = mt >> 1;
-          const uint32_t bp0 = hmul2_bits(B0, dp01[b]), bp1 = hmul2_bits(B1, dp23[b]);
-          const uint32_t W = ws[qq];
-          const uint32_t a[4] = {u4_pair_minus8(W), u4_pair_minus8(W >> 4), u4_pair_minus8(W >> 8),
-                                 u4_pair_minus8(W >> 12)};
-          mma16816(o[mt], a, bp0, bp1);
+          const uint32_t W = ws[qq], X = W >> 8;
+          const uint32_t a[4] = {u4_pair_minus8(W), u4_pair_minus8_hi(W), u4_pair_minus8(X),
+                                 u4_pair_minus8_hi(X)};
+          mma16816(o[mt], a, bp0[b], bp1[b]);
         }
       }
     }
   }
 }
 
-template <int CK, int CV>
-__global__ void __launch_bounds__(kDecodeWarps * 32, 2) decode_split_kernel(const DecodeParams p) {
-  using C = DecodeCfg<CK, CV>;
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ uint64_t bars[kDecodeWarps][C::NS];
+// Position in the flattened unit space: sequence, stream within the
+// sequence (kv head * n_hg + head group), unit within the stream, and the
+// unit's index in the cache (for the bulk copy).
+struct Cursor {
+  int seq, sl, j, n_s;
+  int64_t unit;
+};
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
-  const int split = blockIdx.x;
-  const int kvh = blockIdx.y / p.n_hgroups, hg = blockIdx.y % p.n_hgroups;
-  const int seq = blockIdx.z;
+struct Geo {
+  const int32_t *pfx;
+  int n_seqs, n_kv, n_hg, KH;
+  int64_t ups;  // units per (seq, kv head) stream of the cache
+};
 
-  int len = p.seq_lens[seq];
-  if (len > p.max_len) {
-    if (threadIdx.x == 0 && split == 0 && blockIdx.y == 0) set_err(p.err, KVQ_DEVERR_MAXLEN);
-    len = p.max_len;
+__device__ __forceinline__ int64_t cache_unit(const Geo &q, int seq, int sl, int j) {
+  return (static_cast<int64_t>(seq) * q.n_kv + sl / q.n_hg) * q.ups + j;
+}
+
+// Largest s with pfx[s] * KH <= u (pfx non-decreasing, pfx[0] = 0).
+__device__ __forceinline__ int find_seq(const Geo &q, int64_t u) {
+  int lo = 0, hi = q.n_seqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (static_cast<int64_t>(q.pfx[mid]) * q.KH <= u) lo = mid;
+    else hi = mid - 1;
   }
-  const int t0 = split * p.split_tokens;
-  if (t0 >= len) return;  // whole CTA: empty split
-  const int t1 = min(len, t0 + p.split_tokens);
-  const int n_units = (t1 - t0 + kUnitTokens - 1) / kUnitTokens;
-  const int my_n = n_units > warp ? (n_units - warp + kDecodeWarps - 1) / kDecodeWarps : 0;
+  return lo;
+}
 
-  const int64_t units_per_stream = p.capacity / kUnitTokens;
-  const int64_t stream = static_cast<int64_t>(seq) * p.n_kv + kvh;
-  const int64_t u0 = stream * units_per_stream + t0 / kUnitTokens;
-  const uint8_t *kbase = p.k_cache + u0 * C::UK;
-  const uint8_t *vbase = p.v_cache + u0 * C::UV;
-  uint8_t *ring = smem + warp * C::WARP_SMEM;
-  uint64_t *wb = bars[warp];
-
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < C::NS; ++s) mbar_init(&wb[s], 1);
-    fence_mbar_init();
+__device__ __forceinline__ Cursor cursor_at(const Geo &q, int64_t u) {
+  Cursor c;
+  if (u >= static_cast<int64_t>(q.pfx[q.n_seqs]) * q.KH) {  // past the end: inert
+    c.seq = q.n_seqs;
+    c.sl = c.j = 0;
+    c.n_s = 1;
+    c.unit = 0;
+    return c;
   }
-  __syncwarp();
+  c.seq = find_seq(q, u);
+  c.n_s = q.pfx[c.seq + 1] - q.pfx[c.seq];
+  const int64_t within = u - static_cast<int64_t>(q.pfx[c.seq]) * q.KH;
+  c.sl = static_cast<int>(within / c.n_s);
+  c.j = static_cast<int>(within % c.n_s);
+  c.unit = cache_unit(q, c.seq, c.sl, c.j);
+  return c;
+}
 
-  auto issue = [&](int k) {  // lane 0 only: load unit (warp + k*WARPS) into stage k % NS
-    const int j = warp + k * kDecodeWarps;
-    const int s = k % C::NS;
-    uint8_t *dst = ring + s * C::STAGE;
-    mbar_arrive_expect_tx(&wb[s], C::STAGE);
-    bulk_copy_g2s(dst, kbase + static_cast<int64_t>(j) * C::UK, C::UK, &wb[s]);
-    bulk_copy_g2s(dst + C::UK, vbase + static_cast<int64_t>(j) * C::UV, C::UV, &wb[s]);
-  };
-  const int pre = my_n < C::NS ? my_n : C::NS;
-  if (lane == 0)
-    for (int k = 0; k < pre; ++k) issue(k);
+// Advance a cursor by `step` units (stops being meaningful past the end).
+__device__ __forceinline__ void cursor_advance(Cursor &c, int step, const Geo &q) {
+  c.j += step;
+  if (c.j < c.n_s) {
+    c.unit += step;
+    return;
+  }
+  do {
+    c.j -= c.n_s;
+    if (++c.sl == q.KH) {
+      c.sl = 0;
+      do {
+        ++c.seq;
+      } while (c.seq < q.n_seqs && q.pfx[c.seq + 1] == q.pfx[c.seq]);
+      if (c.seq >= q.n_seqs) return;
+      c.n_s = q.pfx[c.seq + 1] - q.pfx[c.seq];
+    }
+  } while (c.j >= c.n_s);
+  c.unit = cache_unit(q, c.seq, c.sl, c.j);
+}
 
-  // B fragments of Q (n = query head g of this group), with the per-codec
-  // ordering of the k (head-dim) index that matches the K unit layout.
-  const int hq = hg * 8 + g;
-  const bool hvalid = hq < p.G;
-  uint32_t qb[8][2];
-  {
-    const __half *qrow = p.q + (static_cast<int64_t>(seq) * p.n_q + kvh * p.G + (hvalid ? hq : 0)) * kD;
+// Merge partial b into a (per lane; m uniform across the lanes of a head).
+__device__ __forceinline__ void merge_into(float (&o)[8][4], float &m0, float &m1, float &l0,
+                                           float &l1, const float *r) {
+  const float bm0 = r[32], bm1 = r[33], bl0 = r[34], bl1 = r[35];
+  const float M0 = fmaxf(m0, bm0), M1 = fmaxf(m1, bm1);
+  const float sa0 = m0 == -INFINITY ? 0.0f : fast_exp2(m0 - M0);
+  const float sb0 = bm0 == -INFINITY ? 0.0f : fast_exp2(bm0 - M0);
+  const float sa1 = m1 == -INFINITY ? 0.0f : fast_exp2(m1 - M1);
+  const float sb1 = bm1 == -INFINITY ? 0.0f : fast_exp2(bm1 - M1);
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
-      uint2 v = make_uint2(0u, 0u);
-      if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
-      if (CK == KVQ_F16) {
-        qb[c][0] = v.x;
-        qb[c][1] = v.y;
-      } else {
-        qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
-        qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
-      }
+  for (int mt = 0; mt < 8; ++mt) {
+    o[mt][0] = o[mt][0] * sa0 + r[4 * mt + 0] * sb0;
+    o[mt][1] = o[mt][1] * sa1 + r[4 * mt + 1] * sb1;
+    o[mt][2] = o[mt][2] * sa0 + r[4 * mt + 2] * sb0;
+    o[mt][3] = o[mt][3] * sa1 + r[4 * mt + 3] * sb1;
+  }
+  l0 = l0 * sa0 + bl0 * sb0;
+  l1 = l1 * sa1 + bl1 * sb1;
+  m0 = M0;
+  m1 = M1;
+}
+
+__device__ __forceinline__ void store_red(float *r, const float (&o)[8][4], float m0, float m1,
+                                          float l0, float l1) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt)
+    reinterpret_cast<float4 *>(r)[mt] = make_float4(o[mt][0], o[mt][1], o[mt][2], o[mt][3]);
+  reinterpret_cast<float4 *>(r)[8] = make_float4(m0, m1, l0, l1);
+}
+
+__device__ __forceinline__ void cta_bar() {
+  asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads) : "memory");
+}
+
+// Online softmax + PV for N units at once (N = 1 or 2): one max reduction and
+// at most one rescale per call.
+template <int CK, int CV, int N>
+__device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
+                                              const int (&nvalid)[N], int lane,
+                                              const uint32_t (&qb)[8][2], float scale_log2,
+                                              int uk_bytes, float (&o)[8][4], float &m0,
+                                              float &m1, float &l0, float &l1) {
+  const int g = lane >> 2;
+  float sc[N][4];
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    unit_scores<CK>(ku[u], lane, qb, scale_log2, sc[u]);
+    if (nvalid[u] < kUnitTokens) {
+      if (g >= nvalid[u]) sc[u][0] = sc[u][1] = -INFINITY;
+      if (g + 8 >= nvalid[u]) sc[u][2] = sc[u][3] = -INFINITY;
     }
   }
-
-  float o[8][4];
+  float mx0 = fmaxf(sc[0][0], sc[0][2]), mx1 = fmaxf(sc[0][1], sc[0][3]);
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
-  bool ok = true;
-  int k_fail = my_n;
-
-  for (int k = 0; k < my_n; ++k) {
-    const int s = k % C::NS;
-    const uint32_t phase = static_cast<uint32_t>(k / C::NS) & 1u;
-    const bool got = mbar_wait_bounded(&wb[s], phase);
-    if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
-      ok = false;
-      k_fail = k;
-      if (lane == 0) set_err(p.err, KVQ_DEVERR_TIMEOUT);
-      break;
-    }
-    const uint8_t *ku = ring + s * C::STAGE;
-    const uint8_t *vu = ku + C::UK;
-    const int j = warp + k * kDecodeWarps;
-    const int nvalid = min(kUnitTokens, t1 - (t0 + j * kUnitTokens));
-
-    float sc[4];
-    unit_scores<CK>(ku, lane, qb, p.scale_log2, sc);
-    if (nvalid < kUnitTokens) {
-      if (g >= nvalid) sc[0] = sc[1] = -INFINITY;
-      if (g + 8 >= nvalid) sc[2] = sc[3] = -INFINITY;
-    }
-    float mx0 = fmaxf(sc[0], sc[2]), mx1 = fmaxf(sc[1], sc[3]);
+  for (int u = 1; u < N; ++u) {
+    mx0 = fmaxf(mx0, fmaxf(sc[u][0], sc[u][2]));
+    mx1 = fmaxf(mx1, fmaxf(sc[u][1], sc[u][3]));
+  }
 #pragma unroll
-    for (int off = 4; off < 32; off <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-    }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
-      const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
-      l0 *= a0;
-      l1 *= a1;
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  if (__any_sync(0xffffffffu, mn0 > m0 || mn1 > m1)) {
+    const float a0 = fast_exp2(m0 - mn0), a1 = fast_exp2(m1 - mn1);
+    l0 *= a0;
+    l1 *= a1;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
-      }
-      m0 = mn0;
-      m1 = mn1;
+    for (int mt = 0; mt < 8; ++mt) {
+      o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
     }
-    const float p0 = fast_exp2(sc[0] - m0), p1 = fast_exp2(sc[1] - m1);
-    const float p2 = fast_exp2(sc[2] - m0), p3 = fast_exp2(sc[3] - m1);
+    m0 = mn0;
+    m1 = mn1;
+  }
+#pragma unroll
+  for (int u = 0; u < N; ++u) {
+    const float p0 = fast_exp2(sc[u][0] - m0), p1 = fast_exp2(sc[u][1] - m1);
+    const float p2 = fast_exp2(sc[u][2] - m0), p3 = fast_exp2(sc[u][3] - m1);
     l0 += p0 + p2;
     l1 += p1 + p3;
     const uint32_t B0 = movmatrix_trans(pack_half2(p0, p1));
     const uint32_t B1 = movmatrix_trans(pack_half2(p2, p3));
-    unit_pv<CV>(vu, lane, B0, B1, nvalid, o);
-
-    __syncwarp();
-    if (lane == 0 && k + C::NS < my_n) {
-      fence_proxy_async_smem();
-      issue(k + C::NS);
-    }
+    const uint8_t *vu = ku[u] + uk_bytes;
+    if (nvalid[u] == kUnitTokens) unit_pv<CV, true>(vu, lane, B0, B1, nvalid[u], o);
+    else unit_pv<CV, false>(vu, lane, B0, B1, nvalid[u], o);
   }
-  if (!ok) {
-    // Drain copies still in flight into this warp's ring before the CTA moves on.
-    const int issued = min(my_n, k_fail + C::NS);
-    for (int k = k_fail; k < issued; ++k)
-      mbar_wait_bounded(&wb[k % C::NS], static_cast<uint32_t>(k / C::NS) & 1u);
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.0f;
-  }
-
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
-  }
-  __syncthreads();  // every warp is done with its ring: reuse it for the CTA merge
-  float *red_o = reinterpret_cast<float *>(smem);                  // [warp][8 heads][128]
-  float *red_ml = red_o + kDecodeWarps * 8 * kD;                   // [warp][8][2]
-  {
-    float *wo = red_o + warp * 8 * kD;
-    const int h0 = 2 * tig, h1 = 2 * tig + 1;
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      const int dlo = v_dim<CV>(mt, g), dhi = v_dim<CV>(mt, g + 8);
-      wo[h0 * kD + dlo] = ok ? o[mt][0] : 0.0f;
-      wo[h1 * kD + dlo] = ok ? o[mt][1] : 0.0f;
-      wo[h0 * kD + dhi] = ok ? o[mt][2] : 0.0f;
-      wo[h1 * kD + dhi] = ok ? o[mt][3] : 0.0f;
-    }
-    if (g == 0) {
-      red_ml[(warp * 8 + h0) * 2 + 0] = m0;
-      red_ml[(warp * 8 + h0) * 2 + 1] = l0;
-      red_ml[(warp * 8 + h1) * 2 + 0] = m1;
-      red_ml[(warp * 8 + h1) * 2 + 1] = l1;
-    }
-  }
-  __syncthreads();
-  const int heads_here = min(8, p.G - hg * 8);
-  for (int idx = threadIdx.x; idx < heads_here * kD; idx += kDecodeWarps * 32) {
-    const int hh = idx / kD, d = idx % kD;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) M = fmaxf(M, red_ml[(w * 8 + hh) * 2]);
-    float acc = 0.0f, L = 0.0f;
-#pragma unroll
-    for (int w = 0; w < kDecodeWarps; ++w) {
-      const float mw = red_ml[(w * 8 + hh) * 2];
-      const float sw = mw == -INFINITY ? 0.0f : fast_exp2(mw - M);
-      acc = fmaf(sw, red_o[(w * 8 + hh) * kD + d], acc);
-      L = fmaf(sw, red_ml[(w * 8 + hh) * 2 + 1], L);
-    }
-    const int head = kvh * p.G + hg * 8 + hh;
-    const int64_t slot = (static_cast<int64_t>(seq) * p.n_q + head) * p.n_splits + split;
-    p.part_o[slot * kD + d] = acc;
-    if (d == 0) p.part_ml[slot] = make_float2(M, L);
-  }
-}
-
-struct MergeParams {
-  const float *part_o;
-  const float2 *part_ml;
-  const int32_t *seq_lens;
-  __half *out;
-  float *lse;
-  int n_seqs, n_q, max_len, split_tokens, n_splits;
-};
-
-// One warp per (sequence, query head): log-sum-exp merge of the split partials.
-__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int row = blockIdx.x * 4 + warp;
-  if (row >= p.n_seqs * p.n_q) return;
-  const int seq = row / p.n_q;
-  int len = p.seq_lens[seq];
-  len = len < p.max_len ? len : p.max_len;
-  int nv = len > 0 ? (len + p.split_tokens - 1) / p.split_tokens : 0;
-  nv = nv < p.n_splits ? nv : p.n_splits;
-  const float2 *ml = p.part_ml + static_cast<int64_t>(row) * p.n_splits;
-  const float *po = p.part_o + static_cast<int64_t>(row) * p.n_splits * kD;
-  float M = -INFINITY;
-  for (int i = lane; i < nv; i += 32) M = fmaxf(M, ml[i].x);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-  float L = 0.0f;
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (M != -INFINITY) {
-    for (int i = 0; i < nv; ++i) {
-      const float2 v = ml[i];
-      const float w = v.x == -INFINITY ? 0.0f : fast_exp2(v.x - M);
-      const float4 x = reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * kD)[lane];
-      L = fmaf(w, v.y, L);
-      acc.x = fmaf(w, x.x, acc.x);
-      acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z);
-      acc.w = fmaf(w, x.w, acc.w);
-    }
-  }
-  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  __half2 *dst = reinterpret_cast<__half2 *>(p.out + static_cast<int64_t>(row) * kD) + lane * 2;
-  dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-  dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
-  if (p.lse && lane == 0) p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 template <int CK, int CV>
-cudaError_t launch_split(const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+__global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeParams p) {
+  using C = DecodeCfg<CK, CV>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ uint64_t full[C::NS];
+  __shared__ int32_t pfx[kMaxSeqs + 1];
+  __shared__ int abort_flag;
+  __shared__ int last_flag;
+  __shared__ int8_t pend[C::NS];  // 0: idle, 1 + parity: a copy of that phase is in flight
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tig = lane & 3;
+
+  // The previous kernel on the stream (the append) must be complete before
+  // the lengths and the cache are read.
+  grid_dependency_wait();
+
+  // Units per stream of each sequence, prefix-summed (one warp).
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < p.n_seqs; base += 32) {
+      const int s = base + lane;
+      int n = 0;
+      if (s < p.n_seqs) {
+        int len = p.seq_lens[s];
+        if (len > p.max_len) {
+          if (blockIdx.x == 0) set_err(p.err, KVQ_DEVERR_MAXLEN);
+          len = p.max_len;
+        }
+        n = len > 0 ? (len + kUnitTokens - 1) / kUnitTokens : 0;
+      }
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      if (s < p.n_seqs) pfx[s + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      pfx[0] = 0;
+      abort_flag = 0;
+    }
+    for (int s = lane; s < C::NS; s += 32) {
+      mbar_init(&full[s], 1);
+      pend[s] = 0;
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_launch_dependents();
+
+  // Sequences with no keys get no unit, hence no partial: CTA 0 writes their
+  // rows (out = 0, lse = -inf).
+  if (blockIdx.x == 0) {
+    for (int row = warp; row < p.n_seqs * p.n_q; row += kWarps) {
+      const int s = row / p.n_q;
+      if (pfx[s + 1] != pfx[s]) continue;
+      reinterpret_cast<uint2 *>(p.out + static_cast<int64_t>(row) * kD)[lane] = make_uint2(0u, 0u);
+      if (p.lse && lane == 0) p.lse[row] = -INFINITY;
+    }
+  }
+
+  Geo geo;
+  geo.pfx = pfx;
+  geo.n_seqs = p.n_seqs;
+  geo.n_kv = p.n_kv;
+  geo.n_hg = p.n_hg;
+  geo.KH = p.n_kv * p.n_hg;
+  geo.ups = p.capacity / kUnitTokens;
+  const int64_t U = static_cast<int64_t>(pfx[p.n_seqs]) * geo.KH;
+  const int P = gridDim.x;
+  const int64_t u0 = U * blockIdx.x / P;
+  const int64_t u1 = U * (blockIdx.x + 1) / P;
+  const int R = static_cast<int>(u1 - u0);
+  if (R <= 0) return;  // whole CTA: nothing to do
+
+  uint8_t *ring = smem;
+  float *red = reinterpret_cast<float *>(smem + C::RING);
+
+  // Issue unit k of this CTA's slice into stage k % NS (lane 0 of its owner).
+  auto issue = [&](int k, const Cursor &c) {
+    const int s = k % C::NS;
+    uint8_t *dst = ring + s * C::STAGE;
+    pend[s] = static_cast<int8_t>(1 + ((k / C::NS) & 1));
+    mbar_arrive_expect_tx(&full[s], C::STAGE);
+    bulk_copy_g2s(dst, p.k_cache + c.unit * C::UK, C::UK, &full[s]);
+    bulk_copy_g2s(dst + C::UK, p.v_cache + c.unit * C::UV, C::UV, &full[s]);
+  };
+
+  // Prologue: each warp issues its own first stages (k = warp, warp + 8, ...
+  // below NS).  Afterwards the producer cursor pc sits at unit k + NS for the
+  // warp's next unit k.
+  Cursor pc = cursor_at(geo, u0 + warp);
+  if (lane == 0) {
+    Cursor c = pc;
+    for (int k = warp; k < C::NS && k < R; k += kWarps) {
+      issue(k, c);
+      cursor_advance(c, kWarps, geo);
+    }
+  }
+  cursor_advance(pc, C::NS, geo);
+
+  // Walk the segments (stream pieces) of this slice.
+  Cursor seg = cursor_at(geo, u0);
+  int64_t useg = u0;
+  int k_next = warp;  // next unit index (CTA-local) this warp consumes
+  bool ok = true;
+  while (useg < u1) {
+    const int64_t seg_end = min(u1, useg + (seg.n_s - seg.j));
+    const int k0 = static_cast<int>(useg - u0), k1 = static_cast<int>(seg_end - u0);
+    const int seq = seg.seq, kvh = seg.sl / p.n_hg, hg = seg.sl % p.n_hg;
+    int len = p.seq_lens[seq];
+    len = len < p.max_len ? len : p.max_len;
+
+    // B fragments of Q (n = query head g of this group), with the per-codec
+    // order of the k (head-dim) index matching the K unit layout.
+    const int hq = hg * 8 + g;
+    const bool hvalid = hq < p.G;
+    uint32_t qb[8][2];
+    {
+      const __half *qrow =
+          p.q + (static_cast<int64_t>(seq) * p.n_q + kvh * p.G + (hvalid ? hq : 0)) * kD;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+        uint2 v = make_uint2(0u, 0u);
+        if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
+        if (CK == KVQ_F16) {
+          qb[c][0] = v.x;
+          qb[c][1] = v.y;
+        } else {
+          qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+          qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+        }
+      }
+    }
+
+    float o[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+    while (k_next < k1) {
+      const int k = k_next;
+      const bool two = C::PAIR && k + kWarps < k1;
+      const int s0 = k % C::NS;
+      const int s1 = (k + kWarps) % C::NS;
+      bool got = ok && mbar_wait_bounded(&full[s0], static_cast<uint32_t>(k / C::NS) & 1u,
+                                         &abort_flag);
+      if (two)
+        got = got && mbar_wait_bounded(&full[s1],
+                                       static_cast<uint32_t>((k + kWarps) / C::NS) & 1u,
+                                       &abort_flag);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        if (ok && lane == 0) {
+          set_err(p.err, KVQ_DEVERR_TIMEOUT);
+          atomicExch(&abort_flag, 1);
+        }
+        ok = false;
+        k_next += two ? 2 * kWarps : kWarps;
+        continue;
+      }
+      const int j = seg.j + (k - k0);
+      if (two) {
+        if (lane == 0) pend[s0] = pend[s1] = 0;
+        const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
+        const int nv[2] = {min(kUnitTokens, len - j * kUnitTokens),
+                           min(kUnitTokens, len - (j + kWarps) * kUnitTokens)};
+        process_units<CK, CV, 2>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
+      } else {
+        if (lane == 0) pend[s0] = 0;
+        const uint8_t *ku[1] = {ring + s0 * C::STAGE};
+        const int nv[1] = {min(kUnitTokens, len - j * kUnitTokens)};
+        process_units<CK, CV, 1>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
+      }
+      // The consumed stages are free: refill them with units k + NS (+ 8).
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        if (k + C::NS < R) issue(k + C::NS, pc);
+      }
+      cursor_advance(pc, kWarps, geo);
+      if (two) {
+        if (lane == 0 && k + kWarps + C::NS < R) issue(k + kWarps + C::NS, pc);
+        cursor_advance(pc, kWarps, geo);
+      }
+      k_next += two ? 2 * kWarps : kWarps;
+    }
+
+    // Merge the 8 warps' partials for this segment: 8 -> 4 in pairs, then
+    // warp 0 takes in warps 1..3.  Four shared slots, three barriers.
+    float *rs = red + lane * kRedFloats;
+    if (warp >= 4) store_red(rs + (warp - 4) * 32 * kRedFloats, o, m0, m1, l0, l1);
+    cta_bar();
+    if (warp < 4) merge_into(o, m0, m1, l0, l1, rs + warp * 32 * kRedFloats);
+    if (warp >= 1 && warp < 4) store_red(rs + warp * 32 * kRedFloats, o, m0, m1, l0, l1);
+    cta_bar();
+    const int stream = seq * geo.KH + seg.sl;
+    // CTAs whose slices overlap this stream: c_first..c_last; the owner of
+    // unit u is floor(((u + 1) * P - 1) / U).
+    const int64_t S = static_cast<int64_t>(pfx[seq]) * geo.KH + static_cast<int64_t>(seg.sl) * seg.n_s;
+    const int c_first = static_cast<int>(((S + 1) * P - 1) / U);
+    const int c_last = static_cast<int>(((S + seg.n_s) * P - 1) / U);
+    if (warp == 0) {
+#pragma unroll 1
+      for (int w = 1; w < 4; ++w) merge_into(o, m0, m1, l0, l1, rs + w * 32 * kRedFloats);
+#pragma unroll
+      for (int off = 4; off < 32; off <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      }
+      const int64_t slot = static_cast<int64_t>(blockIdx.x) + stream;
+      float *po = p.part_o + slot * 8 * kD;
+      const int h0 = 2 * tig, h1 = 2 * tig + 1;
+      const bool v0 = hg * 8 + h0 < p.G, v1 = hg * 8 + h1 < p.G;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int dlo = v_dim<CV>(mt, g), dhi = v_dim<CV>(mt, g + 8);
+        if (v0) { po[h0 * kD + dlo] = o[mt][0]; po[h0 * kD + dhi] = o[mt][2]; }
+        if (v1) { po[h1 * kD + dlo] = o[mt][1]; po[h1 * kD + dhi] = o[mt][3]; }
+      }
+      if (g == 0) {
+        if (v0) p.part_ml[slot * 8 + h0] = make_float2(ok ? m0 : -INFINITY, ok ? l0 : 0.0f);
+        if (v1) p.part_ml[slot * 8 + h1] = make_float2(ok ? m1 : -INFINITY, ok ? l1 : 0.0f);
+      }
+      // Ticket: the last of the stream's CTAs to get here merges its partials.
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        // Every CTA in c_first..c_last wrote a partial, except (when the grid
+        // is larger than the unit count) CTAs whose slice is empty.
+        unsigned n_parts = static_cast<unsigned>(c_last - c_first + 1);
+        if (U < P)
+          for (int c = c_first; c <= c_last; ++c)
+            if (U * (c + 1) / P == U * c / P) --n_parts;
+        const unsigned old = atomicInc(reinterpret_cast<unsigned *>(p.tickets) + stream,
+                                       n_parts - 1);
+        last_flag = (old == n_parts - 1) ? 1 : 0;
+      }
+    }
+    cta_bar();  // slots free again; last_flag visible
+    if (last_flag) {
+      __threadfence();
+      // Merge the stream's partials: warp h takes head h.  Lane c loads the
+      // (max, sum) of parts c, c+32, ... and computes their weights, so the
+      // accumulation loop only streams the independent output rows.
+      const int heads_here = min(8, p.G - hg * 8);
+      const bool sparse = U < P;  // some CTAs in the span may hold no partial
+      for (int h = warp; h < heads_here; h += kWarps) {
+        float M = -INFINITY;
+        for (int c = c_first + lane; c <= c_last; c += 32)
+          if (!sparse || U * (c + 1) / P != U * c / P)
+            M = fmaxf(M, __ldcg(&p.part_ml[(static_cast<int64_t>(c) + stream) * 8 + h].x));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.0f;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (M != -INFINITY) {
+          for (int cb = c_first; cb <= c_last; cb += 32) {
+            const int c = cb + lane;
+            float wgt = 0.0f;
+            if (c <= c_last && (!sparse || U * (c + 1) / P != U * c / P)) {
+              const float2 ml = __ldcg(&p.part_ml[(static_cast<int64_t>(c) + stream) * 8 + h]);
+              wgt = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - M);
+              L = fmaf(wgt, ml.y, L);
+            }
+            const int n = min(32, c_last - cb + 1);
+            const float *po = p.part_o + ((static_cast<int64_t>(cb) + stream) * 8 + h) * kD + 4 * lane;
+#pragma unroll 8
+            for (int i = 0; i < n; ++i) {
+              const float wi = __shfl_sync(0xffffffffu, wgt, i);
+              if (wi != 0.0f) {
+                const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * 8 * kD));
+                acc.x = fmaf(wi, x.x, acc.x);
+                acc.y = fmaf(wi, x.y, acc.y);
+                acc.z = fmaf(wi, x.z, acc.z);
+                acc.w = fmaf(wi, x.w, acc.w);
+              }
+            }
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
+        __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
+        dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+        dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+        if (p.lse && lane == 0)
+          p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+
+    useg = seg_end;
+    if (useg < u1) seg = cursor_at(geo, useg);
+  }
+
+  // After an aborted run, wait (bounded) for copies still in flight into the ring.
+  __syncthreads();
+  if (abort_flag && lane == 0) {
+    for (int s = warp; s < C::NS; s += kWarps)
+      if (pend[s]) mbar_wait_bounded(&full[s], static_cast<uint32_t>(pend[s] - 1), nullptr, 100000000ull);
+  }
+}
+
+template <int CK, int CV>
+cudaError_t launch_split(const DecodeParams &p, int grid, cudaStream_t stream) {
   using C = DecodeCfg<CK, CV>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -422,12 +687,11 @@ cudaError_t launch_split(const DecodeParams &p, dim3 grid, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_split_kernel<CK, CV><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_split_kernel<CK, CV>, dim3(grid), dim3(kThreads), C::SMEM, stream, p);
 }
 
 template <int CK>
-cudaError_t launch_split_v(int cv, const DecodeParams &p, dim3 grid, cudaStream_t stream) {
+cudaError_t launch_split_v(int cv, const DecodeParams &p, int grid, cudaStream_t stream) {
   switch (cv) {
     case KVQ_F16: return launch_split<CK, KVQ_F16>(p, grid, stream);
     case KVQ_Q8_0: return launch_split<CK, KVQ_Q8_0>(p, grid, stream);
@@ -442,65 +706,50 @@ DecodePlan plan_decode(const kvq_layer &L, int max_len, int num_sms) {
   const int G = L.n_q_heads / L.n_kv_heads;
   pl.n_hgroups = (G + 7) / 8;
   const int64_t streams = static_cast<int64_t>(L.n_seqs) * L.n_kv_heads * pl.n_hgroups;
-  const int64_t max_units = (max_len + kUnitTokens - 1) / kUnitTokens;
-  // Aim at ~4 waves of two resident CTAs per SM; at least two units per warp.
-  const int64_t target = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 2 * 4;
-  int64_t split_units = (streams * max_units + target - 1) / target;
-  const int64_t min_units = 2 * kDecodeWarps;
-  if (split_units < min_units) split_units = min_units;
-  if (split_units > max_units) split_units = max_units > 0 ? max_units : 1;
-  pl.split_tokens = static_cast<int>(split_units * kUnitTokens);
-  pl.n_splits = static_cast<int>((max_len + pl.split_tokens - 1) / pl.split_tokens);
-  if (pl.n_splits < 1) pl.n_splits = 1;
-  const int64_t slots = static_cast<int64_t>(L.n_seqs) * L.n_q_heads * pl.n_splits;
-  pl.ws_o_bytes = slots * kD * sizeof(float);
-  pl.ws_bytes = pl.ws_o_bytes + slots * sizeof(float2);
+  const int64_t max_units = streams * ((max_len + kUnitTokens - 1) / kUnitTokens);
+  // Two resident CTAs per SM, but at least ~32 units (two pairs per warp) per
+  // CTA, so that short contexts do not spread into many tiny partials.
+  int64_t grid = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 2;
+  const int64_t by_work = (max_units + 31) / 32;
+  if (grid > by_work) grid = by_work;
+  if (grid < 1) grid = 1;
+  pl.grid = static_cast<int>(grid);
+  pl.slots = grid + streams;
+  pl.ticket_bytes = kDecodeTicketBytes;  // fixed region: never overlaps another plan's partials
+  pl.ml_bytes = pl.slots * 8 * 8;
+  pl.o_bytes = pl.slots * 8 * kD * 4;
+  pl.ws_bytes = pl.ticket_bytes + pl.ml_bytes + pl.o_bytes;
   return pl;
 }
 
 cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *q, float scale,
                           void *out, float *lse, int max_len, void *workspace,
                           cudaStream_t stream) {
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
   DecodeParams p;
   p.k_cache = static_cast<const uint8_t *>(L.k_cache);
   p.v_cache = static_cast<const uint8_t *>(L.v_cache);
   p.seq_lens = L.seq_lens;
   p.q = static_cast<const __half *>(q);
-  p.part_o = static_cast<float *>(workspace);
-  p.part_ml = reinterpret_cast<float2 *>(static_cast<uint8_t *>(workspace) + pl.ws_o_bytes);
+  p.tickets = reinterpret_cast<int32_t *>(ws);
+  p.part_ml = reinterpret_cast<float2 *>(ws + pl.ticket_bytes);
+  p.part_o = reinterpret_cast<float *>(ws + pl.ticket_bytes + pl.ml_bytes);
+  p.out = static_cast<__half *>(out);
+  p.lse = lse;
   p.err = L.err;
   p.n_seqs = L.n_seqs;
   p.n_kv = L.n_kv_heads;
   p.n_q = L.n_q_heads;
   p.G = L.n_q_heads / L.n_kv_heads;
-  p.n_hgroups = pl.n_hgroups;
+  p.n_hg = pl.n_hgroups;
   p.capacity = L.capacity;
   p.max_len = max_len;
-  p.split_tokens = pl.split_tokens;
-  p.n_splits = pl.n_splits;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const dim3 grid(pl.n_splits, L.n_kv_heads * pl.n_hgroups, L.n_seqs);
-  cudaError_t e;
   switch (L.codec_k) {
-    case KVQ_F16: e = launch_split_v<KVQ_F16>(L.codec_v, p, grid, stream); break;
-    case KVQ_Q8_0: e = launch_split_v<KVQ_Q8_0>(L.codec_v, p, grid, stream); break;
-    default: e = launch_split_v<KVQ_Q4_0>(L.codec_v, p, grid, stream); break;
+    case KVQ_F16: return launch_split_v<KVQ_F16>(L.codec_v, p, pl.grid, stream);
+    case KVQ_Q8_0: return launch_split_v<KVQ_Q8_0>(L.codec_v, p, pl.grid, stream);
+    default: return launch_split_v<KVQ_Q4_0>(L.codec_v, p, pl.grid, stream);
   }
-  if (e != cudaSuccess) return e;
-  MergeParams mp;
-  mp.part_o = p.part_o;
-  mp.part_ml = p.part_ml;
-  mp.seq_lens = L.seq_lens;
-  mp.out = static_cast<__half *>(out);
-  mp.lse = lse;
-  mp.n_seqs = L.n_seqs;
-  mp.n_q = L.n_q_heads;
-  mp.max_len = max_len;
-  mp.split_tokens = pl.split_tokens;
-  mp.n_splits = pl.n_splits;
-  const int rows = L.n_seqs * L.n_q_heads;
-  decode_merge_kernel<<<(rows + 3) / 4, 128, 0, stream>>>(mp);
-  return cudaGetLastError();
 }
 
 }  // namespace kvq

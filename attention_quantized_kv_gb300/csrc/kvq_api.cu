@@ -90,9 +90,17 @@ int kv_append_quantize(const kvq_layer *layer, const void *k_new, const void *v_
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
+// Decode streams: (sequence, kv head, group of up to 8 query heads).
+static bool decode_shape_ok(const kvq_layer *L) {
+  const int64_t G = L->n_q_heads / L->n_kv_heads;
+  const int64_t streams = static_cast<int64_t>(L->n_seqs) * L->n_kv_heads * ((G + 7) / 8);
+  return L->n_seqs <= kvq::kDecodeMaxSeqs && streams <= kvq::kDecodeMaxStreams;
+}
+
 int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes) {
   int st = check_layer(layer);
   if (st != KVQ_OK) return st;
+  if (!decode_shape_ok(layer)) return KVQ_EINVAL;
   if (!bytes || max_len <= 0) return KVQ_EINVAL;
   if (max_len > layer->capacity) return KVQ_ECAPACITY;
   const int sms = device_sms();
@@ -106,6 +114,7 @@ int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, f
   int st = check_layer(layer);
   if (st != KVQ_OK) return st;
   if (!q || !out || max_len <= 0) return KVQ_EINVAL;
+  if (!decode_shape_ok(layer)) return KVQ_EINVAL;
   if (max_len > layer->capacity) return KVQ_ECAPACITY;
   if (!aligned(q, 8) || !aligned(out, 8) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;
   if (!workspace) return KVQ_EWORKSPACE;

@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/kvq.h"
@@ -76,10 +77,19 @@ __device__ __forceinline__ uint32_t s8_pair_02(uint32_t w) {
 __device__ __forceinline__ uint32_t s8_pair_13(uint32_t w) {
   return hsub2_bits(lop3_and_xor(w >> 8, 0x00ff00ffu, 0x64806480u), 0x64806480u);
 }
-// Nibbles at bit 4k and 16+4k of (w) as the exact fp16 pair (n - 8):
+// Nibbles at bits 0..3 and 16..19 of w as the exact fp16 pair (n - 8):
 // the nibble lands in the mantissa of 1024; subtracting 1032 leaves n - 8.
 __device__ __forceinline__ uint32_t u4_pair_minus8(uint32_t w) {
   return hsub2_bits(lop3_and_or(w, 0x000f000fu, 0x64006400u), 0x64086408u);
+}
+// Nibbles at bits 4..7 and 20..23 of w as the exact fp16 pair (n - 8),
+// without a shift: masked in place they give 1024 + 16 n, and one fused
+// multiply-add by 1/16 and -72 leaves n - 8 (every step exact in fp16).
+__device__ __forceinline__ uint32_t u4_pair_minus8_hi(uint32_t w) {
+  const uint32_t x = lop3_and_or(w, 0x00f000f0u, 0x64006400u);
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(r) : "r"(x), "r"(0x2c002c00u), "r"(0xd480d480u));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -145,14 +155,19 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Wait for the given phase of an mbarrier, giving up after ~limit_ns.
+// Wait for the given phase of an mbarrier, giving up after ~limit_ns or as
+// soon as *abort (a shared flag, optional) becomes non-zero.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase,
+                                                  const int *abort = nullptr,
                                                   uint64_t limit_ns = 1000000000ull) {
   if (mbar_try_wait(bar, phase)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, phase)) return true;
-    if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) return false;
+    if ((it & 63u) == 63u) {
+      if (abort && *reinterpret_cast<const volatile int *>(abort)) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
   }
 }
 
@@ -163,6 +178,34 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
 
 __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
   if (err) atomicOr(err, bit);
+}
+
+// Programmatic dependent launch: wait for the previous grid on the stream to
+// complete (and its writes to be visible), and let the next grid launch early.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream drains; it must call
+// grid_dependency_wait() before touching that kernel's results.
+template <typename Kernel, typename Params>
+inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, const Params &params) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, params);
 }
 
 }  // namespace kvq

@@ -13,11 +13,17 @@ cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_n
                           const int32_t *n_new, int max_new, int update_lens,
                           cudaStream_t stream);
 
+constexpr int kDecodeMaxSeqs = 1024;         // sequences per attn_decode call
+constexpr int kDecodeTicketBytes = 64 * 1024;  // per-stream counters at the workspace start
+constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4;
+
 struct DecodePlan {
-  int n_hgroups = 1;     // groups of up to 8 query heads per kv head
-  int split_tokens = 0;  // tokens per split (multiple of 16)
-  int n_splits = 1;      // splits per stream
-  int64_t ws_o_bytes = 0;
+  int n_hgroups = 1;      // groups of up to 8 query heads per kv head
+  int grid = 1;           // CTAs, each an equal slice of the (stream, unit) space
+  int64_t slots = 0;      // partial slots: grid + streams
+  int64_t ticket_bytes = 0;  // workspace: per-stream arrival counters (zero between calls)
+  int64_t ml_bytes = 0;   //            (max, sum) per slot and head
+  int64_t o_bytes = 0;    //            unnormalised output per slot and head
   int64_t ws_bytes = 0;
 };
 

@@ -155,6 +155,13 @@ KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_
 
 /* Decode attention: every query head of every sequence attends all
  * seq_lens[s] cached keys (split-K over the token axis, log-sum-exp merge).
+ * The first 64 KiB of the workspace hold per-stream arrival counters that
+ * must be zero before the first call (zero-fill the workspace once after
+ * allocating it); every call that completes without KVQ_DEVERR_TIMEOUT
+ * leaves them zero again, so one workspace serves any number of calls and
+ * layers without clearing.  Calls that may run concurrently need separate
+ * workspaces.  Limits: 1024 sequences and 16384 streams (sequence x kv head
+ * x group of 8 query heads) per call, else KVQ_EINVAL.
  * q: fp16 [n_seqs][n_q_heads][128] (8-byte aligned); out: fp16
  * [n_seqs][n_q_heads][128]; lse: optional fp32 [n_seqs][n_q_heads] natural-log
  * sum-exp of the scaled scores (NULL to skip).  max_len bounds every

@@ -28,7 +28,7 @@ def _built():
 def run_decode(L, q, max_len, scale):
     out = torch.empty_like(q)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=q.device)
-    ws = torch.empty(kvq.attn_decode_workspace(L, max_len), dtype=torch.uint8, device=q.device)
+    ws = torch.zeros(kvq.attn_decode_workspace(L, max_len), dtype=torch.uint8, device=q.device)
     kvq.attn_decode(L, q, scale, out, lse, max_len, ws)
     torch.cuda.synchronize()
     return out, lse
@@ -118,3 +118,30 @@ def test_decode_is_repeatable_and_lse_consistent():
     o1, l1 = run_decode(L, q, 4096, 0.1)
     o2, l2 = run_decode(L, q, 4096, 0.1)
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_workspace_reused_across_calls_and_geometries():
+    """The ticket counters return to zero: one zeroed workspace serves many
+    calls of different shapes, including grids larger than the unit count."""
+    cases = [wl.Workload("a", "decode", 3, 8, 2, [5000, 17, 300], [(2, 1)], 40),
+             wl.Workload("b", "decode", 1, 4, 4, [20], [(1, 1)], 41),
+             wl.Workload("c", "decode", 7, 16, 2, [1, 2, 3, 40, 0, 700, 16], [(0, 2)], 42),
+             wl.Workload("d", "decode", 2, 4, 2, [3, 1], [(2, 0)], 43)]
+    # case d: max_len far above the lengths, so the grid exceeds the unit count
+    max_lens = [max(w.lens) for w in cases[:3]] + [cases[3].capacity]
+    big = max(kvq.attn_decode_workspace(gpu_layer(w, 0), ml) for w, ml in zip(cases, max_lens))
+    ws = torch.zeros(big, dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        for w, ml in zip(cases, max_lens):
+            L = gpu_layer(w, 0)
+            q = wl.queries(w, 0, 1, "cuda")[:, 0].contiguous()
+            out = torch.empty_like(q)
+            lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+            kvq.attn_decode(L, q, 0.1, out, lse, ml, ws)
+            torch.cuda.synchronize()
+            groups = [(s, h) for s in range(w.n_seqs) for h in range(w.n_kv) if w.lens[s] > 0]
+            check_against_oracle(w, 0, L, q, out, lse, 0.1, groups=groups)
+            for s in range(w.n_seqs):
+                if w.lens[s] == 0:
+                    assert torch.all(out[s] == 0) and torch.all(torch.isneginf(lse[s]))
+    assert torch.count_nonzero(ws[:64]) == 0     # tickets back to zero
