@@ -1,23 +1,583 @@
-// prefill.cu -- causal attention of one prefill chunk (placeholder until the
-// tensor-core kernel lands: the entry point reports "unsupported").
+// prefill.cu -- causal attention of one prefill chunk (ubatch) on the
+// 5th-generation tensor cores.
+//
+// The chunk's queries attend every earlier key of the sequence plus the
+// chunk's own keys up to their position (the ubatch prefill described in the
+// serverAppConfigs commit log: the prompt is processed in ubatches whose
+// buffers are sized by the ubatch alone; the chunk's K/V are quantize-appended
+// first, then attended in their quantized form).
+//
+// Two kernels:
+//  1. dequant_tiles: the attended keys of both sides, dequantized (x^ = d * q,
+//     rounded once to fp16; f16 is copied), written to the workspace as
+//     128-key tiles already in the tensor core's shared-memory operand layout
+//     (two 64-dim halves of 128 rows x 128 bytes, 128-byte swizzle), so that
+//     the attention kernel moves each tile with one 32 KB bulk async copy.
+//     Each key is dequantized once per chunk, not once per query block.
+//  2. prefill_attn: one CTA per (128-query block, query head).  Warp 0 streams
+//     K and V tiles into a two-stage ring (bulk copies, mbarriers).  One
+//     thread of warp 1 issues tcgen05.mma: S = Q K^T (M=128 queries, N=128
+//     keys, K=128 dims, fp16 in, fp32 accumulate) into one of two TMEM
+//     buffers, then O += P V with P (fp16) read from TMEM and O accumulated
+//     in TMEM.  Warps 4..7 (a warpgroup, one query row per thread) run the
+//     online softmax in the log2 domain: tcgen05.ld of the S row, causal
+//     mask, row max, exp2, row sum, tcgen05.st of P over the S columns.  The
+//     running max used for P is only raised (and O, l rescaled) when a row's
+//     max grows by more than 2^8, which keeps O rescales rare and the result
+//     exact (the same max scales O and l).
 #include <cuda_runtime.h>
 
+#include <math.h>
+
+#include "kvq_device.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
+namespace {
+
+constexpr int kBM = 128;                       // query rows per CTA
+constexpr int kBN = 128;                       // keys per tile
+constexpr int kTileBytes = kBN * kD * 2;       // 32 KB: one side of one tile
+constexpr int kHalfBytes = kTileBytes / 2;     // one 64-dim half
+constexpr int kStages = 2;
+constexpr int kThreads = 256;
+constexpr int kSoftmaxWarp0 = 4;
+constexpr float kRescaleThreshold = 8.0f;      // log2 units
+
+// ------------------------------------------------------------------ tcgen05 helpers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                   smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+// Shared-memory matrix descriptor: 128-byte swizzle, given leading/stride
+// byte offsets.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+// Instruction descriptor, kind::f16: fp16 A and B, fp32 D, M = 128, N = 128.
+__host__ __device__ constexpr uint32_t idesc_f16(int b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) |
+         (static_cast<uint32_t>(b_mn_major) << 16) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// 32 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+// 16 consecutive TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
+  uint32_t a[16], b[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) { a[i] = __float_as_uint(v[i]); b[i] = __float_as_uint(v[16 + i]); }
+  tmem_st16(taddr, a);
+  tmem_st16(taddr + 16, b);
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// Byte offset of element (row, dim) inside a 128-row tile in the operand
+// layout: two 64-dim halves of 128 rows x 128 bytes; inside a half the 16-byte
+// chunk index is XOR-ed with (row % 8) (128-byte swizzle).
+__host__ __device__ __forceinline__ int tile_offset(int row, int dim) {
+  return (dim >> 6) * kHalfBytes + row * 128 + ((((dim & 63) >> 3) ^ (row & 7)) << 4) +
+         (dim & 7) * 2;
+}
+
+// ------------------------------------------------------------------ dequant pre-pass
+
+// Dequantized value of (token row r of a unit, dim d), per the cache layout.
+template <int SIDE>
+__device__ __forceinline__ float load_value(int codec, const uint8_t *unit, int r, int d) {
+  const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
+  if (codec == KVQ_F16) {
+    int off;
+    if (SIDE == 0) {
+      const int b = d >> 5, h = (d >> 4) & 1, w = (d >> 2) & 3, i = d & 3;
+      off = (2 * b + rh) * 512 + (4 * g + w) * 16 + h * 8 + i * 2;
+    } else {
+      const int mt = d >> 4, gq = (d & 15) >> 1, s = d & 1;
+      off = mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + s * 2 + par) * 2;
+    }
+    return __half2float(*reinterpret_cast<const __half *>(unit + off));
+  }
+  const int b = d >> 5, e = d & 31;
+  int qoff, soff;
+  float q;
+  if (codec == KVQ_Q8_0) {
+    if (SIDE == 0) {
+      qoff = b * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (2 * rh + (e >> 4)) * 4 + (e & 3);
+      soff = 2048 + g * 16 + rh * 8 + b * 2;
+    } else {
+      const int mt = d >> 4, gq = (d & 15) >> 1, s = d & 1;
+      qoff = (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2 + s;
+      soff = 2048 + tig * 32 + b * 8 + rh * 4 + par * 2;
+    }
+    q = static_cast<float>(static_cast<int8_t>(unit[qoff]));
+  } else {
+    const int jc = e & 15, hi = e >> 4;  // canonical byte jc holds dims jc (low) and jc+16 (high)
+    if (SIDE == 0) {
+      qoff = (b >> 1) * 512 + (4 * g + (jc >> 2)) * 16 + ((b & 1) * 2 + rh) * 4 + (jc & 3);
+      soff = 1024 + g * 16 + rh * 8 + b * 2;
+    } else {
+      const int mt = 2 * b + (jc >> 3), gq = jc & 7;
+      qoff = (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
+      soff = 1024 + tig * 32 + b * 8 + rh * 4 + par * 2;
+    }
+    const int nib = (unit[qoff] >> (4 * hi)) & 0xf;
+    q = static_cast<float>(nib - 8);
+  }
+  const float dsc = __half2float(*reinterpret_cast<const __half *>(unit + soff));
+  return dsc * q;  // exact in fp32
+}
+
+struct DequantParams {
+  const uint8_t *cache[2];
+  int codec[2];
+  uint8_t *tiles[2];   // [n_kv][n_tiles][32 KB]
+  const int32_t *seq_lens;
+  int32_t *err;
+  int seq, n_kv, capacity, kv_len, n_tiles;
+};
+
+// grid: (n_tiles, n_kv, 2 sides); 256 threads; thread = (key row, 64-dim half).
+__global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams p) {
+  grid_dependency_wait();
+  const int tile = blockIdx.x, kvh = blockIdx.y, side = blockIdx.z;
+  if (tile == 0 && kvh == 0 && side == 0 && threadIdx.x == 0 &&
+      p.seq_lens[p.seq] < p.kv_len)
+    set_err(p.err, KVQ_DEVERR_SEQLEN);
+  const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
+  const int key = tile * kBN + row;
+  const int codec = p.codec[side];
+  uint8_t *dst = p.tiles[side] + (static_cast<int64_t>(kvh) * p.n_tiles + tile) * kTileBytes;
+  const int64_t units = p.capacity / kUnitTokens;
+  const uint8_t *unit = p.cache[side] +
+                        ((static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + key / kUnitTokens) *
+                            unit_bytes(codec);
+  const bool valid = key < p.kv_len;
+  const int r = key % kUnitTokens;
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    const int d0 = half * 64 + c * 8;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float a = 0.0f, b = 0.0f;
+      if (valid) {
+        a = side == 0 ? load_value<0>(codec, unit, r, d0 + 2 * i) : load_value<1>(codec, unit, r, d0 + 2 * i);
+        b = side == 0 ? load_value<0>(codec, unit, r, d0 + 2 * i + 1) : load_value<1>(codec, unit, r, d0 + 2 * i + 1);
+      }
+      w[i] = pack_half2(a, b);
+    }
+    *reinterpret_cast<uint4 *>(dst + tile_offset(row, d0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  grid_launch_dependents();
+}
+
+// ------------------------------------------------------------------ attention
+
+struct AttnParams {
+  const uint8_t *ktiles;  // [n_kv][n_tiles][32 KB]
+  const uint8_t *vtiles;
+  const __half *q;        // [n_tok][n_q][128]
+  __half *out;
+  float *lse;
+  int32_t *err;
+  int n_q, G, n_tok, q_start, kv_len, n_tiles;
+  float scale_log2;
+};
+
+struct __align__(8) AttnBars {
+  uint64_t kfull[kStages], vfull[kStages], kempty[kStages], vempty[kStages];
+  uint64_t sfull[2], pfull[2], odone, drain;
+};
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte aligned operand area: Q (32 KB), K stages, V stages.
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t *sq = smem;
+  uint8_t *sk = smem + kTileBytes;
+  uint8_t *sv = sk + kStages * kTileBytes;
+  __shared__ AttnBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qb = blockIdx.x, head = blockIdx.y;
+  const int kvh = head / p.G;
+  const int q0 = qb * kBM;
+  const int rows = min(kBM, p.n_tok - q0);
+  // keys needed: up to the last row's position
+  const int key_end = p.q_start + q0 + rows;  // exclusive
+  const int n_tiles = (key_end + kBN - 1) / kBN;
+  const uint32_t idesc_qk = idesc_f16(0), idesc_pv = idesc_f16(1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bars.kfull[s], 1);
+      mbar_init(&bars.vfull[s], 1);
+      mbar_init(&bars.kempty[s], 1);
+      mbar_init(&bars.vempty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.sfull[b], 1);
+      mbar_init(&bars.pfull[b], 4);  // one arrival per softmax warp
+    }
+    mbar_init(&bars.odone, 1);
+    mbar_init(&bars.drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_base_sh, 512);
+
+  grid_dependency_wait();  // the dequantized tiles come from the previous kernel
+
+  // Q rows of this block into the operand layout (softmax warpgroup).
+  if (warp >= kSoftmaxWarp0) {
+    const int r = threadIdx.x - kSoftmaxWarp0 * 32;
+    const uint4 *src = reinterpret_cast<const uint4 *>(
+        p.q + (static_cast<int64_t>(q0 + (r < rows ? r : 0)) * p.n_q + head) * kD);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = r < rows ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(sq + tile_offset(r, c * 8)) = v;
+    }
+    fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t tm_s[2] = {tmem, tmem + 128};
+  const uint32_t tm_o = tmem + 256;
+
+  const uint8_t *kt = p.ktiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
+  const uint8_t *vt = p.vtiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
+
+  if (warp == 0) {
+    // ---------------- producer: K and V tiles into the two-stage ring
+    if (lane == 0) {
+      int k_issued = 0, v_issued = 0;  // tiles whose copies were started
+      for (int j = 0; j < n_tiles; ++j) {
+        const int s = j % kStages;
+        const uint32_t ph = static_cast<uint32_t>(j / kStages - 1) & 1u;
+        if (j >= kStages && !mbar_wait_bounded(&bars.kempty[s], ph, &abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.kfull[s], kTileBytes);
+        bulk_copy_g2s(sk + s * kTileBytes, kt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
+                      &bars.kfull[s]);
+        k_issued = j + 1;
+        if (j >= kStages && !mbar_wait_bounded(&bars.vempty[s], ph, &abort_flag)) break;
+        mbar_arrive_expect_tx(&bars.vfull[s], kTileBytes);
+        bulk_copy_g2s(sv + s * kTileBytes, vt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
+                      &bars.vfull[s]);
+        v_issued = j + 1;
+      }
+      // After an abort, wait (bounded) for the copies still landing in the ring.
+      if (*reinterpret_cast<volatile int *>(&abort_flag)) {
+        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
+          mbar_wait_bounded(&bars.kfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1u,
+                            nullptr, 100000000ull);
+        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
+          mbar_wait_bounded(&bars.vfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1u,
+                            nullptr, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (one thread)
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(sq);
+      bool ok = true;
+      for (int j = 0; j <= n_tiles && ok; ++j) {
+        if (j < n_tiles) {  // S_j = Q K_j^T into TMEM buffer j % 2
+          const int s = j % kStages;
+          ok = mbar_wait_bounded(&bars.kfull[s], static_cast<uint32_t>(j / kStages) & 1u, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(sk + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+            mma_ss(tm_s[j & 1], smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
+                   idesc_qk, kk > 0);
+          }
+          mma_commit(&bars.sfull[j & 1]);
+          mma_commit(&bars.kempty[s]);
+        }
+        if (j >= 1) {  // O += P_{j-1} V_{j-1}
+          const int jp = j - 1, s = jp % kStages;
+          ok = mbar_wait_bounded(&bars.pfull[jp & 1], static_cast<uint32_t>(jp >> 1) & 1u, &abort_flag) &&
+               mbar_wait_bounded(&bars.vfull[s], static_cast<uint32_t>(jp / kStages) & 1u, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t v_addr = smem_u32(sv + s * kTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // keys 16kk..16kk+15: P columns 8kk.. (fp16 pairs), V rows 16kk.. (two 8-row groups)
+            mma_ts(tm_o, tm_s[jp & 1] + kk * 8, smem_desc(v_addr + kk * 2048, kHalfBytes, 1024),
+                   idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&bars.odone);
+          mma_commit(&bars.vempty[s]);
+        }
+      }
+      if (!ok) {
+        set_err(p.err, KVQ_DEVERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
+      }
+      // drain: completes when every MMA this thread issued has finished (the
+      // epilogue waits on it before reading O; TMEM is freed after it).
+      mma_commit(&bars.drain);
+      mbar_wait_bounded(&bars.drain, 0, nullptr, 100000000ull);
+    }
+  } else if (warp >= kSoftmaxWarp0) {
+    // ---------------- softmax warpgroup: thread = query row
+    const int r = threadIdx.x - kSoftmaxWarp0 * 32;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - kSoftmaxWarp0) * 32) << 16;
+    const int pos = p.q_start + q0 + r;  // absolute position of this query
+    float m = -INFINITY, l = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      ok = mbar_wait_bounded(&bars.sfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u, &abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tm_s[j & 1] + lane_off + c * 32, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+      }
+      tmem_wait_ld();
+      const int kbase = j * kBN;
+      float mx = -INFINITY;
+      if (kbase + kBN - 1 > pos) {  // diagonal tile: keys past the row's position are masked
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] = (kbase + c <= pos) ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          s[c] *= p.scale_log2;
+          mx = fmaxf(mx, s[c]);
+        }
+      }
+      // Raise a row's running max only when it grew by more than the
+      // threshold.  tcgen05.ld/st are warp-collective, so the O rescale runs
+      // for the whole warp when any of its rows needs it (factor 1 elsewhere).
+      const bool raise = mx > m + kRescaleThreshold || m == -INFINITY;
+      const float mnew = raise ? fmaxf(mx, m) : m;
+      const float a = (raise && m != -INFINITY) ? fast_exp2(m - mnew) : 1.0f;
+      if (__any_sync(0xffffffffu, raise && m != -INFINITY)) {
+        // O holds the sum of P V over tiles < j: wait for the last PV, rescale in TMEM
+        bool got = mbar_wait_bounded(&bars.odone, static_cast<uint32_t>(j - 1) & 1u, &abort_flag);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float v[32];
+          tmem_ld32(tm_o + lane_off + c * 32, v);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] *= a;
+          tmem_st32f(tm_o + lane_off + c * 32, v);
+        }
+        tmem_wait_st();
+      }
+      l *= a;
+      m = mnew;
+      // P = exp2(s - m) as fp16 pairs over the first 64 columns of the S buffer
+      float rs = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float a = fast_exp2(s[c * 32 + 2 * i] - m);
+          const float b = fast_exp2(s[c * 32 + 2 * i + 1] - m);
+          rs += a + b;
+          pk[i] = pack_half2(a, b);
+        }
+        tmem_st16(tm_s[j & 1] + lane_off + c * 16, pk);
+      }
+      l += rs;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.pfull[j & 1]);
+    }
+    // epilogue: wait until every MMA has finished (the single-use drain
+    // barrier; a parity wait on odone could alias with the previous phase),
+    // normalise, store the row
+    if (ok) ok = mbar_wait_bounded(&bars.drain, 0, &abort_flag);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok && lane == 0) {
+      set_err(p.err, KVQ_DEVERR_TIMEOUT);
+      atomicExch(&abort_flag, 1);
+    }
+    tc_fence_after();
+    const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+    __half *dst = p.out + (static_cast<int64_t>(q0 + r) * p.n_q + head) * kD;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      tmem_ld32(tm_o + lane_off + c * 32, v);
+      tmem_wait_ld();
+      if (r < rows) {
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = pack_half2(v[2 * i] * inv, v[2 * i + 1] * inv);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          reinterpret_cast<uint4 *>(dst + c * 32)[i] =
+              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      }
+    }
+    if (p.lse && r < rows)
+      p.lse[static_cast<int64_t>(q0 + r) * p.n_q + head] =
+          (ok && l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
 
 PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok) {
   PrefillPlan pl;
   pl.kv_tokens = static_cast<int64_t>(q_start) + n_q_tok;
-  pl.kv_tokens_pad = (pl.kv_tokens + 127) / 128 * 128;
-  pl.ws_k_bytes = static_cast<int64_t>(L.n_kv_heads) * pl.kv_tokens_pad * 128 * 2;
+  const int64_t n_tiles = (pl.kv_tokens + kBN - 1) / kBN;
+  pl.kv_tokens_pad = n_tiles * kBN;
+  pl.ws_k_bytes = static_cast<int64_t>(L.n_kv_heads) * n_tiles * kTileBytes;
   pl.ws_bytes = 2 * pl.ws_k_bytes;
   return pl;
 }
 
-cudaError_t launch_prefill(const kvq_layer &, const PrefillPlan &, int, int, int, const void *,
-                           float, void *, float *, void *, cudaStream_t) {
-  return cudaErrorNotSupported;
+cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, int q_start,
+                           int n_q_tok, const void *q, float scale, void *out, float *lse,
+                           void *workspace, cudaStream_t stream) {
+  const int n_tiles = static_cast<int>(pl.kv_tokens_pad / kBN);
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  DequantParams dp;
+  dp.cache[0] = static_cast<const uint8_t *>(L.k_cache);
+  dp.cache[1] = static_cast<const uint8_t *>(L.v_cache);
+  dp.codec[0] = L.codec_k;
+  dp.codec[1] = L.codec_v;
+  dp.tiles[0] = ws;
+  dp.tiles[1] = ws + pl.ws_k_bytes;
+  dp.seq_lens = L.seq_lens;
+  dp.err = L.err;
+  dp.seq = seq;
+  dp.n_kv = L.n_kv_heads;
+  dp.capacity = L.capacity;
+  dp.kv_len = static_cast<int>(pl.kv_tokens);
+  dp.n_tiles = n_tiles;
+  cudaError_t e = launch_pdl(dequant_tiles_kernel, dim3(n_tiles, L.n_kv_heads, 2), dim3(256), 0,
+                             stream, dp);
+  if (e != cudaSuccess) return e;
+
+  AttnParams ap;
+  ap.ktiles = ws;
+  ap.vtiles = ws + pl.ws_k_bytes;
+  ap.q = static_cast<const __half *>(q);
+  ap.out = static_cast<__half *>(out);
+  ap.lse = lse;
+  ap.err = L.err;
+  ap.n_q = L.n_q_heads;
+  ap.G = L.n_q_heads / L.n_kv_heads;
+  ap.n_tok = n_q_tok;
+  ap.q_start = q_start;
+  ap.kv_len = static_cast<int>(pl.kv_tokens);
+  ap.n_tiles = n_tiles;
+  ap.scale_log2 = scale * 1.4426950408889634f;
+  const int smem = (1 + 2 * kStages) * kTileBytes + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const dim3 grid((n_q_tok + kBM - 1) / kBM, L.n_q_heads);
+  return launch_pdl(prefill_attn_kernel, grid, dim3(kThreads), smem, stream, ap);
 }
 
 }  // namespace kvq
