@@ -143,7 +143,8 @@ int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int
                        size_t ws_bytes, void *stream) {
   int st = check_layer(layer);
   if (st != KVQ_OK) return st;
-  if (!q || !out || q_start < 0 || n_q_tok <= 0 || seq < 0 || seq >= layer->n_seqs)
+  if (!q || !out || q_start < 0 || n_q_tok <= 0 || seq < 0 || seq >= layer->n_seqs ||
+      !(scale > 0.0f))
     return KVQ_EINVAL;
   if (static_cast<int64_t>(q_start) + n_q_tok > layer->capacity) return KVQ_ECAPACITY;
   if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;

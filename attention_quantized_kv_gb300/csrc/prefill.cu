@@ -150,49 +150,59 @@ __host__ __device__ __forceinline__ int tile_offset(int row, int dim) {
 
 // ------------------------------------------------------------------ dequant pre-pass
 
-// Dequantized value of (token row r of a unit, dim d), per the cache layout.
-template <int SIDE>
-__device__ __forceinline__ float load_value(int codec, const uint8_t *unit, int r, int d) {
+// One 32-value block b of token row r of a unit (a shared-memory copy of the
+// cache unit), dequantized: x^ = d * q exactly in fp32, per the cache layout.
+template <int CODEC, int SIDE>
+__device__ __forceinline__ void load_block(const uint8_t *unit, int r, int b, float (&x)[32]) {
   const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
-  if (codec == KVQ_F16) {
-    int off;
-    if (SIDE == 0) {
-      const int b = d >> 5, h = (d >> 4) & 1, w = (d >> 2) & 3, i = d & 3;
-      off = (2 * b + rh) * 512 + (4 * g + w) * 16 + h * 8 + i * 2;
-    } else {
-      const int mt = d >> 4, gq = (d & 15) >> 1, s = d & 1;
-      off = mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + s * 2 + par) * 2;
+  if (CODEC == KVQ_F16) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int d = 32 * b + e;
+      int off;
+      if (SIDE == 0) {
+        off = (2 * b + rh) * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (e >> 4) * 8 + (e & 3) * 2;
+      } else {
+        const int mt = d >> 4, gq = (d & 15) >> 1;
+        off = mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + (d & 1) * 2 + par) * 2;
+      }
+      x[e] = __half2float(*reinterpret_cast<const __half *>(unit + off));
     }
-    return __half2float(*reinterpret_cast<const __half *>(unit + off));
+    return;
   }
-  const int b = d >> 5, e = d & 31;
-  int qoff, soff;
-  float q;
-  if (codec == KVQ_Q8_0) {
-    if (SIDE == 0) {
-      qoff = b * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (2 * rh + (e >> 4)) * 4 + (e & 3);
-      soff = 2048 + g * 16 + rh * 8 + b * 2;
-    } else {
-      const int mt = d >> 4, gq = (d & 15) >> 1, s = d & 1;
-      qoff = (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2 + s;
-      soff = 2048 + tig * 32 + b * 8 + rh * 4 + par * 2;
-    }
-    q = static_cast<float>(static_cast<int8_t>(unit[qoff]));
-  } else {
-    const int jc = e & 15, hi = e >> 4;  // canonical byte jc holds dims jc (low) and jc+16 (high)
-    if (SIDE == 0) {
-      qoff = (b >> 1) * 512 + (4 * g + (jc >> 2)) * 16 + ((b & 1) * 2 + rh) * 4 + (jc & 3);
-      soff = 1024 + g * 16 + rh * 8 + b * 2;
-    } else {
-      const int mt = 2 * b + (jc >> 3), gq = jc & 7;
-      qoff = (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
-      soff = 1024 + tig * 32 + b * 8 + rh * 4 + par * 2;
-    }
-    const int nib = (unit[qoff] >> (4 * hi)) & 0xf;
-    q = static_cast<float>(nib - 8);
-  }
+  const int soff = CODEC == KVQ_Q8_0
+                       ? (SIDE == 0 ? 2048 + g * 16 + rh * 8 + b * 2
+                                    : 2048 + tig * 32 + b * 8 + rh * 4 + par * 2)
+                       : (SIDE == 0 ? 1024 + g * 16 + rh * 8 + b * 2
+                                    : 1024 + tig * 32 + b * 8 + rh * 4 + par * 2);
   const float dsc = __half2float(*reinterpret_cast<const __half *>(unit + soff));
-  return dsc * q;  // exact in fp32
+  if (CODEC == KVQ_Q8_0) {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      int off;
+      if (SIDE == 0) {
+        off = b * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (2 * rh + (e >> 4)) * 4 + (e & 3);
+      } else {
+        const int d = 32 * b + e, mt = d >> 4, gq = (d & 15) >> 1;
+        off = (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2 + (d & 1);
+      }
+      x[e] = dsc * static_cast<float>(static_cast<int8_t>(unit[off]));
+    }
+  } else {
+#pragma unroll
+    for (int jc = 0; jc < 16; ++jc) {  // canonical byte jc: dims jc (low) and jc+16 (high)
+      int off;
+      if (SIDE == 0) {
+        off = (b >> 1) * 512 + (4 * g + (jc >> 2)) * 16 + ((b & 1) * 2 + rh) * 4 + (jc & 3);
+      } else {
+        const int mt = 2 * b + (jc >> 3), gq = jc & 7;
+        off = (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
+      }
+      const int v = unit[off];
+      x[jc] = dsc * static_cast<float>((v & 0xf) - 8);
+      x[jc + 16] = dsc * static_cast<float>((v >> 4) - 8);
+    }
+  }
 }
 
 struct DequantParams {
@@ -204,37 +214,63 @@ struct DequantParams {
   int seq, n_kv, capacity, kv_len, n_tiles;
 };
 
-// grid: (n_tiles, n_kv, 2 sides); 256 threads; thread = (key row, 64-dim half).
+// grid: (n_tiles, n_kv, 2 sides); 256 threads.  The tile's eight 16-token
+// units are first copied into shared memory with coalesced 16-byte loads;
+// then each thread takes (key row, 32-value block) items, dequantizes the
+// block there and writes four 16-byte chunks of the swizzled fp16 tile.
+template <int CODEC, int SIDE>
+__device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *units_sh) {
+  const int tile = blockIdx.x, kvh = blockIdx.y;
+  constexpr int UB = unit_bytes(CODEC);
+  const int64_t units = p.capacity / kUnitTokens;
+  const int u_first = tile * (kBN / kUnitTokens);
+  const int u_end = min(u_first + kBN / kUnitTokens,
+                        static_cast<int>((p.kv_len + kUnitTokens - 1) / kUnitTokens));
+  const uint8_t *src = p.cache[SIDE] +
+                       ((static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + u_first) * UB;
+  const int n16 = (u_end - u_first) * UB / 16;
+  for (int i = threadIdx.x; i < n16; i += 256)
+    reinterpret_cast<uint4 *>(units_sh)[i] = reinterpret_cast<const uint4 *>(src)[i];
+  __syncthreads();
+  uint8_t *dst = p.tiles[SIDE] + (static_cast<int64_t>(kvh) * p.n_tiles + tile) * kTileBytes;
+#pragma unroll 1
+  for (int item = threadIdx.x; item < kBN * 4; item += 256) {
+    const int row = item >> 2, b = item & 3;
+    const int key = tile * kBN + row;
+    float x[32];
+    if (key < p.kv_len) {
+      load_block<CODEC, SIDE>(units_sh + (row / kUnitTokens) * UB, row % kUnitTokens, b, x);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) x[e] = 0.0f;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint4 w;
+      w.x = pack_half2(x[8 * c + 0], x[8 * c + 1]);
+      w.y = pack_half2(x[8 * c + 2], x[8 * c + 3]);
+      w.z = pack_half2(x[8 * c + 4], x[8 * c + 5]);
+      w.w = pack_half2(x[8 * c + 6], x[8 * c + 7]);
+      *reinterpret_cast<uint4 *>(dst + tile_offset(row, 32 * b + 8 * c)) = w;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams p) {
+  __shared__ __align__(16) uint8_t units_sh[kBN / kUnitTokens * 4096];
   grid_dependency_wait();
-  const int tile = blockIdx.x, kvh = blockIdx.y, side = blockIdx.z;
-  if (tile == 0 && kvh == 0 && side == 0 && threadIdx.x == 0 &&
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
       p.seq_lens[p.seq] < p.kv_len)
     set_err(p.err, KVQ_DEVERR_SEQLEN);
-  const int row = threadIdx.x >> 1, half = threadIdx.x & 1;
-  const int key = tile * kBN + row;
-  const int codec = p.codec[side];
-  uint8_t *dst = p.tiles[side] + (static_cast<int64_t>(kvh) * p.n_tiles + tile) * kTileBytes;
-  const int64_t units = p.capacity / kUnitTokens;
-  const uint8_t *unit = p.cache[side] +
-                        ((static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + key / kUnitTokens) *
-                            unit_bytes(codec);
-  const bool valid = key < p.kv_len;
-  const int r = key % kUnitTokens;
-#pragma unroll 1
-  for (int c = 0; c < 8; ++c) {
-    const int d0 = half * 64 + c * 8;
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float a = 0.0f, b = 0.0f;
-      if (valid) {
-        a = side == 0 ? load_value<0>(codec, unit, r, d0 + 2 * i) : load_value<1>(codec, unit, r, d0 + 2 * i);
-        b = side == 0 ? load_value<0>(codec, unit, r, d0 + 2 * i + 1) : load_value<1>(codec, unit, r, d0 + 2 * i + 1);
-      }
-      w[i] = pack_half2(a, b);
-    }
-    *reinterpret_cast<uint4 *>(dst + tile_offset(row, d0)) = make_uint4(w[0], w[1], w[2], w[3]);
+  const int side = blockIdx.z, codec = p.codec[side];
+  if (side == 0) {
+    if (codec == KVQ_F16) dequant_tile<KVQ_F16, 0>(p, units_sh);
+    else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 0>(p, units_sh);
+    else dequant_tile<KVQ_Q4_0, 0>(p, units_sh);
+  } else {
+    if (codec == KVQ_F16) dequant_tile<KVQ_F16, 1>(p, units_sh);
+    else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 1>(p, units_sh);
+    else dequant_tile<KVQ_Q4_0, 1>(p, units_sh);
   }
   grid_launch_dependents();
 }
@@ -418,20 +454,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
       }
       tmem_wait_ld();
       const int kbase = j * kBN;
-      float mx = -INFINITY;
-      if (kbase + kBN - 1 > pos) {  // diagonal tile: keys past the row's position are masked
+      // Row max of the raw scores (scale > 0 keeps the order), 8 independent
+      // partial maxima; keys past the row's position are masked on diagonal tiles.
+      if (kbase + kBN - 1 > pos) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] = (kbase + c <= pos) ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          s[c] *= p.scale_log2;
-          mx = fmaxf(mx, s[c]);
-        }
+        for (int c = 0; c < 128; ++c)
+          if (kbase + c > pos) s[c] = -INFINITY;
       }
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
       // Raise a row's running max only when it grew by more than the
       // threshold.  tcgen05.ld/st are warp-collective, so the O rescale runs
       // for the whole warp when any of its rows needs it (factor 1 elsewhere).
@@ -460,20 +496,24 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
       }
       l *= a;
       m = mnew;
-      // P = exp2(s - m) as fp16 pairs over the first 64 columns of the S buffer
-      float rs = 0.0f;
+      // P = exp2(s * scale_log2 - m) as fp16 pairs over the first 64 columns
+      // of the S buffer; the row sum in 8 independent partials.
+      float sp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+      const float nm = -m;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float a = fast_exp2(s[c * 32 + 2 * i] - m);
-          const float b = fast_exp2(s[c * 32 + 2 * i + 1] - m);
-          rs += a + b;
+          const float a = fast_exp2(fmaf(s[c * 32 + 2 * i], p.scale_log2, nm));
+          const float b = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], p.scale_log2, nm));
+          sp[(2 * i) & 7] += a;
+          sp[(2 * i + 1) & 7] += b;
           pk[i] = pack_half2(a, b);
         }
         tmem_st16(tm_s[j & 1] + lane_off + c * 16, pk);
       }
+      const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       l += rs;
       tmem_wait_st();
       tc_fence_before();

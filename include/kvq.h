@@ -179,9 +179,12 @@ KVQ_API int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int3
 /* Causal attention of one prefill chunk of sequence `seq`: query i (absolute
  * position q_start + i) of head h attends keys 0 .. q_start + i of kv head
  * h / (n_q/n_kv).  The chunk's own keys must already be appended.
- * q: fp16 [n_q_tok][n_q_heads][128]; out: fp16 [n_q_tok][n_q_heads][128];
- * lse: optional fp32 [n_q_tok][n_q_heads].  workspace: device, 16-byte
- * aligned, at least attn_prefill_workspace() bytes. */
+ * q: fp16 [n_q_tok][n_q_heads][128] (16-byte aligned); out: fp16
+ * [n_q_tok][n_q_heads][128] (16-byte aligned); lse: optional fp32
+ * [n_q_tok][n_q_heads]; scale > 0.  The keys and values are dequantized once
+ * into the workspace as fp16 (each value rounded once to fp16, the tensor-core
+ * operand type).  workspace: device, 16-byte aligned, at least
+ * attn_prefill_workspace() bytes. */
 KVQ_API int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int32_t n_q_tok,
                        const void *q, float scale, void *out, float *lse, void *workspace,
                        size_t ws_bytes, void *stream);
