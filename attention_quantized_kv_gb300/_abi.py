@@ -18,8 +18,8 @@ KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN, KVQ_DEVERR_TIMEOUT, KVQ_DEVERR_SEQLEN = 
 
 # Every function the header declares (checked by the tests against include/kvq.h).
 EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kv_append_quantize",
-           "attn_decode_workspace", "attn_decode", "attn_prefill_workspace",
-           "attn_prefill_chunk")
+           "attn_decode_workspace", "attn_decode", "attn_decode_noalloc",
+           "attn_prefill_workspace", "attn_prefill_chunk")
 
 
 class kvq_layer(ctypes.Structure):
@@ -63,6 +63,7 @@ def load(path: str | None = None):
         "kv_append_quantize": (ctypes.c_int, [L, P, P, P, i32, i32, P]),
         "attn_decode_workspace": (ctypes.c_int, [L, i32, sz]),
         "attn_decode": (ctypes.c_int, [L, P, f32, P, P, i32, P, ctypes.c_size_t, P]),
+        "attn_decode_noalloc": (ctypes.c_int, [L, P, f32, P, P, i32, P]),
         "attn_prefill_workspace": (ctypes.c_int, [L, i32, i32, sz]),
         "attn_prefill_chunk": (ctypes.c_int, [L, i32, i32, i32, P, f32, P, P, P,
                                               ctypes.c_size_t, P]),

@@ -171,6 +171,23 @@ KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_
 KVQ_API int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
                 int32_t max_len, void *workspace, size_t ws_bytes, void *stream);
 
+/* attn_decode without a workspace argument, for callers that cannot allocate
+ * device memory where they run attention (an interface that hands them only
+ * the input and output buffers, a loop where a device allocation is not
+ * allowed, a fully committed memory budget).  There is no counterpart in the
+ * source material; it is a convenience of this library.  The scratch that
+ * attn_decode keeps in the caller's workspace lives instead in one 8 MiB
+ * device array inside the library (reserved on every GPU that loads it, until
+ * the process exits); nothing is allocated.  The first call on a device looks
+ * the array up (cudaGetSymbolAddress) and must come before any stream capture.
+ * The array is shared by all calls and keeps the previous call's contents:
+ * the arrival counters are cleared on `stream` before each launch, and calls
+ * that can overlap on the GPU race on it, so issue them in order on one
+ * stream.  A layer whose attn_decode_workspace() exceeds 8 MiB is refused
+ * with KVQ_EWORKSPACE.  Arguments and results are those of attn_decode. */
+KVQ_API int attn_decode_noalloc(const kvq_layer *layer, const void *q, float scale, void *out,
+                                float *lse, int32_t max_len, void *stream);
+
 /* Workspace bytes that attn_prefill_chunk needs for a chunk ending at
  * q_start + n_q_tok. */
 KVQ_API int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int32_t n_q_tok,
