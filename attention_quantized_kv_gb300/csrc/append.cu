@@ -134,7 +134,7 @@ struct AppendParams {
   const __half *x[2];  // k_new, v_new: [n_seqs][max_new][n_kv][128]
   uint8_t *cache[2];
   int codec[2];
-  const int32_t *seq_lens;
+  int32_t *seq_lens;  // read by every row; advanced only by append_small_kernel
   const int32_t *n_new;
   int32_t *err;
   int n_seqs, n_kv, max_new, capacity;
@@ -142,11 +142,8 @@ struct AppendParams {
 
 constexpr int kAppendWarps = 8;
 
-__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendParams p) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+__device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, int lane) {
   const int64_t rows_per_side = static_cast<int64_t>(p.n_seqs) * p.max_new * p.n_kv;
-  if (row >= 2 * rows_per_side) return;
   const int side = row >= rows_per_side ? 1 : 0;
   const int64_t rr = row - side * rows_per_side;
   const int kvh = static_cast<int>(rr % p.n_kv);
@@ -180,14 +177,46 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendParams 
   else store_row<1>(codec, unit, r, lane, raw, q, d16);
 }
 
+// One warp per row (grid covers all rows).
+__global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendParams p) {
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
+  const int64_t rows = 2ll * p.n_seqs * p.max_new * p.n_kv;
+  if (row < rows) append_row(p, row, lane);
+  grid_launch_dependents();
+}
+
+// Small appends (a decode step): one CTA whose warps take all rows, then,
+// once every row has read its position, advances the lengths itself.
+__global__ void __launch_bounds__(kAppendWarps * 32) append_small_kernel(AppendParams p,
+                                                                        int update_lens) {
+  grid_dependency_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = 2ll * p.n_seqs * p.max_new * p.n_kv;
+  for (int64_t row = threadIdx.x >> 5; row < rows; row += kAppendWarps) append_row(p, row, lane);
+  if (update_lens) {
+    __syncthreads();
+    for (int s = threadIdx.x; s < p.n_seqs; s += kAppendWarps * 32) {
+      const int v = p.seq_lens[s] + p.n_new[s];
+      p.seq_lens[s] = v > p.capacity ? p.capacity : v;
+    }
+  }
+  grid_launch_dependents();
+}
+
 __global__ void update_lens_kernel(int32_t *seq_lens, const int32_t *n_new, int n_seqs,
                                    int capacity) {
+  grid_dependency_wait();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < n_seqs) {
     const int v = seq_lens[s] + n_new[s];
     seq_lens[s] = v > capacity ? capacity : v;
   }
+  grid_launch_dependents();
 }
+
+constexpr int64_t kSmallAppendRows = 64;  // at most 8 rows per warp
 
 }  // namespace
 
@@ -209,15 +238,16 @@ cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_n
   p.max_new = max_new;
   p.capacity = L.capacity;
   const int64_t rows = 2ll * L.n_seqs * max_new * L.n_kv_heads;
-  if (rows > 0) {
-    const int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
-    append_kernel<<<static_cast<unsigned>(blocks), kAppendWarps * 32, 0, stream>>>(p);
+  if (rows <= kSmallAppendRows) {
+    return launch_pdl(append_small_kernel, dim3(1), dim3(kAppendWarps * 32), 0, stream, p,
+                      update_lens);
   }
-  if (update_lens) {
-    update_lens_kernel<<<(L.n_seqs + 127) / 128, 128, 0, stream>>>(L.seq_lens, n_new, L.n_seqs,
-                                                                   L.capacity);
-  }
-  return cudaGetLastError();
+  const int64_t blocks = (rows + kAppendWarps - 1) / kAppendWarps;
+  cudaError_t e = launch_pdl(append_kernel, dim3(static_cast<unsigned>(blocks)),
+                             dim3(kAppendWarps * 32), 0, stream, p);
+  if (e != cudaSuccess || !update_lens) return e;
+  return launch_pdl(update_lens_kernel, dim3((L.n_seqs + 127) / 128), dim3(128), 0, stream,
+                    L.seq_lens, n_new, L.n_seqs, L.capacity);
 }
 
 }  // namespace kvq

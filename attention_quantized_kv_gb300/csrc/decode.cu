@@ -369,6 +369,153 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
   }
 }
 
+// B fragments of Q for query head g of head group hg (zero beyond the
+// group), with the per-codec order of the k (head-dim) index that matches the
+// K unit layout.
+template <int CK>
+__device__ __forceinline__ void load_q_frags(const __half *q, int64_t qrow0, int n_q, int G, int hg,
+                                             int lane, uint32_t (&qb)[8][2]) {
+  const int g = lane >> 2, tig = lane & 3;
+  const int hq = hg * 8 + g;
+  const bool hvalid = hq < G;
+  const __half *qrow = q + (qrow0 + (hvalid ? hq : 0)) * kD;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+    uint2 v = make_uint2(0u, 0u);
+    if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
+    if (CK == KVQ_F16) {
+      qb[c][0] = v.x;
+      qb[c][1] = v.y;
+    } else {
+      qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+      qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+    }
+  }
+}
+
+// Last-CTA merge of one stream's partials into out / lse (all 256 threads;
+// called by the CTA whose ticket completed the stream).
+struct MergeArgs {
+  const float2 *part_ml;
+  const float *part_o;
+  __half *out;
+  float *lse;
+  int n_q, G;
+};
+
+__device__ __forceinline__ void merge_stream(const MergeArgs p, float4 *xacc, float *xl,
+                                             int stream, int seq, int kvh, int hg, int c_first,
+                                             int c_last, int64_t S, int n_s, int64_t U, int P) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Merge the stream's partials.  The heads of the group are spread over
+  // the 8 warps (reps warps per head; warp `part` of a head takes parts
+  // j = part, part + reps, ...).  Parts go in windows of 64: lanes fetch
+  // the writer CTA and the (max, sum) of parts lane and lane + 32 once, and
+  // the rows then stream through an 8-row register buffer with their CTA
+  // and weight taken from those lanes by shuffles.  With several warps per
+  // head, warps part > 0 hand their sums to warp part 0 through xacc / xl
+  // (a region no other phase writes) across one CTA barrier.
+  const int heads_here = min(8, p.G - hg * 8);
+  const int reps = kWarps / heads_here >= 4 ? 4 : (kWarps / heads_here >= 2 ? 2 : 1);
+  const int h = warp % heads_here, part = warp / heads_here;
+  const bool active = warp < heads_here * reps;
+  float M = -INFINITY, L = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (active) {
+    // Part j of the stream: with at least one unit per CTA (U >= P) it is
+    // the partial of CTA c_first + j; otherwise CTAs hold at most one unit
+    // and part j is the partial of the owner of unit S + j.
+    const bool sparse = U < P;
+    const int n_live = sparse ? n_s : c_last - c_first + 1;
+    auto cta_of = [&](int j) -> int {
+      return sparse ? static_cast<int>(((S + j + 1) * P - 1) / U) : c_first + j;
+    };
+    const float2 *ml_h = p.part_ml + static_cast<int64_t>(stream) * 8 + h;
+    const float4 *o_h =
+        reinterpret_cast<const float4 *>(p.part_o + (static_cast<int64_t>(stream) * 8 + h) * kD) + lane;
+    int base = 0, ca = 0, cb = 0;
+    float2 mla, mlb;
+    float4 xa[8];
+    // Window `base`: lane data of parts base + lane, base + 32 + lane.
+    auto load_window = [&]() {
+      ca = base + lane < n_live ? cta_of(base + lane) : 0;
+      cb = base + 32 + lane < n_live ? cta_of(base + 32 + lane) : 0;
+      mla = base + lane < n_live ? __ldcg(ml_h + static_cast<int64_t>(ca) * 8)
+                                 : make_float2(-INFINITY, 0.0f);
+      mlb = base + 32 + lane < n_live ? __ldcg(ml_h + static_cast<int64_t>(cb) * 8)
+                                      : make_float2(-INFINITY, 0.0f);
+    };
+    // Rows t0 .. t0+7 of this warp in the window (window-relative part
+    // part + reps * t < 64 for every t < 64 / reps).
+    auto load_rows = [&](float4 (&x)[8], int t0) {
+#pragma unroll
+      for (int t = 0; t < 8; ++t) {
+        const int jr = part + reps * (t0 + t);
+        const int c = __shfl_sync(0xffffffffu, jr < 32 ? ca : cb, jr & 31);
+        x[t] = base + jr < n_live ? __ldcg(o_h + static_cast<int64_t>(c) * (8 * kD / 4))
+                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
+    };
+    load_window();
+    load_rows(xa, 0);
+    M = fmaxf(mla.x, mlb.x);
+    for (int j = 64 + lane; j < n_live; j += 32)
+      M = fmaxf(M, __ldcg(ml_h + static_cast<int64_t>(cta_of(j)) * 8).x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (M != -INFINITY) {
+      const int rows_max = 64 / reps;  // rows of a warp in a full window
+      while (true) {
+        const float wa = mla.x == -INFINITY ? 0.0f : fast_exp2(mla.x - M);
+        const float wb = mlb.x == -INFINITY ? 0.0f : fast_exp2(mlb.x - M);
+        if (lane % reps == part) L += wa * mla.y + wb * mlb.y;  // 32 % reps == 0
+        auto use_rows = [&](const float4 (&x)[8], int t0) {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            const int jr = part + reps * (t0 + t);
+            const float w = __shfl_sync(0xffffffffu, jr < 32 ? wa : wb, jr & 31);
+            acc.x = fmaf(w, x[t].x, acc.x);
+            acc.y = fmaf(w, x[t].y, acc.y);
+            acc.z = fmaf(w, x[t].z, acc.z);
+            acc.w = fmaf(w, x[t].w, acc.w);
+          }
+        };
+        const int rows = min(rows_max, (min(n_live - base, 64) - part + reps - 1) / reps);
+        for (int t0 = 0; t0 < rows; t0 += 8) {
+          use_rows(xa, t0);
+          if (t0 + 8 < rows) load_rows(xa, t0 + 8);
+        }
+        base += 64;
+        if (base >= n_live) break;
+        load_window();
+        load_rows(xa, 0);
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+    }
+    if (part > 0) {
+      xacc[warp * 32 + lane] = acc;
+      if (lane == 0) xl[warp] = L;
+    }
+  }
+  if (reps > 1) cta_bar();  // reps is the same in every warp
+  if (active && part == 0) {
+    for (int r = 1; r < reps; ++r) {
+      const float4 y = xacc[(h + r * heads_here) * 32 + lane];
+      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+      L += xl[h + r * heads_here];
+    }
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
+    __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
+    dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
+    dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    if (p.lse && lane == 0)
+      p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
 template <int CK, int CV>
 __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeParams p) {
   using C = DecodeCfg<CK, CV>;
@@ -377,7 +524,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   __shared__ int32_t pfx[kMaxSeqs + 1];
   __shared__ int abort_flag;
   __shared__ int last_flag;
-  __shared__ int8_t pend[C::NS];  // 0: idle, 1 + parity: a copy of that phase is in flight
+  // merge hand-over (read by warp part 0 of a head before the CTA's next
+  // barrier, written again only after it)
+  __shared__ float4 mrg_acc[kWarps * 32];
+  __shared__ float mrg_l[kWarps];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
@@ -413,10 +563,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       pfx[0] = 0;
       abort_flag = 0;
     }
-    for (int s = lane; s < C::NS; s += 32) {
-      mbar_init(&full[s], 1);
-      pend[s] = 0;
-    }
+    for (int s = lane; s < C::NS; s += 32) mbar_init(&full[s], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -454,12 +601,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   auto issue = [&](int k, const Cursor &c) {
     const int s = k % C::NS;
     uint8_t *dst = ring + s * C::STAGE;
-    pend[s] = static_cast<int8_t>(1 + ((k / C::NS) & 1));
     mbar_arrive_expect_tx(&full[s], C::STAGE);
     bulk_copy_g2s(dst, p.k_cache + c.unit * C::UK, C::UK, &full[s]);
     bulk_copy_g2s(dst + C::UK, p.v_cache + c.unit * C::UV, C::UV, &full[s]);
   };
 
+
+  Cursor seg = cursor_at(geo, u0);
   // Prologue: each warp issues its own first stages (k = warp, warp + 8, ...
   // below NS).  Afterwards the producer cursor pc sits at unit k + NS for the
   // warp's next unit k.
@@ -474,10 +622,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   cursor_advance(pc, C::NS, geo);
 
   // Walk the segments (stream pieces) of this slice.
-  Cursor seg = cursor_at(geo, u0);
   int64_t useg = u0;
   int k_next = warp;  // next unit index (CTA-local) this warp consumes
   bool ok = true;
+  int k_fail = -1;    // first unit not consumed after an abort
   while (useg < u1) {
     const int64_t seg_end = min(u1, useg + (seg.n_s - seg.j));
     const int k0 = static_cast<int>(useg - u0), k1 = static_cast<int>(seg_end - u0);
@@ -485,29 +633,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     int len = p.seq_lens[seq];
     len = len < p.max_len ? len : p.max_len;
 
-    // B fragments of Q (n = query head g of this group), with the per-codec
-    // order of the k (head-dim) index matching the K unit layout.
-    const int hq = hg * 8 + g;
-    const bool hvalid = hq < p.G;
     uint32_t qb[8][2];
-    {
-      const __half *qrow =
-          p.q + (static_cast<int64_t>(seq) * p.n_q + kvh * p.G + (hvalid ? hq : 0)) * kD;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
-        uint2 v = make_uint2(0u, 0u);
-        if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
-        if (CK == KVQ_F16) {
-          qb[c][0] = v.x;
-          qb[c][1] = v.y;
-        } else {
-          qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
-          qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
-        }
-      }
-    }
-
+    load_q_frags<CK>(p.q, static_cast<int64_t>(seq) * p.n_q + kvh * p.G, p.n_q, p.G, hg, lane, qb);
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
@@ -530,19 +657,18 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
           set_err(p.err, KVQ_DEVERR_TIMEOUT);
           atomicExch(&abort_flag, 1);
         }
+        if (ok) k_fail = k;
         ok = false;
         k_next += two ? 2 * kWarps : kWarps;
         continue;
       }
       const int j = seg.j + (k - k0);
       if (two) {
-        if (lane == 0) pend[s0] = pend[s1] = 0;
         const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
         const int nv[2] = {min(kUnitTokens, len - j * kUnitTokens),
                            min(kUnitTokens, len - (j + kWarps) * kUnitTokens)};
         process_units<CK, CV, 2>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
       } else {
-        if (lane == 0) pend[s0] = 0;
         const uint8_t *ku[1] = {ring + s0 * C::STAGE};
         const int nv[1] = {min(kUnitTokens, len - j * kUnitTokens)};
         process_units<CK, CV, 1>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
@@ -615,65 +741,21 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     cta_bar();  // slots free again; last_flag visible
     if (last_flag) {
       __threadfence();
-      // Merge the stream's partials: warp h takes head h.  Lane c loads the
-      // (max, sum) of parts c, c+32, ... and computes their weights, so the
-      // accumulation loop only streams the independent output rows.
-      const int heads_here = min(8, p.G - hg * 8);
-      const bool sparse = U < P;  // some CTAs in the span may hold no partial
-      for (int h = warp; h < heads_here; h += kWarps) {
-        float M = -INFINITY;
-        for (int c = c_first + lane; c <= c_last; c += 32)
-          if (!sparse || U * (c + 1) / P != U * c / P)
-            M = fmaxf(M, __ldcg(&p.part_ml[(static_cast<int64_t>(c) + stream) * 8 + h].x));
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-        float L = 0.0f;
-        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        if (M != -INFINITY) {
-          for (int cb = c_first; cb <= c_last; cb += 32) {
-            const int c = cb + lane;
-            float wgt = 0.0f;
-            if (c <= c_last && (!sparse || U * (c + 1) / P != U * c / P)) {
-              const float2 ml = __ldcg(&p.part_ml[(static_cast<int64_t>(c) + stream) * 8 + h]);
-              wgt = ml.x == -INFINITY ? 0.0f : fast_exp2(ml.x - M);
-              L = fmaf(wgt, ml.y, L);
-            }
-            const int n = min(32, c_last - cb + 1);
-            const float *po = p.part_o + ((static_cast<int64_t>(cb) + stream) * 8 + h) * kD + 4 * lane;
-#pragma unroll 8
-            for (int i = 0; i < n; ++i) {
-              const float wi = __shfl_sync(0xffffffffu, wgt, i);
-              if (wi != 0.0f) {
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(po + static_cast<int64_t>(i) * 8 * kD));
-                acc.x = fmaf(wi, x.x, acc.x);
-                acc.y = fmaf(wi, x.y, acc.y);
-                acc.z = fmaf(wi, x.z, acc.z);
-                acc.w = fmaf(wi, x.w, acc.w);
-              }
-            }
-          }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
-        __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
-        dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-        dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
-        if (p.lse && lane == 0)
-          p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
+      const MergeArgs ma = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
+      merge_stream(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first, c_last, S, seg.n_s, U, P);
     }
 
     useg = seg_end;
     if (useg < u1) seg = cursor_at(geo, useg);
   }
 
-  // After an aborted run, wait (bounded) for copies still in flight into the ring.
-  __syncthreads();
-  if (abort_flag && lane == 0) {
-    for (int s = warp; s < C::NS; s += kWarps)
-      if (pend[s]) mbar_wait_bounded(&full[s], static_cast<uint32_t>(pend[s] - 1), nullptr, 100000000ull);
+  // After an aborted run, wait (bounded) for this warp's copies still in
+  // flight: the units k_fail, k_fail + 8, ... below k_fail + NS were issued
+  // (each after the unit NS before it was consumed) but never consumed.
+  if (k_fail >= 0 && lane == 0) {
+    for (int k = k_fail; k < R && k < k_fail + C::NS; k += kWarps)
+      mbar_wait_bounded(&full[k % C::NS], static_cast<uint32_t>(k / C::NS) & 1u, nullptr,
+                        100000000ull);
   }
 }
 

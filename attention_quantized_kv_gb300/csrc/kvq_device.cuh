@@ -192,9 +192,9 @@ __device__ __forceinline__ void grid_launch_dependents() {
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel on the stream drains; it must call
 // grid_dependency_wait() before touching that kernel's results.
-template <typename Kernel, typename Params>
-inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t stream, const Params &params) {
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -205,7 +205,7 @@ inline cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, params);
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace kvq

@@ -100,6 +100,16 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def wait_first(self, timeout=5.0):
+        """Block until nvidia-smi has written its first sample (it takes a
+        moment to start), so that the load window that follows is sampled."""
+        t_end = time.perf_counter() + timeout
+        while self.proc is not None and time.perf_counter() < t_end:
+            self.f.flush()
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.05)
+
     def stop(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -184,7 +194,16 @@ class OursArm:
             L.seq_lens.copy_(self.init_lens)
 
     def launches_per_step(self):
-        per_layer = (2 if self.w.append_new else 0) + 2
+        """Kernels the library launches per step: the append is one kernel
+        for at most 64 rows (it also advances the lengths), else the encode
+        kernel plus the length update; decode is one kernel, prefill two
+        (dequant pre-pass, attention)."""
+        w = self.w
+        per_layer = 1 if w.kind == "decode" else 2
+        if w.append_new:
+            n_tok = w.append_new if w.kind == "prefill" else 1
+            rows = 2 * w.n_seqs * n_tok * w.n_kv
+            per_layer += 1 if rows <= 64 else 2
         return per_layer * len(self.layers)
 
     def step(self, ev=None, q=None, kn=None, vn=None):
@@ -325,14 +344,13 @@ def run_ours(args, w, rank, world, dist):
     # nvidia-smi sample period)
     clk = ClockSampler(local)
     clk.start()
-    t_end = time.perf_counter() + 1.0
-    n_win = 0
-    while time.perf_counter() < t_end and n_win < 400:
+    clk.wait_first()
+    t_end = time.perf_counter() + 1.5
+    while time.perf_counter() < t_end:
         for _ in range(20):
             _flush_l2(torch, flush)
             arm.reset()
             replay()
-        n_win += 20
         torch.cuda.synchronize()
     step_ms, attn_ms = [], []
     for _ in range(args.steps):
@@ -428,7 +446,7 @@ def run_ours(args, w, rank, world, dist):
         "device_errors": errs,
     }
     if w.kind == "decode":
-        line["roofline"] = {"bound": "hbm", "kernel": "attn_decode (split + merge kernels)",
+        line["roofline"] = {"bound": "hbm", "kernel": "attn_decode (decode_split_kernel)",
                             "achieved": round(achieved_attn, 2), "peak": hbm,
                             "peak_kind": peak_kind, "unit": "GB/s",
                             "frac": round(achieved_attn / hbm, 4),
