@@ -151,9 +151,17 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
 
 // O^T (128 dims x 8 heads) += V^T (dims x 16 tokens) * P^T (16 tokens x heads).
 // FULL: all 16 tokens of the unit are valid (no masking needed).
+//
+// q4_0 V takes the nibbles n as fp16 subnormals, one AND each: rows g of an
+// m-tile get n * 2^-24 (low nibbles), rows g+8 get 16n * 2^-24 (high nibbles
+// masked in place).  Every product with the folded P (an fp16 number) is
+// still exact in fp32.  The offset of the codec, -8 per value, is restored
+// at the end of the segment from corr, whose rows r collect
+// C_b = sum over tokens of d_b(t) p(t, h) for block b = r & 3: one MMA with
+// A rows r holding the scales d_{r&3} of the unit's tokens and B = P^T.
 template <int CV, bool FULL>
 __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0, uint32_t B1,
-                                        int nvalid, float (&o)[8][4]) {
+                                        int nvalid, float (&o)[8][4], float (&corr)[4]) {
   const int tig = lane & 3;
   // token validity of the halves this thread holds: (2tig, 2tig+1) and (+8, +9)
   uint32_t m01 = 0xffffffffu, m23 = 0xffffffffu;
@@ -203,11 +211,17 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
         for (int qq = 0; qq < 4; ++qq) {
           const int mt = 4 * jv + qq, b = mt >> 1;
           const uint32_t W = ws[qq], X = W >> 8;
-          const uint32_t a[4] = {u4_pair_minus8(W), u4_pair_minus8_hi(W), u4_pair_minus8(X),
-                                 u4_pair_minus8_hi(X)};
+          const uint32_t a[4] = {W & 0x000f000fu, W & 0x00f000f0u, X & 0x000f000fu,
+                                 X & 0x00f000f0u};
           mma16816(o[mt], a, bp0[b], bp1[b]);
         }
       }
+      const int g = lane >> 2;
+      // scales of block g & 3 for tokens (2tig, 2tig+1) and (2tig+8, 2tig+9)
+      uint2 dg = lds64(vu + unit_scale_offset(CV) + tig * 32 + (g & 3) * 8);
+      if (!FULL) { dg.x &= m01; dg.y &= m23; }
+      const uint32_t a[4] = {dg.x, dg.x, dg.y, dg.y};
+      mma16816(corr, a, B0, B1);
     }
   }
 }
@@ -253,8 +267,9 @@ __device__ __forceinline__ Cursor cursor_at(const Geo &q, int64_t u) {
   c.seq = find_seq(q, u);
   c.n_s = q.pfx[c.seq + 1] - q.pfx[c.seq];
   const int64_t within = u - static_cast<int64_t>(q.pfx[c.seq]) * q.KH;
-  c.sl = static_cast<int>(within / c.n_s);
-  c.j = static_cast<int>(within % c.n_s);
+  const int64_t sl = within / c.n_s;
+  c.sl = static_cast<int>(sl);
+  c.j = static_cast<int>(within - sl * c.n_s);
   c.unit = cache_unit(q, c.seq, c.sl, c.j);
   return c;
 }
@@ -320,8 +335,8 @@ template <int CK, int CV, int N>
 __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
                                               const int (&nvalid)[N], int lane,
                                               const uint32_t (&qb)[8][2], float scale_log2,
-                                              int uk_bytes, float (&o)[8][4], float &m0,
-                                              float &m1, float &l0, float &l1) {
+                                              int uk_bytes, float (&o)[8][4], float (&corr)[4],
+                                              float &m0, float &m1, float &l0, float &l1) {
   const int g = lane >> 2;
   float sc[N][4];
 #pragma unroll
@@ -352,6 +367,7 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
     for (int mt = 0; mt < 8; ++mt) {
       o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
     }
+    if (CV == KVQ_Q4_0) { corr[0] *= a0; corr[1] *= a1; corr[2] *= a0; corr[3] *= a1; }
     m0 = mn0;
     m1 = mn1;
   }
@@ -364,8 +380,8 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
     const uint32_t B0 = movmatrix_trans(pack_half2(p0, p1));
     const uint32_t B1 = movmatrix_trans(pack_half2(p2, p3));
     const uint8_t *vu = ku[u] + uk_bytes;
-    if (nvalid[u] == kUnitTokens) unit_pv<CV, true>(vu, lane, B0, B1, nvalid[u], o);
-    else unit_pv<CV, false>(vu, lane, B0, B1, nvalid[u], o);
+    if (nvalid[u] == kUnitTokens) unit_pv<CV, true>(vu, lane, B0, B1, nvalid[u], o, corr);
+    else unit_pv<CV, false>(vu, lane, B0, B1, nvalid[u], o, corr);
   }
 }
 
@@ -384,6 +400,29 @@ __device__ __forceinline__ void load_q_frags(const __half *q, int64_t qrow0, int
     const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
     uint2 v = make_uint2(0u, 0u);
     if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
+    if (CK == KVQ_F16) {
+      qb[c][0] = v.x;
+      qb[c][1] = v.y;
+    } else {
+      qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+      qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+    }
+  }
+}
+
+// The same fragments from a copy of the group's query rows in shared memory
+// (nh = rows present; row r is query head hg * 8 + r).
+template <int CK>
+__device__ __forceinline__ void load_q_frags_smem(const __half *qs, int nh, int lane,
+                                                  uint32_t (&qb)[8][2]) {
+  const int g = lane >> 2, tig = lane & 3;
+  const bool hvalid = g < nh;
+  const __half *qrow = qs + (hvalid ? g : 0) * kD;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+    uint2 v = make_uint2(0u, 0u);
+    if (hvalid) v = lds64(qrow + base);
     if (CK == KVQ_F16) {
       qb[c][0] = v.x;
       qb[c][1] = v.y;
@@ -524,6 +563,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   __shared__ int32_t pfx[kMaxSeqs + 1];
   __shared__ int abort_flag;
   __shared__ int last_flag;
+  // query rows of the current and the next segment (bulk copies, one
+  // segment ahead; the first is requested before the ring's copies)
+  __shared__ __align__(128) __half q_s[2][8 * kD];
+  __shared__ uint64_t q_bar[2];
   // merge hand-over (read by warp part 0 of a head before the CTA's next
   // barrier, written again only after it)
   __shared__ float4 mrg_acc[kWarps * 32];
@@ -564,6 +607,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       abort_flag = 0;
     }
     for (int s = lane; s < C::NS; s += 32) mbar_init(&full[s], 1);
+    if (lane < 2) mbar_init(&q_bar[lane], 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -606,8 +650,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     bulk_copy_g2s(dst + C::UK, p.v_cache + c.unit * C::UV, C::UV, &full[s]);
   };
 
+  // Query rows of the segment at cursor c into q_s[buf] (thread 0).
+  const bool q_bulk = (reinterpret_cast<uintptr_t>(p.q) & 15) == 0;
+  auto issue_q = [&](int buf, const Cursor &c) {
+    const int hgc = c.sl % p.n_hg;
+    const uint32_t bytes = static_cast<uint32_t>(min(8, p.G - hgc * 8)) * kD * 2;
+    const __half *src =
+        p.q + (static_cast<int64_t>(c.seq) * p.n_q + (c.sl / p.n_hg) * p.G + hgc * 8) * kD;
+    mbar_arrive_expect_tx(&q_bar[buf], bytes);
+    bulk_copy_g2s(q_s[buf], src, bytes, &q_bar[buf]);
+  };
 
   Cursor seg = cursor_at(geo, u0);
+  int q_iss = 0;  // query-row copies issued (thread 0: segments 0 .. q_iss - 1)
+  if (q_bulk && threadIdx.x == 0) {
+    issue_q(0, seg);
+    q_iss = 1;
+  }
   // Prologue: each warp issues its own first stages (k = warp, warp + 8, ...
   // below NS).  Afterwards the producer cursor pc sits at unit k + NS for the
   // warp's next unit k.
@@ -626,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   int k_next = warp;  // next unit index (CTA-local) this warp consumes
   bool ok = true;
   int k_fail = -1;    // first unit not consumed after an abort
+  int si = 0;         // segment index (its query rows are in q_s[si & 1])
   while (useg < u1) {
     const int64_t seg_end = min(u1, useg + (seg.n_s - seg.j));
     const int k0 = static_cast<int>(useg - u0), k1 = static_cast<int>(seg_end - u0);
@@ -634,10 +694,36 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     len = len < p.max_len ? len : p.max_len;
 
     uint32_t qb[8][2];
-    load_q_frags<CK>(p.q, static_cast<int64_t>(seq) * p.n_q + kvh * p.G, p.n_q, p.G, hg, lane, qb);
+    if (q_bulk) {
+      const int buf = si & 1;
+      bool got_q =
+          ok && mbar_wait_bounded(&q_bar[buf], static_cast<uint32_t>(si >> 1) & 1u, &abort_flag);
+      got_q = __all_sync(0xffffffffu, got_q);
+      if (!got_q && ok) {
+        if (lane == 0) {
+          set_err(p.err, KVQ_DEVERR_TIMEOUT);
+          atomicExch(&abort_flag, 1);
+        }
+        ok = false;
+        k_fail = k_next;
+      }
+      load_q_frags_smem<CK>(q_s[buf], min(8, p.G - hg * 8), lane, qb);
+      // The next segment's rows go out now, a whole segment ahead of their
+      // use (q_s[buf ^ 1] was last read before the previous segment's
+      // barriers).
+      if (threadIdx.x == 0 && seg_end < u1 && ok) {
+        fence_proxy_async_smem();
+        issue_q(buf ^ 1, cursor_at(geo, seg_end));
+        ++q_iss;
+      }
+    } else {
+      load_q_frags<CK>(p.q, static_cast<int64_t>(seq) * p.n_q + kvh * p.G, p.n_q, p.G, hg, lane,
+                       qb);
+    }
     float o[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.0f;
+    float corr[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // q4_0 V: per-block sums of the folded P
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
     while (k_next < k1) {
@@ -667,11 +753,13 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
         const int nv[2] = {min(kUnitTokens, len - j * kUnitTokens),
                            min(kUnitTokens, len - (j + kWarps) * kUnitTokens)};
-        process_units<CK, CV, 2>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
+        process_units<CK, CV, 2>(ku, nv, lane, qb, p.scale_log2, C::UK, o, corr, m0, m1, l0,
+                                 l1);
       } else {
         const uint8_t *ku[1] = {ring + s0 * C::STAGE};
         const int nv[1] = {min(kUnitTokens, len - j * kUnitTokens)};
-        process_units<CK, CV, 1>(ku, nv, lane, qb, p.scale_log2, C::UK, o, m0, m1, l0, l1);
+        process_units<CK, CV, 1>(ku, nv, lane, qb, p.scale_log2, C::UK, o, corr, m0, m1, l0,
+                                 l1);
       }
       // The consumed stages are free: refill them with units k + NS (+ 8).
       __syncwarp();
@@ -685,6 +773,23 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         cursor_advance(pc, kWarps, geo);
       }
       k_next += two ? 2 * kWarps : kWarps;
+    }
+
+    if (CV == KVQ_Q4_0) {
+      // Restore the codec offset: o = 2^24 o - 8 C_b (rows g) and
+      // 2^20 o - 8 C_b (rows g+8), C_b from lane 4b + tig of corr.
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const float c0 = -8.0f * __shfl_sync(0xffffffffu, corr[0], 4 * b + tig);
+        const float c1 = -8.0f * __shfl_sync(0xffffffffu, corr[1], 4 * b + tig);
+#pragma unroll
+        for (int mt = 2 * b; mt < 2 * b + 2; ++mt) {
+          o[mt][0] = fmaf(0x1p24f, o[mt][0], c0);
+          o[mt][1] = fmaf(0x1p24f, o[mt][1], c1);
+          o[mt][2] = fmaf(0x1p20f, o[mt][2], c0);
+          o[mt][3] = fmaf(0x1p20f, o[mt][3], c1);
+        }
+      }
     }
 
     // Merge the 8 warps' partials for this segment: 8 -> 4 in pairs, then
@@ -746,7 +851,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     }
 
     useg = seg_end;
+    ++si;
     if (useg < u1) seg = cursor_at(geo, useg);
+  }
+
+  // Query-row copies: segment i's copy is phase i >> 1 of q_bar[i & 1].
+  // Wait (bounded) for the last one issued into each buffer, which has
+  // already completed unless the run was aborted.
+  if (threadIdx.x == 0) {
+    for (int i = q_iss - 1; i >= 0 && i >= q_iss - 2; --i)
+      mbar_wait_bounded(&q_bar[i & 1], static_cast<uint32_t>(i >> 1) & 1u, nullptr, 100000000ull);
   }
 
   // After an aborted run, wait (bounded) for this warp's copies still in
@@ -762,13 +876,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
 template <int CK, int CV>
 cudaError_t launch_split(const DecodeParams &p, int grid, cudaStream_t stream) {
   using C = DecodeCfg<CK, CV>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<CK, CV>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> optin{0};
+  const cudaError_t e = smem_optin(decode_split_kernel<CK, CV>, C::SMEM, optin);
+  if (e != cudaSuccess) return e;
   return launch_pdl(decode_split_kernel<CK, CV>, dim3(grid), dim3(kThreads), C::SMEM, stream, p);
 }
 

@@ -8,6 +8,8 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
 #include "../../include/kvq.h"
@@ -175,6 +177,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase,
 __device__ __forceinline__ uint4 lds128(const void *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
+__device__ __forceinline__ uint2 lds64(const void *p) {
+  return *reinterpret_cast<const uint2 *>(p);
+}
 
 __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
   if (err) atomicOr(err, bit);
@@ -187,6 +192,21 @@ __device__ __forceinline__ void grid_dependency_wait() {
 }
 __device__ __forceinline__ void grid_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
+// Opt `kernel` in to `bytes` of dynamic shared memory on the current device.
+// The setting belongs to the device, so it is made once per device ordinal
+// (`done` holds one bit per ordinal; ordinals >= 64 set it on every call).
+template <typename Kernel>
+inline cudaError_t smem_optin(Kernel kernel, int bytes, std::atomic<uint64_t> &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
 }
 
 // Launch with programmatic stream serialization: the kernel may start while

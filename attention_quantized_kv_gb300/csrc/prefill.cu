@@ -610,12 +610,9 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   ap.n_tiles = n_tiles;
   ap.scale_log2 = scale * 1.4426950408889634f;
   const int smem = (1 + 2 * kStages) * kTileBytes + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    e = cudaFuncSetAttribute(prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> optin{0};
+  e = smem_optin(prefill_attn_kernel, smem, optin);
+  if (e != cudaSuccess) return e;
   const dim3 grid((n_q_tok + kBM - 1) / kBM, L.n_q_heads);
   return launch_pdl(prefill_attn_kernel, grid, dim3(kThreads), smem, stream, ap);
 }

@@ -150,6 +150,7 @@ class OursArm:
         self.layers, self.ws, self.q, self.kn, self.vn = [], [], [], [], []
         self.max_len = max(w.final_lens())
         self.init_lens = torch.tensor(w.lens, dtype=torch.int32, device=device)
+        self.final_lens = torch.tensor(w.final_lens(), dtype=torch.int32, device=device)
         n_tok = w.append_new if w.kind == "prefill" else 1
         for l, (ck, cv) in enumerate(w.codecs):
             L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device)
@@ -193,6 +194,10 @@ class OursArm:
         for L in self.layers:
             L.seq_lens.copy_(self.init_lens)
 
+    def set_final_lens(self):
+        for L in self.layers:
+            L.seq_lens.copy_(self.final_lens)
+
     def launches_per_step(self):
         """Kernels the library launches per step: the append is one kernel
         for at most 64 rows (it also advances the lengths), else the encode
@@ -206,23 +211,24 @@ class OursArm:
             per_layer += 1 if rows <= 64 else 2
         return per_layer * len(self.layers)
 
-    def step(self, ev=None, q=None, kn=None, vn=None):
-        """One pass of the hot path.  ev: optional list of per-layer (start,
-        end) event pairs recorded around each layer's attention call."""
+    def step(self, q=None, kn=None, vn=None, out=None):
+        """One pass of the hot path: every layer's append (when the workload
+        has one) and attention call.  q / kn / vn / out: optional per-layer
+        replacements of the resident tensors."""
         kvq, w = self.kvq, self.w
         for l, L in enumerate(self.layers):
             if w.append_new:
                 kvq.kv_append_quantize(L, (kn or self.kn)[l], (vn or self.vn)[l], self.n_new)
-            if ev is not None:
-                ev[l][0].record()
-            if w.kind == "decode":
-                kvq.attn_decode(L, (q or self.q)[l], self.scale, self.out[l], self.lse[l],
-                                self.max_len, self.ws[l])
-            else:
-                kvq.attn_prefill_chunk(L, 0, w.lens[0], (q or self.q)[l], self.scale,
-                                       self.out[l], self.lse[l], self.ws[l])
-            if ev is not None:
-                ev[l][1].record()
+            self.attention(l, q, out)
+
+    def attention(self, l, q=None, out=None):
+        L, w = self.layers[l], self.w
+        qq, oo = (q or self.q)[l], (out or self.out)[l]
+        if w.kind == "decode":
+            self.kvq.attn_decode(L, qq, self.scale, oo, self.lse[l], self.max_len, self.ws[l])
+        else:
+            self.kvq.attn_prefill_chunk(L, 0, w.lens[0], qq, self.scale, oo, self.lse[l],
+                                        self.ws[l])
 
     def layer_errs(self):
         return [int(L.err.item()) for L in self.layers]
@@ -280,66 +286,35 @@ def run_ours(args, w, rank, world, dist):
         arm.step()
     torch.cuda.synchronize()
 
-    # The timed step is one CUDA graph replay of the whole step (every layer's
-    # append and attention calls, captured through the C ABI); timing events
-    # recorded inside the graph bracket each layer's attention call.
+    # The timed step is one CUDA graph replay of the whole step: every layer's
+    # append and attention calls, captured through the C ABI, so that
+    # consecutive kernels overlap through programmatic dependent launch.
     n_layers = len(arm.layers)
-    try:
-        ev = [(torch.cuda.Event(enable_timing=True, external=True),
-               torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n_layers)]
-    except TypeError:
-        ev = None
-    graphs = None
-    if ev is not None:
-        arm.reset()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            arm.step(ev)
-        graphs = [g]
-        mode = "one CUDA graph per step (timing events inside the graph)"
-    else:  # older torch: one graph per phase, events between replays
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(n_layers)]
-        mode = "CUDA graphs per layer phase"
-        phase_graphs = []
-        arm.reset()
+    arm.reset()
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        arm.step()
+    # The attention calls alone, for the roofline of the attention kernels.
+    # Timing events between the append and the attention kernel would cut
+    # their overlap, so the attention calls are timed in a replay of their own
+    # (lengths already final, L2 flushed the same way).
+    g_attn = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_attn):
         for l in range(n_layers):
-            ga = None
-            if arm.w.append_new:
-                ga = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(ga):
-                    arm.kvq.kv_append_quantize(arm.layers[l], arm.kn[l], arm.vn[l], arm.n_new)
-            gt = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gt):
-                if arm.w.kind == "decode":
-                    arm.kvq.attn_decode(arm.layers[l], arm.q[l], arm.scale, arm.out[l],
-                                        arm.lse[l], arm.max_len, arm.ws[l])
-                else:
-                    arm.kvq.attn_prefill_chunk(arm.layers[l], 0, arm.w.lens[0], arm.q[l],
-                                               arm.scale, arm.out[l], arm.lse[l], arm.ws[l])
-            phase_graphs.append((ga, gt))
+            arm.attention(l)
     torch.cuda.synchronize()
-
-    def replay():
-        if graphs is not None:
-            graphs[0].replay()
-        else:
-            for l, (ga, gt) in enumerate(phase_graphs):
-                if ga is not None:
-                    ga.replay()
-                ev[l][0].record()
-                gt.replay()
-                ev[l][1].record()
+    mode = ("one CUDA graph replay per step, events outside it; attention kernels "
+            "timed in a replay of their own")
 
     for _ in range(3):
         _flush_l2(torch, flush)
         arm.reset()
-        replay()
+        g_step.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
-    # clocks: sampled over a ~1 s window of the same replayed steps that ends
+    # clocks: sampled over a ~1.5 s window of the same replayed steps that ends
     # with the timed region (the timed region alone is far shorter than one
     # nvidia-smi sample period)
     clk = ClockSampler(local)
@@ -350,19 +325,24 @@ def run_ours(args, w, rank, world, dist):
         for _ in range(20):
             _flush_l2(torch, flush)
             arm.reset()
-            replay()
+            g_step.replay()
         torch.cuda.synchronize()
-    step_ms, attn_ms = [], []
-    for _ in range(args.steps):
-        _flush_l2(torch, flush)
-        arm.reset()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        replay()
-        b.record()
-        b.synchronize()
-        step_ms.append(a.elapsed_time(b))
-        attn_ms.extend(x.elapsed_time(y) for x, y in ev)
+
+    def timed(graph, prepare):
+        ms = []
+        for _ in range(args.steps):
+            _flush_l2(torch, flush)
+            prepare()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            graph.replay()
+            b.record()
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return ms
+
+    step_ms = timed(g_step, arm.reset)
+    attn_ms = timed(g_attn, arm.set_final_lens)
     torch.cuda.synchronize()
     clocks = clk.stop()
     if dist:
@@ -372,16 +352,29 @@ def run_ours(args, w, rank, world, dist):
     attn_bytes = sum(per_layer_bytes) * args.steps
     errs = arm.layer_errs()
 
-    # e2e: through the C ABI with pinned host buffers, copies inside the timed region
-    h_q = [q.cpu().pin_memory() for q in arm.q]
-    h_k = [k.cpu().pin_memory() for k in arm.kn]
-    h_v = [v.cpu().pin_memory() for v in arm.vn]
-    h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in arm.out]
-    d_q = [torch.empty_like(q) for q in arm.q]
-    d_k = [torch.empty_like(k) for k in arm.kn]
-    d_v = [torch.empty_like(v) for v in arm.vn]
-    h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v)
-    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    # e2e: through the C ABI with the step's inputs in one pinned host buffer
+    # (one host-to-device copy) and its outputs gathered by one device-to-host
+    # copy, both inside the timed region; calls launched eagerly.
+    ins = arm.q + arm.kn + arm.vn
+    n_in = sum(t.numel() for t in ins)
+    h_in = torch.empty(n_in, dtype=torch.float16, pin_memory=True)
+    d_in = torch.empty(n_in, dtype=torch.float16, device=dev)
+    views, off = [], 0
+    for t in ins:
+        h_in[off:off + t.numel()].copy_(t.flatten().cpu())
+        views.append(d_in[off:off + t.numel()].view(t.shape))
+        off += t.numel()
+    nl = len(arm.q)
+    d_q, d_k, d_v = views[:nl], views[nl:nl + len(arm.kn)], views[nl + len(arm.kn):]
+    n_out = sum(o.numel() for o in arm.out)
+    d_out = torch.empty(n_out, dtype=torch.float16, device=dev)
+    h_out = torch.empty(n_out, dtype=torch.float16, pin_memory=True)
+    out_views, off = [], 0
+    for o in arm.out:
+        out_views.append(d_out[off:off + o.numel()].view(o.shape))
+        off += o.numel()
+    h2d = n_in * 2
+    d2h = n_out * 2
     e2e_ms = []
     for it in range(args.warmup + args.steps):
         _flush_l2(torch, flush)
@@ -389,11 +382,9 @@ def run_ours(args, w, rank, world, dist):
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        for x, y in zip(d_q + d_k + d_v, h_q + h_k + h_v):
-            x.copy_(y, non_blocking=True)
-        arm.step(None, d_q, d_k or None, d_v or None)
-        for x, y in zip(h_out, arm.out):
-            x.copy_(y, non_blocking=True)
+        d_in.copy_(h_in, non_blocking=True)
+        arm.step(d_q, d_k or None, d_v or None, out_views)
+        h_out.copy_(d_out, non_blocking=True)
         b.record()
         b.synchronize()
         if it >= args.warmup:
@@ -452,8 +443,7 @@ def run_ours(args, w, rank, world, dist):
                             "frac": round(achieved_attn / hbm, 4),
                             "traffic": _traffic_for(w.name)}
     else:
-        fl = flops_step / n_layers
-        tfs = fl / (np.mean(attn_ms) * 1e-3) / 1e12
+        tfs = flops_step / (np.mean(attn_ms) * 1e-3) / 1e12
         line["roofline"] = {"bound": "tensor", "kernel": "attn_prefill_chunk",
                             "achieved": round(tfs, 2), "peak": tf, "peak_kind": peak_kind,
                             "unit": "TFLOP/s", "frac": round(tfs / tf, 4),

@@ -145,3 +145,24 @@ def test_workspace_reused_across_calls_and_geometries():
                 if w.lens[s] == 0:
                     assert torch.all(out[s] == 0) and torch.all(torch.isneginf(lse[s]))
     assert torch.count_nonzero(ws[:64]) == 0     # tickets back to zero
+
+
+@pytest.mark.parametrize("ck,cv", [(2, 2), (1, 0)])
+def test_query_rows_only_8_byte_aligned(ck, cv):
+    """q at an 8-byte (not 16-byte) offset takes the direct-load path for the
+    query rows; it must give the same bits as 16-byte aligned rows, and both
+    must match the oracle.  Many short streams put several segments (so
+    several query-row copies, double-buffered) into each CTA."""
+    lens = [40, 700, 33, 512, 1, 95, 300, 64, 129, 250]
+    w = wl.Workload("t", "decode", len(lens), 16, 2, lens, [(ck, cv)], 300 + ck)
+    L = gpu_layer(w, 0)
+    q = wl.queries(w, 0, 1, "cuda")[:, 0].contiguous()
+    raw = torch.empty(q.numel() + 4, dtype=torch.float16, device="cuda")
+    q8 = raw[4:].view(q.shape)
+    q8.copy_(q)
+    assert q.data_ptr() % 16 == 0 and q8.data_ptr() % 16 == 8
+    scale = 1 / math.sqrt(128)
+    out, lse = run_decode(L, q, max(lens), scale)
+    out8, lse8 = run_decode(L, q8, max(lens), scale)
+    assert torch.equal(out, out8) and torch.equal(lse, lse8)
+    check_against_oracle(w, 0, L, q, out, lse, scale)
