@@ -40,8 +40,12 @@ constexpr int kBN = 128;                       // keys per tile
 constexpr int kTileBytes = kBN * kD * 2;       // 32 KB: one side of one tile
 constexpr int kHalfBytes = kTileBytes / 2;     // one 64-dim half
 constexpr int kStages = 2;
-constexpr int kThreads = 256;
-constexpr int kSoftmaxWarp0 = 4;
+// warps 0-3, 4-7: softmax of heads 0, 1; 8: producer; 9: MMA; 10-11 idle.
+// (Registers are allocated to a CTA in groups of four warps, so ten warps
+// would cost as much as twelve.)
+constexpr int kThreads = 384;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
 constexpr float kRescaleThreshold = 8.0f;      // log2 units
 
 // ------------------------------------------------------------------ tcgen05 helpers
@@ -138,6 +142,30 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32])
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+}
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// Element-wise a * b + c and a + b on fp32 pairs, one instruction each.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 
 // Byte offset of element (row, dim) inside a 128-row tile in the operand
@@ -290,30 +318,44 @@ struct AttnParams {
 
 struct __align__(8) AttnBars {
   uint64_t kfull[kStages], vfull[kStages], kempty[kStages], vempty[kStages];
-  uint64_t sfull[2], pfull[2], odone, drain;
+  uint64_t sfull[2], pfull[2], odone[2], drain;
 };
 
+// One CTA per (128-query block, pair of query heads of one kv head): both
+// heads read the same K and V tiles.  Head e of the pair has its own Q tile,
+// S buffer (TMEM columns 128e..), O accumulator (256 + 128e..) and softmax
+// warpgroup (head 0: warps 0-3, head 1: warps 4-7; a warp's TMEM lane
+// quadrant is warp % 4).  The MMA thread issues, per key tile j,
+//   S0(j)  S1(j)  PV0(j)  S0(j+1)  PV1(j)  S1(j+1)  PV0(j+1) ...
+// so that each warpgroup's softmax of tile j overlaps the tensor core's work
+// for the other head.  An S buffer is rewritten only after the PV that read
+// its P, in issue order (tcgen05.mma from one thread executes in order).
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  // 1024-byte aligned operand area: Q (32 KB), K stages, V stages.
+  // 1024-byte aligned operand area: Q0, Q1 (32 KB each), K stages, V stages.
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t *sq = smem;
-  uint8_t *sk = smem + kTileBytes;
+  uint8_t *sk = smem + 2 * kTileBytes;
   uint8_t *sv = sk + kStages * kTileBytes;
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = blockIdx.x, head = blockIdx.y;
-  const int kvh = head / p.G;
+  const int qb = blockIdx.x;
+  const int npairs = (p.G + 1) / 2;
+  const int kvh = blockIdx.y / npairs, hp = blockIdx.y % npairs;
+  const int h0 = kvh * p.G + 2 * hp;
+  const bool two = 2 * hp + 1 < p.G;  // the pair's second head exists
   const int q0 = qb * kBM;
   const int rows = min(kBM, p.n_tok - q0);
   // keys needed: up to the last row's position
   const int key_end = p.q_start + q0 + rows;  // exclusive
   const int n_tiles = (key_end + kBN - 1) / kBN;
   const uint32_t idesc_qk = idesc_f16(0), idesc_pv = idesc_f16(1);
+  // softmax warpgroup of this warp (-1: producer, MMA or idle warp)
+  const int e = warp < 8 ? (warp >> 2) : -1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -325,25 +367,27 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
     for (int b = 0; b < 2; ++b) {
       mbar_init(&bars.sfull[b], 1);
       mbar_init(&bars.pfull[b], 4);  // one arrival per softmax warp
+      mbar_init(&bars.odone[b], 1);
     }
-    mbar_init(&bars.odone, 1);
     mbar_init(&bars.drain, 1);
     abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&tmem_base_sh, 512);
+  if (warp == kMmaWarp) tmem_alloc(&tmem_base_sh, 512);
 
   grid_dependency_wait();  // the dequantized tiles come from the previous kernel
 
-  // Q rows of this block into the operand layout (softmax warpgroup).
-  if (warp >= kSoftmaxWarp0) {
-    const int r = threadIdx.x - kSoftmaxWarp0 * 32;
+  // Q rows of each head into its operand tile (its softmax warpgroup).
+  if (e >= 0) {
+    const int r = (warp & 3) * 32 + lane;
+    uint8_t *dstq = sq + e * kTileBytes;
+    const bool have = r < rows && (e == 0 || two);
     const uint4 *src = reinterpret_cast<const uint4 *>(
-        p.q + (static_cast<int64_t>(q0 + (r < rows ? r : 0)) * p.n_q + head) * kD);
+        p.q + (static_cast<int64_t>(q0 + (have ? r : 0)) * p.n_q + h0 + (two ? e : 0)) * kD);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 v = r < rows ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(sq + tile_offset(r, c * 8)) = v;
+      const uint4 v = have ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4 *>(dstq + tile_offset(r, c * 8)) = v;
     }
     fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
   }
@@ -352,12 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t tm_s[2] = {tmem, tmem + 128};
-  const uint32_t tm_o = tmem + 256;
+  const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
 
   const uint8_t *kt = p.ktiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
   const uint8_t *vt = p.vtiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
 
-  if (warp == 0) {
+  if (warp == kProducerWarp) {
     // ---------------- producer: K and V tiles into the two-stage ring
     if (lane == 0) {
       int k_issued = 0, v_issued = 0;  // tiles whose copies were started
@@ -385,42 +429,65 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
                             nullptr, 100000000ull);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(sq);
-      bool ok = true;
-      for (int j = 0; j <= n_tiles && ok; ++j) {
-        if (j < n_tiles) {  // S_j = Q K_j^T into TMEM buffer j % 2
-          const int s = j % kStages;
-          ok = mbar_wait_bounded(&bars.kfull[s], static_cast<uint32_t>(j / kStages) & 1u, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t k_addr = smem_u32(sk + s * kTileBytes);
+      const uint32_t q_addr[2] = {smem_u32(sq), smem_u32(sq + kTileBytes)};
+      // S_e = Q_e K_j^T into TMEM buffer e
+      auto qk = [&](int eh, int j) {
+        const uint32_t k_addr = smem_u32(sk + (j % kStages) * kTileBytes);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
-            mma_ss(tm_s[j & 1], smem_desc(q_addr + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
-                   idesc_qk, kk > 0);
-          }
-          mma_commit(&bars.sfull[j & 1]);
-          mma_commit(&bars.kempty[s]);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
+          mma_ss(tm_s[eh], smem_desc(q_addr[eh] + off, 16, 1024), smem_desc(k_addr + off, 16, 1024),
+                 idesc_qk, kk > 0);
         }
-        if (j >= 1) {  // O += P_{j-1} V_{j-1}
-          const int jp = j - 1, s = jp % kStages;
-          ok = mbar_wait_bounded(&bars.pfull[jp & 1], static_cast<uint32_t>(jp >> 1) & 1u, &abort_flag) &&
-               mbar_wait_bounded(&bars.vfull[s], static_cast<uint32_t>(jp / kStages) & 1u, &abort_flag);
+        mma_commit(&bars.sfull[eh]);
+      };
+      // O_e += P_e V_j: keys 16kk..16kk+15 are P columns 8kk.. (fp16 pairs)
+      // and V rows 16kk.. (two 8-row groups)
+      auto pv = [&](int eh, int j) {
+        const uint32_t v_addr = smem_u32(sv + (j % kStages) * kTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(tm_o[eh], tm_s[eh] + kk * 8, smem_desc(v_addr + kk * 2048, kHalfBytes, 1024),
+                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&bars.odone[eh]);
+      };
+      bool ok = n_tiles > 0 && mbar_wait_bounded(&bars.kfull[0], 0, &abort_flag);
+      if (ok) {
+        tc_fence_after();
+        qk(0, 0);
+        if (two) qk(1, 0);
+        mma_commit(&bars.kempty[0]);
+      }
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % kStages, s1 = (j + 1) % kStages;
+        const bool more = j + 1 < n_tiles;
+        ok = mbar_wait_bounded(&bars.pfull[0], static_cast<uint32_t>(j) & 1u, &abort_flag) &&
+             mbar_wait_bounded(&bars.vfull[s], static_cast<uint32_t>(j / kStages) & 1u, &abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        pv(0, j);
+        if (!two) mma_commit(&bars.vempty[s]);
+        if (more) {
+          ok = mbar_wait_bounded(&bars.kfull[s1], static_cast<uint32_t>((j + 1) / kStages) & 1u,
+                                 &abort_flag);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t v_addr = smem_u32(sv + s * kTileBytes);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // keys 16kk..16kk+15: P columns 8kk.. (fp16 pairs), V rows 16kk.. (two 8-row groups)
-            mma_ts(tm_o, tm_s[jp & 1] + kk * 8, smem_desc(v_addr + kk * 2048, kHalfBytes, 1024),
-                   idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&bars.odone);
+          qk(0, j + 1);
+          if (!two) mma_commit(&bars.kempty[s1]);
+        }
+        if (two) {
+          ok = mbar_wait_bounded(&bars.pfull[1], static_cast<uint32_t>(j) & 1u, &abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          pv(1, j);
           mma_commit(&bars.vempty[s]);
+          if (more) {
+            qk(1, j + 1);
+            mma_commit(&bars.kempty[s1]);
+          }
         }
       }
       if (!ok) {
@@ -428,44 +495,55 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
         atomicExch(&abort_flag, 1);
       }
       // drain: completes when every MMA this thread issued has finished (the
-      // epilogue waits on it before reading O; TMEM is freed after it).
+      // epilogues wait on it before reading O; TMEM is freed after it).
       mma_commit(&bars.drain);
       mbar_wait_bounded(&bars.drain, 0, nullptr, 100000000ull);
     }
-  } else if (warp >= kSoftmaxWarp0) {
-    // ---------------- softmax warpgroup: thread = query row
-    const int r = threadIdx.x - kSoftmaxWarp0 * 32;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - kSoftmaxWarp0) * 32) << 16;
+  } else if (e == 0 || (e == 1 && two)) {
+    // ---------------- softmax warpgroup of head e: thread = query row
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tms = tm_s[e], tmo = tm_o[e];
     const int pos = p.q_start + q0 + r;  // absolute position of this query
     float m = -INFINITY, l = 0.0f;
     bool ok = true;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      ok = mbar_wait_bounded(&bars.sfull[j & 1], static_cast<uint32_t>(j >> 1) & 1u, &abort_flag);
+      ok = mbar_wait_bounded(&bars.sfull[e], static_cast<uint32_t>(j) & 1u, &abort_flag);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32(tm_s[j & 1] + lane_off + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-      }
-      tmem_wait_ld();
       const int kbase = j * kBN;
-      // Row max of the raw scores (scale > 0 keeps the order), 8 independent
-      // partial maxima; keys past the row's position are masked on diagonal tiles.
-      if (kbase + kBN - 1 > pos) {
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kbase + c > pos) s[c] = -INFINITY;
-      }
+      // Tiles crossing some row's position (warp-uniform test): the scores of
+      // keys past the row's position are overwritten with -inf in TMEM, so
+      // that pass 2 needs no mask.
+      const bool diag = __any_sync(0xffffffffu, kbase + kBN - 1 > pos);
+      // Pass 1: row max of the raw scores (scale > 0 keeps the order), read
+      // from TMEM 64 columns at a time, 8 independent partial maxima of
+      // three-input max instructions.  The row is read again for P (pass 2),
+      // which keeps it out of registers.
       float mp[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mp[i] = s[i];
+      for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+      for (int c = 0; c < 4; c += 2) {
+        float v0[32], v1[32];
+        tmem_ld32(tms + lane_off + c * 32, v0);
+        tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
+        tmem_wait_ld();
+        if (diag) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            if (kbase + c * 32 + i > pos) v0[i] = -INFINITY;
+            if (kbase + (c + 1) * 32 + i > pos) v1[i] = -INFINITY;
+          }
+          tmem_st32f(tms + lane_off + c * 32, v0);
+          tmem_st32f(tms + lane_off + (c + 1) * 32, v1);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) mp[i & 7] = fmax3(mp[i & 7], v0[i], v1[i]);
+      }
+      if (diag) tmem_wait_st();
       const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                              fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
       // Raise a row's running max only when it grew by more than the
@@ -476,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
       const float a = (raise && m != -INFINITY) ? fast_exp2(m - mnew) : 1.0f;
       if (__any_sync(0xffffffffu, raise && m != -INFINITY)) {
         // O holds the sum of P V over tiles < j: wait for the last PV, rescale in TMEM
-        bool got = mbar_wait_bounded(&bars.odone, static_cast<uint32_t>(j - 1) & 1u, &abort_flag);
+        bool got = mbar_wait_bounded(&bars.odone[e], static_cast<uint32_t>(j - 1) & 1u, &abort_flag);
         got = __all_sync(0xffffffffu, got);
         if (!got) {
           ok = false;
@@ -486,43 +564,54 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float v[32];
-          tmem_ld32(tm_o + lane_off + c * 32, v);
+          tmem_ld32(tmo + lane_off + c * 32, v);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] *= a;
-          tmem_st32f(tm_o + lane_off + c * 32, v);
+          tmem_st32f(tmo + lane_off + c * 32, v);
         }
         tmem_wait_st();
       }
       l *= a;
       m = mnew;
-      // P = exp2(s * scale_log2 - m) as fp16 pairs over the first 64 columns
-      // of the S buffer; the row sum in 8 independent partials.
-      float sp[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
-      const float nm = -m;
+      // Pass 2: P = exp2(s * scale_log2 - m) as fp16 pairs over the first 64
+      // columns of the S buffer (P chunk c lands on columns already read);
+      // scale-and-offset and the row sum (4 partial pairs) in f32x2 ops.
+      float2 sp2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                       make_float2(0.0f, 0.0f)};
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+      for (int c = 0; c < 4; c += 2) {
+        float v0[32], v1[32];
+        tmem_ld32(tms + lane_off + c * 32, v0);
+        tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float a = fast_exp2(fmaf(s[c * 32 + 2 * i], p.scale_log2, nm));
-          const float b = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], p.scale_log2, nm));
-          sp[(2 * i) & 7] += a;
-          sp[(2 * i + 1) & 7] += b;
-          pk[i] = pack_half2(a, b);
+        for (int h = 0; h < 2; ++h) {
+          const float *v = h ? v1 : v0;
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 t = fma2(make_float2(v[2 * i], v[2 * i + 1]), sc2, nm2);
+            const float2 x = make_float2(fast_exp2(t.x), fast_exp2(t.y));
+            sp2[i & 3] = add2(sp2[i & 3], x);
+            pk[i] = pack_half2(x.x, x.y);
+          }
+          tmem_st16(tms + lane_off + (c + h) * 16, pk);
         }
-        tmem_st16(tm_s[j & 1] + lane_off + c * 16, pk);
       }
-      const float rs = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float2 s01 = add2(sp2[0], sp2[1]), s23 = add2(sp2[2], sp2[3]);
+      const float2 s4 = add2(s01, s23);
+      const float rs = s4.x + s4.y;
+
       l += rs;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pfull[j & 1]);
+      if (lane == 0) mbar_arrive(&bars.pfull[e]);
     }
     // epilogue: wait until every MMA has finished (the single-use drain
-    // barrier; a parity wait on odone could alias with the previous phase),
-    // normalise, store the row
+    // barrier), normalise, store the row
     if (ok) ok = mbar_wait_bounded(&bars.drain, 0, &abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok && lane == 0) {
@@ -531,11 +620,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
     }
     tc_fence_after();
     const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
+    const int head = h0 + e;
     __half *dst = p.out + (static_cast<int64_t>(q0 + r) * p.n_q + head) * kD;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float v[32];
-      tmem_ld32(tm_o + lane_off + c * 32, v);
+      tmem_ld32(tmo + lane_off + c * 32, v);
       tmem_wait_ld();
       if (r < rows) {
         uint32_t w[16];
@@ -554,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -609,11 +699,12 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   ap.kv_len = static_cast<int>(pl.kv_tokens);
   ap.n_tiles = n_tiles;
   ap.scale_log2 = scale * 1.4426950408889634f;
-  const int smem = (1 + 2 * kStages) * kTileBytes + 1024;
+  const int smem = (2 + 2 * kStages) * kTileBytes + 1024;
   static std::atomic<uint64_t> optin{0};
   e = smem_optin(prefill_attn_kernel, smem, optin);
   if (e != cudaSuccess) return e;
-  const dim3 grid((n_q_tok + kBM - 1) / kBM, L.n_q_heads);
+  const int G = L.n_q_heads / L.n_kv_heads;
+  const dim3 grid((n_q_tok + kBM - 1) / kBM, L.n_kv_heads * ((G + 1) / 2));
   return launch_pdl(prefill_attn_kernel, grid, dim3(kThreads), smem, stream, ap);
 }
 
