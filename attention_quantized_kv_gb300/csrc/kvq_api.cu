@@ -134,7 +134,9 @@ int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int32_t n_q_
   if (st != KVQ_OK) return st;
   if (!bytes || q_start < 0 || n_q_tok <= 0) return KVQ_EINVAL;
   if (static_cast<int64_t>(q_start) + n_q_tok > layer->capacity) return KVQ_ECAPACITY;
-  *bytes = static_cast<size_t>(kvq::plan_prefill(*layer, q_start, n_q_tok).ws_bytes);
+  const kvq::PrefillPlan pl =
+      kvq::plan_prefill(*layer, q_start, n_q_tok, device_sms());
+  *bytes = static_cast<size_t>(pl.ws_bytes);
   return KVQ_OK;
 }
 
@@ -150,7 +152,8 @@ int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int
   if (!aligned(q, 16) || !aligned(out, 16) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;
   if (!workspace) return KVQ_EWORKSPACE;
   if (!aligned(workspace, 16)) return KVQ_EALIGN;
-  const kvq::PrefillPlan pl = kvq::plan_prefill(*layer, q_start, n_q_tok);
+  const kvq::PrefillPlan pl =
+      kvq::plan_prefill(*layer, q_start, n_q_tok, device_sms());
   if (ws_bytes < static_cast<size_t>(pl.ws_bytes)) return KVQ_EWORKSPACE;
   const cudaError_t e = kvq::launch_prefill(*layer, pl, seq, q_start, n_q_tok, q, scale, out, lse,
                                             workspace, static_cast<cudaStream_t>(stream));

@@ -35,11 +35,16 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
 struct PrefillPlan {
   int64_t kv_tokens = 0;     // keys attended by the chunk: q_start + n_q_tok
   int64_t kv_tokens_pad = 0; // rounded up to the attention tile
-  int64_t ws_k_bytes = 0;    // fp16 K staging [n_kv][kv_tokens_pad][128]
+  int64_t ws_k_bytes = 0;    // fp16 K staging [n_kv][kv_tokens_pad][128] (V the same)
+  int npairs = 0, n_qt = 0;  // query-head pairs per kv head, 128-query tiles
+  int64_t n_items = 0;       // (kv head, head pair, query tile) work items
+  int64_t Tq = 0, W = 0;     // key-tile steps per (kv head, pair); in all
+  int64_t grid = 0;          // persistent CTAs (at most one per SM)
+  int64_t ticket_off = 0, part_off = 0, part_bytes = 0;
   int64_t ws_bytes = 0;
 };
 
-PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok);
+PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok, int num_sms);
 cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, int q_start,
                            int n_q_tok, const void *q, float scale, void *out, float *lse,
                            void *workspace, cudaStream_t stream);

@@ -27,6 +27,8 @@
 //     exact (the same max scales O and l).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include <math.h>
 
 #include "kvq_device.cuh"
@@ -239,7 +241,8 @@ struct DequantParams {
   uint8_t *tiles[2];   // [n_kv][n_tiles][32 KB]
   const int32_t *seq_lens;
   int32_t *err;
-  int seq, n_kv, capacity, kv_len, n_tiles;
+  unsigned *tickets;  // the attention kernel's arrival counters, zeroed here
+  int seq, n_kv, capacity, kv_len, n_tiles, n_items;
 };
 
 // grid: (n_tiles, n_kv, 2 sides); 256 threads.  The tile's eight 16-token
@@ -287,9 +290,10 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
 __global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams p) {
   __shared__ __align__(16) uint8_t units_sh[kBN / kUnitTokens * 4096];
   grid_dependency_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
-      p.seq_lens[p.seq] < p.kv_len)
-    set_err(p.err, KVQ_DEVERR_SEQLEN);
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    if (threadIdx.x == 0 && p.seq_lens[p.seq] < p.kv_len) set_err(p.err, KVQ_DEVERR_SEQLEN);
+    for (int i = threadIdx.x; i < p.n_items; i += blockDim.x) p.tickets[i] = 0u;
+  }
   const int side = blockIdx.z, codec = p.codec[side];
   if (side == 0) {
     if (codec == KVQ_F16) dequant_tile<KVQ_F16, 0>(p, units_sh);
@@ -312,16 +316,77 @@ struct AttnParams {
   __half *out;
   float *lse;
   int32_t *err;
+  float *part;            // partial slots [slot][2][128][kPartStride]: O (unnormalised), m, l
+  unsigned *tickets;      // [n_items] arrival counters (zeroed by the dequant kernel)
   int n_q, G, n_tok, q_start, kv_len, n_tiles;
+  int npairs, n_qt, n_items;
+  int64_t Tq;             // key-tile steps of one (kv head, head pair) group: sum over q tiles
+  int64_t W;              // all key-tile steps: groups * Tq
   float scale_log2;
 };
 
+constexpr int kPartStride = 132;  // floats per partial row: 128 O, m, l, 2 pad (16-byte rows)
+
 struct __align__(8) AttnBars {
   uint64_t kfull[kStages], vfull[kStages], kempty[kStages], vempty[kStages];
-  uint64_t sfull[2], pfull[2], odone[2], drain;
+  uint64_t sfull[2], pfull[2], odone[2], segdone[2], qready[2], ofree[2], drain;
 };
 
-// One CTA per (128-query block, pair of query heads of one kv head): both
+// Key tiles attended by query tile qt (128 rows; the last may be short).
+__device__ __forceinline__ int qt_tiles(const AttnParams &p, int qt) {
+  const int rows_end = min(kBM * (qt + 1), p.n_tok);
+  return (p.q_start + rows_end + kBN - 1) / kBN;
+}
+
+// The work is the list of items (group g = kv head * npairs + head pair,
+// query tile qt), item index g * n_qt + qt, each item a run of qt_tiles(qt)
+// key-tile steps.  CTA c takes the steps [W c / P, W (c + 1) / P): whole
+// items, plus pieces of the first and last ones.  A segment is one item's
+// piece [j_lo, j_hi) of key tiles.
+struct Segment {
+  int g, qt, j_lo, j_hi, nt;  // nt: the item's key tiles
+  int64_t start;              // the item's first step
+};
+struct SegIter {
+  int64_t s, s1;
+  int g, qt;
+  int64_t item_start;  // first step of item (g, qt)
+  __device__ __forceinline__ void init(const AttnParams &p, int64_t s0, int64_t s_end) {
+    s = s0;
+    s1 = s_end;
+    g = static_cast<int>(s0 / p.Tq);
+    int64_t base = static_cast<int64_t>(g) * p.Tq;
+    qt = 0;
+    while (qt + 1 < p.n_qt && base + qt_tiles(p, qt) <= s0) {
+      base += qt_tiles(p, qt);
+      ++qt;
+    }
+    item_start = base;
+  }
+  __device__ __forceinline__ bool next(const AttnParams &p, Segment &seg) {
+    if (s >= s1) return false;
+    const int nt = qt_tiles(p, qt);
+    seg.g = g;
+    seg.qt = qt;
+    seg.nt = nt;
+    seg.start = item_start;
+    seg.j_lo = static_cast<int>(s - item_start);
+    const int64_t end = min(s1, item_start + nt);
+    seg.j_hi = static_cast<int>(end - item_start);
+    s = end;
+    if (end == item_start + nt) {  // on to the next item
+      item_start += nt;
+      if (++qt == p.n_qt) {
+        qt = 0;
+        ++g;
+      }
+    }
+    return true;
+  }
+};
+
+// Persistent CTAs (one per SM) over a balanced split of the key-tile steps of
+// all (128-query block, pair of query heads of one kv head) items: both
 // heads read the same K and V tiles.  Head e of the pair has its own Q tile,
 // S buffer (TMEM columns 128e..), O accumulator (256 + 128e..) and softmax
 // warpgroup (head 0: warps 0-3, head 1: warps 4-7; a warp's TMEM lane
@@ -330,7 +395,14 @@ struct __align__(8) AttnBars {
 // so that each warpgroup's softmax of tile j overlaps the tensor core's work
 // for the other head.  An S buffer is rewritten only after the PV that read
 // its P, in issue order (tcgen05.mma from one thread executes in order).
+// A segment that covers a whole item writes its rows; the pieces of a split
+// item are written as partials (unnormalised O, m, l), and the last CTA to
+// finish a piece of the item (a ticket) merges them (log-sum-exp).
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnParams p) {
+  const int64_t P = gridDim.x;
+  const int64_t s0 = p.W * blockIdx.x / P, s1 = p.W * (blockIdx.x + 1) / P;
+  if (s0 >= s1) return;  // whole CTA: no work (the grid is at most W, so never)
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte aligned operand area: Q0, Q1 (32 KB each), K stages, V stages.
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -341,21 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ int last_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qb = blockIdx.x;
-  const int npairs = (p.G + 1) / 2;
-  const int kvh = blockIdx.y / npairs, hp = blockIdx.y % npairs;
-  const int h0 = kvh * p.G + 2 * hp;
-  const bool two = 2 * hp + 1 < p.G;  // the pair's second head exists
-  const int q0 = qb * kBM;
-  const int rows = min(kBM, p.n_tok - q0);
-  // keys needed: up to the last row's position
-  const int key_end = p.q_start + q0 + rows;  // exclusive
-  const int n_tiles = (key_end + kBN - 1) / kBN;
   const uint32_t idesc_qk = idesc_f16(0), idesc_pv = idesc_f16(1);
   // softmax warpgroup of this warp (-1: producer, MMA or idle warp)
   const int e = warp < 8 ? (warp >> 2) : -1;
+  auto seg_two = [&](const Segment &sg) { return 2 * (sg.g % p.npairs) + 1 < p.G; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -368,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
       mbar_init(&bars.sfull[b], 1);
       mbar_init(&bars.pfull[b], 4);  // one arrival per softmax warp
       mbar_init(&bars.odone[b], 1);
+      mbar_init(&bars.segdone[b], 1);
+      mbar_init(&bars.qready[b], 4);  // the segment's Q written, one arrival per warp
+      mbar_init(&bars.ofree[b], 4);   // the segment's O read, one arrival per warp
     }
     mbar_init(&bars.drain, 1);
     abort_flag = 0;
@@ -377,20 +444,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
 
   grid_dependency_wait();  // the dequantized tiles come from the previous kernel
 
-  // Q rows of each head into its operand tile (its softmax warpgroup).
-  if (e >= 0) {
-    const int r = (warp & 3) * 32 + lane;
-    uint8_t *dstq = sq + e * kTileBytes;
-    const bool have = r < rows && (e == 0 || two);
-    const uint4 *src = reinterpret_cast<const uint4 *>(
-        p.q + (static_cast<int64_t>(q0 + (have ? r : 0)) * p.n_q + h0 + (two ? e : 0)) * kD);
-#pragma unroll
-    for (int c = 0; c < 16; ++c) {
-      const uint4 v = have ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-      *reinterpret_cast<uint4 *>(dstq + tile_offset(r, c * 8)) = v;
-    }
-    fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -398,44 +451,54 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
   const uint32_t tm_s[2] = {tmem, tmem + 128};
   const uint32_t tm_o[2] = {tmem + 256, tmem + 384};
 
-  const uint8_t *kt = p.ktiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
-  const uint8_t *vt = p.vtiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
-
   if (warp == kProducerWarp) {
     // ---------------- producer: K and V tiles into the two-stage ring
     if (lane == 0) {
-      int k_issued = 0, v_issued = 0;  // tiles whose copies were started
-      for (int j = 0; j < n_tiles; ++j) {
-        const int s = j % kStages;
-        const uint32_t ph = static_cast<uint32_t>(j / kStages - 1) & 1u;
-        if (j >= kStages && !mbar_wait_bounded(&bars.kempty[s], ph, &abort_flag)) break;
-        mbar_arrive_expect_tx(&bars.kfull[s], kTileBytes);
-        bulk_copy_g2s(sk + s * kTileBytes, kt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
-                      &bars.kfull[s]);
-        k_issued = j + 1;
-        if (j >= kStages && !mbar_wait_bounded(&bars.vempty[s], ph, &abort_flag)) break;
-        mbar_arrive_expect_tx(&bars.vfull[s], kTileBytes);
-        bulk_copy_g2s(sv + s * kTileBytes, vt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
-                      &bars.vfull[s]);
-        v_issued = j + 1;
+      SegIter it;
+      it.init(p, s0, s1);
+      Segment sg;
+      int t = 0;  // tiles issued by this CTA
+      bool ok = true;
+      while (ok && it.next(p, sg)) {
+        const int kvh = sg.g / p.npairs;
+        const uint8_t *kt = p.ktiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
+        const uint8_t *vt = p.vtiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
+        for (int j = sg.j_lo; j < sg.j_hi; ++j, ++t) {
+          const int s = t % kStages;
+          const uint32_t ph = static_cast<uint32_t>(t / kStages - 1) & 1u;
+          if (t >= kStages && !mbar_wait_bounded(&bars.kempty[s], ph, &abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars.kfull[s], kTileBytes);
+          bulk_copy_g2s(sk + s * kTileBytes, kt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
+                        &bars.kfull[s]);
+          if (t >= kStages && !mbar_wait_bounded(&bars.vempty[s], ph, &abort_flag)) {
+            // the V copy of this tile was not started: drain below counts t + 1 K copies
+            mbar_wait_bounded(&bars.kfull[s], static_cast<uint32_t>(t / kStages) & 1u, nullptr,
+                              100000000ull);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.vfull[s], kTileBytes);
+          bulk_copy_g2s(sv + s * kTileBytes, vt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
+                        &bars.vfull[s]);
+        }
       }
       // After an abort, wait (bounded) for the copies still landing in the ring.
-      if (*reinterpret_cast<volatile int *>(&abort_flag)) {
-        for (int j = max(0, k_issued - kStages); j < k_issued; ++j)
-          mbar_wait_bounded(&bars.kfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1u,
+      if (!ok || *reinterpret_cast<volatile int *>(&abort_flag)) {
+        for (int u = max(0, t - kStages); u < t; ++u) {
+          mbar_wait_bounded(&bars.kfull[u % kStages], static_cast<uint32_t>(u / kStages) & 1u,
                             nullptr, 100000000ull);
-        for (int j = max(0, v_issued - kStages); j < v_issued; ++j)
-          mbar_wait_bounded(&bars.vfull[j % kStages], static_cast<uint32_t>(j / kStages) & 1u,
+          mbar_wait_bounded(&bars.vfull[u % kStages], static_cast<uint32_t>(u / kStages) & 1u,
                             nullptr, 100000000ull);
+        }
       }
     }
   } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer (one thread)
     if (lane == 0) {
       const uint32_t q_addr[2] = {smem_u32(sq), smem_u32(sq + kTileBytes)};
-      // S_e = Q_e K_j^T into TMEM buffer e
-      auto qk = [&](int eh, int j) {
-        const uint32_t k_addr = smem_u32(sk + (j % kStages) * kTileBytes);
+      // S_e = Q_e K^T of ring tile t into TMEM buffer e
+      auto qk = [&](int eh, int t) {
+        const uint32_t k_addr = smem_u32(sk + (t % kStages) * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t off = (kk >> 2) * kHalfBytes + (kk & 3) * 32;
@@ -444,202 +507,375 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
         }
         mma_commit(&bars.sfull[eh]);
       };
-      // O_e += P_e V_j: keys 16kk..16kk+15 are P columns 8kk.. (fp16 pairs)
-      // and V rows 16kk.. (two 8-row groups)
-      auto pv = [&](int eh, int j) {
-        const uint32_t v_addr = smem_u32(sv + (j % kStages) * kTileBytes);
+      // O_e (+)= P_e V of ring tile t: keys 16kk..16kk+15 are P columns 8kk..
+      // (fp16 pairs) and V rows 16kk.. (two 8-row groups)
+      auto pv = [&](int eh, int t, bool first) {
+        const uint32_t v_addr = smem_u32(sv + (t % kStages) * kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           mma_ts(tm_o[eh], tm_s[eh] + kk * 8, smem_desc(v_addr + kk * 2048, kHalfBytes, 1024),
-                 idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                 idesc_pv, (!first || kk > 0) ? 1u : 0u);
         mma_commit(&bars.odone[eh]);
       };
-      bool ok = n_tiles > 0 && mbar_wait_bounded(&bars.kfull[0], 0, &abort_flag);
-      if (ok) {
-        tc_fence_after();
-        qk(0, 0);
-        if (two) qk(1, 0);
-        mma_commit(&bars.kempty[0]);
-      }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j % kStages, s1 = (j + 1) % kStages;
-        const bool more = j + 1 < n_tiles;
-        ok = mbar_wait_bounded(&bars.pfull[0], static_cast<uint32_t>(j) & 1u, &abort_flag) &&
-             mbar_wait_bounded(&bars.vfull[s], static_cast<uint32_t>(j / kStages) & 1u, &abort_flag);
+      SegIter it;
+      it.init(p, s0, s1);
+      Segment sg;
+      int t = 0;            // ring tile index
+      int u[2] = {0, 0};    // tiles per head (sfull / pfull / odone phases)
+      int k[2] = {0, 0};    // segments per head (ready / segdone phases)
+      bool ok = true;
+      while (ok && it.next(p, sg)) {
+        const bool two = seg_two(sg);
+        const int n = sg.j_hi - sg.j_lo;
+        // Q of this segment written (its S can start while the previous
+        // segment's O is still being read; the first PV waits for that)
+        ok = mbar_wait_bounded(&bars.qready[0], static_cast<uint32_t>(k[0]) & 1u, &abort_flag) &&
+             (!two || mbar_wait_bounded(&bars.qready[1], static_cast<uint32_t>(k[1]) & 1u, &abort_flag)) &&
+             mbar_wait_bounded(&bars.kfull[t % kStages], static_cast<uint32_t>(t / kStages) & 1u,
+                               &abort_flag);
         if (!ok) break;
         tc_fence_after();
-        pv(0, j);
-        if (!two) mma_commit(&bars.vempty[s]);
-        if (more) {
-          ok = mbar_wait_bounded(&bars.kfull[s1], static_cast<uint32_t>((j + 1) / kStages) & 1u,
-                                 &abort_flag);
+        qk(0, t);
+        if (two) qk(1, t);
+        mma_commit(&bars.kempty[t % kStages]);
+        for (int jj = 0; jj < n && ok; ++jj, ++t) {
+          const int s = t % kStages;
+          const bool more = jj + 1 < n;
+          ok = mbar_wait_bounded(&bars.pfull[0], static_cast<uint32_t>(u[0]) & 1u, &abort_flag) &&
+               mbar_wait_bounded(&bars.vfull[s], static_cast<uint32_t>(t / kStages) & 1u, &abort_flag) &&
+               (jj > 0 || k[0] == 0 ||
+                mbar_wait_bounded(&bars.ofree[0], static_cast<uint32_t>(k[0] - 1) & 1u, &abort_flag));
           if (!ok) break;
           tc_fence_after();
-          qk(0, j + 1);
-          if (!two) mma_commit(&bars.kempty[s1]);
-        }
-        if (two) {
-          ok = mbar_wait_bounded(&bars.pfull[1], static_cast<uint32_t>(j) & 1u, &abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          pv(1, j);
-          mma_commit(&bars.vempty[s]);
+          pv(0, t, jj == 0);
+          ++u[0];
+          if (!two) mma_commit(&bars.vempty[s]);
           if (more) {
-            qk(1, j + 1);
-            mma_commit(&bars.kempty[s1]);
+            ok = mbar_wait_bounded(&bars.kfull[(t + 1) % kStages],
+                                   static_cast<uint32_t>((t + 1) / kStages) & 1u, &abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            qk(0, t + 1);
+            if (!two) mma_commit(&bars.kempty[(t + 1) % kStages]);
           }
+          if (two) {
+            ok = mbar_wait_bounded(&bars.pfull[1], static_cast<uint32_t>(u[1]) & 1u, &abort_flag) &&
+                 (jj > 0 || k[1] == 0 ||
+                  mbar_wait_bounded(&bars.ofree[1], static_cast<uint32_t>(k[1] - 1) & 1u, &abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            pv(1, t, jj == 0);
+            ++u[1];
+            mma_commit(&bars.vempty[s]);
+            if (more) {
+              qk(1, t + 1);
+              mma_commit(&bars.kempty[(t + 1) % kStages]);
+            }
+          }
+        }
+        if (!ok) break;
+        // the segment's O is complete once every MMA issued so far is
+        mma_commit(&bars.segdone[0]);
+        ++k[0];
+        if (two) {
+          mma_commit(&bars.segdone[1]);
+          ++k[1];
         }
       }
       if (!ok) {
         set_err(p.err, KVQ_DEVERR_TIMEOUT);
         atomicExch(&abort_flag, 1);
       }
-      // drain: completes when every MMA this thread issued has finished (the
-      // epilogues wait on it before reading O; TMEM is freed after it).
+      // drain: completes when every MMA this thread issued has finished
+      // (TMEM is freed after it).
       mma_commit(&bars.drain);
       mbar_wait_bounded(&bars.drain, 0, nullptr, 100000000ull);
     }
-  } else if (e == 0 || (e == 1 && two)) {
+  } else if (e >= 0) {
     // ---------------- softmax warpgroup of head e: thread = query row
     const int quad = warp & 3;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tms = tm_s[e], tmo = tm_o[e];
-    const int pos = p.q_start + q0 + r;  // absolute position of this query
-    float m = -INFINITY, l = 0.0f;
+    uint8_t *dstq = sq + e * kTileBytes;
+    SegIter it;
+    it.init(p, s0, s1);
+    Segment sg;
+    int u = 0, kseg = 0;  // tiles and segments of this head
     bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      ok = mbar_wait_bounded(&bars.sfull[e], static_cast<uint32_t>(j) & 1u, &abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      const int kbase = j * kBN;
-      // Tiles crossing some row's position (warp-uniform test): the scores of
-      // keys past the row's position are overwritten with -inf in TMEM, so
-      // that pass 2 needs no mask.
-      const bool diag = __any_sync(0xffffffffu, kbase + kBN - 1 > pos);
-      // Pass 1: row max of the raw scores (scale > 0 keeps the order), read
-      // from TMEM 64 columns at a time, 8 independent partial maxima of
-      // three-input max instructions.  The row is read again for P (pass 2),
-      // which keeps it out of registers.
-      float mp[8];
+    // Q rows of this head of segment `q` into its operand tile, then tell the
+    // MMA thread.
+    auto load_q = [&](const Segment &q) {
+      const int hq = (q.g / p.npairs) * p.G + 2 * (q.g % p.npairs) + e;
+      const int qq0 = q.qt * kBM;
+      const bool have = r < min(kBM, p.n_tok - qq0);
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+          p.q + (static_cast<int64_t>(qq0 + (have ? r : 0)) * p.n_q + hq) * kD);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float v0[32], v1[32];
-        tmem_ld32(tms + lane_off + c * 32, v0);
-        tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
-        tmem_wait_ld();
-        if (diag) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (kbase + c * 32 + i > pos) v0[i] = -INFINITY;
-            if (kbase + (c + 1) * 32 + i > pos) v1[i] = -INFINITY;
-          }
-          tmem_st32f(tms + lane_off + c * 32, v0);
-          tmem_st32f(tms + lane_off + (c + 1) * 32, v1);
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i) mp[i & 7] = fmax3(mp[i & 7], v0[i], v1[i]);
+      for (int c = 0; c < 16; ++c) {
+        const uint4 v = have ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(dstq + tile_offset(r, c * 8)) = v;
       }
-      if (diag) tmem_wait_st();
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
-      // Raise a row's running max only when it grew by more than the
-      // threshold.  tcgen05.ld/st are warp-collective, so the O rescale runs
-      // for the whole warp when any of its rows needs it (factor 1 elsewhere).
-      const bool raise = mx > m + kRescaleThreshold || m == -INFINITY;
-      const float mnew = raise ? fmaxf(mx, m) : m;
-      const float a = (raise && m != -INFINITY) ? fast_exp2(m - mnew) : 1.0f;
-      if (__any_sync(0xffffffffu, raise && m != -INFINITY)) {
-        // O holds the sum of P V over tiles < j: wait for the last PV, rescale in TMEM
-        bool got = mbar_wait_bounded(&bars.odone[e], static_cast<uint32_t>(j - 1) & 1u, &abort_flag);
-        got = __all_sync(0xffffffffu, got);
-        if (!got) {
-          ok = false;
+      fence_proxy_async_smem();  // generic-proxy writes, read by the tensor core
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.qready[e]);
+    };
+    // the next segment this head takes part in (e == 1 skips single heads)
+    auto next_mine = [&](SegIter &i2, Segment &q) {
+      while (i2.next(p, q))
+        if (e == 0 || seg_two(q)) return true;
+      return false;
+    };
+    bool have_seg = next_mine(it, sg);
+    if (have_seg) load_q(sg);
+    while (have_seg) {
+      const bool two = seg_two(sg);
+      const int kvh = sg.g / p.npairs, hp = sg.g % p.npairs;
+      const int head = kvh * p.G + 2 * hp + e;
+      const int q0 = sg.qt * kBM;
+      const int rows = min(kBM, p.n_tok - q0);
+      const int pos = p.q_start + q0 + r;  // absolute position of this query
+      float m = -INFINITY, l = 0.0f;
+      // After an abort (ok false) the segment loop still runs to the end with
+      // no waits, so that both warpgroups pass the same named barriers.
+      for (int j = sg.j_lo; j < sg.j_hi && ok; ++j, ++u) {
+        ok = mbar_wait_bounded(&bars.sfull[e], static_cast<uint32_t>(u) & 1u, &abort_flag);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+          if (lane == 0) atomicExch(&abort_flag, 1);
           break;
         }
         tc_fence_after();
+        const int kbase = j * kBN;
+        // Tiles crossing some row's position (warp-uniform test): the scores of
+        // keys past the row's position are overwritten with -inf in TMEM, so
+        // that pass 2 needs no mask.
+        const bool diag = __any_sync(0xffffffffu, kbase + kBN - 1 > pos);
+        // Pass 1: row max of the raw scores (scale > 0 keeps the order), read
+        // from TMEM 64 columns at a time, 8 independent partial maxima of
+        // three-input max instructions.  The row is read again for P (pass 2),
+        // which keeps it out of registers.
+        float mp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; c += 2) {
+          float v0[32], v1[32];
+          tmem_ld32(tms + lane_off + c * 32, v0);
+          tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
+          tmem_wait_ld();
+          if (diag) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              if (kbase + c * 32 + i > pos) v0[i] = -INFINITY;
+              if (kbase + (c + 1) * 32 + i > pos) v1[i] = -INFINITY;
+            }
+            tmem_st32f(tms + lane_off + c * 32, v0);
+            tmem_st32f(tms + lane_off + (c + 1) * 32, v1);
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mp[i & 7] = fmax3(mp[i & 7], v0[i], v1[i]);
+        }
+        if (diag) tmem_wait_st();
+        const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * p.scale_log2;
+        // Raise a row's running max only when it grew by more than the
+        // threshold.  tcgen05.ld/st are warp-collective, so the O rescale runs
+        // for the whole warp when any of its rows needs it (factor 1 elsewhere).
+        const bool raise = mx > m + kRescaleThreshold || m == -INFINITY;
+        const float mnew = raise ? fmaxf(mx, m) : m;
+        const float a = (raise && m != -INFINITY) ? fast_exp2(m - mnew) : 1.0f;
+        if (__any_sync(0xffffffffu, raise && m != -INFINITY)) {
+          // O holds the sum of P V over this segment's earlier tiles: wait for
+          // the last PV (tile u - 1 of this head), rescale in TMEM
+          bool got = mbar_wait_bounded(&bars.odone[e], static_cast<uint32_t>(u - 1) & 1u, &abort_flag);
+          got = __all_sync(0xffffffffu, got);
+          if (!got) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            float v[32];
+            tmem_ld32(tmo + lane_off + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] *= a;
+            tmem_st32f(tmo + lane_off + c * 32, v);
+          }
+          tmem_wait_st();
+        }
+        l *= a;
+        m = mnew;
+        // Pass 2: P = exp2(s * scale_log2 - m) as fp16 pairs over the first 64
+        // columns of the S buffer (P chunk c lands on columns already read);
+        // scale-and-offset and the row sum (4 partial pairs) in f32x2 ops.
+        float2 sp2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                         make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        // A piece of an item past some rows' positions leaves those rows with
+        // every key masked (m = -inf): their P is 0, not exp2(-inf + inf).
+        const float nm = m == -INFINITY ? 0.0f : -m;
+        const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(nm, nm);
+#pragma unroll
+        for (int c = 0; c < 4; c += 2) {
+          float v0[32], v1[32];
+          tmem_ld32(tms + lane_off + c * 32, v0);
+          tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float *v = h ? v1 : v0;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float2 tt = fma2(make_float2(v[2 * i], v[2 * i + 1]), sc2, nm2);
+              const float2 x = make_float2(fast_exp2(tt.x), fast_exp2(tt.y));
+              sp2[i & 3] = add2(sp2[i & 3], x);
+              pk[i] = pack_half2(x.x, x.y);
+            }
+            tmem_st16(tms + lane_off + (c + h) * 16, pk);
+          }
+        }
+        const float2 s01 = add2(sp2[0], sp2[1]), s23 = add2(sp2[2], sp2[3]);
+        const float2 s4 = add2(s01, s23);
+        l += s4.x + s4.y;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.pfull[e]);
+      }
+      // The next segment's Q can go in now: this segment's last S has been
+      // read, so its QK MMAs are done with the Q tile.
+      Segment nsg;
+      const bool have_next = next_mine(it, nsg);
+      if (have_next) load_q(nsg);
+      // the segment's O: wait for its last MMA
+      if (ok) ok = mbar_wait_bounded(&bars.segdone[e], static_cast<uint32_t>(kseg) & 1u, &abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      ++kseg;
+      tc_fence_after();
+      const bool whole = sg.j_lo == 0 && sg.j_hi == sg.nt;
+      const int64_t item = static_cast<int64_t>(sg.g) * p.n_qt + sg.qt;
+      const int64_t row = static_cast<int64_t>(q0 + r) * p.n_q + head;
+      float *prow = p.part +
+                    ((static_cast<int64_t>(blockIdx.x) + item) * 2 * kBM + e * kBM + r) * kPartStride;
+      if (whole) {
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+        __half *dst = p.out + row * kD;
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           float v[32];
           tmem_ld32(tmo + lane_off + c * 32, v);
           tmem_wait_ld();
+          if (r < rows) {
+            uint32_t w[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] *= a;
-          tmem_st32f(tmo + lane_off + c * 32, v);
+            for (int i = 0; i < 16; ++i) w[i] = pack_half2(v[2 * i] * inv, v[2 * i + 1] * inv);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              reinterpret_cast<uint4 *>(dst + c * 32)[i] =
+                  make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+          }
         }
-        tmem_wait_st();
+        tc_fence_before();  // O read: the next segment's first PV may overwrite it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars.ofree[e]);
+        if (p.lse && r < rows)
+          p.lse[row] = l > 0.0f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+        sg = nsg;
+        have_seg = have_next;
+        continue;
       }
-      l *= a;
-      m = mnew;
-      // Pass 2: P = exp2(s * scale_log2 - m) as fp16 pairs over the first 64
-      // columns of the S buffer (P chunk c lands on columns already read);
-      // scale-and-offset and the row sum (4 partial pairs) in f32x2 ops.
-      float2 sp2[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
-                       make_float2(0.0f, 0.0f)};
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
-#pragma unroll
-      for (int c = 0; c < 4; c += 2) {
-        float v0[32], v1[32];
-        tmem_ld32(tms + lane_off + c * 32, v0);
-        tmem_ld32(tms + lane_off + (c + 1) * 32, v1);
+      // A piece of a split item: write the partial row (O as accumulated, in
+      // the scale of m; m in log2 units; l), then take a ticket.
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32(tmo + lane_off + c * 32, v);
         tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float *v = h ? v1 : v0;
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float2 t = fma2(make_float2(v[2 * i], v[2 * i + 1]), sc2, nm2);
-            const float2 x = make_float2(fast_exp2(t.x), fast_exp2(t.y));
-            sp2[i & 3] = add2(sp2[i & 3], x);
-            pk[i] = pack_half2(x.x, x.y);
-          }
-          tmem_st16(tms + lane_off + (c + h) * 16, pk);
-        }
+        for (int i = 0; i < 8; ++i)
+          reinterpret_cast<float4 *>(prow + c * 32)[i] =
+              make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
       }
-      const float2 s01 = add2(sp2[0], sp2[1]), s23 = add2(sp2[2], sp2[3]);
-      const float2 s4 = add2(s01, s23);
-      const float rs = s4.x + s4.y;
-
-      l += rs;
-      tmem_wait_st();
-      tc_fence_before();
+      tc_fence_before();  // O read: the next segment's first PV may overwrite it
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.pfull[e]);
-    }
-    // epilogue: wait until every MMA has finished (the single-use drain
-    // barrier), normalise, store the row
-    if (ok) ok = mbar_wait_bounded(&bars.drain, 0, &abort_flag);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok && lane == 0) {
-      set_err(p.err, KVQ_DEVERR_TIMEOUT);
-      atomicExch(&abort_flag, 1);
-    }
-    tc_fence_after();
-    const float inv = (ok && l > 0.0f) ? 1.0f / l : 0.0f;
-    const int head = h0 + e;
-    __half *dst = p.out + (static_cast<int64_t>(q0 + r) * p.n_q + head) * kD;
+      if (lane == 0) mbar_arrive(&bars.ofree[e]);
+      reinterpret_cast<float2 *>(prow + kD)[0] = make_float2(m, l);
+      __threadfence();
+      // every row of both heads written before the ticket (named barrier 1
+      // for a pair of heads, 2 for a single head: warpgroup 1 never meets 2)
+      const int bar_id = two ? 1 : 2, nthr = two ? 256 : 128;
+      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
+      // CTAs holding a piece of the item: owners of its first and last step
+      // (the owner of step s is floor(((s + 1) P - 1) / W); with W >= P every
+      // CTA owns at least one step)
+      const int64_t c_first = ((sg.start + 1) * P - 1) / p.W;
+      const int64_t c_last = ((sg.start + sg.nt) * P - 1) / p.W;
+      if (threadIdx.x == 0) {
+        const unsigned n_parts = static_cast<unsigned>(c_last - c_first + 1);
+        const unsigned old = atomicInc(p.tickets + item, n_parts - 1);
+        last_flag = old == n_parts - 1 ? 1 : 0;
+      }
+      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
+      if (last_flag) {
+        __threadfence();
+        // merge this row over the item's pieces (slots c + item), 32 dims at a time
+        float M = -INFINITY, L = 0.0f;
+        for (int64_t c = c_first; c <= c_last; ++c)
+          M = fmaxf(M, __ldcg(p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride + kD));
+        for (int64_t c = c_first; c <= c_last; ++c) {
+          const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
+              p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride + kD));
+          if (ml.x != -INFINITY) L = fmaf(fast_exp2(ml.x - M), ml.y, L);
+        }
+        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+        __half *dst = p.out + row * kD;
 #pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      tmem_ld32(tmo + lane_off + c * 32, v);
-      tmem_wait_ld();
-      if (r < rows) {
-        uint32_t w[16];
+        for (int cc = 0; cc < 4; ++cc) {
+          float4 acc[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = pack_half2(v[2 * i] * inv, v[2 * i + 1] * inv);
+          for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+          for (int64_t c = c_first; c <= c_last; ++c) {
+            const float *pr = p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride;
+            const float mk = __ldcg(pr + kD);
+            const float w = mk == -INFINITY ? 0.0f : fast_exp2(mk - M);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          reinterpret_cast<uint4 *>(dst + c * 32)[i] =
-              make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            for (int i = 0; i < 8; ++i) {
+              const float4 x = __ldcg(reinterpret_cast<const float4 *>(pr + cc * 32) + i);
+              acc[i].x = fmaf(w, x.x, acc[i].x);
+              acc[i].y = fmaf(w, x.y, acc[i].y);
+              acc[i].z = fmaf(w, x.z, acc[i].z);
+              acc[i].w = fmaf(w, x.w, acc[i].w);
+            }
+          }
+          if (r < rows) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w0 = pack_half2(acc[2 * i].x * inv, acc[2 * i].y * inv);
+              const uint32_t w1 = pack_half2(acc[2 * i].z * inv, acc[2 * i].w * inv);
+              const uint32_t w2 = pack_half2(acc[2 * i + 1].x * inv, acc[2 * i + 1].y * inv);
+              const uint32_t w3 = pack_half2(acc[2 * i + 1].z * inv, acc[2 * i + 1].w * inv);
+              reinterpret_cast<uint4 *>(dst + cc * 32)[i] = make_uint4(w0, w1, w2, w3);
+            }
+          }
+        }
+        if (p.lse && r < rows)
+          p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      }
+      // the flag is read by every thread before anyone takes the next ticket
+      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
+      sg = nsg;
+      have_seg = have_next;
+    }
+    if (!ok) {
+      if (lane == 0) {
+        set_err(p.err, KVQ_DEVERR_TIMEOUT);
+        atomicExch(&abort_flag, 1);
       }
     }
-    if (p.lse && r < rows)
-      p.lse[static_cast<int64_t>(q0 + r) * p.n_q + head] =
-          (ok && l > 0.0f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
   }
 
   tc_fence_before();
@@ -652,13 +888,31 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
 
 }  // namespace
 
-PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok) {
+// Key tiles attended by query tile qt of a chunk (host copy of qt_tiles).
+static int64_t host_qt_tiles(int q_start, int n_q_tok, int qt) {
+  const int64_t rows_end = std::min<int64_t>(static_cast<int64_t>(kBM) * (qt + 1), n_q_tok);
+  return (q_start + rows_end + kBN - 1) / kBN;
+}
+
+PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok, int num_sms) {
   PrefillPlan pl;
   pl.kv_tokens = static_cast<int64_t>(q_start) + n_q_tok;
   const int64_t n_tiles = (pl.kv_tokens + kBN - 1) / kBN;
   pl.kv_tokens_pad = n_tiles * kBN;
   pl.ws_k_bytes = static_cast<int64_t>(L.n_kv_heads) * n_tiles * kTileBytes;
-  pl.ws_bytes = 2 * pl.ws_k_bytes;
+  const int G = L.n_q_heads / L.n_kv_heads;
+  pl.npairs = (G + 1) / 2;
+  pl.n_qt = (n_q_tok + kBM - 1) / kBM;
+  pl.n_items = static_cast<int64_t>(L.n_kv_heads) * pl.npairs * pl.n_qt;
+  pl.Tq = 0;
+  for (int qt = 0; qt < pl.n_qt; ++qt) pl.Tq += host_qt_tiles(q_start, n_q_tok, qt);
+  pl.W = static_cast<int64_t>(L.n_kv_heads) * pl.npairs * pl.Tq;
+  pl.grid = std::max<int64_t>(1, std::min<int64_t>(num_sms > 0 ? num_sms : 148, pl.W));
+  // tickets after the K and V tiles (256-byte aligned), then the partial slots
+  pl.ticket_off = 2 * pl.ws_k_bytes;
+  pl.part_off = pl.ticket_off + (pl.n_items * 4 + 255) / 256 * 256;
+  pl.part_bytes = (pl.grid + pl.n_items) * 2 * kBM * kPartStride * 4;
+  pl.ws_bytes = pl.part_off + pl.part_bytes;
   return pl;
 }
 
@@ -676,11 +930,13 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   dp.tiles[1] = ws + pl.ws_k_bytes;
   dp.seq_lens = L.seq_lens;
   dp.err = L.err;
+  dp.tickets = reinterpret_cast<unsigned *>(ws + pl.ticket_off);
   dp.seq = seq;
   dp.n_kv = L.n_kv_heads;
   dp.capacity = L.capacity;
   dp.kv_len = static_cast<int>(pl.kv_tokens);
   dp.n_tiles = n_tiles;
+  dp.n_items = static_cast<int>(pl.n_items);
   cudaError_t e = launch_pdl(dequant_tiles_kernel, dim3(n_tiles, L.n_kv_heads, 2), dim3(256), 0,
                              stream, dp);
   if (e != cudaSuccess) return e;
@@ -692,20 +948,26 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   ap.out = static_cast<__half *>(out);
   ap.lse = lse;
   ap.err = L.err;
+  ap.part = reinterpret_cast<float *>(ws + pl.part_off);
+  ap.tickets = reinterpret_cast<unsigned *>(ws + pl.ticket_off);
   ap.n_q = L.n_q_heads;
   ap.G = L.n_q_heads / L.n_kv_heads;
   ap.n_tok = n_q_tok;
   ap.q_start = q_start;
   ap.kv_len = static_cast<int>(pl.kv_tokens);
   ap.n_tiles = n_tiles;
+  ap.npairs = pl.npairs;
+  ap.n_qt = pl.n_qt;
+  ap.n_items = static_cast<int>(pl.n_items);
+  ap.Tq = pl.Tq;
+  ap.W = pl.W;
   ap.scale_log2 = scale * 1.4426950408889634f;
   const int smem = (2 + 2 * kStages) * kTileBytes + 1024;
   static std::atomic<uint64_t> optin{0};
   e = smem_optin(prefill_attn_kernel, smem, optin);
   if (e != cudaSuccess) return e;
-  const int G = L.n_q_heads / L.n_kv_heads;
-  const dim3 grid((n_q_tok + kBM - 1) / kBM, L.n_kv_heads * ((G + 1) / 2));
-  return launch_pdl(prefill_attn_kernel, grid, dim3(kThreads), smem, stream, ap);
+  return launch_pdl(prefill_attn_kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(kThreads),
+                    smem, stream, ap);
 }
 
 }  // namespace kvq
