@@ -82,6 +82,15 @@ def _load():
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int64, ctypes.c_int, u16p, ctypes.c_double,
                                            u8p, f64p, f64p]
+        lib.kvqo_requantize_side.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, u8p, u8p,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p]
+        ip = ctypes.POINTER(ctypes.c_int)
+        lib.kvqo_bits_per_value.argtypes = [ctypes.c_int]
+        lib.kvqo_bits_per_value.restype = ctypes.c_double
+        lib.kvqo_aggregate_bpv.argtypes = [ip, ctypes.c_int]
+        lib.kvqo_aggregate_bpv.restype = ctypes.c_double
+        lib.kvqo_ladder_next.argtypes = [ip, ctypes.c_int, ip, ctypes.c_int, ctypes.c_double,
+                                         ip, ip]
         lib.kvqo_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -246,3 +255,39 @@ def prefill_chunk(codec_k: int, codec_v: int, cache_k: np.ndarray, cache_v: np.n
     if rc:
         raise ValueError(f"oracle prefill failed ({rc})")
     return out, lse
+
+
+# --------------------------------------------------------------------------- degrade ladder
+
+def requantize_side(src_codec: int, dst_codec: int, side: int, cache: np.ndarray, n_seqs: int,
+                    n_kv: int, capacity: int, seq_lens) -> np.ndarray:
+    """Re-encode tokens [0, seq_lens[s]) of one side's cache into a new cache of
+    dst_codec (zero elsewhere)."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    out = np.zeros(cache_bytes(dst_codec, n_seqs, n_kv, capacity), np.uint8)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    rc = _load().kvqo_requantize_side(src_codec, dst_codec, side, _ptr(cache, ctypes.c_uint8),
+                                      _ptr(out, ctypes.c_uint8), n_seqs, n_kv, capacity,
+                                      _ptr(lens, ctypes.c_int32))
+    if rc:
+        raise ValueError(f"oracle requantize failed ({rc})")
+    return out
+
+
+def bits_per_value(codec: int) -> float:
+    return float(_load().kvqo_bits_per_value(codec))
+
+
+def aggregate_bpv(codecs) -> float:
+    c = np.ascontiguousarray(codecs, dtype=np.intc)
+    return float(_load().kvqo_aggregate_bpv(_ptr(c, ctypes.c_int), len(c)))
+
+
+def ladder_next(codecs, order, floor_bpv: float):
+    """(tensor, new codec) of the next banded degrade step, or None."""
+    c = np.ascontiguousarray(codecs, dtype=np.intc)
+    o = np.ascontiguousarray(order, dtype=np.intc)
+    t, k = ctypes.c_int(-1), ctypes.c_int(-1)
+    got = _load().kvqo_ladder_next(_ptr(c, ctypes.c_int), len(c), _ptr(o, ctypes.c_int), len(o),
+                                   float(floor_bpv), ctypes.byref(t), ctypes.byref(k))
+    return (t.value, k.value) if got else None

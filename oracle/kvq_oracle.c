@@ -29,6 +29,15 @@
  *    every cached key; a prefill chunk attends causally (query at absolute
  *    position P sees keys 0..P), after the chunk's own keys were appended
  *    (the ubatch discussion of the serverAppConfigs commit log).
+ *  - Degrading one (layer, side) tensor down the classic ladder (the same
+ *    VBR section: the cache degrades one tensor at a time, f16 -> q8_0 ->
+ *    q4_0, and the classic order is strictly banded, every movable tensor
+ *    reaching q8_0 before any reaches q4_0; a degrade stops at the last step
+ *    whose aggregate bits per value stays at or above the floor).  A tensor is
+ *    re-encoded from its decoded values: x^ (exact in fp32) goes through the
+ *    encoder of the new codec as fp32 input; an f16 target rounds x^ to fp16.
+ *    Bits per value of a codec = row bytes * 8 / 128; the aggregate over
+ *    tensors of equal size is their mean.
  *  - The cache byte layout, written from its specification (the library's
  *    public header documents the same layout): the cache of one layer and
  *    side is [seq][kv_head][capacity/16 units][unit bytes]; a unit holds 16
@@ -134,12 +143,10 @@ static int kvqo_all_finite(const float *x, int n)
     return 1;
 }
 
-/* q8_0: 34 bytes = d16 (2) + 32 x int8. Returns 0, or -1 for non-finite input. */
-int kvqo_q8_0_encode_block(const uint16_t *x16, uint8_t *out)
+/* q8_0 of 32 fp32 values: 34 bytes = d16 (2) + 32 x int8.
+ * Returns 0, or -1 for non-finite input. */
+int kvqo_q8_0_encode_block_f32(const float *x, uint8_t *out)
 {
-    float x[32];
-    for (int j = 0; j < 32; ++j)
-        x[j] = kvqo_half_to_float(x16[j]);
     if (!kvqo_all_finite(x, 32))
         return -1;
     float amax = 0.0f;
@@ -163,12 +170,19 @@ int kvqo_q8_0_encode_block(const uint16_t *x16, uint8_t *out)
     return 0;
 }
 
-/* q4_0: 18 bytes = d16 (2) + 16 bytes, byte j = q[j] | q[j+16] << 4. */
-int kvqo_q4_0_encode_block(const uint16_t *x16, uint8_t *out)
+/* The same from 32 fp16 values (converted to fp32 exactly). */
+int kvqo_q8_0_encode_block(const uint16_t *x16, uint8_t *out)
 {
     float x[32];
     for (int j = 0; j < 32; ++j)
         x[j] = kvqo_half_to_float(x16[j]);
+    return kvqo_q8_0_encode_block_f32(x, out);
+}
+
+/* q4_0 of 32 fp32 values: 18 bytes = d16 (2) + 16 bytes,
+ * byte j = q[j] | q[j+16] << 4. */
+int kvqo_q4_0_encode_block_f32(const float *x, uint8_t *out)
+{
     if (!kvqo_all_finite(x, 32))
         return -1;
     int jmax = 0;
@@ -195,6 +209,14 @@ int kvqo_q4_0_encode_block(const uint16_t *x16, uint8_t *out)
     for (int j = 0; j < 16; ++j)
         out[2 + j] = (uint8_t)((q[j] & 0xf) | ((q[j + 16] & 0xf) << 4));
     return 0;
+}
+
+int kvqo_q4_0_encode_block(const uint16_t *x16, uint8_t *out)
+{
+    float x[32];
+    for (int j = 0; j < 32; ++j)
+        x[j] = kvqo_half_to_float(x16[j]);
+    return kvqo_q4_0_encode_block_f32(x, out);
 }
 
 void kvqo_q8_0_decode_block(const uint8_t *in, double *out)
@@ -403,6 +425,102 @@ int kvqo_dequant_stream(int codec, int side, const uint8_t *cache, int n_kv, int
     for (int64_t t = 0; t < n_tokens; ++t) {
         kvqo_get_row(st, codec, side, t, row);
         kvqo_decode_rows(codec, 1, row, out + t * KVQO_D);
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Degrade ladder: re-encode one tensor; bits per value; the banded step.    */
+/* ------------------------------------------------------------------------ */
+
+/* Re-encode tokens [0, seq_lens[s]) of every (seq, kv_head) stream of one
+ * side from src_codec to dst_codec (dst is a separate cache of dst_codec).
+ * Each row is decoded to fp32 (exact: d16 * q or d16 * (n - 8), or the fp16
+ * value) and encoded again: q8_0 / q4_0 by the fp32 formulas above, f16 by
+ * rounding to fp16.  Returns 0, or -1 on bad arguments. */
+int kvqo_requantize_side(int src_codec, int dst_codec, int side, const uint8_t *src,
+                         uint8_t *dst, int n_seqs, int n_kv, int capacity,
+                         const int32_t *seq_lens)
+{
+    if (kvqo_row_bytes(src_codec) < 0 || kvqo_row_bytes(dst_codec) < 0 ||
+        capacity % KVQO_UNIT_TOKENS)
+        return -1;
+    uint8_t row[256], out[256];
+    double xd[KVQO_D];
+    float x[KVQO_D];
+    for (int s = 0; s < n_seqs; ++s) {
+        if (seq_lens[s] < 0 || seq_lens[s] > capacity)
+            return -1;
+        for (int h = 0; h < n_kv; ++h) {
+            const uint8_t *ss = kvqo_stream((uint8_t *)src, src_codec, n_kv, capacity, s, h);
+            uint8_t *ds = kvqo_stream(dst, dst_codec, n_kv, capacity, s, h);
+            for (int64_t t = 0; t < seq_lens[s]; ++t) {
+                kvqo_get_row(ss, src_codec, side, t, row);
+                kvqo_decode_rows(src_codec, 1, row, xd);
+                for (int d = 0; d < KVQO_D; ++d)
+                    x[d] = (float)xd[d]; /* exact: the products fit fp32 */
+                if (dst_codec == KVQO_F16) {
+                    for (int d = 0; d < KVQO_D; ++d) {
+                        uint16_t hb = kvqo_float_to_half_rn(x[d]);
+                        out[2 * d] = (uint8_t)(hb & 0xffu);
+                        out[2 * d + 1] = (uint8_t)(hb >> 8);
+                    }
+                } else {
+                    for (int b = 0; b < 4; ++b) {
+                        int rc = dst_codec == KVQO_Q8_0
+                                     ? kvqo_q8_0_encode_block_f32(x + 32 * b, out + 34 * b)
+                                     : kvqo_q4_0_encode_block_f32(x + 32 * b, out + 18 * b);
+                        if (rc)
+                            return -1;
+                    }
+                }
+                kvqo_put_row(ds, dst_codec, side, t, out);
+            }
+        }
+    }
+    return 0;
+}
+
+/* Bits per value of a codec: row bytes * 8 / head_dim (16, 8.5, 4.5). */
+double kvqo_bits_per_value(int codec)
+{
+    int rb = kvqo_row_bytes(codec);
+    return rb < 0 ? -1.0 : rb * 8.0 / KVQO_D;
+}
+
+/* Aggregate bits per value of n tensors holding equally many values. */
+double kvqo_aggregate_bpv(const int *codecs, int n)
+{
+    double sum = 0.0;
+    for (int i = 0; i < n; ++i)
+        sum += kvqo_bits_per_value(codecs[i]);
+    return n > 0 ? sum / n : 0.0;
+}
+
+/* The next step of the banded classic ladder: the first tensor in `order`
+ * (n_order movable tensor indices, price order) still above rung q8_0 goes to
+ * q8_0; once every movable tensor is at q8_0 or below, the first one still
+ * above q4_0 goes to q4_0.  The step is taken only if the aggregate over all
+ * n tensors afterwards is >= floor_bpv.  Writes the tensor and its new codec
+ * and returns 1, or returns 0 when no step remains. */
+int kvqo_ladder_next(const int *codecs, int n, const int *order, int n_order, double floor_bpv,
+                     int *tensor, int *codec)
+{
+    static const int rungs[2] = {KVQO_Q8_0, KVQO_Q4_0};
+    for (int k = 0; k < 2; ++k) {
+        for (int i = 0; i < n_order; ++i) {
+            int t = order[i];
+            if (codecs[t] < rungs[k]) { /* codec ids grow as bits shrink */
+                double sum = 0.0;
+                for (int j = 0; j < n; ++j)
+                    sum += kvqo_bits_per_value(j == t ? rungs[k] : codecs[j]);
+                if (sum / n < floor_bpv)
+                    return 0;
+                *tensor = t;
+                *codec = rungs[k];
+                return 1;
+            }
+        }
     }
     return 0;
 }

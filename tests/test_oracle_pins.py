@@ -393,3 +393,126 @@ def test_prefill_chunk_is_causal_over_cached_plus_new_keys():
     sub_o, _ = oracle.prefill_chunk(ck, cv, cache_k, cache_v, n_kv, n_q, cap, 0, cached, q, 0.125,
                                     rows=[0, 8])
     assert np.array_equal(sub_o[[0, 8]], out[[0, 8]]) and np.isnan(sub_o[1]).all()
+
+
+# --------------------------------------------------------------------------- degrade ladder
+
+_VBR = json.load(open(os.path.join(GOLDEN, "vbr_ladder.json")))
+
+
+def test_bits_per_value_follow_the_codec_table():
+    sizes = json.load(open(os.path.join(GOLDEN, "codec_sizes.json")))["bits_per_value"]
+    assert oracle.bits_per_value(oracle.F16) == sizes["f16"]
+    assert oracle.bits_per_value(oracle.Q8_0) == sizes["q8_0"]
+    assert oracle.bits_per_value(oracle.Q4_0) == sizes["q4_0"]
+
+
+def test_aggregate_bpv_reproduces_the_pages_first_two_steps():
+    # the pages' 15.75 then 15.51 for 32 tensors fit a rung of 8.125 bits (two
+    # decimals); the mean itself is checked with exact rationals, and with q8_0
+    # the same two steps give the derived values.
+    for k, printed in enumerate(_VBR["facts"]["qwen35_example"]["first_aggregates"], start=1):
+        exact = Fraction((32 - k) * 16, 1) + k * Fraction(65, 8)
+        assert round(float(exact / 32), 2) == printed
+    want = _VBR["derived"]["q8_0_first_two_aggregates_32_tensors"]
+    assert oracle.aggregate_bpv([0] * 31 + [1]) == want[0]
+    assert oracle.aggregate_bpv([0] * 30 + [1, 1]) == want[1]
+    rng = np.random.default_rng(5)
+    for _ in range(20):
+        c = rng.integers(0, 3, rng.integers(1, 40))
+        brute = sum(Fraction(oracle.ROW_BYTES[int(x)] * 8, 128) for x in c) / len(c)
+        assert oracle.aggregate_bpv(c) == float(brute)
+
+
+def _run_ladder(codecs, order, floor):
+    codecs = list(codecs)
+    steps = []
+    while True:
+        st = oracle.ladder_next(codecs, order, floor)
+        if st is None:
+            return codecs, steps
+        t, k = st
+        assert k == codecs[t] + 1 or (codecs[t] == 0 and k == 1)  # one rung at a time
+        codecs[t] = k
+        steps.append(st)
+
+
+def test_ladder_is_banded_and_has_tensors_times_rungs_steps():
+    n = _VBR["facts"]["qwen35_example"]["tensors"]
+    order = list(np.random.default_rng(6).permutation(n))
+    final, steps = _run_ladder([0] * n, order, oracle.bits_per_value(oracle.Q4_0))
+    assert len(steps) == _VBR["derived"]["classic_steps_32_tensors"] == 2 * n
+    assert final == [2] * n
+    # banded: the first n steps take every tensor to q8_0, in price order
+    assert steps[:n] == [(t, 1) for t in order]
+    assert steps[n:] == [(t, 2) for t in order]
+
+
+def test_ladder_stops_at_the_floor_and_never_moves_pinned_tensors():
+    n = 32
+    final, steps = _run_ladder([0] * n, list(range(n)), 15.7)
+    assert steps == [(0, 1)]  # 15.765625 >= 15.7 > 15.53125
+    # the floor is inclusive
+    final, steps = _run_ladder([0] * n, list(range(n)), 15.53125)
+    assert steps == [(0, 1), (1, 1)]
+    # tensors missing from the order (pinned) keep their codec
+    order = [t for t in range(n) if t % 2 == 1]
+    final, steps = _run_ladder([0] * n, order, 0.0)
+    assert all(final[t] == 0 for t in range(0, n, 2))
+    assert all(final[t] == 2 for t in order) and len(steps) == 2 * len(order)
+    # a tensor already below f16 starts where it is
+    final, steps = _run_ladder([1, 0, 2, 0], [0, 1, 2, 3], 0.0)
+    assert steps == [(1, 1), (3, 1), (0, 2), (1, 2), (3, 2)]
+
+
+def _cache_from_rows(codec, side, rows16, n_seqs, n_kv, capacity, lens):
+    cache = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, capacity), np.uint8)
+    oracle.append_side(codec, side, cache, n_seqs, n_kv, capacity, [0] * n_seqs, lens, rows16)
+    return cache
+
+
+@pytest.mark.parametrize("side", [0, 1])
+@pytest.mark.parametrize("dst", [1, 2])
+def test_requantize_from_f16_equals_appending_the_same_rows(side, dst):
+    n_seqs, n_kv, capacity, lens = 2, 2, 256, [40, 17]
+    rng = np.random.default_rng(7 + side + 2 * dst)
+    rows = (rng.standard_normal((n_seqs, max(lens), n_kv, 128)) * 3).astype(np.float16)
+    src = _cache_from_rows(0, side, rows, n_seqs, n_kv, capacity, lens)
+    got = oracle.requantize_side(0, dst, side, src, n_seqs, n_kv, capacity, lens)
+    want = _cache_from_rows(dst, side, rows, n_seqs, n_kv, capacity, lens)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("side", [0, 1])
+def test_requantize_q8_to_q4_equals_q4_of_fp16_exact_values(side):
+    # q8_0 blocks with power-of-two scales and small quants decode to values
+    # that fp16 holds exactly, so q8_0 -> q4_0 must equal appending those fp16
+    # values with q4_0.
+    n_seqs, n_kv, capacity, lens = 1, 2, 256, [33]
+    rng = np.random.default_rng(8 + side)
+    q = rng.integers(-127, 128, (n_seqs, 33, n_kv, 128))
+    q[..., ::32] = 127  # amax 127 per block, so d = 2^e exactly
+    e = rng.integers(-8, 2, (n_seqs, 33, n_kv, 4))
+    vals = (q.reshape(n_seqs, 33, n_kv, 4, 32) * (2.0 ** e)[..., None]).reshape(q.shape)
+    vals16 = vals.astype(np.float16)
+    assert np.array_equal(vals16.astype(np.float64), vals)  # exact in fp16
+    src = _cache_from_rows(1, side, vals16, n_seqs, n_kv, capacity, lens)
+    back = oracle.dequant_stream(1, side, src, n_kv, capacity, 0, 0, 33)
+    assert np.array_equal(back, vals[0, :, 0].astype(np.float64))
+    got = oracle.requantize_side(1, 2, side, src, n_seqs, n_kv, capacity, lens)
+    want = _cache_from_rows(2, side, vals16, n_seqs, n_kv, capacity, lens)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("src_codec", [1, 2])
+def test_requantize_to_f16_rounds_the_decoded_values(src_codec):
+    n_seqs, n_kv, capacity, lens = 1, 1, 256, [20]
+    rng = np.random.default_rng(9)
+    rows = rng.standard_normal((1, 20, 1, 128)).astype(np.float16)
+    src = _cache_from_rows(src_codec, 1, rows, n_seqs, n_kv, capacity, lens)
+    got = oracle.requantize_side(src_codec, 0, 1, src, n_seqs, n_kv, capacity, lens)
+    dec = oracle.dequant_stream(src_codec, 1, src, n_kv, capacity, 0, 0, 20)
+    f16 = oracle.dequant_stream(0, 1, got, n_kv, capacity, 0, 0, 20)
+    assert np.array_equal(f16, dec.astype(np.float16).astype(np.float64))  # numpy RN
+    # tokens past the length stay untouched (zero)
+    assert not got[oracle.cache_bytes(0, 1, 1, 32):].any()
