@@ -91,13 +91,14 @@ class KVLayer:
 
     def desc(self) -> kvq_layer:
         """The C descriptor (rebuilt only when a buffer was replaced)."""
-        key = (_ptr(self.k_cache), _ptr(self.v_cache), _ptr(self.seq_lens), _ptr(self.err))
+        key = (_ptr(self.k_cache), _ptr(self.v_cache), _ptr(self.seq_lens), _ptr(self.err),
+               self.codec_k, self.codec_v)
         if self._desc is None or self._desc_key != key:
             d = kvq_layer()
             d.n_seqs, d.n_kv_heads, d.n_q_heads = self.n_seqs, self.n_kv_heads, self.n_q_heads
             d.head_dim, d.capacity = self.head_dim, self.capacity
             d.codec_k, d.codec_v, d.reserved = self.codec_k, self.codec_v, 0
-            d.k_cache, d.v_cache, d.seq_lens, d.err = key
+            d.k_cache, d.v_cache, d.seq_lens, d.err = key[:4]
             self._desc, self._desc_key = d, key
         return self._desc
 
@@ -152,3 +153,55 @@ def attn_prefill_chunk(layer: KVLayer, seq: int, q_start: int, q, scale: float, 
                                           _ptr(lse), _ptr(workspace),
                                           int(workspace.numel() * workspace.element_size()),
                                           _stream_ptr(stream)), "attn_prefill_chunk")
+
+
+# --------------------------------------------------------------------------- degrade ladder
+
+def kv_requantize(layer: KVLayer, side: int, dst_codec: int, dst_cache, stream=None) -> None:
+    """Re-encode side ``side`` (0 = K, 1 = V) of ``layer`` with ``dst_codec`` into
+    ``dst_cache`` (uint8 device tensor of kvq_cache_bytes(dst_codec, ...) bytes)."""
+    assert dst_cache.dtype == torch.uint8 and dst_cache.is_contiguous()
+    nb = kvq_cache_bytes(dst_codec, layer.n_seqs, layer.n_kv_heads, layer.capacity,
+                         layer.head_dim)
+    if dst_cache.numel() != nb:
+        raise ValueError(f"dst_cache must hold {nb} bytes")
+    d = layer.desc()
+    _check(_abi.load().kv_requantize(ctypes.byref(d), int(side), int(dst_codec), _ptr(dst_cache),
+                                     _stream_ptr(stream)), "kv_requantize")
+
+
+def degrade(layer: KVLayer, side: int, dst_codec: int, stream=None) -> None:
+    """Move one side of ``layer`` to ``dst_codec``: a new, zeroed cache buffer
+    (torch allocation; rows past the lengths stay zero), the re-encode, then
+    the layer points at the new buffer."""
+    nb = kvq_cache_bytes(dst_codec, layer.n_seqs, layer.n_kv_heads, layer.capacity,
+                         layer.head_dim)
+    src = layer.k_cache if side == 0 else layer.v_cache
+    dst = torch.zeros(nb, dtype=torch.uint8, device=src.device)
+    kv_requantize(layer, side, dst_codec, dst, stream)
+    if side == 0:
+        layer.k_cache, layer.codec_k = dst, dst_codec
+    else:
+        layer.v_cache, layer.codec_v = dst, dst_codec
+
+
+def aggregate_bpv(codecs) -> float:
+    arr = (ctypes.c_int32 * len(codecs))(*[int(c) for c in codecs])
+    v = float(_abi.load().kvq_aggregate_bpv(arr, len(codecs)))
+    if v < 0:
+        raise ValueError("invalid codecs")
+    return v
+
+
+def ladder_next(codecs, floor_bpv: float, order=None):
+    """(tensor, codec) of the next banded degrade step, or None."""
+    arr = (ctypes.c_int32 * len(codecs))(*[int(c) for c in codecs])
+    if order is None:
+        ordp, n_order = None, 0
+    else:
+        ordp = (ctypes.c_int32 * len(order))(*[int(t) for t in order])
+        n_order = len(order)
+    t, k = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    _check(_abi.load().kvq_ladder_next(arr, len(codecs), ordp, n_order, float(floor_bpv),
+                                       ctypes.byref(t), ctypes.byref(k)), "kvq_ladder_next")
+    return None if t.value < 0 else (t.value, k.value)

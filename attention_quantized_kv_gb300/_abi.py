@@ -19,7 +19,8 @@ KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN, KVQ_DEVERR_TIMEOUT, KVQ_DEVERR_SEQLEN = 
 # Every function the header declares (checked by the tests against include/kvq.h).
 EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kv_append_quantize",
            "attn_decode_workspace", "attn_decode", "attn_decode_noalloc",
-           "attn_prefill_workspace", "attn_prefill_chunk")
+           "attn_prefill_workspace", "attn_prefill_chunk", "kv_requantize", "kvq_aggregate_bpv",
+           "kvq_ladder_next")
 
 
 class kvq_layer(ctypes.Structure):
@@ -67,6 +68,11 @@ def load(path: str | None = None):
         "attn_prefill_workspace": (ctypes.c_int, [L, i32, i32, sz]),
         "attn_prefill_chunk": (ctypes.c_int, [L, i32, i32, i32, P, f32, P, P, P,
                                               ctypes.c_size_t, P]),
+        "kv_requantize": (ctypes.c_int, [L, i32, i32, P, P]),
+        "kvq_aggregate_bpv": (ctypes.c_double, [ctypes.POINTER(i32), i32]),
+        "kvq_ladder_next": (ctypes.c_int, [ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
+                                           ctypes.c_double, ctypes.POINTER(i32),
+                                           ctypes.POINTER(i32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -130,6 +130,85 @@ __device__ __forceinline__ void store_row(int codec, uint8_t *unit, int r, int l
   }
 }
 
+// Read one row (token row r of `unit`) into the lane-held form of store_row:
+// lane l gets dims 4l..4l+3 as fp32, the decoded values x^ = d16 * q (q8_0),
+// d16 * (n - 8) (q4_0) or the fp16 values, all exact in fp32.
+template <int SIDE>
+__device__ __forceinline__ void load_row(int codec, const uint8_t *unit, int r, int lane,
+                                         float (&x)[4]) {
+  const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
+  const int b = lane >> 3, lb = lane & 7;
+  if (codec == KVQ_F16) {
+    if (SIDE == 0) {
+      const int h = (lane >> 2) & 1, w = lane & 3;
+      const uint2 raw =
+          *reinterpret_cast<const uint2 *>(unit + (2 * b + rh) * 512 + (4 * g + w) * 16 + h * 8);
+      const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
+      const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
+      x[0] = __low2float(h01); x[1] = __high2float(h01);
+      x[2] = __low2float(h23); x[3] = __high2float(h23);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int d = 4 * lane + i, mt = d >> 4, gq = (d & 15) >> 1, sb = d & 1;
+        x[i] = __half2float(*reinterpret_cast<const __half *>(
+            unit + mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + sb * 2 + par) * 2));
+      }
+    }
+    return;
+  }
+  if (codec == KVQ_Q8_0) {
+    int q[4];
+    int soff;
+    if (SIDE == 0) {
+      const int h = lb >> 2, w = lane & 3;
+      const uint32_t word =
+          *reinterpret_cast<const uint32_t *>(unit + b * 512 + (4 * g + w) * 16 + (2 * rh + h) * 4);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = static_cast<int8_t>((word >> (8 * i)) & 0xffu);
+      soff = 2048 + g * 16 + rh * 8 + b * 2;
+    } else {
+#pragma unroll
+      for (int pp = 0; pp < 2; ++pp) {
+        const int d = 4 * lane + 2 * pp, mt = d >> 4, gq = (d & 15) >> 1;
+        const uint32_t v = *reinterpret_cast<const uint16_t *>(
+            unit + (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2);
+        q[2 * pp] = static_cast<int8_t>(v & 0xffu);
+        q[2 * pp + 1] = static_cast<int8_t>(v >> 8);
+      }
+      soff = 2048 + tig * 32 + b * 8 + rh * 4 + par * 2;
+    }
+    const float d = __half2float(*reinterpret_cast<const __half *>(unit + soff));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = d * static_cast<float>(q[i]);
+    return;
+  }
+  // q4_0: lanes lb < 4 hold canonical bytes jc = 4lb..4lb+3 (low nibbles),
+  // lanes lb + 4 the same bytes' high nibbles.
+  const int l4 = lb & 3, hi = lb >> 2;
+  uint32_t bytes[4];
+  if (SIDE == 0) {
+    const uint32_t word = *reinterpret_cast<const uint32_t *>(
+        unit + (b >> 1) * 512 + (4 * g + l4) * 16 + ((b & 1) * 2 + rh) * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bytes[i] = (word >> (8 * i)) & 0xffu;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int jc = 4 * l4 + i, mt = 2 * b + (jc >> 3), gq = jc & 7;
+      bytes[i] = unit[(mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh];
+    }
+  }
+  const int soff = SIDE == 0 ? 1024 + g * 16 + rh * 8 + b * 2
+                             : 1024 + tig * 32 + b * 8 + rh * 4 + par * 2;
+  const float d = __half2float(*reinterpret_cast<const __half *>(unit + soff));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = hi ? static_cast<int>(bytes[i] >> 4) : static_cast<int>(bytes[i] & 0xfu);
+    x[i] = d * static_cast<float>(n - 8);
+  }
+}
+
 struct AppendParams {
   const __half *x[2];  // k_new, v_new: [n_seqs][max_new][n_kv][128]
   uint8_t *cache[2];
@@ -218,7 +297,62 @@ __global__ void update_lens_kernel(int32_t *seq_lens, const int32_t *n_new, int 
 
 constexpr int64_t kSmallAppendRows = 64;  // at most 8 rows per warp
 
+struct RequantParams {
+  const uint8_t *src;
+  uint8_t *dst;
+  const int32_t *seq_lens;
+  int src_codec, dst_codec, n_kv, capacity;
+};
+
+// One CTA per (16-token unit, kv head, sequence); warp r re-encodes token row
+// r of the unit when it is below the sequence's length: decode (exact, fp32),
+// then the append encoder of the new codec (an f16 target rounds to fp16).
+template <int SIDE>
+__global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams p) {
+  grid_dependency_wait();
+  const int u = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
+  const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int len = min(p.seq_lens[s], p.capacity);
+  if (u * kUnitTokens + r < len) {
+    const int64_t stream = static_cast<int64_t>(s) * p.n_kv + kvh;
+    const int64_t units = p.capacity / kUnitTokens;
+    const uint8_t *su = p.src + (stream * units + u) * unit_bytes(p.src_codec);
+    uint8_t *du = p.dst + (stream * units + u) * unit_bytes(p.dst_codec);
+    float x[4];
+    load_row<SIDE>(p.src_codec, su, r, lane, x);
+    int q[4] = {0, 0, 0, 0};
+    __half d16 = __float2half_rn(0.0f);
+    uint2 raw = make_uint2(0u, 0u);
+    if (p.dst_codec == KVQ_Q8_0) {
+      encode_q8(x, q, d16);
+    } else if (p.dst_codec == KVQ_Q4_0) {
+      encode_q4(x, lane, q, d16);
+    } else {
+      const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
+      raw.x = *reinterpret_cast<const uint32_t *>(&h01);
+      raw.y = *reinterpret_cast<const uint32_t *>(&h23);
+    }
+    store_row<SIDE>(p.dst_codec, du, r, lane, raw, q, d16);
+  }
+  grid_launch_dependents();
+}
+
 }  // namespace
+
+cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *dst_cache,
+                           cudaStream_t stream) {
+  RequantParams p;
+  p.src = static_cast<const uint8_t *>(side == 0 ? L.k_cache : L.v_cache);
+  p.dst = static_cast<uint8_t *>(dst_cache);
+  p.seq_lens = L.seq_lens;
+  p.src_codec = side == 0 ? L.codec_k : L.codec_v;
+  p.dst_codec = dst_codec;
+  p.n_kv = L.n_kv_heads;
+  p.capacity = L.capacity;
+  const dim3 grid(L.capacity / kUnitTokens, L.n_kv_heads, L.n_seqs);
+  return side == 0 ? launch_pdl(requant_kernel<0>, grid, dim3(kUnitTokens * 32), 0, stream, p)
+                   : launch_pdl(requant_kernel<1>, grid, dim3(kUnitTokens * 32), 0, stream, p);
+}
 
 cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_new,
                           const int32_t *n_new, int max_new, int update_lens,

@@ -160,4 +160,69 @@ int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
+int kv_requantize(const kvq_layer *layer, int32_t side, int32_t dst_codec, void *dst_cache,
+                  void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (side != 0 && side != 1) return KVQ_EINVAL;
+  if (!valid_codec(dst_codec)) return KVQ_EUNSUPPORTED;
+  if (!dst_cache) return KVQ_EINVAL;
+  if (!aligned(dst_cache, 16)) return KVQ_EALIGN;
+  // out of place: the destination must not overlap the source
+  const void *src = side == 0 ? layer->k_cache : layer->v_cache;
+  const int src_codec = side == 0 ? layer->codec_k : layer->codec_v;
+  const uint8_t *s0 = static_cast<const uint8_t *>(src);
+  const uint8_t *d0 = static_cast<const uint8_t *>(dst_cache);
+  const int64_t sb = kvq_cache_bytes(src_codec, layer->n_seqs, layer->n_kv_heads,
+                                     layer->capacity, kHeadDim);
+  const int64_t db = kvq_cache_bytes(dst_codec, layer->n_seqs, layer->n_kv_heads,
+                                     layer->capacity, kHeadDim);
+  if (d0 < s0 + sb && s0 < d0 + db) return KVQ_EINVAL;
+  const cudaError_t e =
+      kvq::launch_requant(*layer, side, dst_codec, dst_cache, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+double kvq_aggregate_bpv(const int32_t *codecs, int32_t n) {
+  if (!codecs || n <= 0) return -1.0;
+  double sum = 0.0;
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t rb = kvq_row_bytes(codecs[i], kHeadDim);
+    if (rb < 0) return -1.0;
+    sum += static_cast<double>(rb) * 8.0 / kHeadDim;
+  }
+  return sum / n;
+}
+
+int kvq_ladder_next(const int32_t *codecs, int32_t n, const int32_t *order, int32_t n_order,
+                    double floor_bpv, int32_t *tensor, int32_t *codec) {
+  if (!codecs || n <= 0 || !tensor || !codec || n_order < 0 || (n_order > 0 && !order))
+    return KVQ_EINVAL;
+  for (int32_t i = 0; i < n; ++i)
+    if (!valid_codec(codecs[i])) return KVQ_EUNSUPPORTED;
+  for (int32_t i = 0; i < n_order; ++i)
+    if (order[i] < 0 || order[i] >= n) return KVQ_EINVAL;
+  const bool all = order == nullptr;
+  const int32_t m = all ? n : n_order;
+  *tensor = -1;
+  *codec = -1;
+  double total = 0.0;
+  for (int32_t i = 0; i < n; ++i) total += kvq_row_bytes(codecs[i], kHeadDim) * 8.0 / kHeadDim;
+  const int rungs[2] = {KVQ_Q8_0, KVQ_Q4_0};
+  for (int k = 0; k < 2; ++k) {
+    for (int32_t i = 0; i < m; ++i) {
+      const int32_t t = all ? i : order[i];
+      if (codecs[t] < rungs[k]) {  // codec ids grow as bits shrink
+        const double after = total - kvq_row_bytes(codecs[t], kHeadDim) * 8.0 / kHeadDim +
+                             kvq_row_bytes(rungs[k], kHeadDim) * 8.0 / kHeadDim;
+        if (after / n < floor_bpv) return KVQ_OK;
+        *tensor = t;
+        *codec = rungs[k];
+        return KVQ_OK;
+      }
+    }
+  }
+  return KVQ_OK;
+}
+
 }  // extern "C"

@@ -13,6 +13,11 @@ cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_n
                           const int32_t *n_new, int max_new, int update_lens,
                           cudaStream_t stream);
 
+// Re-encode one side of the layer into dst_cache (dst_codec): tokens below
+// each sequence's length (append.cu).
+cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *dst_cache,
+                           cudaStream_t stream);
+
 constexpr int kDecodeMaxSeqs = 1024;         // sequences per attn_decode call
 constexpr int kDecodeTicketBytes = 64 * 1024;  // per-stream counters at the workspace start
 constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4;

@@ -6,6 +6,9 @@
  *   kv_append_quantize   quantize new K/V rows into the cache (f16 / q8_0 / q4_0)
  *   attn_decode          split-K decode attention over every cached key
  *   attn_prefill_chunk   causal attention of one prefill chunk (ubatch)
+ *   kv_requantize        degrade one (layer, side) tensor to another codec
+ *   kvq_aggregate_bpv    aggregate bits per value of a set of tensors
+ *   kvq_ladder_next      the next step of the banded classic degrade ladder
  *
  * Sources.  The codecs and their sizes follow the "Codecs" table of the
  * buun-llama-cpp listing (f16 16.0, q8_0 8.5, q4_0 4.5 bits per value); the
@@ -205,6 +208,44 @@ KVQ_API int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int3
 KVQ_API int attn_prefill_chunk(const kvq_layer *layer, int32_t seq, int32_t q_start, int32_t n_q_tok,
                        const void *q, float scale, void *out, float *lse, void *workspace,
                        size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Degrade ladder ("VBR -- Variable Bit-Rate KV Cache" section of the
+ * buun-llama-cpp listing: the cache degrades one (layer, side) tensor at a
+ * time down the classic f16 -> q8_0 -> q4_0 ladder; the classic order is
+ * strictly banded, every movable tensor reaching q8_0 before any reaches
+ * q4_0; degrades stop at the last step whose aggregate bits per value stays
+ * at or above the floor).
+ * ------------------------------------------------------------------------ */
+
+/* Re-encode side `side` (0 = K, 1 = V) of the layer with codec dst_codec into
+ * dst_cache: for every sequence s and kv head, tokens [0, seq_lens[s]) are
+ * decoded (exactly, as fp32: d16 * q, d16 * (n - 8), or the fp16 value) and
+ * encoded again with the append encoder of dst_codec (an f16 target rounds to
+ * fp16); tokens past the length are not written.  From f16 the result equals
+ * appending the original rows with dst_codec.
+ * dst_cache: device, kvq_cache_bytes(dst_codec, ...) bytes, 16-byte aligned,
+ * not overlapping the source (the degrade is done out of place; the caller
+ * then points the layer's side at dst_cache and sets its codec).  Any pair of
+ * codecs is accepted. */
+KVQ_API int kv_requantize(const kvq_layer *layer, int32_t side, int32_t dst_codec, void *dst_cache,
+                          void *stream);
+
+/* Aggregate bits per value of n tensors holding equally many values: the mean
+ * of the codecs' bits per value (16, 8.5, 4.5).  -1 on bad arguments.  Host
+ * only. */
+KVQ_API double kvq_aggregate_bpv(const int32_t *codecs, int32_t n);
+
+/* The next degrade step of the banded classic ladder for n tensors with the
+ * given codecs.  order: the n_order movable tensor indices in price order
+ * (tensors missing from it are pinned and never move); NULL with n_order = 0
+ * means every tensor in index order.  The first tensor in order still above
+ * q8_0 goes to q8_0; once none is, the first one still above q4_0 goes to
+ * q4_0; the step is taken only if the aggregate bits per value afterwards is
+ * >= floor_bpv.  On KVQ_OK, *tensor and *codec hold the step, or *tensor = -1
+ * when no step remains.  Host only. */
+KVQ_API int kvq_ladder_next(const int32_t *codecs, int32_t n, const int32_t *order,
+                            int32_t n_order, double floor_bpv, int32_t *tensor, int32_t *codec);
 
 #ifdef __cplusplus
 }

@@ -4,6 +4,7 @@ import ctypes
 import os
 import re
 
+import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
@@ -110,3 +111,18 @@ def test_oracle_and_library_share_no_code():
             assert "import oracle" not in txt and "from oracle" not in txt, f
     otxt = open(os.path.join(ROOT, "oracle", "kvq_oracle.c")).read()
     assert "#include \"" not in otxt and "kvq.h" not in otxt
+
+
+def test_ladder_planner_and_aggregate_match_the_oracle():
+    """Host logic of the library (no GPU involved) against the oracle."""
+    import oracle
+    import attention_quantized_kv_gb300 as kvq
+    rng = np.random.default_rng(12)
+    for _ in range(200):
+        n = int(rng.integers(1, 12))
+        codecs = [int(c) for c in rng.integers(0, 3, n)]
+        order = [int(t) for t in rng.permutation(n)[:int(rng.integers(0, n + 1))]]
+        floor = float(rng.choice([0.0, 4.5, 8.5, 10.0, 16.0, float(rng.uniform(4, 16))]))
+        assert kvq.aggregate_bpv(codecs) == oracle.aggregate_bpv(codecs)
+        assert kvq.ladder_next(codecs, floor, order) == oracle.ladder_next(codecs, order, floor)
+        assert kvq.ladder_next(codecs, floor) == oracle.ladder_next(codecs, list(range(n)), floor)
