@@ -304,35 +304,62 @@ struct RequantParams {
   int src_codec, dst_codec, n_kv, capacity;
 };
 
-// One CTA per (16-token unit, kv head, sequence); warp r re-encodes token row
-// r of the unit when it is below the sequence's length: decode (exact, fp32),
-// then the append encoder of the new codec (an f16 target rounds to fp16).
+constexpr int kRqUnits = 8;  // units per CTA of the re-encode kernel
+
+// One CTA per run of kRqUnits 16-token units of one (sequence, kv head)
+// stream.  The source units are copied into shared memory with coalesced
+// 16-byte loads (all of them requested before any is used); warp w then
+// re-encodes rows w, w + 16, ... below the sequence's length there (decode
+// exactly to fp32, then the append encoder of the new codec; an f16 target
+// rounds to fp16) into a shared copy of the destination units, which go out
+// with coalesced 16-byte stores.  The unit holding the sequence's last tokens
+// first reads its destination bytes, so that its rows past the length keep
+// them.
 template <int SIDE>
 __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams p) {
+  extern __shared__ uint4 rq_smem[];
   grid_dependency_wait();
-  const int u = blockIdx.x, kvh = blockIdx.y, s = blockIdx.z;
-  const int r = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.y, s = blockIdx.z;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int len = min(p.seq_lens[s], p.capacity);
-  if (u * kUnitTokens + r < len) {
+  const int u0 = blockIdx.x * kRqUnits;
+  const int n_units = min(kRqUnits, (len + kUnitTokens - 1) / kUnitTokens - u0);
+  if (n_units > 0) {
     const int64_t stream = static_cast<int64_t>(s) * p.n_kv + kvh;
     const int64_t units = p.capacity / kUnitTokens;
-    const uint8_t *su = p.src + (stream * units + u) * unit_bytes(p.src_codec);
-    uint8_t *du = p.dst + (stream * units + u) * unit_bytes(p.dst_codec);
-    float x[4];
-    load_row<SIDE>(p.src_codec, su, r, lane, x);
-    int q[4] = {0, 0, 0, 0};
-    __half d16 = __float2half_rn(0.0f);
-    uint2 raw = make_uint2(0u, 0u);
-    if (p.dst_codec == KVQ_Q8_0) {
-      encode_q8(x, q, d16);
-    } else if (p.dst_codec == KVQ_Q4_0) {
-      encode_q4(x, lane, q, d16);
-    } else {
-      const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
-      raw.x = *reinterpret_cast<const uint32_t *>(&h01);
-      raw.y = *reinterpret_cast<const uint32_t *>(&h23);
+    const int sb = unit_bytes(p.src_codec), db = unit_bytes(p.dst_codec);
+    uint4 *sbuf = rq_smem;
+    uint4 *dbuf = rq_smem + kRqUnits * sb / 16;
+    const uint4 *su = reinterpret_cast<const uint4 *>(p.src + (stream * units + u0) * sb);
+    uint4 *du = reinterpret_cast<uint4 *>(p.dst + (stream * units + u0) * db);
+    for (int i = threadIdx.x; i < n_units * sb / 16; i += blockDim.x) sbuf[i] = su[i];
+    if ((u0 + n_units) * kUnitTokens > len) {  // the last unit is partial
+      const int base = (n_units - 1) * db / 16;
+      for (int i = threadIdx.x; i < db / 16; i += blockDim.x) dbuf[base + i] = du[base + i];
     }
-    store_row<SIDE>(p.dst_codec, du, r, lane, raw, q, d16);
+    __syncthreads();
+    const int rows = min(n_units * kUnitTokens, len - u0 * kUnitTokens);
+    for (int row = warp; row < rows; row += kUnitTokens) {
+      const int ul = row / kUnitTokens, r = row % kUnitTokens;
+      float x[4];
+      load_row<SIDE>(p.src_codec, reinterpret_cast<const uint8_t *>(sbuf) + ul * sb, r, lane, x);
+      int q[4] = {0, 0, 0, 0};
+      __half d16 = __float2half_rn(0.0f);
+      uint2 raw = make_uint2(0u, 0u);
+      if (p.dst_codec == KVQ_Q8_0) {
+        encode_q8(x, q, d16);
+      } else if (p.dst_codec == KVQ_Q4_0) {
+        encode_q4(x, lane, q, d16);
+      } else {
+        const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
+        raw.x = *reinterpret_cast<const uint32_t *>(&h01);
+        raw.y = *reinterpret_cast<const uint32_t *>(&h23);
+      }
+      store_row<SIDE>(p.dst_codec, reinterpret_cast<uint8_t *>(dbuf) + ul * db, r, lane, raw,
+                      q, d16);
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n_units * db / 16; i += blockDim.x) du[i] = dbuf[i];
   }
   grid_launch_dependents();
 }
@@ -349,9 +376,20 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
   p.dst_codec = dst_codec;
   p.n_kv = L.n_kv_heads;
   p.capacity = L.capacity;
-  const dim3 grid(L.capacity / kUnitTokens, L.n_kv_heads, L.n_seqs);
-  return side == 0 ? launch_pdl(requant_kernel<0>, grid, dim3(kUnitTokens * 32), 0, stream, p)
-                   : launch_pdl(requant_kernel<1>, grid, dim3(kUnitTokens * 32), 0, stream, p);
+  const int units = L.capacity / kUnitTokens;
+  const dim3 grid((units + kRqUnits - 1) / kRqUnits, L.n_kv_heads, L.n_seqs);
+  const int smem = kRqUnits * (unit_bytes(p.src_codec) + unit_bytes(dst_codec));
+  cudaError_t e;
+  if (side == 0) {
+    static std::atomic<uint64_t> optin{0};
+    e = smem_optin(requant_kernel<0>, kRqUnits * 2 * 4096, optin);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(requant_kernel<0>, grid, dim3(kUnitTokens * 32), smem, stream, p);
+  }
+  static std::atomic<uint64_t> optin{0};
+  e = smem_optin(requant_kernel<1>, kRqUnits * 2 * 4096, optin);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(requant_kernel<1>, grid, dim3(kUnitTokens * 32), smem, stream, p);
 }
 
 cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_new,

@@ -43,7 +43,7 @@ HEAD_DIM = 128
 @dataclass
 class Workload:
     name: str
-    kind: str                 # "decode" or "prefill"
+    kind: str                 # "decode", "prefill" or "degrade"
     n_seqs: int
     n_q: int
     n_kv: int
@@ -97,11 +97,16 @@ def get(name: str) -> Workload:
         return Workload(name, "prefill", 1, 32, 8, [32768], [(Q8_0, Q8_0)], 4, append_new=2048,
                         description="1 seq, 32768 cached + 2048-token ubatch appended, causal "
                                     "attention of 2048 queries over 34816 keys, 32q/8kv, q8_0")
+    if name == "degrade_f16_q8_2x200704":
+        return Workload(name, "degrade", 2, 32, 4, [200704, 200704], [(F16, F16)], 3,
+                        extra={"side": 0, "dst": Q8_0},
+                        description="one degrade-ladder step: re-encode the K side of a "
+                                    "2 x 200704-key layer (4 kv heads) from f16 to q8_0")
     raise KeyError(name)
 
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
-       "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k"]
+       "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704"]
 
 
 # ------------------------------------------------------------------ draws

@@ -63,7 +63,11 @@ def step_work(w):
     total_b, total_f, per_layer = 0, 0, []
     for ck, cv in w.codecs:
         app = w.n_seqs * w.append_new * w.n_kv * (2 * 256 + ROW[ck] + ROW[cv])
-        if w.kind == "decode":
+        if w.kind == "degrade":
+            src = ck if w.extra["side"] == 0 else cv
+            kv = sum(lens) * w.n_kv * (ROW[src] + ROW[w.extra["dst"]])
+            qo, fl = 0, 0
+        elif w.kind == "decode":
             kv = sum(lens) * w.n_kv * (ROW[ck] + ROW[cv])
             qo = 2 * w.n_seqs * w.n_q * 256
             fl = sum(lens) * w.n_q * 4 * 128
@@ -157,7 +161,11 @@ class OursArm:
             self._fill(L, l)
             self.layers.append(L)
             qq = wl.queries(w, l, n_tok, device)
-            if w.kind == "decode":
+            if w.kind == "degrade":
+                # the step's output: the re-encoded side, in its own buffer
+                self.q.append(qq[:0, 0].contiguous())
+                nb = kvq.kvq_cache_bytes(w.extra["dst"], w.n_seqs, w.n_kv, w.capacity)
+            elif w.kind == "decode":
                 self.q.append(qq[:, 0].contiguous())
                 nb = kvq.attn_decode_workspace(L, self.max_len)
             else:
@@ -204,7 +212,7 @@ class OursArm:
         kernel plus the length update; decode is one kernel, prefill two
         (dequant pre-pass, attention)."""
         w = self.w
-        per_layer = 1 if w.kind == "decode" else 2
+        per_layer = 1 if w.kind in ("decode", "degrade") else 2
         if w.append_new:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
@@ -224,7 +232,9 @@ class OursArm:
     def attention(self, l, q=None, out=None):
         L, w = self.layers[l], self.w
         qq, oo = (q or self.q)[l], (out or self.out)[l]
-        if w.kind == "decode":
+        if w.kind == "degrade":
+            self.kvq.kv_requantize(L, w.extra["side"], w.extra["dst"], self.ws[l])
+        elif w.kind == "decode":
             self.kvq.attn_decode(L, qq, self.scale, oo, self.lse[l], self.max_len, self.ws[l])
         else:
             self.kvq.attn_prefill_chunk(L, 0, w.lens[0], qq, self.scale, oo, self.lse[l],
@@ -436,8 +446,10 @@ def run_ours(args, w, rank, world, dist):
         "clocks": clocks,
         "device_errors": errs,
     }
-    if w.kind == "decode":
-        line["roofline"] = {"bound": "hbm", "kernel": "attn_decode (decode_split_kernel)",
+    if w.kind in ("decode", "degrade"):
+        kname = ("attn_decode (decode_split_kernel)" if w.kind == "decode"
+                 else "kv_requantize (requant_kernel)")
+        line["roofline"] = {"bound": "hbm", "kernel": kname,
                             "achieved": round(achieved_attn, 2), "peak": hbm,
                             "peak_kind": peak_kind, "unit": "GB/s",
                             "frac": round(achieved_attn / hbm, 4),
@@ -508,7 +520,10 @@ class OracleArm:
             ck, cv = w.codecs[l]
             T = w.final_lens()[s]
             app = w.append_new * (2 * 256 + ROW[ck] + ROW[cv])
-            if w.kind == "decode":
+            if w.kind == "degrade":
+                src = ck if w.extra["side"] == 0 else cv
+                tot += T * (ROW[src] + ROW[w.extra["dst"]])
+            elif w.kind == "decode":
                 tot += T * (ROW[ck] + ROW[cv]) + 2 * G * 256 + app
             else:
                 frac = len(self.rows) / w.append_new
@@ -527,7 +542,11 @@ class OracleArm:
                               kn.reshape(1, -1, 1, 128))
                 o.append_side(cv, 1, vc, 1, 1, w.capacity, [w.lens[s]], [w.append_new],
                               vn.reshape(1, -1, 1, 128))
-            if w.kind == "decode":
+            if w.kind == "degrade":
+                side = w.extra["side"]
+                o.requantize_side(ck if side == 0 else cv, w.extra["dst"], side,
+                                  kc if side == 0 else vc, 1, 1, w.capacity, [w.lens[s]])
+            elif w.kind == "decode":
                 o.decode_layer(ck, cv, kc, vc, 1, 1, G, w.capacity, [w.final_lens()[s]],
                                np.ascontiguousarray(q[0]), self.scale)
             else:
