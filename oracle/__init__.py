@@ -91,6 +91,11 @@ def _load():
         lib.kvqo_aggregate_bpv.restype = ctypes.c_double
         lib.kvqo_ladder_next.argtypes = [ip, ctypes.c_int, ip, ctypes.c_int, ctypes.c_double,
                                          ip, ip]
+        lib.kvqo_paged_unit.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int,
+                                        i32p, ctypes.c_int, ctypes.c_int]
+        lib.kvqo_paged_unit.restype = ctypes.c_int64
+        lib.kvqo_page_move.argtypes = [ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       i32p, ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int]
         lib.kvqo_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -291,3 +296,47 @@ def ladder_next(codecs, order, floor_bpv: float):
     got = _load().kvqo_ladder_next(_ptr(c, ctypes.c_int), len(c), _ptr(o, ctypes.c_int), len(o),
                                    float(floor_bpv), ctypes.byref(t), ctypes.byref(k))
     return (t.value, k.value) if got else None
+
+
+# --------------------------------------------------------------------------- paged layout
+
+PAGE_TOKENS = 256
+
+
+def pool_bytes(codec: int, n_pages: int, n_kv: int) -> int:
+    return n_pages * n_kv * PAGE_TOKENS * ROW_BYTES[codec]
+
+
+def paged_unit(s: int, h: int, j: int, n_kv: int, table, n_pages: int) -> int:
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    return int(_load().kvqo_paged_unit(s, h, j, n_kv, _ptr(t, ctypes.c_int32), t.shape[1],
+                                       n_pages))
+
+
+def to_pool(codec: int, cache: np.ndarray, n_seqs: int, n_kv: int, capacity: int, table,
+            n_pages: int, pool: np.ndarray = None) -> np.ndarray:
+    """Scatter a contiguous cache into a page pool (new zeroed pool unless given)."""
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    if pool is None:
+        pool = np.zeros(pool_bytes(codec, n_pages, n_kv), np.uint8)
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    rc = _load().kvqo_page_move(codec, _ptr(cache, ctypes.c_uint8), n_seqs, n_kv, capacity,
+                                _ptr(t, ctypes.c_int32), t.shape[1], _ptr(pool, ctypes.c_uint8),
+                                n_pages, 1)
+    if rc:
+        raise ValueError("bad paged geometry")
+    return pool
+
+
+def from_pool(codec: int, pool: np.ndarray, n_seqs: int, n_kv: int, capacity: int, table,
+              n_pages: int) -> np.ndarray:
+    """Gather a page pool back into a contiguous cache (unmapped pages zero)."""
+    t = np.ascontiguousarray(table, dtype=np.int32)
+    cache = np.zeros(cache_bytes(codec, n_seqs, n_kv, capacity), np.uint8)
+    pool = np.ascontiguousarray(pool, dtype=np.uint8)
+    rc = _load().kvqo_page_move(codec, _ptr(cache, ctypes.c_uint8), n_seqs, n_kv, capacity,
+                                _ptr(t, ctypes.c_int32), t.shape[1], _ptr(pool, ctypes.c_uint8),
+                                n_pages, 0)
+    if rc:
+        raise ValueError("bad paged geometry")
+    return cache

@@ -38,6 +38,14 @@
  *    encoder of the new codec as fp32 input; an f16 target rounds x^ to fp16.
  *    Bits per value of a codec = row bytes * 8 / 128; the aggregate over
  *    tensors of equal size is their mean.
+ *  - Paged caches (block-level KV management of the vLLM PagedAttention
+ *    entry in the references of the buun-llama-cpp listing; pools shared by
+ *    slots and 256-aligned, serverAppConfigs commit log): a page is 256
+ *    tokens (16 units) of every kv head of one sequence; a side's pool is
+ *    [n_pages][n_kv_head][16 units][unit bytes]; unit j of stream (s, h)
+ *    lives at pool unit (table[s][j / 16] * n_kv + h) * 16 + j % 16.  The
+ *    oracle computes on the contiguous layout and moves whole units between
+ *    the two layouts (kvqo_page_scatter / kvqo_page_gather).
  *  - The cache byte layout, written from its specification (the library's
  *    public header documents the same layout): the cache of one layer and
  *    side is [seq][kv_head][capacity/16 units][unit bytes]; a unit holds 16
@@ -426,6 +434,52 @@ int kvqo_dequant_stream(int codec, int side, const uint8_t *cache, int n_kv, int
         kvqo_get_row(st, codec, side, t, row);
         kvqo_decode_rows(codec, 1, row, out + t * KVQO_D);
     }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged layout: units moved between a contiguous cache and a page pool.     */
+/* ------------------------------------------------------------------------ */
+
+#define KVQO_PAGE_UNITS 16
+
+/* Pool unit index of unit j of stream (s, h), or -1 for an unmapped page. */
+int64_t kvqo_paged_unit(int s, int h, int64_t j, int n_kv, const int32_t *table,
+                        int pages_per_seq, int n_pages)
+{
+    int64_t pg = j / KVQO_PAGE_UNITS;
+    if (pg >= pages_per_seq)
+        return -1;
+    int32_t page = table[(int64_t)s * pages_per_seq + pg];
+    if (page < 0 || page >= n_pages)
+        return -1;
+    return ((int64_t)page * n_kv + h) * KVQO_PAGE_UNITS + j % KVQO_PAGE_UNITS;
+}
+
+/* Copy every unit of the contiguous cache [n_seqs][n_kv][capacity/16] whose
+ * page is mapped into the pool (to_pool != 0), or back (to_pool == 0).
+ * capacity must equal pages_per_seq * 256.  Returns 0 or -1. */
+int kvqo_page_move(int codec, uint8_t *cache, int n_seqs, int n_kv, int capacity,
+                   const int32_t *table, int pages_per_seq, uint8_t *pool, int n_pages,
+                   int to_pool)
+{
+    int64_t ub = kvqo_unit_bytes(codec);
+    if (ub < 0 || capacity != pages_per_seq * KVQO_PAGE_UNITS * KVQO_UNIT_TOKENS)
+        return -1;
+    int64_t units = capacity / KVQO_UNIT_TOKENS;
+    for (int s = 0; s < n_seqs; ++s)
+        for (int h = 0; h < n_kv; ++h)
+            for (int64_t j = 0; j < units; ++j) {
+                int64_t pu = kvqo_paged_unit(s, h, j, n_kv, table, pages_per_seq, n_pages);
+                if (pu < 0)
+                    continue;
+                uint8_t *c = cache + (((int64_t)s * n_kv + h) * units + j) * ub;
+                uint8_t *q = pool + pu * ub;
+                if (to_pool)
+                    memcpy(q, c, (size_t)ub);
+                else
+                    memcpy(c, q, (size_t)ub);
+            }
     return 0;
 }
 

@@ -516,3 +516,50 @@ def test_requantize_to_f16_rounds_the_decoded_values(src_codec):
     assert np.array_equal(f16, dec.astype(np.float16).astype(np.float64))  # numpy RN
     # tokens past the length stay untouched (zero)
     assert not got[oracle.cache_bytes(0, 1, 1, 32):].any()
+
+
+# --------------------------------------------------------------------------- paged layout
+
+def test_paged_unit_address_hand_example():
+    # 2 sequences x 2 pages, 3 kv heads; sequence 1's first page is pool page 0
+    table = np.array([[3, 1], [0, -1]], np.int32)
+    n_kv, n_pages = 3, 4
+    # unit j of stream (s, h) -> (table[s][j // 16] * n_kv + h) * 16 + j % 16
+    assert oracle.paged_unit(0, 0, 0, n_kv, table, n_pages) == (3 * 3 + 0) * 16
+    assert oracle.paged_unit(0, 2, 17, n_kv, table, n_pages) == (1 * 3 + 2) * 16 + 1
+    assert oracle.paged_unit(1, 1, 15, n_kv, table, n_pages) == (0 * 3 + 1) * 16 + 15
+    assert oracle.paged_unit(1, 0, 16, n_kv, table, n_pages) == -1   # unmapped page
+    assert oracle.paged_unit(0, 0, 32, n_kv, table, n_pages) == -1   # past pages_per_seq
+
+
+@pytest.mark.parametrize("codec", [0, 1, 2])
+def test_pool_with_one_kv_head_and_identity_table_is_the_contiguous_cache(codec):
+    n_seqs, n_kv, pps = 3, 1, 2
+    cap = pps * 256
+    rng = np.random.default_rng(40 + codec)
+    cache = rng.integers(0, 256, oracle.cache_bytes(codec, n_seqs, n_kv, cap)).astype(np.uint8)
+    table = np.arange(n_seqs * pps, dtype=np.int32).reshape(n_seqs, pps)
+    pool = oracle.to_pool(codec, cache, n_seqs, n_kv, cap, table, n_seqs * pps)
+    assert np.array_equal(pool, cache)
+
+
+@pytest.mark.parametrize("codec", [0, 1, 2])
+def test_pool_round_trip_under_a_shuffled_table(codec):
+    n_seqs, n_kv, pps, n_pages = 3, 2, 3, 11
+    cap = pps * 256
+    rng = np.random.default_rng(50 + codec)
+    cache = rng.integers(0, 256, oracle.cache_bytes(codec, n_seqs, n_kv, cap)).astype(np.uint8)
+    pages = rng.permutation(n_pages)[:n_seqs * pps].astype(np.int32)
+    table = pages.reshape(n_seqs, pps).copy()
+    table[2, 2] = -1  # an unmapped page: its units do not survive the round trip
+    pool = oracle.to_pool(codec, cache, n_seqs, n_kv, cap, table, n_pages)
+    back = oracle.from_pool(codec, pool, n_seqs, n_kv, cap, table, n_pages)
+    ub = 16 * oracle.ROW_BYTES[codec]
+    units = cap // 16
+    want = cache.copy().reshape(n_seqs, n_kv, units, ub)
+    want[2, :, 32:48] = 0
+    assert np.array_equal(back.reshape(n_seqs, n_kv, units, ub), want)
+    # every pool unit that a mapped page covers holds exactly one source unit
+    used = {int(p) for p in table.flatten() if p >= 0}
+    assert not pool.reshape(n_pages, n_kv * 16, ub)[[p for p in range(n_pages)
+                                                      if p not in used]].any()
