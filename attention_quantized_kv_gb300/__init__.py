@@ -16,12 +16,13 @@ import torch
 
 from . import _abi
 from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN,
-                   KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT, kvq_layer)
+                   KVQ_DEVERR_PAGE, KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT, kvq_layer)
 
 __all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "CODEC_NAMES", "KVQError", "KVLayer",
            "kv_append_quantize", "attn_decode_workspace", "attn_decode",
            "attn_prefill_workspace", "attn_prefill_chunk", "kvq_row_bytes", "kvq_cache_bytes",
-           "default_scale"]
+           "kvq_pool_bytes", "KVQ_DEVERR_PAGE", "kv_requantize", "degrade", "aggregate_bpv",
+           "ladder_next", "default_scale"]
 
 CODEC_NAMES = {KVQ_F16: "f16", KVQ_Q8_0: "q8_0", KVQ_Q4_0: "q4_0"}
 HEAD_DIM = 128
@@ -61,21 +62,41 @@ def kvq_cache_bytes(codec: int, n_seqs: int, n_kv_heads: int, capacity: int,
     return int(_abi.load().kvq_cache_bytes(codec, n_seqs, n_kv_heads, capacity, head_dim))
 
 
+def kvq_pool_bytes(codec: int, n_pages: int, n_kv_heads: int,
+                   head_dim: int = HEAD_DIM) -> int:
+    return int(_abi.load().kvq_pool_bytes(codec, n_pages, n_kv_heads, head_dim))
+
+
 class KVLayer:
     """One layer's cache: torch-owned device buffers plus the C descriptor.
 
     ``k_cache``/``v_cache`` are uint8 tensors in the layout of include/kvq.h,
-    ``seq_lens`` int32 [n_seqs] and ``err`` one int32 error word.
+    ``seq_lens`` int32 [n_seqs] and ``err`` one int32 error word.  Paged
+    layers (``n_pages`` > 0) hold page pools instead, and ``block_table``
+    (int32 [n_seqs][capacity / 256], device) maps each sequence's pages to
+    pool pages (-1: not mapped; default: every page mapped, in order).
     """
 
     def __init__(self, n_seqs: int, n_kv_heads: int, n_q_heads: int, capacity: int,
                  codec_k: int, codec_v: int, device="cuda", head_dim: int = HEAD_DIM,
-                 k_cache=None, v_cache=None):
+                 k_cache=None, v_cache=None, n_pages: int = 0, block_table=None):
         self.n_seqs, self.n_kv_heads, self.n_q_heads = n_seqs, n_kv_heads, n_q_heads
         self.capacity, self.codec_k, self.codec_v, self.head_dim = (capacity, codec_k, codec_v,
                                                                     head_dim)
-        kb = kvq_cache_bytes(codec_k, n_seqs, n_kv_heads, capacity, head_dim)
-        vb = kvq_cache_bytes(codec_v, n_seqs, n_kv_heads, capacity, head_dim)
+        self.n_pages = int(n_pages)
+        self.block_table = None
+        if self.n_pages > 0:
+            pps = capacity // 256
+            if block_table is None:
+                block_table = torch.arange(n_seqs * pps, dtype=torch.int32,
+                                           device=device).reshape(n_seqs, pps)
+            assert block_table.dtype == torch.int32 and block_table.shape == (n_seqs, pps)
+            self.block_table = block_table.contiguous()
+            kb = kvq_pool_bytes(codec_k, self.n_pages, n_kv_heads, head_dim)
+            vb = kvq_pool_bytes(codec_v, self.n_pages, n_kv_heads, head_dim)
+        else:
+            kb = kvq_cache_bytes(codec_k, n_seqs, n_kv_heads, capacity, head_dim)
+            vb = kvq_cache_bytes(codec_v, n_seqs, n_kv_heads, capacity, head_dim)
         if kb < 0 or vb < 0:
             raise ValueError("invalid cache geometry (capacity must be a multiple of 256, "
                              "head_dim 128, codecs f16/q8_0/q4_0)")
@@ -92,13 +113,18 @@ class KVLayer:
     def desc(self) -> kvq_layer:
         """The C descriptor (rebuilt only when a buffer was replaced)."""
         key = (_ptr(self.k_cache), _ptr(self.v_cache), _ptr(self.seq_lens), _ptr(self.err),
-               self.codec_k, self.codec_v)
+               self.codec_k, self.codec_v, _ptr(self.block_table), self.n_pages)
         if self._desc is None or self._desc_key != key:
             d = kvq_layer()
             d.n_seqs, d.n_kv_heads, d.n_q_heads = self.n_seqs, self.n_kv_heads, self.n_q_heads
             d.head_dim, d.capacity = self.head_dim, self.capacity
             d.codec_k, d.codec_v, d.reserved = self.codec_k, self.codec_v, 0
             d.k_cache, d.v_cache, d.seq_lens, d.err = key[:4]
+            if self.n_pages > 0:
+                d.pages_per_seq, d.block_table, d.n_pages = (self.capacity // 256,
+                                                             _ptr(self.block_table), self.n_pages)
+            else:
+                d.pages_per_seq, d.block_table, d.n_pages = 0, None, 0
             self._desc, self._desc_key = d, key
         return self._desc
 
@@ -157,12 +183,17 @@ def attn_prefill_chunk(layer: KVLayer, seq: int, q_start: int, q, scale: float, 
 
 # --------------------------------------------------------------------------- degrade ladder
 
+def _side_bytes(layer: KVLayer, codec: int) -> int:
+    if layer.n_pages > 0:
+        return kvq_pool_bytes(codec, layer.n_pages, layer.n_kv_heads, layer.head_dim)
+    return kvq_cache_bytes(codec, layer.n_seqs, layer.n_kv_heads, layer.capacity, layer.head_dim)
+
+
 def kv_requantize(layer: KVLayer, side: int, dst_codec: int, dst_cache, stream=None) -> None:
     """Re-encode side ``side`` (0 = K, 1 = V) of ``layer`` with ``dst_codec`` into
     ``dst_cache`` (uint8 device tensor of kvq_cache_bytes(dst_codec, ...) bytes)."""
     assert dst_cache.dtype == torch.uint8 and dst_cache.is_contiguous()
-    nb = kvq_cache_bytes(dst_codec, layer.n_seqs, layer.n_kv_heads, layer.capacity,
-                         layer.head_dim)
+    nb = _side_bytes(layer, dst_codec)
     if dst_cache.numel() != nb:
         raise ValueError(f"dst_cache must hold {nb} bytes")
     d = layer.desc()
@@ -174,8 +205,7 @@ def degrade(layer: KVLayer, side: int, dst_codec: int, stream=None) -> None:
     """Move one side of ``layer`` to ``dst_codec``: a new, zeroed cache buffer
     (torch allocation; rows past the lengths stay zero), the re-encode, then
     the layer points at the new buffer."""
-    nb = kvq_cache_bytes(dst_codec, layer.n_seqs, layer.n_kv_heads, layer.capacity,
-                         layer.head_dim)
+    nb = _side_bytes(layer, dst_codec)
     src = layer.k_cache if side == 0 else layer.v_cache
     dst = torch.zeros(nb, dtype=torch.uint8, device=src.device)
     kv_requantize(layer, side, dst_codec, dst, stream)

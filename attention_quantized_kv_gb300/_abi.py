@@ -15,9 +15,11 @@ LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 KVQ_F16, KVQ_Q8_0, KVQ_Q4_0 = 0, 1, 2
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECAPACITY, KVQ_EALIGN, KVQ_EWORKSPACE, KVQ_ECUDA = range(7)
 KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN, KVQ_DEVERR_TIMEOUT, KVQ_DEVERR_SEQLEN = 1, 2, 4, 8
+KVQ_DEVERR_PAGE = 16
 
 # Every function the header declares (checked by the tests against include/kvq.h).
-EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kv_append_quantize",
+EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kvq_pool_bytes",
+           "kv_append_quantize",
            "attn_decode_workspace", "attn_decode", "attn_decode_noalloc",
            "attn_prefill_workspace", "attn_prefill_chunk", "kv_requantize", "kvq_aggregate_bpv",
            "kvq_ladder_next")
@@ -32,11 +34,14 @@ class kvq_layer(ctypes.Structure):
         ("capacity", ctypes.c_int32),
         ("codec_k", ctypes.c_int32),
         ("codec_v", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("pages_per_seq", ctypes.c_int32),
         ("k_cache", ctypes.c_void_p),
         ("v_cache", ctypes.c_void_p),
         ("seq_lens", ctypes.c_void_p),
         ("err", ctypes.c_void_p),
+        ("block_table", ctypes.c_void_p),
+        ("n_pages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -61,6 +66,7 @@ def load(path: str | None = None):
         "kvq_status_str": (ctypes.c_char_p, [ctypes.c_int]),
         "kvq_row_bytes": (i64, [ctypes.c_int, i32]),
         "kvq_cache_bytes": (i64, [ctypes.c_int, i32, i32, i32, i32]),
+        "kvq_pool_bytes": (i64, [ctypes.c_int, i32, i32, i32]),
         "kv_append_quantize": (ctypes.c_int, [L, P, P, P, i32, i32, P]),
         "attn_decode_workspace": (ctypes.c_int, [L, i32, sz]),
         "attn_decode": (ctypes.c_int, [L, P, f32, P, P, i32, P, ctypes.c_size_t, P]),

@@ -216,7 +216,8 @@ struct AppendParams {
   int32_t *seq_lens;  // read by every row; advanced only by append_small_kernel
   const int32_t *n_new;
   int32_t *err;
-  int n_seqs, n_kv, max_new, capacity;
+  const int32_t *table;  // paged layers: block table; nullptr: contiguous
+  int n_seqs, n_kv, max_new, capacity, pages_per_seq, n_pages;
 };
 
 constexpr int kAppendWarps = 8;
@@ -247,10 +248,21 @@ __device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, i
   __half d16 = __float2half_rn(0.0f);
   if (codec == KVQ_Q8_0) encode_q8(x, q, d16);
   else if (codec == KVQ_Q4_0) encode_q4(x, lane, q, d16);
-  const int64_t units = p.capacity / kUnitTokens;
-  uint8_t *unit = p.cache[side] +
-                  ((static_cast<int64_t>(s) * p.n_kv + kvh) * units + pos / kUnitTokens) *
-                      unit_bytes(codec);
+  int64_t unit_idx;
+  if (p.table) {
+    const int pg =
+        page_of(p.table, p.pages_per_seq, p.n_pages, s, pos / (kUnitTokens * kPageUnits));
+    if (pg < 0) {
+      if (lane == 0) set_err(p.err, KVQ_DEVERR_PAGE);
+      return;
+    }
+    unit_idx = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits +
+               (pos / kUnitTokens) % kPageUnits;
+  } else {
+    unit_idx = (static_cast<int64_t>(s) * p.n_kv + kvh) * (p.capacity / kUnitTokens) +
+               pos / kUnitTokens;
+  }
+  uint8_t *unit = p.cache[side] + unit_idx * unit_bytes(codec);
   const int r = static_cast<int>(pos % kUnitTokens);
   if (side == 0) store_row<0>(codec, unit, r, lane, raw, q, d16);
   else store_row<1>(codec, unit, r, lane, raw, q, d16);
@@ -301,10 +313,13 @@ struct RequantParams {
   const uint8_t *src;
   uint8_t *dst;
   const int32_t *seq_lens;
-  int src_codec, dst_codec, n_kv, capacity;
+  int32_t *err;
+  const int32_t *table;  // paged layers: block table; nullptr: contiguous
+  int src_codec, dst_codec, n_kv, capacity, pages_per_seq, n_pages;
 };
 
 constexpr int kRqUnits = 8;  // units per CTA of the re-encode kernel
+static_assert(kPageUnits % kRqUnits == 0, "a run of units must lie inside one page");
 
 // One CTA per run of kRqUnits 16-token units of one (sequence, kv head)
 // stream.  The source units are copied into shared memory with coalesced
@@ -325,13 +340,23 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
   const int u0 = blockIdx.x * kRqUnits;
   const int n_units = min(kRqUnits, (len + kUnitTokens - 1) / kUnitTokens - u0);
   if (n_units > 0) {
-    const int64_t stream = static_cast<int64_t>(s) * p.n_kv + kvh;
-    const int64_t units = p.capacity / kUnitTokens;
+    // first unit of the run (a run lies inside one page: kPageUnits % kRqUnits == 0)
+    int64_t uidx;
+    if (p.table) {
+      const int pg = page_of(p.table, p.pages_per_seq, p.n_pages, s, u0 / kPageUnits);
+      if (pg < 0) {
+        if (threadIdx.x == 0) set_err(p.err, KVQ_DEVERR_PAGE);
+        return;  // whole CTA
+      }
+      uidx = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits + u0 % kPageUnits;
+    } else {
+      uidx = (static_cast<int64_t>(s) * p.n_kv + kvh) * (p.capacity / kUnitTokens) + u0;
+    }
     const int sb = unit_bytes(p.src_codec), db = unit_bytes(p.dst_codec);
     uint4 *sbuf = rq_smem;
     uint4 *dbuf = rq_smem + kRqUnits * sb / 16;
-    const uint4 *su = reinterpret_cast<const uint4 *>(p.src + (stream * units + u0) * sb);
-    uint4 *du = reinterpret_cast<uint4 *>(p.dst + (stream * units + u0) * db);
+    const uint4 *su = reinterpret_cast<const uint4 *>(p.src + uidx * sb);
+    uint4 *du = reinterpret_cast<uint4 *>(p.dst + uidx * db);
     for (int i = threadIdx.x; i < n_units * sb / 16; i += blockDim.x) sbuf[i] = su[i];
     if ((u0 + n_units) * kUnitTokens > len) {  // the last unit is partial
       const int base = (n_units - 1) * db / 16;
@@ -372,6 +397,10 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
   p.src = static_cast<const uint8_t *>(side == 0 ? L.k_cache : L.v_cache);
   p.dst = static_cast<uint8_t *>(dst_cache);
   p.seq_lens = L.seq_lens;
+  p.err = L.err;
+  p.table = L.pages_per_seq > 0 ? L.block_table : nullptr;
+  p.pages_per_seq = L.pages_per_seq;
+  p.n_pages = L.n_pages;
   p.src_codec = side == 0 ? L.codec_k : L.codec_v;
   p.dst_codec = dst_codec;
   p.n_kv = L.n_kv_heads;
@@ -405,10 +434,13 @@ cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_n
   p.seq_lens = L.seq_lens;
   p.n_new = n_new;
   p.err = L.err;
+  p.table = L.pages_per_seq > 0 ? L.block_table : nullptr;
   p.n_seqs = L.n_seqs;
   p.n_kv = L.n_kv_heads;
   p.max_new = max_new;
   p.capacity = L.capacity;
+  p.pages_per_seq = L.pages_per_seq;
+  p.n_pages = L.n_pages;
   const int64_t rows = 2ll * L.n_seqs * max_new * L.n_kv_heads;
   if (rows <= kSmallAppendRows) {
     return launch_pdl(append_small_kernel, dim3(1), dim3(kAppendWarps * 32), 0, stream, p,

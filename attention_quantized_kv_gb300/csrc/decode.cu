@@ -61,7 +61,8 @@ struct DecodeParams {
   __half *out;      // [n_seqs][n_q][128]
   float *lse;       // [n_seqs][n_q] or null
   int32_t *err;
-  int n_seqs, n_kv, n_q, G, n_hg, capacity, max_len;
+  const int32_t *table;  // paged layers: block table; nullptr: contiguous
+  int n_seqs, n_kv, n_q, G, n_hg, capacity, max_len, pages_per_seq, n_pages;
   float scale_log2;
 };
 
@@ -231,14 +232,26 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
 // unit's index in the cache (for the bulk copy).
 struct Cursor {
   int seq, sl, j, n_s;
-  int64_t unit;
+  int64_t unit;   // contiguous layers: the unit's index in the cache
+  int pg0, pg1;   // paged layers: pool pages of pages j/16 and j/16 + 1 of the stream
 };
 
 struct Geo {
   const int32_t *pfx;
   int n_seqs, n_kv, n_hg, KH;
-  int64_t ups;  // units per (seq, kv head) stream of the cache
+  int64_t ups;           // units per (seq, kv head) stream of the cache
+  const int32_t *table;  // paged layers: block table; nullptr: contiguous
+  int pps, n_pages;
 };
+
+// Paged layers: the cursor's pool pages, this page and the next one of the
+// stream (-1 past the stream or for an entry outside the pool); the next
+// page's entry is requested a whole page ahead of its first use.
+__device__ __forceinline__ void cursor_pages(const Geo &q, Cursor &c) {
+  const int pj = c.j / kPageUnits;
+  c.pg0 = page_of(q.table, q.pps, q.n_pages, c.seq, pj);
+  c.pg1 = (pj + 1) * kPageUnits < c.n_s ? page_of(q.table, q.pps, q.n_pages, c.seq, pj + 1) : -1;
+}
 
 __device__ __forceinline__ int64_t cache_unit(const Geo &q, int seq, int sl, int j) {
   return (static_cast<int64_t>(seq) * q.n_kv + sl / q.n_hg) * q.ups + j;
@@ -271,14 +284,26 @@ __device__ __forceinline__ Cursor cursor_at(const Geo &q, int64_t u) {
   c.sl = static_cast<int>(sl);
   c.j = static_cast<int>(within - sl * c.n_s);
   c.unit = cache_unit(q, c.seq, c.sl, c.j);
+  if (q.table) cursor_pages(q, c);
   return c;
 }
 
 // Advance a cursor by `step` units (stops being meaningful past the end).
 __device__ __forceinline__ void cursor_advance(Cursor &c, int step, const Geo &q) {
+  const int old_page = c.j / kPageUnits;
   c.j += step;
   if (c.j < c.n_s) {
     c.unit += step;
+    if (q.table) {
+      const int pj = c.j / kPageUnits;
+      if (pj == old_page + 1) {  // the common crossing: shift, request the next entry
+        c.pg0 = c.pg1;
+        c.pg1 = (pj + 1) * kPageUnits < c.n_s
+                    ? page_of(q.table, q.pps, q.n_pages, c.seq, pj + 1) : -1;
+      } else if (pj != old_page) {
+        cursor_pages(q, c);
+      }
+    }
     return;
   }
   do {
@@ -293,6 +318,15 @@ __device__ __forceinline__ void cursor_advance(Cursor &c, int step, const Geo &q
     }
   } while (c.j >= c.n_s);
   c.unit = cache_unit(q, c.seq, c.sl, c.j);
+  if (q.table) cursor_pages(q, c);
+}
+
+// Index of the cursor's unit in the cache (contiguous) or the pool (paged;
+// an entry outside the pool reads pool page 0, flagged by the caller).
+__device__ __forceinline__ int64_t cursor_unit(const Geo &q, const Cursor &c) {
+  if (!q.table) return c.unit;
+  const int pg = c.pg0 < 0 ? 0 : c.pg0;
+  return (static_cast<int64_t>(pg) * q.n_kv + c.sl / q.n_hg) * kPageUnits + c.j % kPageUnits;
 }
 
 // Merge partial b into a (per lane; m uniform across the lanes of a head).
@@ -631,6 +665,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   geo.n_hg = p.n_hg;
   geo.KH = p.n_kv * p.n_hg;
   geo.ups = p.capacity / kUnitTokens;
+  geo.table = p.table;
+  geo.pps = p.pages_per_seq;
+  geo.n_pages = p.n_pages;
   const int64_t U = static_cast<int64_t>(pfx[p.n_seqs]) * geo.KH;
   const int P = gridDim.x;
   const int64_t u0 = U * blockIdx.x / P;
@@ -645,9 +682,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   auto issue = [&](int k, const Cursor &c) {
     const int s = k % C::NS;
     uint8_t *dst = ring + s * C::STAGE;
+    const int64_t unit = cursor_unit(geo, c);
+    if (geo.table && c.pg0 < 0) set_err(p.err, KVQ_DEVERR_PAGE);
     mbar_arrive_expect_tx(&full[s], C::STAGE);
-    bulk_copy_g2s(dst, p.k_cache + c.unit * C::UK, C::UK, &full[s]);
-    bulk_copy_g2s(dst + C::UK, p.v_cache + c.unit * C::UV, C::UV, &full[s]);
+    bulk_copy_g2s(dst, p.k_cache + unit * C::UK, C::UK, &full[s]);
+    bulk_copy_g2s(dst + C::UK, p.v_cache + unit * C::UV, C::UV, &full[s]);
   };
 
   // Query rows of the segment at cursor c into q_s[buf] (thread 0).
@@ -929,6 +968,9 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
   p.out = static_cast<__half *>(out);
   p.lse = lse;
   p.err = L.err;
+  p.table = L.pages_per_seq > 0 ? L.block_table : nullptr;
+  p.pages_per_seq = L.pages_per_seq;
+  p.n_pages = L.n_pages;
   p.n_seqs = L.n_seqs;
   p.n_kv = L.n_kv_heads;
   p.n_q = L.n_q_heads;

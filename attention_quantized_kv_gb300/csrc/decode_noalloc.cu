@@ -82,6 +82,11 @@ int attn_decode_noalloc(const kvq_layer *L, const void *q, float scale, void *ou
   if (!L->k_cache || !L->v_cache || !L->seq_lens || !q || !out || max_len <= 0)
     return KVQ_EINVAL;
   if (L->capacity % 256 != 0) return KVQ_EALIGN;
+  if (L->pages_per_seq < 0) return KVQ_EINVAL;
+  if (L->pages_per_seq > 0 &&
+      (!L->block_table || L->n_pages <= 0 ||
+       static_cast<int64_t>(L->pages_per_seq) * 256 != L->capacity))
+    return KVQ_EINVAL;
   if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16) || !aligned(L->seq_lens, 4) ||
       (L->err && !aligned(L->err, 4)) || !aligned(q, 8) || !aligned(out, 8) ||
       (lse && !aligned(lse, 4)))

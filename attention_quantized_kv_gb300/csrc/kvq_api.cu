@@ -26,6 +26,12 @@ int check_layer(const kvq_layer *L) {
   if (L->n_q_heads % L->n_kv_heads != 0) return KVQ_EINVAL;
   if (!L->k_cache || !L->v_cache || !L->seq_lens) return KVQ_EINVAL;
   if (L->capacity % 256 != 0) return KVQ_EALIGN;
+  if (L->pages_per_seq < 0) return KVQ_EINVAL;
+  if (L->pages_per_seq > 0) {  // paged: a block table over pools of n_pages pages
+    if (!L->block_table || L->n_pages <= 0) return KVQ_EINVAL;
+    if (static_cast<int64_t>(L->pages_per_seq) * 256 != L->capacity) return KVQ_EINVAL;
+    if (!aligned(L->block_table, 4)) return KVQ_EALIGN;
+  }
   if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16) || !aligned(L->seq_lens, 4) ||
       (L->err && !aligned(L->err, 4)))
     return KVQ_EALIGN;
@@ -66,6 +72,12 @@ const char *kvq_status_str(int status) {
 int64_t kvq_row_bytes(int codec, int32_t head_dim) {
   if (head_dim != kHeadDim || !valid_codec(codec)) return -1;
   return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : 72;
+}
+
+int64_t kvq_pool_bytes(int codec, int32_t n_pages, int32_t n_kv_heads, int32_t head_dim) {
+  const int64_t rb = kvq_row_bytes(codec, head_dim);
+  if (rb < 0 || n_pages <= 0 || n_kv_heads <= 0) return -1;
+  return rb * 256 * n_kv_heads * static_cast<int64_t>(n_pages);
 }
 
 int64_t kvq_cache_bytes(int codec, int32_t n_seqs, int32_t n_kv_heads, int32_t capacity,
@@ -173,10 +185,13 @@ int kv_requantize(const kvq_layer *layer, int32_t side, int32_t dst_codec, void 
   const int src_codec = side == 0 ? layer->codec_k : layer->codec_v;
   const uint8_t *s0 = static_cast<const uint8_t *>(src);
   const uint8_t *d0 = static_cast<const uint8_t *>(dst_cache);
-  const int64_t sb = kvq_cache_bytes(src_codec, layer->n_seqs, layer->n_kv_heads,
-                                     layer->capacity, kHeadDim);
-  const int64_t db = kvq_cache_bytes(dst_codec, layer->n_seqs, layer->n_kv_heads,
-                                     layer->capacity, kHeadDim);
+  const bool paged = layer->pages_per_seq > 0;
+  const int64_t sb = paged ? kvq_pool_bytes(src_codec, layer->n_pages, layer->n_kv_heads, kHeadDim)
+                           : kvq_cache_bytes(src_codec, layer->n_seqs, layer->n_kv_heads,
+                                             layer->capacity, kHeadDim);
+  const int64_t db = paged ? kvq_pool_bytes(dst_codec, layer->n_pages, layer->n_kv_heads, kHeadDim)
+                           : kvq_cache_bytes(dst_codec, layer->n_seqs, layer->n_kv_heads,
+                                             layer->capacity, kHeadDim);
   if (d0 < s0 + sb && s0 < d0 + db) return KVQ_EINVAL;
   const cudaError_t e =
       kvq::launch_requant(*layer, side, dst_codec, dst_cache, static_cast<cudaStream_t>(stream));

@@ -181,6 +181,18 @@ __device__ __forceinline__ uint2 lds64(const void *p) {
   return *reinterpret_cast<const uint2 *>(p);
 }
 
+// Paged layers: a page is kPageUnits units (256 tokens) of every kv head of
+// one sequence; unit j of (sequence s, kv head h) is pool unit
+// (page * n_kv + h) * kPageUnits + j % kPageUnits with page =
+// table[s * pages_per_seq + j / kPageUnits].  page_of returns that entry, or
+// -1 when it is outside [0, n_pages).
+constexpr int kPageUnits = 16;
+__device__ __forceinline__ int page_of(const int32_t *table, int pages_per_seq, int n_pages,
+                                       int s, int64_t page_idx) {
+  const int pg = table[static_cast<int64_t>(s) * pages_per_seq + page_idx];
+  return (pg >= 0 && pg < n_pages) ? pg : -1;
+}
+
 __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
   if (err) atomicOr(err, bit);
 }

@@ -242,7 +242,8 @@ struct DequantParams {
   const int32_t *seq_lens;
   int32_t *err;
   unsigned *tickets;  // the attention kernel's arrival counters, zeroed here
-  int seq, n_kv, capacity, kv_len, n_tiles, n_items;
+  const int32_t *table;  // paged layers: block table; nullptr: contiguous
+  int seq, n_kv, capacity, kv_len, n_tiles, n_items, pages_per_seq, n_pages;
 };
 
 // grid: (n_tiles, n_kv, 2 sides); 256 threads.  The tile's eight 16-token
@@ -257,8 +258,19 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
   const int u_first = tile * (kBN / kUnitTokens);
   const int u_end = min(u_first + kBN / kUnitTokens,
                         static_cast<int>((p.kv_len + kUnitTokens - 1) / kUnitTokens));
-  const uint8_t *src = p.cache[SIDE] +
-                       ((static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + u_first) * UB;
+  // the tile's units (a tile lies inside one page: kPageUnits % (kBN / 16) == 0)
+  int64_t uidx;
+  if (p.table) {
+    int pg = page_of(p.table, p.pages_per_seq, p.n_pages, p.seq, u_first / kPageUnits);
+    if (pg < 0) {
+      if (threadIdx.x == 0) set_err(p.err, KVQ_DEVERR_PAGE);
+      pg = 0;  // read pool page 0 in its place
+    }
+    uidx = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits + u_first % kPageUnits;
+  } else {
+    uidx = (static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + u_first;
+  }
+  const uint8_t *src = p.cache[SIDE] + uidx * UB;
   const int n16 = (u_end - u_first) * UB / 16;
   for (int i = threadIdx.x; i < n16; i += 256)
     reinterpret_cast<uint4 *>(units_sh)[i] = reinterpret_cast<const uint4 *>(src)[i];
@@ -931,6 +943,9 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   dp.seq_lens = L.seq_lens;
   dp.err = L.err;
   dp.tickets = reinterpret_cast<unsigned *>(ws + pl.ticket_off);
+  dp.table = L.pages_per_seq > 0 ? L.block_table : nullptr;
+  dp.pages_per_seq = L.pages_per_seq;
+  dp.n_pages = L.n_pages;
   dp.seq = seq;
   dp.n_kv = L.n_kv_heads;
   dp.capacity = L.capacity;

@@ -75,6 +75,21 @@
  *   The layout stores exactly the canonical bytes (8.5 / 4.5 / 16 bits per
  *   value); it only orders them so that each thread of the decode kernel
  *   reads its tensor-core operand fragments with aligned 16-byte loads.
+ *
+ * Paged layout (kvq_layer.pages_per_seq > 0; block-level KV management as in
+ * the vLLM PagedAttention entry of the buun-llama-cpp references, with the
+ * pool shared by the sequences and 256-aligned as in the serverAppConfigs
+ * commit log):
+ *   a page is 256 tokens (16 units) of every kv head of one sequence; each
+ *   side's pool is [n_pages][n_kv_heads][16 units][unit_bytes]
+ *   (kvq_pool_bytes()); block_table[s][p] is the pool page that holds
+ *   tokens 256p .. 256p + 255 of sequence s (-1: not mapped).  Unit j of
+ *   (sequence s, kv head h) is pool unit
+ *   (block_table[s][j / 16] * n_kv_heads + h) * 16 + j % 16.  capacity is
+ *   then pages_per_seq * 256.  Every page a call touches (tokens below the
+ *   length, or being appended) must be mapped to a page in [0, n_pages);
+ *   otherwise the device sets KVQ_DEVERR_PAGE and skips the row (append,
+ *   re-encode) or reads pool page 0 in its place (attention).
  * ------------------------------------------------------------------------
  */
 #ifndef KVQ_H
@@ -112,11 +127,13 @@ typedef enum {
 #define KVQ_DEVERR_MAXLEN 2   /* decode: seq_lens[s] > max_len; keys past max_len ignored */
 #define KVQ_DEVERR_TIMEOUT 4  /* a bounded wait on an async copy gave up */
 #define KVQ_DEVERR_SEQLEN 8   /* prefill: seq_lens[seq] < q_start + n_q_tok */
+#define KVQ_DEVERR_PAGE 16    /* paged: a block-table entry outside [0, n_pages) */
 
 /* One layer's cache.  All pointers are device pointers owned by the caller.
- * k_cache / v_cache: kvq_cache_bytes() bytes each, 16-byte aligned, in the
- * layout above.  seq_lens: int32[n_seqs], the number of valid tokens of each
- * sequence.  err: optional int32 error word (NULL to skip). */
+ * k_cache / v_cache: kvq_cache_bytes() bytes each (kvq_pool_bytes() when
+ * paged), 16-byte aligned, in the layouts above.  seq_lens: int32[n_seqs],
+ * the number of valid tokens of each sequence.  err: optional int32 error
+ * word (NULL to skip). */
 typedef struct kvq_layer {
     int32_t n_seqs;
     int32_t n_kv_heads;
@@ -125,11 +142,14 @@ typedef struct kvq_layer {
     int32_t capacity;   /* tokens per (seq, kv head) stream; multiple of 256 */
     int32_t codec_k;    /* kvq_codec of the K side */
     int32_t codec_v;    /* kvq_codec of the V side */
-    int32_t reserved;   /* must be 0 */
+    int32_t pages_per_seq; /* 0: contiguous caches; > 0: paged (capacity = 256 * this) */
     void *k_cache;
     void *v_cache;
     int32_t *seq_lens;
     int32_t *err;
+    const int32_t *block_table; /* paged: int32 [n_seqs][pages_per_seq], device; else NULL */
+    int32_t n_pages;            /* paged: pages in each side's pool; else 0 */
+    int32_t reserved;           /* must be 0 */
 } kvq_layer;
 
 /* Human-readable name of a status code (static string). */
@@ -137,6 +157,10 @@ KVQ_API const char *kvq_status_str(int status);
 
 /* Bytes of one canonical row (256 / 136 / 72 for head_dim 128), or -1. */
 KVQ_API int64_t kvq_row_bytes(int codec, int32_t head_dim);
+
+/* Bytes of one side's page pool: n_pages * n_kv_heads * 256 * row bytes, or
+ * -1 on bad arguments. */
+KVQ_API int64_t kvq_pool_bytes(int codec, int32_t n_pages, int32_t n_kv_heads, int32_t head_dim);
 
 /* Bytes of one side's cache for the given geometry, or -1 on bad arguments. */
 KVQ_API int64_t kvq_cache_bytes(int codec, int32_t n_seqs, int32_t n_kv_heads, int32_t capacity,
