@@ -97,6 +97,13 @@ def get(name: str) -> Workload:
         return Workload(name, "prefill", 1, 32, 8, [32768], [(Q8_0, Q8_0)], 4, append_new=2048,
                         description="1 seq, 32768 cached + 2048-token ubatch appended, causal "
                                     "attention of 2048 queries over 34816 keys, 32q/8kv, q8_0")
+    if name == "decode_ragged16_kf16_vq8_paged":
+        w = get("decode_ragged16_kf16_vq8")
+        w.name = name
+        w.extra = {"paged": True, "page_seed": 12}
+        w.description = ("decode_ragged16_kf16_vq8 over a paged pool: 256-token pages, "
+                         "block table shuffled from seed 12, pool = pages needed + 5%")
+        return w
     if name == "degrade_f16_q8_2x200704":
         return Workload(name, "degrade", 2, 32, 4, [200704, 200704], [(F16, F16)], 3,
                         extra={"side": 0, "dst": Q8_0},
@@ -106,7 +113,8 @@ def get(name: str) -> Workload:
 
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
-       "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704"]
+       "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
+       "decode_ragged16_kf16_vq8_paged"]
 
 
 # ------------------------------------------------------------------ draws
@@ -168,3 +176,20 @@ def kv_rows(w: Workload, layer: int, side: int, seq: int, start: int, count: int
 def queries(w: Workload, layer: int, n_tok: int, device="cpu") -> torch.Tensor:
     """fp16 [n_seqs, n_tok, n_q, 128] query rows of one layer."""
     return normal_fp16((w.n_seqs, n_tok, w.n_q, HEAD_DIM), w.seed, 900_000 + layer, device)
+
+
+def page_table(w: Workload):
+    """(block table int32 [n_seqs][capacity/256], pool pages) of a paged
+    workload: every page a sequence uses (final lengths) mapped to a distinct
+    pool page, in an order shuffled from the workload's page seed; unused
+    pages -1."""
+    pps = w.capacity // 256
+    need = [(n + 255) // 256 for n in w.final_lens()]
+    n_pages = int(sum(need) * 1.05) + 1
+    pages = np.random.default_rng(w.extra["page_seed"]).permutation(n_pages)
+    t = -np.ones((w.n_seqs, pps), np.int32)
+    k = 0
+    for s in range(w.n_seqs):
+        t[s, :need[s]] = pages[k:k + need[s]]
+        k += need[s]
+    return t, n_pages

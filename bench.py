@@ -156,8 +156,16 @@ class OursArm:
         self.init_lens = torch.tensor(w.lens, dtype=torch.int32, device=device)
         self.final_lens = torch.tensor(w.final_lens(), dtype=torch.int32, device=device)
         n_tok = w.append_new if w.kind == "prefill" else 1
+        paged = bool(w.extra.get("paged"))
+        if paged:
+            table, n_pages = wl.page_table(w)
+            table = torch.from_numpy(table).to(device)
         for l, (ck, cv) in enumerate(w.codecs):
-            L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device)
+            if paged:
+                L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device,
+                                n_pages=n_pages, block_table=table)
+            else:
+                L = kvq.KVLayer(w.n_seqs, w.n_kv, w.n_q, w.capacity, ck, cv, device=device)
             self._fill(L, l)
             self.layers.append(L)
             qq = wl.queries(w, l, n_tok, device)
