@@ -96,6 +96,14 @@ def _load():
         lib.kvqo_paged_unit.restype = ctypes.c_int64
         lib.kvqo_page_move.argtypes = [ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        i32p, ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int]
+        lib.kvqo_probe_mass.argtypes = [ctypes.c_int, u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, i32p, u16p, ctypes.c_double, f64p]
+        f32p = ctypes.POINTER(ctypes.c_float)
+        lib.kvqo_evict_select.argtypes = [f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_int, i32p]
+        lib.kvqo_compact_side.argtypes = [ctypes.c_int, ctypes.c_int, u8p, u8p, ctypes.c_int,
+                                          ctypes.c_int, ctypes.c_int, i32p, i32p, i32p,
+                                          ctypes.c_int]
         lib.kvqo_num_threads.restype = ctypes.c_int
         _lib = lib
         return lib
@@ -340,3 +348,52 @@ def from_pool(codec: int, pool: np.ndarray, n_seqs: int, n_kv: int, capacity: in
     if rc:
         raise ValueError("bad paged geometry")
     return cache
+
+
+# --------------------------------------------------------------------------- probe-scored eviction
+
+def probe_mass(codec_k: int, cache_k: np.ndarray, n_seqs: int, n_kv: int, n_q: int,
+               capacity: int, seq_lens, q, scale: float) -> np.ndarray:
+    """fp64 [n_seqs, capacity]: per token, the softmax weight summed over query heads."""
+    qb = _as_half_bits(q).reshape(-1)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    cache_k = np.ascontiguousarray(cache_k, dtype=np.uint8)
+    out = np.zeros((n_seqs, capacity), np.float64)
+    rc = _load().kvqo_probe_mass(codec_k, _ptr(cache_k, ctypes.c_uint8), n_seqs, n_kv, n_q,
+                                 capacity, _ptr(lens, ctypes.c_int32), _ptr(qb, ctypes.c_uint16),
+                                 float(scale), _ptr(out, ctypes.c_double))
+    if rc:
+        raise ValueError("oracle probe failed")
+    return out
+
+
+def evict_select(score, length: int, n_sink: int, n_recent: int, n_evict: int) -> np.ndarray:
+    sc = np.ascontiguousarray(score, dtype=np.float32)
+    out = np.zeros(max(n_evict, 1), np.int32)
+    w = _load().kvqo_evict_select(_ptr(sc, ctypes.c_float), int(length), int(n_sink),
+                                  int(n_recent), int(n_evict), _ptr(out, ctypes.c_int32))
+    if w < 0:
+        raise MemoryError
+    return out[:w]
+
+
+def compact_side(codec: int, side: int, cache: np.ndarray, n_seqs: int, n_kv: int,
+                 capacity: int, seq_lens, evict) -> np.ndarray:
+    """Cache with the listed positions of each sequence removed (evict: list of
+    increasing position lists)."""
+    me = max(1, max(len(e) for e in evict))
+    ev = np.zeros((n_seqs, me), np.int32)
+    nev = np.zeros(n_seqs, np.int32)
+    for s, e in enumerate(evict):
+        ev[s, :len(e)] = e
+        nev[s] = len(e)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    out = np.zeros(cache_bytes(codec, n_seqs, n_kv, capacity), np.uint8)
+    rc = _load().kvqo_compact_side(codec, side, _ptr(cache, ctypes.c_uint8),
+                                   _ptr(out, ctypes.c_uint8), n_seqs, n_kv, capacity,
+                                   _ptr(lens, ctypes.c_int32), _ptr(ev, ctypes.c_int32),
+                                   _ptr(nev, ctypes.c_int32), me)
+    if rc:
+        raise ValueError("oracle compaction failed")
+    return out

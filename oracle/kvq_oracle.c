@@ -46,6 +46,15 @@
  *    lives at pool unit (table[s][j / 16] * n_kv + h) * 16 + j % 16.  The
  *    oracle computes on the contiguous layout and moves whole units between
  *    the two layouts (kvqo_page_scatter / kvqo_page_gather).
+ *  - Probe-scored eviction (the Sparse KV eviction item of the Officina
+ *    "How It Works" list: an attention probe, q.K softmax with exponential
+ *    decay, scores the cells; the lowest-scored middle cells are evicted
+ *    first; sinks and recent cells are protected).  The probe mass of token t
+ *    of a sequence is the softmax weight the decode query of every query head
+ *    puts on t, summed over the query heads; score = decay * score + mass.
+ *    Eviction picks the n lowest (score, t) pairs among the middle tokens
+ *    [n_sink, len - n_recent) and removes them: the kept tokens move down
+ *    in order, bytes unchanged.
  *  - The cache byte layout, written from its specification (the library's
  *    public header documents the same layout): the cache of one layer and
  *    side is [seq][kv_head][capacity/16 units][unit bytes]; a unit holds 16
@@ -573,6 +582,122 @@ int kvqo_ladder_next(const int *codecs, int n, const int *order, int n_order, do
                 *tensor = t;
                 *codec = rungs[k];
                 return 1;
+            }
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Probe-scored eviction.                                                    */
+/* ------------------------------------------------------------------------ */
+
+/* mass[s][t] (t < seq_lens[s], capacity columns) = sum over the n_q query
+ * heads of softmax_t(scale * q_h . k^_t) over the sequence's keys, in fp64. */
+int kvqo_probe_mass(int codec_k, const uint8_t *cache_k, int n_seqs, int n_kv, int n_q,
+                    int capacity, const int32_t *seq_lens, const uint16_t *q, double scale,
+                    double *mass)
+{
+    if (n_kv <= 0 || n_q % n_kv)
+        return -1;
+    int G = n_q / n_kv;
+    for (int s = 0; s < n_seqs; ++s) {
+        int64_t T = seq_lens[s];
+        if (T < 0 || T > capacity)
+            return -1;
+        double *m = mass + (int64_t)s * capacity;
+        for (int64_t t = 0; t < capacity; ++t)
+            m[t] = 0.0;
+        if (T == 0)
+            continue;
+        double *K = (double *)malloc(sizeof(double) * (size_t)T * KVQO_D);
+        double *sc = (double *)malloc(sizeof(double) * (size_t)T);
+        if (!K || !sc) {
+            free(K); free(sc);
+            return -1;
+        }
+        for (int h = 0; h < n_kv; ++h) {
+            kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, s, h, T, K);
+            for (int j = 0; j < G; ++j) {
+                const uint16_t *qh = q + ((int64_t)s * n_q + (int64_t)h * G + j) * KVQO_D;
+                double mx = -INFINITY;
+                for (int64_t t = 0; t < T; ++t) {
+                    double d = 0.0;
+                    for (int c = 0; c < KVQO_D; ++c)
+                        d += kvqo_half_to_double(qh[c]) * K[t * KVQO_D + c];
+                    sc[t] = scale * d;
+                    if (sc[t] > mx)
+                        mx = sc[t];
+                }
+                double sum = 0.0;
+                for (int64_t t = 0; t < T; ++t)
+                    sum += exp(sc[t] - mx);
+                for (int64_t t = 0; t < T; ++t)
+                    m[t] += exp(sc[t] - mx) / sum;
+            }
+        }
+        free(K);
+        free(sc);
+    }
+    return 0;
+}
+
+/* The n_evict positions t in [n_sink, len - n_recent) with the smallest
+ * (score[t], t), written in increasing t.  Returns how many were written
+ * (fewer when the middle range is shorter). */
+int kvqo_evict_select(const float *score, int len, int n_sink, int n_recent, int n_evict,
+                      int32_t *out)
+{
+    int lo = n_sink, hi = len - n_recent;
+    if (hi <= lo || n_evict <= 0)
+        return 0;
+    int n = hi - lo, k = n_evict < n ? n_evict : n;
+    uint8_t *taken = (uint8_t *)calloc((size_t)n, 1);
+    if (!taken)
+        return -1;
+    for (int r = 0; r < k; ++r) { /* k passes of a plain minimum search */
+        int best = -1;
+        for (int i = 0; i < n; ++i) {
+            if (taken[i])
+                continue;
+            if (best < 0 || score[lo + i] < score[lo + best])
+                best = i; /* strict: the lower t keeps a tie */
+        }
+        taken[best] = 1;
+    }
+    int w = 0;
+    for (int i = 0; i < n; ++i)
+        if (taken[i])
+            out[w++] = lo + i;
+    free(taken);
+    return w;
+}
+
+/* Remove the listed positions (increasing, below seq_lens[s]) of every
+ * sequence from one side's cache: kept tokens move down in order, bytes
+ * unchanged; dst is a separate cache of the same codec (zero elsewhere).
+ * evict: [n_seqs][max_evict] positions, n_ev[s] of them used. */
+int kvqo_compact_side(int codec, int side, const uint8_t *src, uint8_t *dst, int n_seqs,
+                      int n_kv, int capacity, const int32_t *seq_lens, const int32_t *evict,
+                      const int32_t *n_ev, int max_evict)
+{
+    if (kvqo_row_bytes(codec) < 0)
+        return -1;
+    uint8_t row[256];
+    for (int s = 0; s < n_seqs; ++s) {
+        const int32_t *ev = evict + (int64_t)s * max_evict;
+        for (int h = 0; h < n_kv; ++h) {
+            const uint8_t *ss = kvqo_stream((uint8_t *)src, codec, n_kv, capacity, s, h);
+            uint8_t *ds = kvqo_stream(dst, codec, n_kv, capacity, s, h);
+            int e = 0;
+            int64_t w = 0;
+            for (int64_t t = 0; t < seq_lens[s]; ++t) {
+                if (e < n_ev[s] && ev[e] == t) {
+                    ++e;
+                    continue;
+                }
+                kvqo_get_row(ss, codec, side, t, row);
+                kvqo_put_row(ds, codec, side, w++, row);
             }
         }
     }

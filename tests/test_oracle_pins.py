@@ -563,3 +563,78 @@ def test_pool_round_trip_under_a_shuffled_table(codec):
     used = {int(p) for p in table.flatten() if p >= 0}
     assert not pool.reshape(n_pages, n_kv * 16, ub)[[p for p in range(n_pages)
                                                       if p not in used]].any()
+
+
+# --------------------------------------------------------------------------- probe-scored eviction
+
+def _probe_cache(rng, codec, n_seqs, n_kv, cap, lens, scale_rows=1.0):
+    rows = (rng.standard_normal((n_seqs, max(lens), n_kv, 128)) * scale_rows).astype(np.float16)
+    c = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, cap), np.uint8)
+    oracle.append_side(codec, 0, c, n_seqs, n_kv, cap, [0] * n_seqs, lens, rows)
+    return c, rows
+
+
+def test_probe_mass_sums_to_the_head_count_and_is_flat_for_a_zero_query():
+    n_seqs, n_kv, n_q, cap, lens = 2, 2, 6, 256, [50, 7]
+    rng = np.random.default_rng(80)
+    c, _ = _probe_cache(rng, 1, n_seqs, n_kv, cap, lens)
+    q = rng.standard_normal((n_seqs, n_q, 128)).astype(np.float16)
+    m = oracle.probe_mass(1, c, n_seqs, n_kv, n_q, cap, lens, q, 0.1)
+    for s in range(n_seqs):
+        assert m[s, :lens[s]].sum() == pytest.approx(n_q, rel=1e-12)
+        assert not m[s, lens[s]:].any()
+    m0 = oracle.probe_mass(1, c, n_seqs, n_kv, n_q, cap, lens, np.zeros_like(q), 0.1)
+    for s in range(n_seqs):
+        assert np.allclose(m0[s, :lens[s]], n_q / lens[s], rtol=1e-12)
+
+
+def test_probe_mass_of_a_dominant_key_and_the_gqa_mapping():
+    # f16 keys: query head j of kv head h sees keys of kv head h only
+    n_seqs, n_kv, n_q, cap, T = 1, 2, 4, 256, 9
+    K = np.zeros((1, T, n_kv, 128), np.float16)
+    K[0, 3, 0, 0] = 8.0   # kv head 0: key 3 dominates for q e_0
+    K[0, 6, 1, 1] = 8.0   # kv head 1: key 6 dominates for q e_1
+    c = np.zeros(oracle.cache_bytes(0, 1, n_kv, cap), np.uint8)
+    oracle.append_side(0, 0, c, 1, n_kv, cap, [0], [T], K)
+    q = np.zeros((1, n_q, 128), np.float16)
+    q[0, 0:2, 0] = 8.0    # query heads 0, 1 -> kv head 0
+    q[0, 2:4, 1] = 8.0    # query heads 2, 3 -> kv head 1
+    m = oracle.probe_mass(0, c, 1, n_kv, n_q, cap, [T], q, 1.0)
+    w = 1.0 / (1.0 + (T - 1) * math.exp(-64.0))  # softmax weight of the dominant key
+    assert m[0, 3] == pytest.approx(2 * w, rel=1e-12)
+    assert m[0, 6] == pytest.approx(2 * w, rel=1e-12)
+    assert m[0, :T].sum() == pytest.approx(n_q, rel=1e-12)
+
+
+def test_evict_select_against_brute_force_and_protection():
+    rng = np.random.default_rng(81)
+    for _ in range(300):
+        length = int(rng.integers(0, 60))
+        sink, recent, n_ev = (int(rng.integers(0, 6)), int(rng.integers(0, 6)),
+                              int(rng.integers(0, 20)))
+        sc = rng.integers(0, 8, length).astype(np.float32)  # many ties
+        got = oracle.evict_select(sc, length, sink, recent, n_ev)
+        mid = list(range(sink, max(sink, length - recent)))
+        want = sorted(sorted(mid, key=lambda t: (sc[t], t))[:n_ev])
+        assert list(got) == want
+        assert all(sink <= t < length - recent for t in got)
+
+
+@pytest.mark.parametrize("codec", [0, 1, 2])
+@pytest.mark.parametrize("side", [0, 1])
+def test_compaction_equals_appending_the_kept_rows(codec, side):
+    n_seqs, n_kv, cap, lens = 2, 2, 256, [40, 17]
+    rng = np.random.default_rng(82 + codec + 3 * side)
+    rows = rng.standard_normal((n_seqs, max(lens), n_kv, 128)).astype(np.float16)
+    c = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, cap), np.uint8)
+    oracle.append_side(codec, side, c, n_seqs, n_kv, cap, [0] * n_seqs, lens, rows)
+    evict = [[1, 2, 17, 39], [0, 16]]
+    got = oracle.compact_side(codec, side, c, n_seqs, n_kv, cap, lens, evict)
+    kept_lens = [lens[s] - len(evict[s]) for s in range(n_seqs)]
+    kept = np.zeros((n_seqs, max(kept_lens), n_kv, 128), np.float16)
+    for s in range(n_seqs):
+        keep = [t for t in range(lens[s]) if t not in evict[s]]
+        kept[s, :len(keep)] = rows[s, keep]
+    want = np.zeros_like(c)
+    oracle.append_side(codec, side, want, n_seqs, n_kv, cap, [0] * n_seqs, kept_lens, kept)
+    assert np.array_equal(got, want)
