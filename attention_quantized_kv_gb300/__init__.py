@@ -3,7 +3,8 @@
 A thin Python layer over libkvq's C ABI (include/kvq.h).  PyTorch provides
 device memory and streams; every step of the path (quantize-on-append,
 split-K decode attention with its log-sum-exp merge, chunked-prefill
-attention) runs in the library's sm_103a kernels.  The functions below only
+attention, the degrade ladder's re-encode, probe-scored eviction) runs in the
+library's sm_103a kernels.  The functions below only
 marshal arguments: they take torch tensors, pass their device pointers and
 raise ``KVQError`` on a non-zero status.
 """
@@ -15,14 +16,16 @@ import math
 import torch
 
 from . import _abi
-from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN,
-                   KVQ_DEVERR_PAGE, KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT, kvq_layer)
+from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_DEVERR_CAPACITY, KVQ_DEVERR_EVICT,
+                   KVQ_DEVERR_MAXLEN, KVQ_DEVERR_PAGE, KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT,
+                   kvq_layer)
 
 __all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "CODEC_NAMES", "KVQError", "KVLayer",
            "kv_append_quantize", "attn_decode_workspace", "attn_decode",
            "attn_prefill_workspace", "attn_prefill_chunk", "kvq_row_bytes", "kvq_cache_bytes",
            "kvq_pool_bytes", "KVQ_DEVERR_PAGE", "kv_requantize", "degrade", "aggregate_bpv",
-           "ladder_next", "default_scale"]
+           "ladder_next", "default_scale", "KVQ_DEVERR_EVICT", "kv_probe_scores",
+           "kv_evict_select", "kv_compact", "evict"]
 
 CODEC_NAMES = {KVQ_F16: "f16", KVQ_Q8_0: "q8_0", KVQ_Q4_0: "q4_0"}
 HEAD_DIM = 128
@@ -235,3 +238,71 @@ def ladder_next(codecs, floor_bpv: float, order=None):
     _check(_abi.load().kvq_ladder_next(arr, len(codecs), ordp, n_order, float(floor_bpv),
                                        ctypes.byref(t), ctypes.byref(k)), "kvq_ladder_next")
     return None if t.value < 0 else (t.value, k.value)
+
+
+# --------------------------------------------------------------------------- probe eviction
+
+def kv_probe_scores(layer: KVLayer, q, scale: float, lse, decay: float, scores,
+                    stream=None) -> None:
+    """Fold one probe into ``scores`` (fp32 [n_seqs, capacity], device, in place):
+    score = decay * score + the softmax mass the decode query ``q`` (fp16
+    [n_seqs, n_q, 128]) puts on each token, summed over the query heads; ``lse``
+    is attn_decode's fp32 [n_seqs, n_q] output for the same q and scale."""
+    assert q.dtype == torch.float16 and q.is_contiguous()
+    assert lse.dtype == torch.float32 and lse.is_contiguous()
+    assert scores.dtype == torch.float32 and scores.is_contiguous()
+    assert scores.numel() == layer.n_seqs * layer.capacity
+    assert lse.numel() == layer.n_seqs * layer.n_q_heads
+    d = layer.desc()
+    _check(_abi.load().kv_probe_scores(ctypes.byref(d), _ptr(q), float(scale), _ptr(lse),
+                                       float(decay), _ptr(scores), _stream_ptr(stream)),
+           "kv_probe_scores")
+
+
+def kv_evict_select(layer: KVLayer, scores, n_sink: int, n_recent: int, n_evict: int, evict,
+                    n_evicted, stream=None) -> None:
+    """Per sequence, the n_evict lowest (score, position) middle positions in
+    increasing order into ``evict`` (int32 [n_seqs, n_evict]) and their count
+    into ``n_evicted`` (int32 [n_seqs])."""
+    assert scores.dtype == torch.float32 and scores.numel() == layer.n_seqs * layer.capacity
+    assert evict.dtype == torch.int32 and evict.numel() >= layer.n_seqs * max(int(n_evict), 0)
+    assert n_evicted.dtype == torch.int32 and n_evicted.numel() == layer.n_seqs
+    d = layer.desc()
+    _check(_abi.load().kv_evict_select(ctypes.byref(d), _ptr(scores), int(n_sink), int(n_recent),
+                                       int(n_evict), _ptr(evict), _ptr(n_evicted),
+                                       _stream_ptr(stream)), "kv_evict_select")
+
+
+def kv_compact(layer: KVLayer, evict, n_evicted, k_dst, v_dst, scores=None, scores_dst=None,
+               lens_dst=None, stream=None) -> None:
+    """Remove the listed positions (``evict`` int32 [n_seqs, max_evict]) from both
+    sides into ``k_dst``/``v_dst`` (uint8, the sizes of the layer's caches);
+    optionally the scores and the new lengths too."""
+    assert evict.dtype == torch.int32 and evict.dim() == 2 and evict.is_contiguous()
+    assert n_evicted.dtype == torch.int32 and n_evicted.numel() == layer.n_seqs
+    assert k_dst.dtype == torch.uint8 and v_dst.dtype == torch.uint8
+    if k_dst.numel() != _side_bytes(layer, layer.codec_k) or \
+            v_dst.numel() != _side_bytes(layer, layer.codec_v):
+        raise ValueError("k_dst / v_dst must have the sizes of the layer's caches")
+    d = layer.desc()
+    _check(_abi.load().kv_compact(ctypes.byref(d), _ptr(evict), _ptr(n_evicted),
+                                  int(evict.shape[1]), _ptr(k_dst), _ptr(v_dst), _ptr(scores),
+                                  _ptr(scores_dst), _ptr(lens_dst), _stream_ptr(stream)),
+           "kv_compact")
+
+
+def evict(layer: KVLayer, scores, n_sink: int, n_recent: int, n_evict: int, stream=None):
+    """Select and remove up to n_evict tokens per sequence: new zeroed cache
+    buffers (torch allocations), the layer repointed at them and at the new
+    lengths.  Returns (compacted scores, evict list, n_evicted)."""
+    dev = layer.k_cache.device
+    ev = torch.zeros((layer.n_seqs, max(int(n_evict), 1)), dtype=torch.int32, device=dev)
+    nev = torch.zeros(layer.n_seqs, dtype=torch.int32, device=dev)
+    kv_evict_select(layer, scores, n_sink, n_recent, n_evict, ev, nev, stream)
+    k_dst = torch.zeros_like(layer.k_cache)
+    v_dst = torch.zeros_like(layer.v_cache)
+    s_dst = torch.zeros_like(scores)
+    lens = torch.empty_like(layer.seq_lens)
+    kv_compact(layer, ev, nev, k_dst, v_dst, scores, s_dst, lens, stream)
+    layer.k_cache, layer.v_cache, layer.seq_lens = k_dst, v_dst, lens
+    return s_dst, ev, nev

@@ -15,14 +15,14 @@ LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 KVQ_F16, KVQ_Q8_0, KVQ_Q4_0 = 0, 1, 2
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECAPACITY, KVQ_EALIGN, KVQ_EWORKSPACE, KVQ_ECUDA = range(7)
 KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN, KVQ_DEVERR_TIMEOUT, KVQ_DEVERR_SEQLEN = 1, 2, 4, 8
-KVQ_DEVERR_PAGE = 16
+KVQ_DEVERR_PAGE, KVQ_DEVERR_EVICT = 16, 32
 
 # Every function the header declares (checked by the tests against include/kvq.h).
 EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kvq_pool_bytes",
            "kv_append_quantize",
            "attn_decode_workspace", "attn_decode", "attn_decode_noalloc",
            "attn_prefill_workspace", "attn_prefill_chunk", "kv_requantize", "kvq_aggregate_bpv",
-           "kvq_ladder_next")
+           "kvq_ladder_next", "kv_probe_scores", "kv_evict_select", "kv_compact")
 
 
 class kvq_layer(ctypes.Structure):
@@ -79,6 +79,9 @@ def load(path: str | None = None):
         "kvq_ladder_next": (ctypes.c_int, [ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
                                            ctypes.c_double, ctypes.POINTER(i32),
                                            ctypes.POINTER(i32)]),
+        "kv_probe_scores": (ctypes.c_int, [L, P, f32, P, f32, P, P]),
+        "kv_evict_select": (ctypes.c_int, [L, P, i32, i32, i32, P, P, P]),
+        "kv_compact": (ctypes.c_int, [L, P, P, i32, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -198,6 +198,69 @@ int kv_requantize(const kvq_layer *layer, int32_t side, int32_t dst_codec, void 
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
+static bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+  const uint8_t *x = static_cast<const uint8_t *>(a), *y = static_cast<const uint8_t *>(b);
+  return x < y + nb && y < x + na;
+}
+
+// Bytes of one side's cache (or pool, for a paged layer).
+static int64_t side_bytes(const kvq_layer *L, int codec) {
+  return L->pages_per_seq > 0
+             ? kvq_pool_bytes(codec, L->n_pages, L->n_kv_heads, kHeadDim)
+             : kvq_cache_bytes(codec, L->n_seqs, L->n_kv_heads, L->capacity, kHeadDim);
+}
+
+int kv_probe_scores(const kvq_layer *layer, const void *q, float scale, const float *lse,
+                    float decay, float *scores, void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!q || !lse || !scores) return KVQ_EINVAL;
+  if (!aligned(q, 8) || !aligned(lse, 4) || !aligned(scores, 4)) return KVQ_EALIGN;
+  const cudaError_t e = kvq::launch_probe(*layer, q, scale, lse, decay, scores,
+                                          static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+int kv_evict_select(const kvq_layer *layer, const float *scores, int32_t n_sink,
+                    int32_t n_recent, int32_t n_evict, int32_t *evict, int32_t *n_evicted,
+                    void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!scores || !evict || !n_evicted || n_sink < 0 || n_recent < 0 || n_evict < 0)
+    return KVQ_EINVAL;
+  if (!aligned(scores, 4) || !aligned(evict, 4) || !aligned(n_evicted, 4)) return KVQ_EALIGN;
+  const cudaError_t e =
+      kvq::launch_evict_select(*layer, scores, n_sink, n_recent, n_evict, evict, n_evicted,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
+int kv_compact(const kvq_layer *layer, const int32_t *evict, const int32_t *n_evicted,
+               int32_t max_evict, void *k_dst, void *v_dst, const float *scores,
+               float *scores_dst, int32_t *lens_dst, void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!evict || !n_evicted || max_evict < 0 || !k_dst || !v_dst) return KVQ_EINVAL;
+  if ((scores == nullptr) != (scores_dst == nullptr)) return KVQ_EINVAL;
+  if (!aligned(evict, 4) || !aligned(n_evicted, 4) || !aligned(k_dst, 16) ||
+      !aligned(v_dst, 16) || (scores && !aligned(scores, 4)) ||
+      (scores_dst && !aligned(scores_dst, 4)) || (lens_dst && !aligned(lens_dst, 4)))
+    return KVQ_EALIGN;
+  const int64_t kb = side_bytes(layer, layer->codec_k), vb = side_bytes(layer, layer->codec_v);
+  if (overlaps(k_dst, kb, layer->k_cache, kb) || overlaps(k_dst, kb, layer->v_cache, vb) ||
+      overlaps(v_dst, vb, layer->k_cache, kb) || overlaps(v_dst, vb, layer->v_cache, vb) ||
+      overlaps(k_dst, kb, v_dst, vb))
+    return KVQ_EINVAL;
+  const int64_t sb = static_cast<int64_t>(layer->n_seqs) * layer->capacity * 4;
+  if (scores && overlaps(scores, sb, scores_dst, sb)) return KVQ_EINVAL;
+  if (lens_dst && overlaps(lens_dst, 4 * layer->n_seqs, layer->seq_lens, 4 * layer->n_seqs))
+    return KVQ_EINVAL;
+  const cudaError_t e =
+      kvq::launch_compact(*layer, evict, n_evicted, max_evict, k_dst, v_dst, scores, scores_dst,
+                          lens_dst, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
 double kvq_aggregate_bpv(const int32_t *codecs, int32_t n) {
   if (!codecs || n <= 0) return -1.0;
   double sum = 0.0;

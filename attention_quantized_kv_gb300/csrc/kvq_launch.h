@@ -54,4 +54,14 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
                            int n_q_tok, const void *q, float scale, void *out, float *lse,
                            void *workspace, cudaStream_t stream);
 
+// Probe-scored eviction (evict.cu).
+cudaError_t launch_probe(const kvq_layer &L, const void *q, float scale, const float *lse,
+                         float decay, float *scores, cudaStream_t stream);
+cudaError_t launch_evict_select(const kvq_layer &L, const float *scores, int n_sink,
+                                int n_recent, int n_evict, int32_t *evict, int32_t *n_evicted,
+                                cudaStream_t stream);
+cudaError_t launch_compact(const kvq_layer &L, const int32_t *evict, const int32_t *n_evicted,
+                           int max_evict, void *k_dst, void *v_dst, const float *scores,
+                           float *scores_dst, int32_t *lens_dst, cudaStream_t stream);
+
 }  // namespace kvq

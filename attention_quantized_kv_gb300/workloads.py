@@ -24,6 +24,13 @@ Workloads (head_dim 128 throughout):
                          16 layers, 2 sequences x 200704 keys, 32 query / 4 KV
                          heads; each of the 32 (layer, side) tensors is f16,
                          q8_0 or q4_0 (11/11/10, shuffled by seed 3), N(0,1).
+  evict_ragged16_kf16_vq8
+                         the decode_ragged16_kf16_vq8 cache and query; one
+                         probe-scored eviction step: decode (with its
+                         log-sum-exp), probe scores (decay 0.9), selection of
+                         the 2048 lowest middle cells per sequence (4 sink and
+                         1024 recent cells protected) and compaction of K, V,
+                         scores and lengths into second buffers.
   prefill_q8_32k_plus_2k 1 sequence with 32768 cached keys plus a 2048-token
                          ubatch quantize-appended, then causal attention of the
                          2048 queries over 34816 keys; 32 query / 8 KV heads,
@@ -43,7 +50,7 @@ HEAD_DIM = 128
 @dataclass
 class Workload:
     name: str
-    kind: str                 # "decode", "prefill" or "degrade"
+    kind: str                 # "decode", "prefill", "degrade" or "evict"
     n_seqs: int
     n_q: int
     n_kv: int
@@ -109,12 +116,34 @@ def get(name: str) -> Workload:
                         extra={"side": 0, "dst": Q8_0},
                         description="one degrade-ladder step: re-encode the K side of a "
                                     "2 x 200704-key layer (4 kv heads) from f16 to q8_0")
+    if name == "evict_ragged16_kf16_vq8":
+        w = get("decode_ragged16_kf16_vq8")
+        w.name, w.kind = name, "evict"
+        w.extra = {"n_sink": 4, "n_recent": 1024, "n_evict": 2048, "decay": 0.9,
+                   "score_seed": 13}
+        w.description = ("decode_ragged16_kf16_vq8 + one probe-scored eviction: probe "
+                         "(decay 0.9), 2048 lowest middle cells per seq (4 sink / 1024 recent "
+                         "protected), compaction of K, V, scores and lengths")
+        return w
     raise KeyError(name)
 
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
        "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
-       "decode_ragged16_kf16_vq8_paged"]
+       "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8"]
+
+
+def n_evicted(w: Workload) -> list:
+    """Cells an eviction step of workload w removes from each sequence."""
+    e = w.extra
+    return [max(0, min(e["n_evict"], n - e["n_sink"] - e["n_recent"])) for n in w.final_lens()]
+
+
+def initial_scores(w: Workload, device="cpu") -> torch.Tensor:
+    """fp32 [n_seqs, capacity]: the running scores before the step (a probe
+    history), uniform in [0, 1) from the workload's score seed."""
+    g = _gen(device, w.extra["score_seed"], 0)
+    return torch.rand((w.n_seqs, w.capacity), generator=g, device=device, dtype=torch.float32)
 
 
 # ------------------------------------------------------------------ draws

@@ -57,12 +57,38 @@ def _peaks():
 
 # ------------------------------------------------------------------ algorithmic work
 
+def evict_work(w, lens, n_ev, ck, cv):
+    """Algorithmic bytes of one probe-scored eviction step over sequences of
+    the given lengths: (decode, probe, select, compact).  Decode reads K and V
+    once; the probe reads K once more and reads and writes each token's score;
+    the selection reads the middle scores and writes the list; compaction
+    reads and writes the kept rows of both sides and their scores, and reads
+    the list."""
+    e = w.extra
+    dec = sum(lens) * w.n_kv * (ROW[ck] + ROW[cv]) + len(lens) * w.n_q * (2 * 256 + 4)
+    probe = sum(lens) * (w.n_kv * ROW[ck] + 8) + len(lens) * w.n_q * (256 + 4)
+    mid = sum(max(0, n - e["n_sink"] - e["n_recent"]) for n in lens)
+    sel = 4 * mid + 4 * sum(n_ev)
+    kept = [n - k for n, k in zip(lens, n_ev)]
+    comp = sum(kept) * (2 * w.n_kv * (ROW[ck] + ROW[cv]) + 8) + 4 * sum(n_ev)
+    return dec, probe, sel, comp
+
+
 def step_work(w):
-    """(bytes, flops, decode_bytes_per_layer list) of one step of workload w."""
+    """(bytes, flops, roofline-kernel bytes per layer) of one step of workload
+    w; the roofline kernel is the attention call, the re-encode, or (eviction
+    steps) the compaction."""
     lens = w.final_lens()
     total_b, total_f, per_layer = 0, 0, []
     for ck, cv in w.codecs:
         app = w.n_seqs * w.append_new * w.n_kv * (2 * 256 + ROW[ck] + ROW[cv])
+        if w.kind == "evict":
+            from attention_quantized_kv_gb300 import workloads as wl
+            dec, probe, sel, comp = evict_work(w, lens, wl.n_evicted(w), ck, cv)
+            per_layer.append(comp)
+            total_b += dec + probe + sel + comp + app
+            total_f += sum(lens) * w.n_q * 4 * 128 + sum(lens) * w.n_q * 2 * 128
+            continue
         if w.kind == "degrade":
             src = ck if w.extra["side"] == 0 else cv
             kv = sum(lens) * w.n_kv * (ROW[src] + ROW[w.extra["dst"]])
@@ -173,7 +199,7 @@ class OursArm:
                 # the step's output: the re-encoded side, in its own buffer
                 self.q.append(qq[:0, 0].contiguous())
                 nb = kvq.kvq_cache_bytes(w.extra["dst"], w.n_seqs, w.n_kv, w.capacity)
-            elif w.kind == "decode":
+            elif w.kind in ("decode", "evict"):
                 self.q.append(qq[:, 0].contiguous())
                 nb = kvq.attn_decode_workspace(L, self.max_len)
             else:
@@ -190,6 +216,21 @@ class OursArm:
         self.n_new = torch.full((w.n_seqs,), w.append_new, dtype=torch.int32, device=device)
         self.out = [torch.empty_like(q) for q in self.q]
         self.lse = [torch.empty(q.shape[:2], dtype=torch.float32, device=device) for q in self.q]
+        if w.kind == "evict":
+            # running scores (reset to the probe history before every step),
+            # the eviction lists and the compaction's second buffers
+            e = w.extra
+            self.scores0 = [wl.initial_scores(w, device) for _ in self.layers]
+            self.scores = [s0.clone() for s0 in self.scores0]
+            self.ev = [torch.zeros((w.n_seqs, e["n_evict"]), dtype=torch.int32, device=device)
+                       for _ in self.layers]
+            self.nev = [torch.zeros(w.n_seqs, dtype=torch.int32, device=device)
+                        for _ in self.layers]
+            self.k_dst = [torch.zeros_like(L.k_cache) for L in self.layers]
+            self.v_dst = [torch.zeros_like(L.v_cache) for L in self.layers]
+            self.s_dst = [torch.zeros_like(s0) for s0 in self.scores0]
+            self.lens_dst = [torch.zeros(w.n_seqs, dtype=torch.int32, device=device)
+                             for _ in self.layers]
         torch.cuda.synchronize()
 
     def _fill(self, L, l, chunk=8192):
@@ -209,6 +250,9 @@ class OursArm:
     def reset(self):
         for L in self.layers:
             L.seq_lens.copy_(self.init_lens)
+        if self.w.kind == "evict":
+            for sc, s0 in zip(self.scores, self.scores0):
+                sc.copy_(s0)
 
     def set_final_lens(self):
         for L in self.layers:
@@ -218,9 +262,10 @@ class OursArm:
         """Kernels the library launches per step: the append is one kernel
         for at most 64 rows (it also advances the lengths), else the encode
         kernel plus the length update; decode is one kernel, prefill two
-        (dequant pre-pass, attention)."""
+        (dequant pre-pass, attention), an eviction step five (decode, probe,
+        selection, compaction of K and of V)."""
         w = self.w
-        per_layer = 1 if w.kind in ("decode", "degrade") else 2
+        per_layer = {"decode": 1, "degrade": 1, "prefill": 2, "evict": 5}[w.kind]
         if w.append_new:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
@@ -237,10 +282,29 @@ class OursArm:
                 kvq.kv_append_quantize(L, (kn or self.kn)[l], (vn or self.vn)[l], self.n_new)
             self.attention(l, q, out)
 
+    def roofline_calls(self, l):
+        """The calls of the kernel the roofline line is about: the attention
+        call, the re-encode, or (eviction steps) the compaction."""
+        if self.w.kind == "evict":
+            self.compact(l)
+        else:
+            self.attention(l)
+
+    def compact(self, l):
+        self.kvq.kv_compact(self.layers[l], self.ev[l], self.nev[l], self.k_dst[l],
+                            self.v_dst[l], self.scores[l], self.s_dst[l], self.lens_dst[l])
+
     def attention(self, l, q=None, out=None):
         L, w = self.layers[l], self.w
         qq, oo = (q or self.q)[l], (out or self.out)[l]
-        if w.kind == "degrade":
+        if w.kind == "evict":
+            e = w.extra
+            self.kvq.attn_decode(L, qq, self.scale, oo, self.lse[l], self.max_len, self.ws[l])
+            self.kvq.kv_probe_scores(L, qq, self.scale, self.lse[l], e["decay"], self.scores[l])
+            self.kvq.kv_evict_select(L, self.scores[l], e["n_sink"], e["n_recent"],
+                                     e["n_evict"], self.ev[l], self.nev[l])
+            self.compact(l)
+        elif w.kind == "degrade":
             self.kvq.kv_requantize(L, w.extra["side"], w.extra["dst"], self.ws[l])
         elif w.kind == "decode":
             self.kvq.attn_decode(L, qq, self.scale, oo, self.lse[l], self.max_len, self.ws[l])
@@ -336,10 +400,11 @@ def run_ours(args, w, rank, world, dist):
     g_attn = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_attn):
         for l in range(n_layers):
-            arm.attention(l)
+            arm.roofline_calls(l)
     torch.cuda.synchronize()
-    mode = ("one CUDA graph replay per step, events outside it; attention kernels "
-            "timed in a replay of their own")
+    mode = ("one CUDA graph replay per step, events outside it; "
+            + ("compaction kernels" if w.kind == "evict" else "attention kernels")
+            + " timed in a replay of their own")
 
     for _ in range(3):
         _flush_l2(torch, flush)
@@ -487,9 +552,10 @@ def run_ours(args, w, rank, world, dist):
         "clocks": clocks,
         "device_errors": errs,
     }
-    if w.kind in ("decode", "degrade"):
-        kname = ("attn_decode (decode_split_kernel)" if w.kind == "decode"
-                 else "kv_requantize (requant_kernel)")
+    if w.kind in ("decode", "degrade", "evict"):
+        kname = {"decode": "attn_decode (decode_split_kernel)",
+                 "degrade": "kv_requantize (requant_kernel)",
+                 "evict": "kv_compact (compact_kernel, K and V launches)"}[w.kind]
         line["roofline"] = {"bound": "hbm", "kernel": kname,
                             "achieved": round(achieved_attn, 2), "peak": hbm,
                             "peak_kind": peak_kind, "unit": "GB/s",
@@ -515,6 +581,9 @@ class OracleArm:
         from attention_quantized_kv_gb300 import workloads as wl
         self.w, self.oracle, self.scale = w, oracle, 1.0 / math.sqrt(128)
         dev = "cuda" if torch.cuda.is_available() else "cpu"
+        if w.kind == "evict":
+            self._init_evict(wl, dev)
+            return
         G = w.n_q // w.n_kv
         # sample: (layer, seq, kv head) groups, in order, until the sample's
         # attended keys reach ~40M x rows (a few seconds of fp64 work per step)
@@ -553,8 +622,54 @@ class OracleArm:
                             + (f", {len(self.rows)} of {w.append_new} query rows"
                                if self.rows else ""))
 
+    def _init_evict(self, wl, dev):
+        """Eviction steps need every kv head of a sequence (the probe sums over
+        all query heads): the sample is whole sequences, in order, until the
+        attended keys reach ~2e7 x query heads."""
+        w, o = self.w, self.oracle
+        (ck, cv), = w.codecs
+        seqs, budget = [], 0
+        for s in range(w.n_seqs):
+            if seqs and budget > 1e6:
+                break
+            seqs.append(s)
+            budget += w.final_lens()[s] * w.n_q
+        self.seqs, self.ev_caches, self.ev_q, self.ev_sc = seqs, [], [], []
+        sc0 = wl.initial_scores(w, dev).cpu().numpy()
+        for s in seqs:
+            n = w.lens[s]
+            cs = []
+            for side, codec in ((0, ck), (1, cv)):
+                rows = wl.kv_rows(w, 0, side, s, 0, n, dev).cpu().numpy()
+                c = np.zeros(o.cache_bytes(codec, 1, w.n_kv, w.capacity), np.uint8)
+                o.append_side(codec, side, c, 1, w.n_kv, w.capacity, [0], [n],
+                              rows.reshape(1, n, w.n_kv, 128))
+                cs.append(c)
+            self.ev_caches.append(cs)
+            self.ev_q.append(wl.queries(w, 0, 1, dev)[s, 0].cpu().numpy())
+            self.ev_sc.append(sc0[s])
+        self.sample_desc = f"{len(seqs)} of {w.n_seqs} sequences (all kv heads)"
+        self.groups = None
+
+    def _step_evict(self):
+        w, o, e = self.w, self.oracle, self.w.extra
+        (ck, cv), = w.codecs
+        for s, (kc, vc), q, sc in zip(self.seqs, self.ev_caches, self.ev_q, self.ev_sc):
+            n = [w.final_lens()[s]]
+            o.decode_layer(ck, cv, kc, vc, 1, w.n_kv, w.n_q, w.capacity, n, q[None], self.scale)
+            mass = o.probe_mass(ck, kc, 1, w.n_kv, w.n_q, w.capacity, n, q[None], self.scale)
+            score = (e["decay"] * sc.astype(np.float64) + mass[0]).astype(np.float32)
+            ev = o.evict_select(score, n[0], e["n_sink"], e["n_recent"], e["n_evict"])
+            o.compact_side(ck, 0, kc, 1, w.n_kv, w.capacity, n, [ev])
+            o.compact_side(cv, 1, vc, 1, w.n_kv, w.capacity, n, [ev])
+
     def sample_bytes(self):
         w = self.w
+        if w.kind == "evict":
+            from attention_quantized_kv_gb300 import workloads as wl
+            lens = [w.final_lens()[s] for s in self.seqs]
+            n_ev = [wl.n_evicted(w)[s] for s in self.seqs]
+            return sum(evict_work(w, lens, n_ev, *w.codecs[0]))
         tot = 0
         G = w.n_q // w.n_kv
         for (l, s, h) in self.groups:
@@ -573,6 +688,9 @@ class OracleArm:
 
     def step(self):
         w, o = self.w, self.oracle
+        if w.kind == "evict":
+            self._step_evict()
+            return
         G = w.n_q // w.n_kv
         for (l, s, h), cs, q in zip(self.groups, self.caches, self.q):
             ck, cv = w.codecs[l]

@@ -128,6 +128,7 @@ typedef enum {
 #define KVQ_DEVERR_TIMEOUT 4  /* a bounded wait on an async copy gave up */
 #define KVQ_DEVERR_SEQLEN 8   /* prefill: seq_lens[seq] < q_start + n_q_tok */
 #define KVQ_DEVERR_PAGE 16    /* paged: a block-table entry outside [0, n_pages) */
+#define KVQ_DEVERR_EVICT 32   /* kv_compact: an eviction list not increasing below the length */
 
 /* One layer's cache.  All pointers are device pointers owned by the caller.
  * k_cache / v_cache: kvq_cache_bytes() bytes each (kvq_pool_bytes() when
@@ -270,6 +271,57 @@ KVQ_API double kvq_aggregate_bpv(const int32_t *codecs, int32_t n);
  * when no step remains.  Host only. */
 KVQ_API int kvq_ladder_next(const int32_t *codecs, int32_t n, const int32_t *order,
                             int32_t n_order, double floor_bpv, int32_t *tensor, int32_t *codec);
+
+/* ------------------------------------------------------------------------
+ * Probe-scored eviction (the Sparse KV eviction item of the Officina "How It
+ * Works" list: an attention probe, a q.K softmax with exponential decay,
+ * scores the cells; the lowest-scored middle cells are evicted first; the
+ * sink cells at the start and the recent cells at the end are protected).
+ * Scores are fp32 [n_seqs][capacity] by logical position, for contiguous and
+ * paged layers alike.
+ * ------------------------------------------------------------------------ */
+
+/* Fold one probe into the scores: for every sequence s and token
+ * t < seq_lens[s],
+ *   mass_t = sum over the query heads h of exp(scale * q_h . k^_t - lse[s][h])
+ * (the softmax weight head h puts on t; k^ the decoded key of h's kv head) and
+ *   scores[s][t] = decay * scores[s][t] + mass_t.
+ * Entries at t >= seq_lens[s] are not touched.  q: fp16 [n_seqs][n_q][128]
+ * (8-byte aligned), the query of the decode step; lse: fp32 [n_seqs][n_q],
+ * the natural-log log-sum-exp that attn_decode wrote for the same q, scale
+ * and cache (the probe reads K once more and never recomputes it); scores:
+ * device, 4-byte aligned.  Results are deterministic (a fixed summation
+ * order). */
+KVQ_API int kv_probe_scores(const kvq_layer *layer, const void *q, float scale, const float *lse,
+                            float decay, float *scores, void *stream);
+
+/* For every sequence s, the min(n_evict, len - n_recent - n_sink) positions t
+ * in [n_sink, len - n_recent) with the smallest (scores[s][t], t) pairs
+ * (equal scores: the lower position first; -0 equals +0; NaN scores are
+ * outside the contract and order after every number), written in increasing
+ * order to evict[s][0 ..); n_evicted[s] = their count (0 when the middle
+ * range is empty).  evict: device int32 [n_seqs][n_evict]; n_evicted: device
+ * int32 [n_seqs]; n_sink, n_recent >= 0, n_evict >= 0. */
+KVQ_API int kv_evict_select(const kvq_layer *layer, const float *scores, int32_t n_sink,
+                            int32_t n_recent, int32_t n_evict, int32_t *evict,
+                            int32_t *n_evicted, void *stream);
+
+/* Remove the listed tokens from both sides of every sequence: the kept tokens
+ * t < seq_lens[s] move down in order into k_dst / v_dst, bytes unchanged
+ * (same codecs and layout as the layer's caches, same block table for a paged
+ * layer).  evict: device int32 [n_seqs][max_evict], the n_evicted[s] first
+ * entries of row s increasing and below seq_lens[s] (as kv_evict_select
+ * writes them; otherwise the device sets KVQ_DEVERR_EVICT and the result is
+ * unspecified but in bounds).  Inside the last unit written, rows past the new
+ * length are zero; units past it are not written.  Optional (null to skip):
+ * scores_dst[s][w] = scores[s][source of w] for w below the new length, and
+ * lens_dst[s] = seq_lens[s] - n_evicted[s].  Every destination is out of
+ * place (it must not overlap the layer's caches or the scores); the caller
+ * then points the layer at k_dst, v_dst and lens_dst.  k_dst, v_dst: 16-byte
+ * aligned, kvq_cache_bytes (kvq_pool_bytes for a paged layer) of the codecs. */
+KVQ_API int kv_compact(const kvq_layer *layer, const int32_t *evict, const int32_t *n_evicted,
+                       int32_t max_evict, void *k_dst, void *v_dst, const float *scores,
+                       float *scores_dst, int32_t *lens_dst, void *stream);
 
 #ifdef __cplusplus
 }
