@@ -30,6 +30,7 @@
 //    eviction list.
 #include <cuda_runtime.h>
 
+#include <limits.h>
 #include <math.h>
 
 #include "kvq_device.cuh"
@@ -380,7 +381,7 @@ struct RowBits {
   static constexpr int kMinBit = P0 < P1 ? (P0 < P2 ? (P0 < P3 ? P0 : P3) : (P2 < P3 ? P2 : P3))
                                          : (P1 < P2 ? (P1 < P3 ? P1 : P3) : (P2 < P3 ? P2 : P3));
   static constexpr int kPiece = kMinBit >= 4 ? 16 : (1 << kMinBit);  // bytes per gather
-  __device__ static __forceinline__ int row_of(uint32_t x) {
+  __host__ __device__ static constexpr int row_of(uint32_t x) {
     return static_cast<int>(((x >> P0) & 1u) | (((x >> P1) & 1u) << 1) | (((x >> P2) & 1u) << 2) |
                             (((x >> P3) & 1u) << 3));
   }
@@ -434,8 +435,8 @@ constexpr int kCpSlots = 16;                   // source units staged at a time
 static_assert(kPageUnits % kCpUnits == 0, "a destination run lies inside one page");
 
 struct CompactParams {
-  const uint8_t *src;
-  uint8_t *dst;
+  const uint8_t *src[2];  // K, V caches (or pools)
+  uint8_t *dst[2];
   const int32_t *seq_lens;
   const int32_t *evict;   // [n_seqs][max_evict], increasing
   const int32_t *n_ev;    // [n_seqs]
@@ -445,7 +446,6 @@ struct CompactParams {
   int32_t *err;
   const int32_t *table;
   int max_evict, n_kv, capacity, pages_per_seq, n_pages;
-  int first;              // 1: this launch also writes scores, lengths and checks the lists
 };
 
 struct CompactSmem {
@@ -454,8 +454,9 @@ struct CompactSmem {
   int32_t offd[kCpRows];     // shared-memory offset of the row in the values region
   int32_t offs[kCpRows];     // ... in the scales region
   int32_t slot_unit[kCpRows];  // source unit of each slot
-  int64_t slot_gidx[kCpSlots];  // its index in the cache or pool (-1: bad page)
   int32_t red[kCpThreads / 32];
+  int32_t win[kCpThreads];   // a window of c_j = e[j] - j of the eviction list
+  uint64_t bar;              // completion of the round's bulk copies
 };
 
 __device__ __forceinline__ int64_t unit_index(const CompactParams &p, int s, int kvh, int u) {
@@ -473,12 +474,16 @@ __device__ __forceinline__ uint4 gather_chunk(const uint8_t *stage, const int32_
                                               int rows_valid, uint32_t x0) {
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   constexpr int P = R::kPiece;
+  // x0 is 16-aligned, so x0 + j (j < 16) has x0's bits above bit 3 and j's
+  // below: the row and the row-free offset split into a per-chunk part and
+  // a compile-time part.
+  const int rbase = ud * kUnitTokens + R::row_of(x0);
+  const uint8_t *cbase = stage + (x0 & ~R::kMask);
 #pragma unroll
   for (int j = 0; j < 16; j += P) {
-    const uint32_t x = x0 + j;
-    const int i = ud * kUnitTokens + R::row_of(x);
+    const int i = rbase + R::row_of(static_cast<uint32_t>(j));
     if (i >= rows_valid) continue;  // rows past the new length stay zero
-    const uint8_t *src = stage + off[i] + (x & ~R::kMask);
+    const uint8_t *src = cbase + off[i] + (static_cast<uint32_t>(j) & ~R::kMask);
     if (P == 16) {
       const uint4 v = *reinterpret_cast<const uint4 *>(src);
       w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
@@ -497,55 +502,64 @@ __device__ __forceinline__ uint4 gather_chunk(const uint8_t *stage, const int32_
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// One CTA's run of kCpUnits destination units of one (sequence, kv head,
+// side): source rows by binary search, distinct source units in slots,
+// rounds of destination units whose sources fit kCpSlots slots.  Each round's
+// source units arrive by bulk async copies on one mbarrier (all of them in
+// flight together), then every thread gathers 16-byte destination chunks and
+// stores them straight to global memory.
 template <int CODEC, int SIDE>
-__global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams p) {
+__device__ __forceinline__ void compact_run(const CompactParams &p, CompactSmem &sm,
+                                            uint8_t *stage, int s, int kvh, int u0, int len,
+                                            int n, int rows) {
   using L = UnitRows<CODEC, SIDE>;
   using D = typename L::D;
   using S = typename L::S;
   constexpr int UB = unit_bytes(CODEC);
   constexpr int CH = UB / 16;  // 16-byte chunks per unit
-  extern __shared__ uint4 cp_stage[];
-  __shared__ CompactSmem sm;
-  grid_dependency_wait();
-  const int s = blockIdx.z, kvh = blockIdx.y, u0 = blockIdx.x * kCpUnits;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int len = min(max(p.seq_lens[s], 0), p.capacity);
-  const int n = min(max(p.n_ev[s], 0), min(p.max_evict, len));
-  const int new_len = len - n;
   const int32_t *ev = p.evict + static_cast<int64_t>(s) * p.max_evict;
-  if (p.first && kvh == 0) {
-    if (blockIdx.x == 0) {
-      // the list must be increasing positions below the length
-      bool bad = p.n_ev[s] < 0 || p.n_ev[s] > min(p.max_evict, len);
-      for (int j = tid; j < n && !bad; j += kCpThreads)
-        bad = ev[j] < 0 || ev[j] >= len || (j > 0 && ev[j] <= ev[j - 1]);
-      if (bad) set_err(p.err, KVQ_DEVERR_EVICT);
-      if (tid == 0 && p.lens_dst) p.lens_dst[s] = new_len;
+  // Source token of destination row w: w plus the number of evicted
+  // positions e[j] with c_j = e[j] - j <= w (c is non-decreasing).  The count
+  // at the run's first row comes from a parallel search (each round tests
+  // kCpThreads evenly spaced candidates: two rounds for 65536 entries); the
+  // rows then count inside windows of the list staged in shared memory.
+  const int w0 = u0 * kUnitTokens;
+  int lo = 0, hi = n;  // the count a0 lies in [lo, hi]
+  while (lo < hi) {
+    const int step = (hi - lo + kCpThreads - 1) / kCpThreads;
+    const int j = lo + tid * step;
+    const bool le = j < hi && ev[j] - j <= w0;
+    const int m = __syncthreads_count(le);  // le holds for a prefix of the candidates
+    if (m == 0) {
+      hi = lo;
+    } else {
+      const int last = lo + (m - 1) * step;
+      hi = min(hi, lo + m * step);
+      lo = last + 1;
     }
   }
-  const int rows = min(kCpRows, new_len - u0 * kUnitTokens);
-  if (rows <= 0) {
-    grid_launch_dependents();
-    return;
-  }
-  // source token of each destination row: w plus the number of evicted
-  // positions e[j] with e[j] - j <= w (non-decreasing in j)
-  if (tid < kCpRows) {
-    int src = 0;
-    if (tid < rows) {
-      const int w = u0 * kUnitTokens + tid;
-      int a = 0, b = n;
+  int cnt = -1;  // this row's count once its window held it
+  for (int base = lo;; base += kCpThreads) {
+    sm.win[tid] = base + tid < n ? ev[base + tid] - (base + tid) : INT_MAX;
+    __syncthreads();
+    bool open = false;
+    if (tid < rows && cnt < 0) {
+      const int w = w0 + tid;
+      int a = 0, b = kCpThreads;  // entries of the window with c <= w
       while (a < b) {
-        const int m = (a + b) >> 1;
-        if (ev[m] - m <= w) a = m + 1;
-        else b = m;
+        const int mid = (a + b) >> 1;
+        if (sm.win[mid] <= w) a = mid + 1;
+        else b = mid;
       }
-      src = min(max(w + a, 0), len - 1);
+      if (a < kCpThreads || base + kCpThreads >= n) cnt = base + a;
+      else open = true;  // every entry of the window counts: look further
     }
-    sm.srcpos[tid] = src;
+    if (!__syncthreads_or(open)) break;
   }
+  if (tid < kCpRows) sm.srcpos[tid] = tid < rows ? min(max(w0 + tid + cnt, 0), len - 1) : 0;
   __syncthreads();
-  if (p.first && kvh == 0 && p.scores && tid < rows) {
+  if (SIDE == 0 && kvh == 0 && p.scores && tid < rows) {
     const int64_t base = static_cast<int64_t>(s) * p.capacity;
     p.scores_dst[base + u0 * kUnitTokens + tid] = p.scores[base + sm.srcpos[tid]];
   }
@@ -568,39 +582,50 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams
     if (head) sm.slot_unit[slot] = su;
   }
   __syncthreads();
-  uint8_t *stage = reinterpret_cast<uint8_t *>(cp_stage);
   const int n_units = (rows + kUnitTokens - 1) / kUnitTokens;
   const int64_t d_unit0 = unit_index(p, s, kvh, u0);
   if (d_unit0 < 0) {
     if (tid == 0) set_err(p.err, KVQ_DEVERR_PAGE);
     return;
   }
+  const uint8_t *src = p.src[SIDE];
+  uint8_t *dst = p.dst[SIDE];
+  uint32_t phase = 0;
   int ua = 0;
   while (ua < n_units) {  // rounds of destination units whose sources fit the slots
     const int s_first = sm.slot[ua * kUnitTokens];
     int ub = ua + 1;
     while (ub < n_units && sm.slot[min((ub + 1) * kUnitTokens, rows) - 1] - s_first < kCpSlots)
       ++ub;
-    const int s_last = sm.slot[min(ub * kUnitTokens, rows) - 1];
-    const int n_sl = s_last - s_first + 1;
-    if (tid < n_sl) sm.slot_gidx[tid] = unit_index(p, s, kvh, sm.slot_unit[s_first + tid]);
+    const int n_sl = sm.slot[min(ub * kUnitTokens, rows) - 1] - s_first + 1;
+    if (tid == 0) {
+      // the previous round's reads of the stage are ordered before these
+      // async writes by the barrier that ended the round and this fence
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(&sm.bar, static_cast<uint32_t>(n_sl * UB));
+      for (int k = 0; k < n_sl; ++k) {
+        int64_t gi = unit_index(p, s, kvh, sm.slot_unit[s_first + k]);
+        if (gi < 0) {
+          set_err(p.err, KVQ_DEVERR_PAGE);
+          gi = 0;
+        }
+        bulk_copy_g2s(stage + k * UB, src + gi * UB, UB, &sm.bar);
+      }
+    }
     if (tid < kCpRows && tid >= ua * kUnitTokens && tid < min(ub * kUnitTokens, rows)) {
       const int rel = sm.slot[tid] - s_first, rs = sm.srcpos[tid] % kUnitTokens;
       sm.offd[tid] = rel * UB + D::kBase + static_cast<int>(D::dep(rs));
       sm.offs[tid] = rel * UB + S::kBase + static_cast<int>(S::dep(rs));
     }
     __syncthreads();
-    for (int c = tid; c < n_sl * CH; c += kCpThreads) {
-      const int k = c / CH, part = c - k * CH;
-      const int64_t gi = sm.slot_gidx[k];
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (gi >= 0) v = __ldcs(reinterpret_cast<const uint4 *>(p.src + gi * UB) + part);
-      cp_stage[c] = v;
+    const bool ok = mbar_wait_bounded(&sm.bar, phase);
+    if (__syncthreads_or(!ok)) {
+      // copies still in flight after the limit: flag, wait once more, leave
+      if (tid == 0) set_err(p.err, KVQ_DEVERR_TIMEOUT);
+      mbar_wait_bounded(&sm.bar, phase);
+      return;
     }
-    if (tid == 0)
-      for (int k = 0; k < n_sl; ++k)
-        if (sm.slot_gidx[k] < 0) set_err(p.err, KVQ_DEVERR_PAGE);
-    __syncthreads();
+    phase ^= 1u;
     for (int c = tid; c < (ub - ua) * CH; c += kCpThreads) {
       const int ud = ua + c / CH;
       const uint32_t x = static_cast<uint32_t>(c % CH) * 16u;
@@ -609,30 +634,63 @@ __global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams
         v = gather_chunk<D>(stage, sm.offd, ud, rows, x - D::kBase);
       else
         v = gather_chunk<S>(stage, sm.offs, ud, rows, x - S::kBase);
-      reinterpret_cast<uint4 *>(p.dst + (d_unit0 + ud) * UB)[x / 16] = v;
+      reinterpret_cast<uint4 *>(dst + (d_unit0 + ud) * UB)[x / 16] = v;
     }
     __syncthreads();
     ua = ub;
   }
+}
+
+// blockIdx = (run of kCpUnits destination units, kv head * 2 + side, sequence):
+// both sides in one launch, so that the K and V runs are in flight together.
+template <int CK, int CV>
+__global__ void __launch_bounds__(kCpThreads) compact_kernel(const CompactParams p) {
+  extern __shared__ __align__(128) uint8_t cp_stage[];
+  __shared__ CompactSmem sm;
+  const int s = blockIdx.z, kvh = blockIdx.y >> 1, side = blockIdx.y & 1;
+  const int u0 = blockIdx.x * kCpUnits, tid = threadIdx.x;
+  if (tid == 0) {
+    mbar_init(&sm.bar, 1);
+    fence_mbar_init();
+  }
+  grid_dependency_wait();
+  const int len = min(max(p.seq_lens[s], 0), p.capacity);
+  const int n = min(max(p.n_ev[s], 0), min(p.max_evict, len));
+  const int new_len = len - n;
+  if (side == 0 && kvh == 0 && blockIdx.x == 0) {
+    // the list must hold increasing positions below the length
+    const int32_t *ev = p.evict + static_cast<int64_t>(s) * p.max_evict;
+    bool bad = p.n_ev[s] < 0 || p.n_ev[s] > min(p.max_evict, len);
+    for (int j = tid; j < n && !bad; j += kCpThreads)
+      bad = ev[j] < 0 || ev[j] >= len || (j > 0 && ev[j] <= ev[j - 1]);
+    if (bad) set_err(p.err, KVQ_DEVERR_EVICT);
+    if (tid == 0 && p.lens_dst) p.lens_dst[s] = new_len;
+  }
+  const int rows = min(kCpRows, new_len - u0 * kUnitTokens);
+  if (rows > 0) {
+    __syncthreads();  // the mbarrier's initialisation is visible to every thread
+    if (side == 0) compact_run<CK, 0>(p, sm, cp_stage, s, kvh, u0, len, n, rows);
+    else compact_run<CV, 1>(p, sm, cp_stage, s, kvh, u0, len, n, rows);
+  }
   grid_launch_dependents();
 }
 
-template <int CODEC, int SIDE>
+template <int CK, int CV>
 cudaError_t launch_compact_t(const CompactParams &p, dim3 grid, cudaStream_t stream) {
-  constexpr int smem = kCpSlots * unit_bytes(CODEC);
+  constexpr int ub = unit_bytes(CK) > unit_bytes(CV) ? unit_bytes(CK) : unit_bytes(CV);
+  constexpr int smem = kCpSlots * ub;
   static std::atomic<uint64_t> optin{0};
-  const cudaError_t e = smem_optin(compact_kernel<CODEC, SIDE>, smem, optin);
+  const cudaError_t e = smem_optin(compact_kernel<CK, CV>, smem, optin);
   if (e != cudaSuccess) return e;
-  return launch_pdl(compact_kernel<CODEC, SIDE>, grid, dim3(kCpThreads), smem, stream, p);
+  return launch_pdl(compact_kernel<CK, CV>, grid, dim3(kCpThreads), smem, stream, p);
 }
 
-template <int SIDE>
-cudaError_t launch_compact_side(int codec, const CompactParams &p, dim3 grid,
-                                cudaStream_t stream) {
-  switch (codec) {
-    case KVQ_F16: return launch_compact_t<KVQ_F16, SIDE>(p, grid, stream);
-    case KVQ_Q8_0: return launch_compact_t<KVQ_Q8_0, SIDE>(p, grid, stream);
-    default: return launch_compact_t<KVQ_Q4_0, SIDE>(p, grid, stream);
+template <int CK>
+cudaError_t launch_compact_v(int cv, const CompactParams &p, dim3 grid, cudaStream_t stream) {
+  switch (cv) {
+    case KVQ_F16: return launch_compact_t<CK, KVQ_F16>(p, grid, stream);
+    case KVQ_Q8_0: return launch_compact_t<CK, KVQ_Q8_0>(p, grid, stream);
+    default: return launch_compact_t<CK, KVQ_Q4_0>(p, grid, stream);
   }
 }
 
@@ -684,6 +742,10 @@ cudaError_t launch_compact(const kvq_layer &L, const int32_t *evict, const int32
                            int max_evict, void *k_dst, void *v_dst, const float *scores,
                            float *scores_dst, int32_t *lens_dst, cudaStream_t stream) {
   CompactParams p;
+  p.src[0] = static_cast<const uint8_t *>(L.k_cache);
+  p.src[1] = static_cast<const uint8_t *>(L.v_cache);
+  p.dst[0] = static_cast<uint8_t *>(k_dst);
+  p.dst[1] = static_cast<uint8_t *>(v_dst);
   p.seq_lens = L.seq_lens;
   p.evict = evict;
   p.n_ev = n_evicted;
@@ -697,16 +759,12 @@ cudaError_t launch_compact(const kvq_layer &L, const int32_t *evict, const int32
   p.capacity = L.capacity;
   p.pages_per_seq = L.pages_per_seq;
   p.n_pages = L.n_pages;
-  const dim3 grid(L.capacity / kCpRows, L.n_kv_heads, L.n_seqs);
-  p.src = static_cast<const uint8_t *>(L.k_cache);
-  p.dst = static_cast<uint8_t *>(k_dst);
-  p.first = 1;
-  cudaError_t e = launch_compact_side<0>(L.codec_k, p, grid, stream);
-  if (e != cudaSuccess) return e;
-  p.src = static_cast<const uint8_t *>(L.v_cache);
-  p.dst = static_cast<uint8_t *>(v_dst);
-  p.first = 0;
-  return launch_compact_side<1>(L.codec_v, p, grid, stream);
+  const dim3 grid(L.capacity / kCpRows, 2 * L.n_kv_heads, L.n_seqs);
+  switch (L.codec_k) {
+    case KVQ_F16: return launch_compact_v<KVQ_F16>(L.codec_v, p, grid, stream);
+    case KVQ_Q8_0: return launch_compact_v<KVQ_Q8_0>(L.codec_v, p, grid, stream);
+    default: return launch_compact_v<KVQ_Q4_0>(L.codec_v, p, grid, stream);
+  }
 }
 
 }  // namespace kvq

@@ -262,10 +262,10 @@ class OursArm:
         """Kernels the library launches per step: the append is one kernel
         for at most 64 rows (it also advances the lengths), else the encode
         kernel plus the length update; decode is one kernel, prefill two
-        (dequant pre-pass, attention), an eviction step five (decode, probe,
-        selection, compaction of K and of V)."""
+        (dequant pre-pass, attention), an eviction step four (decode, probe,
+        selection, compaction of both sides)."""
         w = self.w
-        per_layer = {"decode": 1, "degrade": 1, "prefill": 2, "evict": 5}[w.kind]
+        per_layer = {"decode": 1, "degrade": 1, "prefill": 2, "evict": 4}[w.kind]
         if w.append_new:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
@@ -555,7 +555,7 @@ def run_ours(args, w, rank, world, dist):
     if w.kind in ("decode", "degrade", "evict"):
         kname = {"decode": "attn_decode (decode_split_kernel)",
                  "degrade": "kv_requantize (requant_kernel)",
-                 "evict": "kv_compact (compact_kernel, K and V launches)"}[w.kind]
+                 "evict": "kv_compact (compact_kernel)"}[w.kind]
         line["roofline"] = {"bound": "hbm", "kernel": kname,
                             "achieved": round(achieved_attn, 2), "peak": hbm,
                             "peak_kind": peak_kind, "unit": "GB/s",
