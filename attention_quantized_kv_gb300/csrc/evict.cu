@@ -1,9 +1,10 @@
 // evict.cu -- probe-scored eviction over a block-quantized KV cache.
 //
-// The Sparse KV eviction item of the Officina "How It Works" list: an
-// attention probe (q.K softmax with exponential decay) scores the cache
-// cells, the lowest-scored middle cells are evicted first, and the attention
-// sinks (first cells) and the recent cells are protected.  Three kernels:
+// The "Sparse KV eviction" item of the "How It Works" section of the GitHot
+// listing of VITRIOL: an attention probe (q.K softmax with exponential decay)
+// scores the cache cells, the lowest-scored middle cells are evicted first,
+// and the attention sinks (first cells) and the recent cells are protected.
+// Three kernels:
 //
 //  * probe_kernel: for every token t below a sequence's length, the softmax
 //    weight that the decode query of every query head puts on t, summed over
@@ -431,7 +432,7 @@ template <> struct UnitRows<KVQ_Q4_0, 1> {
 constexpr int kCpThreads = 256;
 constexpr int kCpUnits = 8;                    // destination units per CTA
 constexpr int kCpRows = kCpUnits * kUnitTokens;  // 128 destination rows
-constexpr int kCpSlots = 16;                   // source units staged at a time
+constexpr int kCpSlots = 10;                   // source units staged at a time
 static_assert(kPageUnits % kCpUnits == 0, "a destination run lies inside one page");
 
 struct CompactParams {
@@ -456,6 +457,8 @@ struct CompactSmem {
   int32_t slot_unit[kCpRows];  // source unit of each slot
   int32_t red[kCpThreads / 32];
   int32_t win[kCpThreads];   // a window of c_j = e[j] - j of the eviction list
+  int64_t offgd[kUnitTokens];  // a unit gathered from global memory: row offsets
+  int64_t offgs[kUnitTokens];
   uint64_t bar;              // completion of the round's bulk copies
 };
 
@@ -468,9 +471,11 @@ __device__ __forceinline__ int64_t unit_index(const CompactParams &p, int s, int
 }
 
 // Gather one 16-byte chunk (offset x0 inside region R of destination unit
-// ud of the run) from the staged source units.
-template <typename R>
-__device__ __forceinline__ uint4 gather_chunk(const uint8_t *stage, const int32_t *off, int ud,
+// ud of the run) from the source units: staged in shared memory (off: int32
+// offsets into the stage) or, for a unit with too many source units, read
+// straight from the cache (off: int64 offsets into it).
+template <typename R, typename OffT>
+__device__ __forceinline__ uint4 gather_chunk(const uint8_t *stage, const OffT *off, int ud,
                                               int rows_valid, uint32_t x0) {
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   constexpr int P = R::kPiece;
@@ -507,7 +512,9 @@ __device__ __forceinline__ uint4 gather_chunk(const uint8_t *stage, const int32_
 // rounds of destination units whose sources fit kCpSlots slots.  Each round's
 // source units arrive by bulk async copies on one mbarrier (all of them in
 // flight together), then every thread gathers 16-byte destination chunks and
-// stores them straight to global memory.
+// stores them straight to global memory.  A destination unit whose rows come
+// from more than kCpSlots source units (many evictions inside 16 kept rows)
+// is gathered from global memory directly.
 template <int CODEC, int SIDE>
 __device__ __forceinline__ void compact_run(const CompactParams &p, CompactSmem &sm,
                                             uint8_t *stage, int s, int kvh, int u0, int len,
@@ -594,6 +601,34 @@ __device__ __forceinline__ void compact_run(const CompactParams &p, CompactSmem 
   int ua = 0;
   while (ua < n_units) {  // rounds of destination units whose sources fit the slots
     const int s_first = sm.slot[ua * kUnitTokens];
+    if (sm.slot[min((ua + 1) * kUnitTokens, rows) - 1] - s_first >= kCpSlots) {
+      // this unit's rows come from more source units than the stage holds:
+      // gather it straight from global memory
+      const int r0 = ua * kUnitTokens, r1 = min(r0 + kUnitTokens, rows);
+      if (tid >= r0 && tid < r1) {
+        int64_t gi = unit_index(p, s, kvh, sm.srcpos[tid] / kUnitTokens);
+        if (gi < 0) {
+          set_err(p.err, KVQ_DEVERR_PAGE);
+          gi = 0;
+        }
+        const int rs = sm.srcpos[tid] % kUnitTokens;
+        sm.offgd[tid - r0] = gi * UB + D::kBase + D::dep(rs);
+        sm.offgs[tid - r0] = gi * UB + S::kBase + S::dep(rs);
+      }
+      __syncthreads();
+      for (int c = tid; c < CH; c += kCpThreads) {
+        const uint32_t x = static_cast<uint32_t>(c) * 16u;
+        uint4 v;
+        if (!L::kScales || x < static_cast<uint32_t>(S::kBase))
+          v = gather_chunk<D>(src, sm.offgd, 0, r1 - r0, x - D::kBase);
+        else
+          v = gather_chunk<S>(src, sm.offgs, 0, r1 - r0, x - S::kBase);
+        reinterpret_cast<uint4 *>(dst + (d_unit0 + ua) * UB)[c] = v;
+      }
+      __syncthreads();
+      ++ua;
+      continue;
+    }
     int ub = ua + 1;
     while (ub < n_units && sm.slot[min((ub + 1) * kUnitTokens, rows) - 1] - s_first < kCpSlots)
       ++ub;

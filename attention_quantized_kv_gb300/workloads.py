@@ -125,12 +125,18 @@ def get(name: str) -> Workload:
                          "(decay 0.9), 2048 lowest middle cells per seq (4 sink / 1024 recent "
                          "protected), compaction of K, V, scores and lengths")
         return w
+    if name == "evict_ragged4_kf16_vq8":
+        w = get("evict_ragged16_kf16_vq8")
+        w.name, w.n_seqs, w.lens = name, 4, w.lens[:4]
+        w.description = ("the first 4 sequences of evict_ragged16_kf16_vq8 (a profiling "
+                         "size: ~1.4 GB of caches with the compaction's second buffers)")
+        return w
     raise KeyError(name)
 
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
        "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
-       "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8"]
+       "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8", "evict_ragged4_kf16_vq8"]
 
 
 def n_evicted(w: Workload) -> list:

@@ -327,8 +327,9 @@ def _flush_l2(torch, bufs):
 
 
 def _traffic_for(workload):
-    """dram bytes per launch of the decode/prefill kernels from a committed ncu
-    summary, if it was taken on the current kernel sources; else None."""
+    """dram bytes per launch of the roofline kernel (decode, prefill attention
+    or compaction) from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -342,7 +343,8 @@ def _traffic_for(workload):
 
 def _kernel_source_hash(kind):
     names = {"decode": ["decode.cu", "kvq_device.cuh"],
-             "prefill": ["prefill.cu", "kvq_device.cuh"]}[kind]
+             "prefill": ["prefill.cu", "kvq_device.cuh"],
+             "evict": ["evict.cu", "kvq_device.cuh"]}[kind]
     h = hashlib.sha256()
     for n in names:
         with open(os.path.join(ROOT, "attention_quantized_kv_gb300", "csrc", n), "rb") as f:

@@ -273,10 +273,11 @@ KVQ_API int kvq_ladder_next(const int32_t *codecs, int32_t n, const int32_t *ord
                             int32_t n_order, double floor_bpv, int32_t *tensor, int32_t *codec);
 
 /* ------------------------------------------------------------------------
- * Probe-scored eviction (the Sparse KV eviction item of the Officina "How It
- * Works" list: an attention probe, a q.K softmax with exponential decay,
- * scores the cells; the lowest-scored middle cells are evicted first; the
- * sink cells at the start and the recent cells at the end are protected).
+ * Probe-scored eviction (the "Sparse KV eviction" item of the "How It Works"
+ * section of the GitHot listing of VITRIOL: an attention probe, a q.K softmax
+ * with exponential decay, scores the cells; the lowest-scored middle cells
+ * are evicted first; the sink cells at the start and the recent cells at the
+ * end are protected).
  * Scores are fp32 [n_seqs][capacity] by logical position, for contiguous and
  * paged layers alike.
  * ------------------------------------------------------------------------ */

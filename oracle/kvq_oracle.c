@@ -46,10 +46,10 @@
  *    lives at pool unit (table[s][j / 16] * n_kv + h) * 16 + j % 16.  The
  *    oracle computes on the contiguous layout and moves whole units between
  *    the two layouts (kvqo_page_scatter / kvqo_page_gather).
- *  - Probe-scored eviction (the Sparse KV eviction item of the Officina
- *    "How It Works" list: an attention probe, q.K softmax with exponential
- *    decay, scores the cells; the lowest-scored middle cells are evicted
- *    first; sinks and recent cells are protected).  The probe mass of token t
+ *  - Probe-scored eviction (the "Sparse KV eviction" item of the "How It
+ *    Works" section of the GitHot listing of VITRIOL: an attention probe,
+ *    q.K softmax with exponential decay, scores the cells; the lowest-scored
+ *    middle cells are evicted first; sinks and recent cells are protected).  The probe mass of token t
  *    of a sequence is the softmax weight the decode query of every query head
  *    puts on t, summed over the query heads; score = decay * score + mass.
  *    Eviction picks the n lowest (score, t) pairs among the middle tokens

@@ -1,5 +1,5 @@
-"""Probe-scored eviction on the GPU (the Sparse KV eviction item of the
-Officina "How It Works" list): probe scores within the derived tolerance of
+"""Probe-scored eviction on the GPU (the "Sparse KV eviction" item of the
+"How It Works" section of the GitHot listing of VITRIOL): probe scores within the derived tolerance of
 the oracle's fp64 probe mass, selections identical to the oracle's on
 oracle-side scores, compacted caches bit-exact against the oracle's
 compaction, and the whole decode -> probe -> select -> compact -> decode
