@@ -7,9 +7,10 @@ imported by it: only the tests, ``__graft_entry__.smoke()`` and the CPU
 baseline leg of ``bench.py`` use it.
 
 Every function follows a definition stated in ``kvq_oracle.c``'s header:
-the f16 / q8_0 / q4_0 block formats (sizes from the "Codecs" table of the
-buun-llama-cpp listing), the cache layout of the library's public header, and
-the plain softmax-attention definition evaluated in fp64.
+the f16 / q8_0 / q4_0 block formats and the rotated turbo4 row format (sizes
+from the "Codecs" table of the buun-llama-cpp listing), the cache layout of
+the library's public header, and the plain softmax-attention definition
+evaluated in fp64.
 """
 from __future__ import annotations
 
@@ -25,11 +26,11 @@ _SRC = os.path.join(_HERE, "kvq_oracle.c")
 _BUILD = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD, "libkvq_oracle.so")
 
-F16, Q8_0, Q4_0 = 0, 1, 2
+F16, Q8_0, Q4_0, TURBO4 = 0, 1, 2, 3
 SIDE_K, SIDE_V = 0, 1
 D = 128
 UNIT_TOKENS = 16
-ROW_BYTES = {F16: 256, Q8_0: 136, Q4_0: 72}
+ROW_BYTES = {F16: 256, Q8_0: 136, Q4_0: 72, TURBO4: 66}
 
 _lock = threading.Lock()
 _lib = None
@@ -105,6 +106,13 @@ def _load():
                                           ctypes.c_int, ctypes.c_int, i32p, i32p, i32p,
                                           ctypes.c_int]
         lib.kvqo_num_threads.restype = ctypes.c_int
+        u64p = ctypes.POINTER(ctypes.c_uint64)
+        lib.kvqo_splitmix64_next.argtypes = [u64p]
+        lib.kvqo_splitmix64_next.restype = ctypes.c_uint64
+        lib.kvqo_turbo_signs.argtypes = [ip]
+        lib.kvqo_fwht128_f32.argtypes = [ctypes.POINTER(ctypes.c_float)]
+        lib.kvqo_fwht128_f64.argtypes = [f64p]
+        lib.kvqo_turbo4_rotated.argtypes = [u8p, f64p]
         _lib = lib
         return lib
 
@@ -135,6 +143,39 @@ def half_to_float(bits: int) -> float:
 
 def float_to_half_bits(x: float) -> int:
     return int(_load().kvqo_float_to_half_rn(float(np.float32(x))))
+
+
+# --------------------------------------------------------------------------- turbo4 pieces
+
+def splitmix64(seed: int, n: int) -> list:
+    """The first n outputs of SplitMix64 from ``seed``."""
+    st = ctypes.c_uint64(seed)
+    return [int(_load().kvqo_splitmix64_next(ctypes.byref(st))) for _ in range(n)]
+
+
+def turbo_signs() -> np.ndarray:
+    out = np.zeros(D, np.int32)
+    _load().kvqo_turbo_signs(out.ctypes.data_as(ctypes.POINTER(ctypes.c_int)))
+    return out
+
+
+def fwht128(x, dtype=np.float64) -> np.ndarray:
+    """Unnormalised Sylvester-order FWHT of a 128-vector in fp32 or fp64."""
+    a = np.ascontiguousarray(x, dtype=dtype).copy()
+    assert a.shape == (D,)
+    if dtype == np.float32:
+        _load().kvqo_fwht128_f32(_ptr(a, ctypes.c_float))
+    else:
+        _load().kvqo_fwht128_f64(_ptr(a, ctypes.c_double))
+    return a
+
+
+def turbo4_rotated(row: np.ndarray) -> np.ndarray:
+    """y^ = d16 * (q - 8) of one canonical turbo4 row."""
+    r = np.ascontiguousarray(row, dtype=np.uint8)
+    out = np.zeros(D, np.float64)
+    _load().kvqo_turbo4_rotated(_ptr(r, ctypes.c_uint8), _ptr(out, ctypes.c_double))
+    return out
 
 
 # --------------------------------------------------------------------------- codecs

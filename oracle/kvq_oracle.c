@@ -20,6 +20,22 @@
  *            d = m / -8 (fp32 RN); t = x / d (0 if d == 0); u = t + 8.5 (fp32 RN);
  *            q = min(15, trunc(u)); byte j = q[j] | q[j+16] << 4; stored fp16_RN(d).
  *    Decoding is exact: x^ = d16 * q (q8_0), d16 * (q - 8) (q4_0).
+ *  - turbo4, a Walsh-Hadamard-rotated 4-bit scalar codec at 4.125 bits per
+ *    value (the turbo4 row of the same "Codecs" table; its "How it works"
+ *    list: an FWHT rotation with random sign flips makes the entries of a KV
+ *    vector close to i.i.d. Gaussian).  The pages give only the rotation and
+ *    the size (4 bits per value + 16 bits per 128-value row); this library's
+ *    reading, written out here:
+ *      signs s_j = -1 where bit 63 of output j (j = 0..127) of SplitMix64
+ *            seeded with 0x4B5651 is set, else +1;
+ *      t = s * x (fp32), then the unnormalised fast Walsh-Hadamard transform
+ *            in Sylvester order, stage h = 1, 2, ..., 64 turning each pair
+ *            (j, j + h) with j & h == 0 into (a + b, a - b), fp32 additions;
+ *      y = t / 8 (exact); then the q4_0 rule over all 128 values of y (one
+ *            scale per row); nibbles packed per 32-value group as in q4_0.
+ *    Decoding: y^ = d16 * (q - 8), x^ = s * H y^ / 16 (H H = 128 I, so the
+ *    rotation is orthogonal up to the exact factors 1/8 and 1/16; x^ is
+ *    exact in fp32 and fp64).  Canonical row: d16 then 64 packed bytes.
  *  - The per-(layer, side) codec choice of the classic F16 -> Q8_0 -> Q4_0
  *    ladder ("VBR -- Variable Bit-Rate KV Cache" section of the same listing)
  *    is just the codec argument of every call below.
@@ -72,7 +88,8 @@
 #define KVQO_D 128
 #define KVQO_UNIT_TOKENS 16
 
-enum { KVQO_F16 = 0, KVQO_Q8_0 = 1, KVQO_Q4_0 = 2 };
+enum { KVQO_F16 = 0, KVQO_Q8_0 = 1, KVQO_Q4_0 = 2, KVQO_TURBO4 = 3 };
+#define KVQO_TURBO_SEED 0x4B5651ull
 enum { KVQO_SIDE_K = 0, KVQO_SIDE_V = 1 };
 
 /* ------------------------------------------------------------------------ */
@@ -254,13 +271,132 @@ void kvqo_q4_0_decode_block(const uint8_t *in, double *out)
     }
 }
 
-/* Canonical row bytes for head_dim 128: the row's four blocks end to end. */
+/* ---- turbo4 ---------------------------------------------------------- */
+
+/* SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014): the state advances by 0x9E3779B97F4A7C15 and is
+ * mixed by two xor-shift-multiply steps and a final xor-shift. */
+uint64_t kvqo_splitmix64_next(uint64_t *state)
+{
+    uint64_t z = (*state += 0x9E3779B97F4A7C15ull);
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+/* The 128 turbo4 sign flips, +1 or -1. */
+void kvqo_turbo_signs(int *sgn)
+{
+    uint64_t st = KVQO_TURBO_SEED;
+    for (int j = 0; j < KVQO_D; ++j)
+        sgn[j] = (kvqo_splitmix64_next(&st) >> 63) ? -1 : 1;
+}
+
+/* In-place unnormalised fast Walsh-Hadamard transform of 128 values. */
+void kvqo_fwht128_f32(float *t)
+{
+    for (int h = 1; h < KVQO_D; h <<= 1)
+        for (int i = 0; i < KVQO_D; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                float a = t[j], b = t[j + h];
+                t[j] = a + b;
+                t[j + h] = a - b;
+            }
+}
+
+void kvqo_fwht128_f64(double *t)
+{
+    for (int h = 1; h < KVQO_D; h <<= 1)
+        for (int i = 0; i < KVQO_D; i += 2 * h)
+            for (int j = i; j < i + h; ++j) {
+                double a = t[j], b = t[j + h];
+                t[j] = a + b;
+                t[j + h] = a - b;
+            }
+}
+
+/* turbo4 of one row of 128 fp32 values: 66 bytes = d16 (2) + 64 bytes,
+ * byte 16 g + j (group g of 32, j < 16) = q[32 g + j] | q[32 g + j + 16] << 4.
+ * Returns 0, or -1 for non-finite input. */
+int kvqo_turbo4_encode_row_f32(const float *x, uint8_t *out)
+{
+    if (!kvqo_all_finite(x, KVQO_D))
+        return -1;
+    int sgn[KVQO_D];
+    kvqo_turbo_signs(sgn);
+    float y[KVQO_D];
+    for (int j = 0; j < KVQO_D; ++j)
+        y[j] = sgn[j] < 0 ? -x[j] : x[j];
+    kvqo_fwht128_f32(y);
+    for (int j = 0; j < KVQO_D; ++j)
+        y[j] = y[j] * 0.125f;
+    int jmax = 0;
+    float amax = fabsf(y[0]);
+    for (int j = 1; j < KVQO_D; ++j) {
+        float a = fabsf(y[j]);
+        if (a > amax) { /* strict: the lowest index keeps a tie */
+            amax = a;
+            jmax = j;
+        }
+    }
+    float m = y[jmax];
+    float d = m / -8.0f;
+    uint16_t d16 = kvqo_float_to_half_rn(d);
+    out[0] = (uint8_t)(d16 & 0xffu);
+    out[1] = (uint8_t)(d16 >> 8);
+    int q[KVQO_D];
+    for (int j = 0; j < KVQO_D; ++j) {
+        float t = (d != 0.0f) ? y[j] / d : 0.0f;
+        float u = t + 8.5f;
+        int v = (int)u; /* truncation toward zero; u >= 0.5 here */
+        q[j] = v > 15 ? 15 : v;
+    }
+    for (int g = 0; g < 4; ++g)
+        for (int j = 0; j < 16; ++j)
+            out[2 + 16 * g + j] =
+                (uint8_t)((q[32 * g + j] & 0xf) | ((q[32 * g + j + 16] & 0xf) << 4));
+    return 0;
+}
+
+int kvqo_turbo4_encode_row(const uint16_t *x16, uint8_t *out)
+{
+    float x[KVQO_D];
+    for (int j = 0; j < KVQO_D; ++j)
+        x[j] = kvqo_half_to_float(x16[j]);
+    return kvqo_turbo4_encode_row_f32(x, out);
+}
+
+/* The rotated values y^ = d16 * (q - 8) of one turbo4 row (exact). */
+void kvqo_turbo4_rotated(const uint8_t *in, double *yh)
+{
+    double d = kvqo_half_to_double((uint16_t)(in[0] | (in[1] << 8)));
+    for (int g = 0; g < 4; ++g)
+        for (int j = 0; j < 16; ++j) {
+            yh[32 * g + j] = d * (double)((int)(in[2 + 16 * g + j] & 0xf) - 8);
+            yh[32 * g + j + 16] = d * (double)((int)(in[2 + 16 * g + j] >> 4) - 8);
+        }
+}
+
+/* x^ = s * H y^ / 16 of one turbo4 row (exact in fp64). */
+void kvqo_turbo4_decode_row(const uint8_t *in, double *out)
+{
+    int sgn[KVQO_D];
+    kvqo_turbo_signs(sgn);
+    kvqo_turbo4_rotated(in, out);
+    kvqo_fwht128_f64(out);
+    for (int j = 0; j < KVQO_D; ++j)
+        out[j] = sgn[j] * out[j] / 16.0;
+}
+
+/* Canonical row bytes for head_dim 128: the row's four blocks end to end
+ * (turbo4: the row's scale, then its 64 packed bytes). */
 int kvqo_row_bytes(int codec)
 {
     switch (codec) {
     case KVQO_F16: return 2 * KVQO_D;
     case KVQO_Q8_0: return 4 * 34;
     case KVQO_Q4_0: return 4 * 18;
+    case KVQO_TURBO4: return 2 + KVQO_D / 2;
     default: return -1;
     }
 }
@@ -285,6 +421,10 @@ int kvqo_encode_rows(int codec, int64_t n, const uint16_t *x, uint8_t *out)
                 o[2 * d] = (uint8_t)(xr[d] & 0xffu);
                 o[2 * d + 1] = (uint8_t)(xr[d] >> 8);
             }
+        } else if (codec == KVQO_TURBO4) {
+            int rc = kvqo_turbo4_encode_row(xr, o);
+            if (rc)
+                return rc;
         } else {
             for (int b = 0; b < 4; ++b) {
                 int rc = codec == KVQO_Q8_0 ? kvqo_q8_0_encode_block(xr + 32 * b, o + 34 * b)
@@ -312,6 +452,8 @@ int kvqo_decode_rows(int codec, int64_t n, const uint8_t *in, double *out)
         } else if (codec == KVQO_Q8_0) {
             for (int b = 0; b < 4; ++b)
                 kvqo_q8_0_decode_block(r + 34 * b, o + 32 * b);
+        } else if (codec == KVQO_TURBO4) {
+            kvqo_turbo4_decode_row(r, o);
         } else {
             for (int b = 0; b < 4; ++b)
                 kvqo_q4_0_decode_block(r + 18 * b, o + 32 * b);
@@ -365,6 +507,22 @@ int kvqo_unit_offset(int codec, int side, int r, int cb)
             return 1024 + tig * 32 + b * 8 + rh * 4 + par * 2 + o;
         }
         int jc = o - 2; /* canonical packed byte 0..15 of block b */
+        if (side == KVQO_SIDE_K) {
+            int w = jc >> 2, i = jc & 3;
+            return (b >> 1) * 512 + (4 * g + w) * 16 + ((b & 1) * 2 + rh) * 4 + i;
+        } else {
+            int mt = 2 * b + (jc >> 3), gq = jc & 7;
+            return (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
+        }
+    }
+    if (codec == KVQO_TURBO4) {
+        /* packed bytes at the q4_0 places of group b; one scale per row */
+        if (cb < 2) {
+            if (side == KVQO_SIDE_K)
+                return 1024 + g * 4 + rh * 2 + cb;
+            return 1024 + tig * 8 + rh * 4 + par * 2 + cb;
+        }
+        int b = (cb - 2) >> 4, jc = (cb - 2) & 15;
         if (side == KVQO_SIDE_K) {
             int w = jc >> 2, i = jc & 3;
             return (b >> 1) * 512 + (4 * g + w) * 16 + ((b & 1) * 2 + rh) * 4 + i;
@@ -498,9 +656,9 @@ int kvqo_page_move(int codec, uint8_t *cache, int n_seqs, int n_kv, int capacity
 
 /* Re-encode tokens [0, seq_lens[s]) of every (seq, kv_head) stream of one
  * side from src_codec to dst_codec (dst is a separate cache of dst_codec).
- * Each row is decoded to fp32 (exact: d16 * q or d16 * (n - 8), or the fp16
- * value) and encoded again: q8_0 / q4_0 by the fp32 formulas above, f16 by
- * rounding to fp16.  Returns 0, or -1 on bad arguments. */
+ * Each row is decoded to fp32 (exact: d16 * q or d16 * (n - 8), the fp16
+ * value, or turbo4's x^) and encoded again: q8_0 / q4_0 / turbo4 by the fp32
+ * formulas above, f16 by rounding to fp16.  Returns 0, or -1 on bad arguments. */
 int kvqo_requantize_side(int src_codec, int dst_codec, int side, const uint8_t *src,
                          uint8_t *dst, int n_seqs, int n_kv, int capacity,
                          const int32_t *seq_lens)
@@ -528,6 +686,9 @@ int kvqo_requantize_side(int src_codec, int dst_codec, int side, const uint8_t *
                         out[2 * d] = (uint8_t)(hb & 0xffu);
                         out[2 * d + 1] = (uint8_t)(hb >> 8);
                     }
+                } else if (dst_codec == KVQO_TURBO4) {
+                    if (kvqo_turbo4_encode_row_f32(x, out))
+                        return -1;
                 } else {
                     for (int b = 0; b < 4; ++b) {
                         int rc = dst_codec == KVQO_Q8_0

@@ -206,7 +206,7 @@ def test_q8_0_exact_rational_rounding_on_sampled_blocks():
 
 # ---------------------------------------------------------------- cache layout
 
-@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0, oracle.TURBO4])
 @pytest.mark.parametrize("side", [oracle.SIDE_K, oracle.SIDE_V])
 def test_unit_layout_is_a_bijection(codec, side):
     tab = oracle.unit_offset_table(codec, side)
@@ -215,7 +215,7 @@ def test_unit_layout_is_a_bijection(codec, side):
     assert np.array_equal(np.sort(tab.ravel()), np.arange(ub))
 
 
-@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0])
+@pytest.mark.parametrize("codec", [oracle.F16, oracle.Q8_0, oracle.Q4_0, oracle.TURBO4])
 def test_append_then_dequant_round_trip_in_pieces(codec):
     rng = np.random.default_rng(3)
     n_seqs, n_kv, cap = 2, 3, 64
@@ -472,7 +472,7 @@ def _cache_from_rows(codec, side, rows16, n_seqs, n_kv, capacity, lens):
 
 
 @pytest.mark.parametrize("side", [0, 1])
-@pytest.mark.parametrize("dst", [1, 2])
+@pytest.mark.parametrize("dst", [1, 2, 3])
 def test_requantize_from_f16_equals_appending_the_same_rows(side, dst):
     n_seqs, n_kv, capacity, lens = 2, 2, 256, [40, 17]
     rng = np.random.default_rng(7 + side + 2 * dst)
@@ -504,7 +504,7 @@ def test_requantize_q8_to_q4_equals_q4_of_fp16_exact_values(side):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("src_codec", [1, 2])
+@pytest.mark.parametrize("src_codec", [1, 2, 3])
 def test_requantize_to_f16_rounds_the_decoded_values(src_codec):
     n_seqs, n_kv, capacity, lens = 1, 1, 256, [20]
     rng = np.random.default_rng(9)
@@ -543,7 +543,7 @@ def test_pool_with_one_kv_head_and_identity_table_is_the_contiguous_cache(codec)
     assert np.array_equal(pool, cache)
 
 
-@pytest.mark.parametrize("codec", [0, 1, 2])
+@pytest.mark.parametrize("codec", [0, 1, 2, 3])
 def test_pool_round_trip_under_a_shuffled_table(codec):
     n_seqs, n_kv, pps, n_pages = 3, 2, 3, 11
     cap = pps * 256
@@ -620,7 +620,7 @@ def test_evict_select_against_brute_force_and_protection():
         assert all(sink <= t < length - recent for t in got)
 
 
-@pytest.mark.parametrize("codec", [0, 1, 2])
+@pytest.mark.parametrize("codec", [0, 1, 2, 3])
 @pytest.mark.parametrize("side", [0, 1])
 def test_compaction_equals_appending_the_kept_rows(codec, side):
     n_seqs, n_kv, cap, lens = 2, 2, 256, [40, 17]
@@ -638,3 +638,112 @@ def test_compaction_equals_appending_the_kept_rows(codec, side):
     want = np.zeros_like(c)
     oracle.append_side(codec, side, want, n_seqs, n_kv, cap, [0] * n_seqs, kept_lens, kept)
     assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------- turbo4 (rotated 4-bit)
+
+def test_splitmix64_published_outputs():
+    g = _golden("splitmix64.json")
+    assert oracle.splitmix64(g["seed"], len(g["outputs"])) == [int(v) for v in g["outputs"]]
+
+
+def test_turbo_signs_are_bit_63_of_the_generator():
+    outs = oracle.splitmix64(0x4B5651, 128)
+    want = np.array([-1 if (v >> 63) else 1 for v in outs], np.int32)
+    got = oracle.turbo_signs()
+    assert np.array_equal(got, want)
+    assert 40 < (got > 0).sum() < 88  # sign flips, not a constant
+
+
+def test_fwht_is_the_sylvester_hadamard_matrix():
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64)
+    rng = np.random.default_rng(90)
+    xi = rng.integers(-1000, 1000, 128).astype(np.float64)  # exact in fp32 and fp64
+    assert np.array_equal(oracle.fwht128(xi), H @ xi)
+    assert np.array_equal(oracle.fwht128(xi.astype(np.float32), np.float32), (H @ xi).astype(np.float32))
+    x = rng.standard_normal(128)
+    assert np.allclose(oracle.fwht128(x), H @ x, rtol=0, atol=1e-12)
+    assert np.allclose(oracle.fwht128(oracle.fwht128(x)), 128 * x, rtol=0, atol=1e-11)
+
+
+def test_turbo4_hand_derived_rows():
+    g = _golden("turbo4_rows.json")
+    s = oracle.turbo_signs()
+    assert s[0] == 1
+    for r in g["rows"]:
+        x = np.zeros(128) if r["x"] == "e0" else s.astype(np.float64)
+        if r["x"] == "e0":
+            x[0] = 1.0
+        row = oracle.encode_rows(oracle.TURBO4, x.astype(np.float16)[None])[0]
+        assert row.tobytes().hex() == r["bytes_hex"], r["name"]
+        dec = oracle.decode_rows(oracle.TURBO4, row[None])[0]
+        assert np.array_equal(dec, x), r["name"]
+
+
+def test_turbo4_round_trip_and_quantisation_bound():
+    """y = H(s x)/8 recomputed with the Hadamard matrix in fp64; the stored
+    y^ = d16 (q - 8) is within d16/2 (+ the fp16 rounding of d) of y except
+    for values clamped to 15 (within |d|); x^ = s H y^ / 16 exactly, and
+    ||x^ - x|| = ||y^ - y|| / sqrt(2) (the rotation is orthogonal up to the
+    exact factors)."""
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64)
+    s = oracle.turbo_signs().astype(np.float64)
+    rng = np.random.default_rng(91)
+    x = rng.standard_normal((400, 128))
+    x[:, [3, 77]] *= 8.0  # outlier channels
+    x[:100] *= 1e-3
+    x = x.astype(np.float16)
+    rows = oracle.encode_rows(oracle.TURBO4, x)
+    dec = oracle.decode_rows(oracle.TURBO4, rows)
+    for i in range(len(x)):
+        xd = x[i].astype(np.float64)
+        y = H @ (s * xd) / 8
+        yh = oracle.turbo4_rotated(rows[i])
+        d16 = oracle.half_to_float(int(rows[i][0]) | (int(rows[i][1]) << 8))
+        jm = int(np.argmax(np.abs(y)))
+        d = np.float32(y[jm]) / np.float32(-8.0)
+        q = np.round(yh / d16 + 8).astype(int)
+        err = np.abs(y - yh)
+        clamped = q == 15
+        bound = abs(d16) / 2 + np.abs(q - 8) * abs(float(d) - d16) + 1e-6 * abs(d16)
+        assert (err[~clamped] <= bound[~clamped]).all()
+        assert (err[clamped] <= abs(d16) * 1.0001 + 1e-6 * abs(d16)).all()
+        assert np.array_equal(dec[i], s * (H @ yh) / 16)
+        assert np.linalg.norm(dec[i] - xd) == pytest.approx(np.linalg.norm(yh - y) / math.sqrt(2),
+                                                            rel=1e-9)
+
+
+def test_turbo4_bits_per_value_follow_the_codec_table():
+    g = _golden("codec_sizes.json")
+    assert oracle.bits_per_value(oracle.TURBO4) == g["bits_per_value"]["turbo4"]
+    assert oracle.ROW_BYTES[oracle.TURBO4] == g["derived"]["row_bytes"]["turbo4"]
+
+
+def test_turbo4_attention_equals_attention_over_decoded_rows():
+    """decode_layer over a turbo4 cache is softmax attention over x^ (the
+    oracle never attends in the rotated space), and q . x^ = (H s q / 16) . y^."""
+    from scipy.linalg import hadamard
+    H = hadamard(128).astype(np.float64)
+    s = oracle.turbo_signs().astype(np.float64)
+    rng = np.random.default_rng(92)
+    n_kv, n_q, cap, T = 1, 2, 256, 30
+    k = rng.standard_normal((1, T, n_kv, 128)).astype(np.float16)
+    v = rng.standard_normal((1, T, n_kv, 128)).astype(np.float16)
+    ck = np.zeros(oracle.cache_bytes(3, 1, n_kv, cap), np.uint8)
+    cv = np.zeros_like(ck)
+    oracle.append_side(3, 0, ck, 1, n_kv, cap, [0], [T], k)
+    oracle.append_side(3, 1, cv, 1, n_kv, cap, [0], [T], v)
+    q = rng.standard_normal((1, n_q, 128)).astype(np.float16)
+    out, lse = oracle.decode_layer(3, 3, ck, cv, 1, n_kv, n_q, cap, [T], q, 0.1)
+    K = oracle.dequant_stream(3, 0, ck, n_kv, cap, 0, 0, T)
+    V = oracle.dequant_stream(3, 1, cv, n_kv, cap, 0, 0, T)
+    ro, rl = _softmax_attn_numpy(q[0], K, V, 0.1)
+    assert np.allclose(out[0], ro, rtol=0, atol=1e-12)
+    assert np.allclose(lse[0], rl, rtol=0, atol=1e-12)
+    rows = oracle.encode_rows(3, k[0, :, 0])
+    qr = H @ (s * q[0, 0].astype(np.float64)) / 16
+    for t in range(T):
+        assert float(q[0, 0].astype(np.float64) @ K[t]) == pytest.approx(
+            float(qr @ oracle.turbo4_rotated(rows[t])), rel=1e-12, abs=1e-12)
