@@ -16,18 +16,19 @@ import math
 import torch
 
 from . import _abi
-from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_DEVERR_CAPACITY, KVQ_DEVERR_EVICT,
+from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_TURBO4, KVQ_DEVERR_CAPACITY,
+                   KVQ_DEVERR_EVICT,
                    KVQ_DEVERR_MAXLEN, KVQ_DEVERR_PAGE, KVQ_DEVERR_SEQLEN, KVQ_DEVERR_TIMEOUT,
                    kvq_layer)
 
-__all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "CODEC_NAMES", "KVQError", "KVLayer",
+__all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "KVQ_TURBO4", "CODEC_NAMES", "KVQError", "KVLayer",
            "kv_append_quantize", "attn_decode_workspace", "attn_decode",
            "attn_prefill_workspace", "attn_prefill_chunk", "kvq_row_bytes", "kvq_cache_bytes",
            "kvq_pool_bytes", "KVQ_DEVERR_PAGE", "kv_requantize", "degrade", "aggregate_bpv",
            "ladder_next", "default_scale", "KVQ_DEVERR_EVICT", "kv_probe_scores",
            "kv_evict_select", "kv_compact", "evict"]
 
-CODEC_NAMES = {KVQ_F16: "f16", KVQ_Q8_0: "q8_0", KVQ_Q4_0: "q4_0"}
+CODEC_NAMES = {KVQ_F16: "f16", KVQ_Q8_0: "q8_0", KVQ_Q4_0: "q4_0", KVQ_TURBO4: "turbo4"}
 HEAD_DIM = 128
 
 
@@ -102,7 +103,7 @@ class KVLayer:
             vb = kvq_cache_bytes(codec_v, n_seqs, n_kv_heads, capacity, head_dim)
         if kb < 0 or vb < 0:
             raise ValueError("invalid cache geometry (capacity must be a multiple of 256, "
-                             "head_dim 128, codecs f16/q8_0/q4_0)")
+                             "head_dim 128, codecs f16/q8_0/q4_0/turbo4)")
         self.k_cache = k_cache if k_cache is not None else torch.empty(kb, dtype=torch.uint8,
                                                                         device=device)
         self.v_cache = v_cache if v_cache is not None else torch.empty(vb, dtype=torch.uint8,

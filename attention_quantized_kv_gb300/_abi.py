@@ -12,7 +12,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "_build", "libkvq.so")
 
-KVQ_F16, KVQ_Q8_0, KVQ_Q4_0 = 0, 1, 2
+KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_TURBO4 = 0, 1, 2, 3
 KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECAPACITY, KVQ_EALIGN, KVQ_EWORKSPACE, KVQ_ECUDA = range(7)
 KVQ_DEVERR_CAPACITY, KVQ_DEVERR_MAXLEN, KVQ_DEVERR_TIMEOUT, KVQ_DEVERR_SEQLEN = 1, 2, 4, 8
 KVQ_DEVERR_PAGE, KVQ_DEVERR_EVICT = 16, 32

@@ -56,6 +56,41 @@ __device__ __forceinline__ void encode_q4(const float (&x)[4], int lane, int (&q
   }
 }
 
+// turbo4: signs, FWHT and the factor 1/8 (the rotation of the row, exact
+// order of the definition), then the q4_0 rule over all 128 rotated values
+// (32 lanes, lowest dim wins ties).
+__device__ __forceinline__ void encode_turbo4(const float (&x)[4], int lane, int (&q)[4],
+                                              __half &d16) {
+  float y[4] = {x[0], x[1], x[2], x[3]};
+  turbo_flip_lane(y, lane);
+  fwht128_warp(y, lane);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] *= 0.125f;
+  float best = fabsf(y[0]);
+  float m = y[0];
+  int idx = 4 * lane;
+#pragma unroll
+  for (int i = 1; i < 4; ++i) {
+    const float a = fabsf(y[i]);
+    if (a > best) { best = a; m = y[i]; idx = 4 * lane + i; }
+  }
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const float om = __shfl_xor_sync(0xffffffffu, m, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ob > best || (ob == best && oi < idx)) { best = ob; m = om; idx = oi; }
+  }
+  const float d = __fdiv_rn(m, -8.0f);
+  d16 = __float2half_rn(d);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float t = d != 0.0f ? __fdiv_rn(y[i], d) : 0.0f;
+    const int v = static_cast<int>(__fadd_rn(t, 8.5f));  // truncation; u >= 0.5
+    q[i] = v > 15 ? 15 : v;
+  }
+}
+
 __device__ __forceinline__ void st_u16(uint8_t *p, uint32_t v) {
   *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(v);
 }
@@ -101,8 +136,9 @@ __device__ __forceinline__ void store_row(int codec, uint8_t *unit, int r, int l
     }
     return;
   }
-  // q4_0: canonical byte jc = q[jc] | q[jc+16] << 4; lanes lb<4 hold jc = 4lb..4lb+3
-  // and fetch the high nibbles from lane lb+4 of the same block.
+  // q4_0 and turbo4: canonical byte jc of block (group) b = q[jc] | q[jc+16]
+  // << 4; lanes lb<4 hold jc = 4lb..4lb+3 and fetch the high nibbles from
+  // lane lb+4 of the same block.
   int hi[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) hi[i] = __shfl_down_sync(0xffffffffu, q[i], 4);
@@ -123,6 +159,12 @@ __device__ __forceinline__ void store_row(int codec, uint8_t *unit, int r, int l
       }
     }
   }
+  if (codec == KVQ_TURBO4) {  // one scale per row
+    if (lane == 0)
+      st_u16(unit + (SIDE == 0 ? 1024 + g * 4 + rh * 2 : 1024 + tig * 8 + rh * 4 + par * 2),
+             dbits);
+    return;
+  }
   if (lb == 0) {
     const int off = SIDE == 0 ? 1024 + g * 16 + rh * 8 + b * 2
                               : 1024 + tig * 32 + b * 8 + rh * 4 + par * 2;
@@ -132,7 +174,8 @@ __device__ __forceinline__ void store_row(int codec, uint8_t *unit, int r, int l
 
 // Read one row (token row r of `unit`) into the lane-held form of store_row:
 // lane l gets dims 4l..4l+3 as fp32, the decoded values x^ = d16 * q (q8_0),
-// d16 * (n - 8) (q4_0) or the fp16 values, all exact in fp32.
+// d16 * (n - 8) (q4_0), s * H (d16 * (n - 8)) / 16 (turbo4) or the fp16
+// values, all exact in fp32.
 template <int SIDE>
 __device__ __forceinline__ void load_row(int codec, const uint8_t *unit, int r, int lane,
                                          float (&x)[4]) {
@@ -181,6 +224,11 @@ __device__ __forceinline__ void load_row(int codec, const uint8_t *unit, int r, 
     const float d = __half2float(*reinterpret_cast<const __half *>(unit + soff));
 #pragma unroll
     for (int i = 0; i < 4; ++i) x[i] = d * static_cast<float>(q[i]);
+    return;
+  }
+  if (codec == KVQ_TURBO4) {
+    turbo4_row_rotated<SIDE>(unit, r, lane, x);
+    turbo_unrotate_lane(x, lane);
     return;
   }
   // q4_0: lanes lb < 4 hold canonical bytes jc = 4lb..4lb+3 (low nibbles),
@@ -248,6 +296,7 @@ __device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, i
   __half d16 = __float2half_rn(0.0f);
   if (codec == KVQ_Q8_0) encode_q8(x, q, d16);
   else if (codec == KVQ_Q4_0) encode_q4(x, lane, q, d16);
+  else if (codec == KVQ_TURBO4) encode_turbo4(x, lane, q, d16);
   int64_t unit_idx;
   if (p.table) {
     const int pg =
@@ -375,6 +424,8 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
         encode_q8(x, q, d16);
       } else if (p.dst_codec == KVQ_Q4_0) {
         encode_q4(x, lane, q, d16);
+      } else if (p.dst_codec == KVQ_TURBO4) {
+        encode_turbo4(x, lane, q, d16);
       } else {
         const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
         raw.x = *reinterpret_cast<const uint32_t *>(&h01);

@@ -2,9 +2,11 @@
 //
 // Computes, for every (sequence, query head), o = softmax(scale * q K^T) V
 // over all cached keys, with K and V dequantized from f16 / q8_0 / q4_0 blocks
-// (the codecs of the "Codecs" table of the buun-llama-cpp listing; the K and
-// V sides are typed independently, as in its VBR section's per-(layer, side)
-// ladder).  Work is cut along the token axis; each piece produces a partial
+// or turbo4 rotated rows (the codecs of the "Codecs" table of the
+// buun-llama-cpp listing; the K and V sides are typed independently, as in
+// its VBR section's per-(layer, side) ladder).  turbo4 is never un-rotated
+// per token: the query is rotated once (q . x^ = (H s q / 16) . y^), V is
+// accumulated in the rotated space and the merged output is rotated back.  Work is cut along the token axis; each piece produces a partial
 // (running max m, running sum l, unnormalised o) and a second kernel merges
 // the partials of each (sequence, head) with the log-sum-exp identity: the
 // last CTA to finish a stream (an atomic ticket, no waiting) merges its
@@ -92,7 +94,7 @@ __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
 // Head-dim index of accumulator row (m-row) of m-tile mt for the V codec.
 template <int CV>
 __device__ __forceinline__ int v_dim(int mt, int mrow) {
-  if (CV == KVQ_Q4_0) {
+  if (nibble_codec(CV)) {
     const int b = mt >> 1, hh = mt & 1;
     return 32 * b + 8 * hh + (mrow & 7) + (mrow >> 3) * 16;
   }
@@ -115,6 +117,31 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
       mma16816(s, a0, qb[2 * b][0], qb[2 * b][1]);
       mma16816(s, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
     }
+  } else if (CK == KVQ_TURBO4) {
+    // one scale per row: the four 32-dim groups share one accumulator
+    const uint32_t sc = *reinterpret_cast<const uint32_t *>(ku + 1024 + g * 4);
+    float sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int jv = 0; jv < 2; ++jv) {
+      const uint4 w = lds128(ku + jv * 512 + lane * 16);
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int b = 2 * jv + hb;
+        const uint32_t W0 = hb ? w.z : w.x, W1 = hb ? w.w : w.y;
+        const uint32_t X0 = W0 >> 8, X1 = W1 >> 8;
+        const uint32_t a0[4] = {u4_pair_minus8(W0), u4_pair_minus8(W1), u4_pair_minus8(X0),
+                                u4_pair_minus8(X1)};
+        const uint32_t a1[4] = {u4_pair_minus8_hi(W0), u4_pair_minus8_hi(W1),
+                                u4_pair_minus8_hi(X0), u4_pair_minus8_hi(X1)};
+        mma16816(sb, a0, qb[2 * b][0], qb[2 * b][1]);
+        mma16816(sb, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
+      }
+    }
+    const float dlo = half_bits_to_float(sc & 0xffffu), dhi = half_bits_to_float(sc >> 16);
+    s[0] = dlo * sb[0];
+    s[1] = dlo * sb[1];
+    s[2] = dhi * sb[2];
+    s[3] = dhi * sb[3];
   } else {
     const uint4 sc = lds128(ku + unit_scale_offset(CK) + g * 16);
     const uint32_t dl[2] = {sc.x, sc.y}, dh[2] = {sc.z, sc.w};
@@ -179,10 +206,17 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
       mma16816(o[mt], a, B0, B1);
     }
   } else {
-    const uint4 s01 = lds128(vu + unit_scale_offset(CV) + tig * 32);
-    const uint4 s23 = lds128(vu + unit_scale_offset(CV) + tig * 32 + 16);
-    uint32_t dp01[4] = {s01.x, s01.z, s23.x, s23.z};
-    uint32_t dp23[4] = {s01.y, s01.w, s23.y, s23.w};
+    uint32_t dp01[4], dp23[4];
+    if (CV == KVQ_TURBO4) {  // one scale per token: (2tig, 2tig+1), (2tig+8, 2tig+9)
+      const uint2 sv = lds64(vu + 1024 + tig * 8);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) { dp01[b] = sv.x; dp23[b] = sv.y; }
+    } else {
+      const uint4 s01 = lds128(vu + unit_scale_offset(CV) + tig * 32);
+      const uint4 s23 = lds128(vu + unit_scale_offset(CV) + tig * 32 + 16);
+      dp01[0] = s01.x; dp01[1] = s01.z; dp01[2] = s23.x; dp01[3] = s23.z;
+      dp23[0] = s01.y; dp23[1] = s01.w; dp23[2] = s23.y; dp23[3] = s23.w;
+    }
     if (!FULL) {
 #pragma unroll
       for (int b = 0; b < 4; ++b) { dp01[b] &= m01; dp23[b] &= m23; }
@@ -219,7 +253,8 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
       }
       const int g = lane >> 2;
       // scales of block g & 3 for tokens (2tig, 2tig+1) and (2tig+8, 2tig+9)
-      uint2 dg = lds64(vu + unit_scale_offset(CV) + tig * 32 + (g & 3) * 8);
+      uint2 dg = CV == KVQ_TURBO4 ? lds64(vu + 1024 + tig * 8)
+                                  : lds64(vu + unit_scale_offset(CV) + tig * 32 + (g & 3) * 8);
       if (!FULL) { dg.x &= m01; dg.y &= m23; }
       const uint32_t a[4] = {dg.x, dg.x, dg.y, dg.y};
       mma16816(corr, a, B0, B1);
@@ -401,7 +436,7 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
     for (int mt = 0; mt < 8; ++mt) {
       o[mt][0] *= a0; o[mt][1] *= a1; o[mt][2] *= a0; o[mt][3] *= a1;
     }
-    if (CV == KVQ_Q4_0) { corr[0] *= a0; corr[1] *= a1; corr[2] *= a0; corr[3] *= a1; }
+    if (nibble_codec(CV)) { corr[0] *= a0; corr[1] *= a1; corr[2] *= a0; corr[3] *= a1; }
     m0 = mn0;
     m1 = mn1;
   }
@@ -429,17 +464,23 @@ __device__ __forceinline__ void load_q_frags(const __half *q, int64_t qrow0, int
   const int hq = hg * 8 + g;
   const bool hvalid = hq < G;
   const __half *qrow = q + (qrow0 + (hvalid ? hq : 0)) * kD;
+  if (CK == KVQ_TURBO4) {
+    rotated_q_frags(qrow, hvalid, tig, qb, [](const __half *p) {
+      return *reinterpret_cast<const uint2 *>(p);
+    });
+  } else {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
-    uint2 v = make_uint2(0u, 0u);
-    if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
-    if (CK == KVQ_F16) {
-      qb[c][0] = v.x;
-      qb[c][1] = v.y;
-    } else {
-      qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
-      qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+    for (int c = 0; c < 8; ++c) {
+      const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+      uint2 v = make_uint2(0u, 0u);
+      if (hvalid) v = *reinterpret_cast<const uint2 *>(qrow + base);
+      if (CK == KVQ_F16) {
+        qb[c][0] = v.x;
+        qb[c][1] = v.y;
+      } else {
+        qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+        qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+      }
     }
   }
 }
@@ -452,17 +493,21 @@ __device__ __forceinline__ void load_q_frags_smem(const __half *qs, int nh, int 
   const int g = lane >> 2, tig = lane & 3;
   const bool hvalid = g < nh;
   const __half *qrow = qs + (hvalid ? g : 0) * kD;
+  if (CK == KVQ_TURBO4) {
+    rotated_q_frags(qrow, hvalid, tig, qb, [](const __half *p) { return lds64(p); });
+  } else {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
-    uint2 v = make_uint2(0u, 0u);
-    if (hvalid) v = lds64(qrow + base);
-    if (CK == KVQ_F16) {
-      qb[c][0] = v.x;
-      qb[c][1] = v.y;
-    } else {
-      qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
-      qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+    for (int c = 0; c < 8; ++c) {
+      const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+      uint2 v = make_uint2(0u, 0u);
+      if (hvalid) v = lds64(qrow + base);
+      if (CK == KVQ_F16) {
+        qb[c][0] = v.x;
+        qb[c][1] = v.y;
+      } else {
+        qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+        qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+      }
     }
   }
 }
@@ -477,6 +522,7 @@ struct MergeArgs {
   int n_q, G;
 };
 
+template <bool ROT>
 __device__ __forceinline__ void merge_stream(const MergeArgs p, float4 *xacc, float *xl,
                                              int stream, int seq, int kvh, int hg, int c_first,
                                              int c_last, int64_t S, int n_s, int64_t U, int P) {
@@ -581,9 +627,11 @@ __device__ __forceinline__ void merge_stream(const MergeArgs p, float4 *xacc, fl
     }
     const float inv = L > 0.0f ? 1.0f / L : 0.0f;
     const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
+    float ov[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+    if (ROT) turbo_unrotate_lane(ov, lane);  // turbo4 V: back from the rotated space
     __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
-    dst[0] = __floats2half2_rn(acc.x * inv, acc.y * inv);
-    dst[1] = __floats2half2_rn(acc.z * inv, acc.w * inv);
+    dst[0] = __floats2half2_rn(ov[0], ov[1]);
+    dst[1] = __floats2half2_rn(ov[2], ov[3]);
     if (p.lse && lane == 0)
       p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   }
@@ -814,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       k_next += two ? 2 * kWarps : kWarps;
     }
 
-    if (CV == KVQ_Q4_0) {
+    if (nibble_codec(CV)) {
       // Restore the codec offset: o = 2^24 o - 8 C_b (rows g) and
       // 2^20 o - 8 C_b (rows g+8), C_b from lane 4b + tig of corr.
 #pragma unroll
@@ -886,7 +934,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     if (last_flag) {
       __threadfence();
       const MergeArgs ma = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
-      merge_stream(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first, c_last, S, seg.n_s, U, P);
+      merge_stream<CV == KVQ_TURBO4>(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first, c_last,
+                                     S, seg.n_s, U, P);
     }
 
     useg = seg_end;
@@ -926,7 +975,8 @@ cudaError_t launch_split_v(int cv, const DecodeParams &p, int grid, cudaStream_t
   switch (cv) {
     case KVQ_F16: return launch_split<CK, KVQ_F16>(p, grid, stream);
     case KVQ_Q8_0: return launch_split<CK, KVQ_Q8_0>(p, grid, stream);
-    default: return launch_split<CK, KVQ_Q4_0>(p, grid, stream);
+    case KVQ_Q4_0: return launch_split<CK, KVQ_Q4_0>(p, grid, stream);
+    default: return launch_split<CK, KVQ_TURBO4>(p, grid, stream);
   }
 }
 
@@ -982,7 +1032,8 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
   switch (L.codec_k) {
     case KVQ_F16: return launch_split_v<KVQ_F16>(L.codec_v, p, pl.grid, stream);
     case KVQ_Q8_0: return launch_split_v<KVQ_Q8_0>(L.codec_v, p, pl.grid, stream);
-    default: return launch_split_v<KVQ_Q4_0>(L.codec_v, p, pl.grid, stream);
+    case KVQ_Q4_0: return launch_split_v<KVQ_Q4_0>(L.codec_v, p, pl.grid, stream);
+    default: return launch_split_v<KVQ_TURBO4>(L.codec_v, p, pl.grid, stream);
   }
 }
 

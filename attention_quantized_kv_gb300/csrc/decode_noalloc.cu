@@ -73,8 +73,8 @@ int attn_decode_noalloc(const kvq_layer *L, const void *q, float scale, void *ou
   // Argument checks (the same rules as attn_decode).
   if (!L) return KVQ_EINVAL;
   if (L->head_dim != 128) return KVQ_EUNSUPPORTED;
-  const bool codecs_ok = L->codec_k >= KVQ_F16 && L->codec_k <= KVQ_Q4_0 &&
-                         L->codec_v >= KVQ_F16 && L->codec_v <= KVQ_Q4_0;
+  const bool codecs_ok = L->codec_k >= KVQ_F16 && L->codec_k <= KVQ_TURBO4 &&
+                         L->codec_v >= KVQ_F16 && L->codec_v <= KVQ_TURBO4;
   if (!codecs_ok) return KVQ_EUNSUPPORTED;
   if (L->n_seqs <= 0 || L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->capacity <= 0 ||
       L->reserved != 0 || L->n_q_heads % L->n_kv_heads != 0)

@@ -64,7 +64,7 @@ template <int CK>
 struct KFrag {
   static constexpr int NW = CK == KVQ_F16 ? 8 : (CK == KVQ_Q8_0 ? 4 : 2);
   uint4 w[NW];
-  uint4 sc;
+  uint4 sc;  // turbo4: .x = scales of rows g and g + 8
 };
 
 template <int CK>
@@ -72,7 +72,9 @@ __device__ __forceinline__ void kfrag_load(const uint8_t *ku, int lane, KFrag<CK
 #pragma unroll
   for (int c = 0; c < KFrag<CK>::NW; ++c)
     f.w[c] = __ldcs(reinterpret_cast<const uint4 *>(ku + c * 512 + lane * 16));
-  if (CK != KVQ_F16)
+  if (CK == KVQ_TURBO4)
+    f.sc.x = __ldcs(reinterpret_cast<const unsigned int *>(ku + 1024 + (lane >> 2) * 4));
+  else if (CK != KVQ_F16)
     f.sc = __ldcs(reinterpret_cast<const uint4 *>(ku + unit_scale_offset(CK) + (lane >> 2) * 16));
 }
 
@@ -92,6 +94,28 @@ __device__ __forceinline__ void kfrag_scores(const KFrag<CK> &f, const uint32_t 
       mma16816(s, a0, qb[2 * b][0], qb[2 * b][1]);
       mma16816(s, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
     }
+    return;
+  }
+  if (CK == KVQ_TURBO4) {  // one scale per row: one accumulator for the four groups
+    float sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint4 w = f.w[b >> 1];
+      const uint32_t W0 = (b & 1) ? w.z : w.x, W1 = (b & 1) ? w.w : w.y;
+      const uint32_t X0 = W0 >> 8, X1 = W1 >> 8;
+      const uint32_t a0[4] = {u4_pair_minus8(W0), u4_pair_minus8(W1), u4_pair_minus8(X0),
+                              u4_pair_minus8(X1)};
+      const uint32_t a1[4] = {u4_pair_minus8_hi(W0), u4_pair_minus8_hi(W1),
+                              u4_pair_minus8_hi(X0), u4_pair_minus8_hi(X1)};
+      mma16816(sb, a0, qb[2 * b][0], qb[2 * b][1]);
+      mma16816(sb, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
+    }
+    const float dlo = __half2float(__ushort_as_half(static_cast<unsigned short>(f.sc.x)));
+    const float dhi = __half2float(__ushort_as_half(static_cast<unsigned short>(f.sc.x >> 16)));
+    s[0] = dlo * sb[0];
+    s[1] = dlo * sb[1];
+    s[2] = dhi * sb[2];
+    s[3] = dhi * sb[3];
     return;
   }
   const uint32_t dl[2] = {f.sc.x, f.sc.y}, dh[2] = {f.sc.z, f.sc.w};
@@ -134,17 +158,22 @@ __device__ __forceinline__ void probe_q_frags(const __half *qrow0, int nh, int l
   const int g = lane >> 2, tig = lane & 3;
   const bool hvalid = g < nh;
   const __half *qrow = qrow0 + (hvalid ? g : 0) * kD;
+  if (CK == KVQ_TURBO4) {  // turbo4 keys: the rotated query
+    rotated_q_frags(qrow, hvalid, tig, qb,
+                    [](const __half *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); });
+  } else {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
-    uint2 v = make_uint2(0u, 0u);
-    if (hvalid) v = __ldg(reinterpret_cast<const uint2 *>(qrow + base));
-    if (CK == KVQ_F16) {
-      qb[c][0] = v.x;
-      qb[c][1] = v.y;
-    } else {
-      qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
-      qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+    for (int c = 0; c < 8; ++c) {
+      const int base = 32 * (c >> 1) + 16 * (c & 1) + 4 * tig;
+      uint2 v = make_uint2(0u, 0u);
+      if (hvalid) v = __ldg(reinterpret_cast<const uint2 *>(qrow + base));
+      if (CK == KVQ_F16) {
+        qb[c][0] = v.x;
+        qb[c][1] = v.y;
+      } else {
+        qb[c][0] = __byte_perm(v.x, v.y, 0x5410);
+        qb[c][1] = __byte_perm(v.x, v.y, 0x7632);
+      }
     }
   }
 }
@@ -413,6 +442,11 @@ template <> struct UnitRows<KVQ_Q4_0, 0> {
   using S = RowBits<1024, 128, 4, 5, 6, 3>;
   static constexpr bool kScales = true;
 };
+template <> struct UnitRows<KVQ_TURBO4, 0> {
+  using D = RowBits<0, 1024, 6, 7, 8, 2>;
+  using S = RowBits<1024, 32, 2, 3, 4, 1>;
+  static constexpr bool kScales = true;
+};
 template <> struct UnitRows<KVQ_F16, 1> {
   using D = RowBits<0, 4096, 1, 4, 5, 3>;
   using S = D;
@@ -426,6 +460,11 @@ template <> struct UnitRows<KVQ_Q8_0, 1> {
 template <> struct UnitRows<KVQ_Q4_0, 1> {
   using D = RowBits<0, 1024, 1, 4, 5, 0>;
   using S = RowBits<1024, 128, 1, 5, 6, 2>;
+  static constexpr bool kScales = true;
+};
+template <> struct UnitRows<KVQ_TURBO4, 1> {
+  using D = RowBits<0, 1024, 1, 4, 5, 0>;
+  using S = RowBits<1024, 32, 1, 3, 4, 2>;
   static constexpr bool kScales = true;
 };
 
@@ -725,7 +764,8 @@ cudaError_t launch_compact_v(int cv, const CompactParams &p, dim3 grid, cudaStre
   switch (cv) {
     case KVQ_F16: return launch_compact_t<CK, KVQ_F16>(p, grid, stream);
     case KVQ_Q8_0: return launch_compact_t<CK, KVQ_Q8_0>(p, grid, stream);
-    default: return launch_compact_t<CK, KVQ_Q4_0>(p, grid, stream);
+    case KVQ_Q4_0: return launch_compact_t<CK, KVQ_Q4_0>(p, grid, stream);
+    default: return launch_compact_t<CK, KVQ_TURBO4>(p, grid, stream);
   }
 }
 
@@ -754,7 +794,8 @@ cudaError_t launch_probe(const kvq_layer &L, const void *q, float scale, const f
   switch (L.codec_k) {
     case KVQ_F16: return launch_pdl(probe_kernel<KVQ_F16>, grid, dim3(kProbeWarps * 32), 0, stream, p);
     case KVQ_Q8_0: return launch_pdl(probe_kernel<KVQ_Q8_0>, grid, dim3(kProbeWarps * 32), 0, stream, p);
-    default: return launch_pdl(probe_kernel<KVQ_Q4_0>, grid, dim3(kProbeWarps * 32), 0, stream, p);
+    case KVQ_Q4_0: return launch_pdl(probe_kernel<KVQ_Q4_0>, grid, dim3(kProbeWarps * 32), 0, stream, p);
+    default: return launch_pdl(probe_kernel<KVQ_TURBO4>, grid, dim3(kProbeWarps * 32), 0, stream, p);
   }
 }
 
@@ -798,7 +839,8 @@ cudaError_t launch_compact(const kvq_layer &L, const int32_t *evict, const int32
   switch (L.codec_k) {
     case KVQ_F16: return launch_compact_v<KVQ_F16>(L.codec_v, p, grid, stream);
     case KVQ_Q8_0: return launch_compact_v<KVQ_Q8_0>(L.codec_v, p, grid, stream);
-    default: return launch_compact_v<KVQ_Q4_0>(L.codec_v, p, grid, stream);
+    case KVQ_Q4_0: return launch_compact_v<KVQ_Q4_0>(L.codec_v, p, grid, stream);
+    default: return launch_compact_v<KVQ_TURBO4>(L.codec_v, p, grid, stream);
   }
 }
 

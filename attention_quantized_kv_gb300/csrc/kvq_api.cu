@@ -12,7 +12,9 @@ namespace {
 
 constexpr int kHeadDim = 128;
 
-bool valid_codec(int c) { return c == KVQ_F16 || c == KVQ_Q8_0 || c == KVQ_Q4_0; }
+bool valid_codec(int c) {
+  return c == KVQ_F16 || c == KVQ_Q8_0 || c == KVQ_Q4_0 || c == KVQ_TURBO4;
+}
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -71,7 +73,7 @@ const char *kvq_status_str(int status) {
 
 int64_t kvq_row_bytes(int codec, int32_t head_dim) {
   if (head_dim != kHeadDim || !valid_codec(codec)) return -1;
-  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : 72;
+  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : codec == KVQ_Q4_0 ? 72 : 66;
 }
 
 int64_t kvq_pool_bytes(int codec, int32_t n_pages, int32_t n_kv_heads, int32_t head_dim) {

@@ -20,12 +20,159 @@ constexpr int kD = 128;          // head_dim
 constexpr int kUnitTokens = 16;  // tokens per layout unit
 
 __host__ __device__ constexpr int row_bytes(int codec) {
-  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : 72;
+  return codec == KVQ_F16 ? 256 : codec == KVQ_Q8_0 ? 136 : codec == KVQ_Q4_0 ? 72 : 66;
 }
 __host__ __device__ constexpr int unit_bytes(int codec) { return kUnitTokens * row_bytes(codec); }
-// Byte offset of the scale area inside a unit (q8_0 / q4_0 only).
+// Byte offset of the scale area inside a unit (q8_0 / q4_0 / turbo4 only).
 __host__ __device__ constexpr int unit_scale_offset(int codec) {
   return codec == KVQ_Q8_0 ? 2048 : 1024;
+}
+// Codecs whose quants are nibbles in the q4_0 places of the unit.
+__host__ __device__ constexpr bool nibble_codec(int codec) {
+  return codec == KVQ_Q4_0 || codec == KVQ_TURBO4;
+}
+
+// ---------------------------------------------------------------- turbo4 rotation
+
+// SplitMix64 (Steele, Lea and Flood, OOPSLA 2014): output n (0-based) of the
+// generator seeded with `seed`; the state advances by 0x9E3779B97F4A7C15 per
+// output and is mixed by two xor-shift-multiply steps and an xor-shift.
+__host__ __device__ constexpr uint64_t splitmix64_at(uint64_t seed, int n) {
+  const uint64_t z0 = seed + 0x9E3779B97F4A7C15ull * static_cast<uint64_t>(n + 1);
+  const uint64_t z1 = (z0 ^ (z0 >> 30)) * 0xBF58476D1CE4E5B9ull;
+  const uint64_t z2 = (z1 ^ (z1 >> 27)) * 0x94D049BB133111EBull;
+  return z2 ^ (z2 >> 31);
+}
+// turbo4 sign flips as a 128-bit mask: bit j set <=> s_j = -1 (bit 63 of
+// output j from seed 0x4B5651).  Word w holds dims 32w .. 32w + 31.
+__host__ __device__ constexpr uint32_t turbo_sign_word(int w) {
+  uint32_t m = 0;
+  for (int j = 0; j < 32; ++j)
+    m |= static_cast<uint32_t>(splitmix64_at(0x4B5651ull, 32 * w + j) >> 63) << j;
+  return m;
+}
+__device__ __forceinline__ uint32_t turbo_signs(int w) {
+  constexpr uint32_t w0 = turbo_sign_word(0), w1 = turbo_sign_word(1), w2 = turbo_sign_word(2),
+                     w3 = turbo_sign_word(3);
+  return w == 0 ? w0 : w == 1 ? w1 : w == 2 ? w2 : w3;
+}
+
+// Unnormalised Sylvester-order FWHT of a 128-vector held four per lane (lane
+// l: elements 4l .. 4l + 3): stages h = 1, 2 inside the lane, then h = 4 ..
+// 64 against lane l ^ (h / 4); every output is the single fp32 addition or
+// subtraction (lower - upper) of the pair, as in the definition.
+__device__ __forceinline__ void fwht128_warp(float (&v)[4], int lane) {
+  const float a0 = __fadd_rn(v[0], v[1]), a1 = __fsub_rn(v[0], v[1]);
+  const float a2 = __fadd_rn(v[2], v[3]), a3 = __fsub_rn(v[2], v[3]);
+  v[0] = __fadd_rn(a0, a2);
+  v[2] = __fsub_rn(a0, a2);
+  v[1] = __fadd_rn(a1, a3);
+  v[3] = __fsub_rn(a1, a3);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[i], m);
+      v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+    }
+  }
+}
+
+// Sign flips of the four elements 4l .. 4l + 3 held by lane l.
+__device__ __forceinline__ void turbo_flip_lane(float (&v)[4], int lane) {
+  const uint32_t bits = turbo_signs(lane >> 3) >> (4 * (lane & 7));
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if ((bits >> i) & 1u) v[i] = -v[i];
+}
+
+// x^ = s * H y^ / 16 for a row held four per lane (exact in fp32 for
+// decoded turbo4 values).
+__device__ __forceinline__ void turbo_unrotate_lane(float (&v)[4], int lane) {
+  fwht128_warp(v, lane);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] *= 0.0625f;
+  turbo_flip_lane(v, lane);
+}
+
+// y^ = d16 * (n - 8) of token row r of a turbo4 unit (exact in fp32), lane l
+// holding rotated elements 4l .. 4l + 3: lanes 8b + lb with lb < 4 read the
+// low nibbles of canonical bytes 4 lb .. 4 lb + 3 of group b, lanes lb >= 4
+// the high nibbles of bytes 4 (lb - 4) .. (elements + 16).
+template <int SIDE>
+__device__ __forceinline__ void turbo4_row_rotated(const uint8_t *unit, int r, int lane,
+                                                   float (&y)[4]) {
+  const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
+  const int b = lane >> 3, lb = lane & 7, l4 = lb & 3, hi = lb >> 2;
+  uint32_t bytes[4];
+  if (SIDE == 0) {
+    const uint32_t word = *reinterpret_cast<const uint32_t *>(
+        unit + (b >> 1) * 512 + (4 * g + l4) * 16 + ((b & 1) * 2 + rh) * 4);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bytes[i] = (word >> (8 * i)) & 0xffu;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int jc = 4 * l4 + i, mt = 2 * b + (jc >> 3), gq = jc & 7;
+      bytes[i] = unit[(mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh];
+    }
+  }
+  const float d = __half2float(*reinterpret_cast<const __half *>(
+      unit + 1024 + (SIDE == 0 ? g * 4 + rh * 2 : tig * 8 + rh * 4 + par * 2)));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = hi ? static_cast<int>(bytes[i] >> 4) : static_cast<int>(bytes[i] & 0xfu);
+    y[i] = d * static_cast<float>(n - 8);
+  }
+}
+
+// The rotated query H (s * q) / 16 of the head held by one quad of lanes in
+// the tensor-core fragment order: lane tig holds dims 16c + 4 tig + i as
+// v[c][i] (c < 8, i < 4).  Stages on bits 0-1 (i) and 4-6 (c) stay in the
+// lane, bits 2-3 (tig) go across the quad; the order of the stages does not
+// matter here (the query side is rounded to fp16 afterwards anyway).
+__device__ __forceinline__ void turbo_rotate_q_quad(float (&v)[8][4], int tig) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t bits = turbo_signs(c >> 1) >> (16 * (c & 1) + 4 * tig);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if ((bits >> i) & 1u) v[c][i] = -v[c][i];
+  }
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const float a0 = v[c][0] + v[c][1], a1 = v[c][0] - v[c][1];
+    const float a2 = v[c][2] + v[c][3], a3 = v[c][2] - v[c][3];
+    v[c][0] = a0 + a2; v[c][2] = a0 - a2; v[c][1] = a1 + a3; v[c][3] = a1 - a3;
+  }
+#pragma unroll
+  for (int m = 1; m < 4; m <<= 1) {
+    const bool upper = (tig & m) != 0;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, v[c][i], m);
+        v[c][i] = upper ? o - v[c][i] : v[c][i] + o;
+      }
+  }
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+      if ((c & h) == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = v[c][i], b = v[c + h][i];
+          v[c][i] = a + b;
+          v[c + h][i] = a - b;
+        }
+      }
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[c][i] *= 0.0625f;
 }
 
 // ---------------------------------------------------------------- tensor-core MMA
@@ -195,6 +342,30 @@ __device__ __forceinline__ int page_of(const int32_t *table, int pages_per_seq, 
 
 __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
   if (err) atomicOr(err, bit);
+}
+
+// turbo4 keys: the B fragments of the rotated query H (s * q) / 16 (fp32,
+// rounded to fp16 once), in the nibble codecs' k order; `ld` reads the 4
+// halves at a row offset (global or shared memory).
+template <typename Ld>
+__device__ __forceinline__ void rotated_q_frags(const __half *qrow, bool hvalid, int tig,
+                                                uint32_t (&qb)[8][2], Ld ld) {
+  float v[8][4];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint2 r = make_uint2(0u, 0u);
+    if (hvalid) r = ld(qrow + 16 * c + 4 * tig);
+    const __half2 h01 = *reinterpret_cast<const __half2 *>(&r.x);
+    const __half2 h23 = *reinterpret_cast<const __half2 *>(&r.y);
+    v[c][0] = __low2float(h01); v[c][1] = __high2float(h01);
+    v[c][2] = __low2float(h23); v[c][3] = __high2float(h23);
+  }
+  turbo_rotate_q_quad(v, tig);
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    qb[c][0] = pack_half2(v[c][0], v[c][2]);
+    qb[c][1] = pack_half2(v[c][1], v[c][3]);
+  }
 }
 
 // Programmatic dependent launch: wait for the previous grid on the stream to

@@ -276,25 +276,41 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
     reinterpret_cast<uint4 *>(units_sh)[i] = reinterpret_cast<const uint4 *>(src)[i];
   __syncthreads();
   uint8_t *dst = p.tiles[SIDE] + (static_cast<int64_t>(kvh) * p.n_tiles + tile) * kTileBytes;
+  if (CODEC == KVQ_TURBO4) {
+    // a warp per key row: y^ from the nibbles, then x^ = s * H y^ / 16 across
+    // the warp (exact), rounded to fp16 once like every other codec
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll 1
-  for (int item = threadIdx.x; item < kBN * 4; item += 256) {
-    const int row = item >> 2, b = item & 3;
-    const int key = tile * kBN + row;
-    float x[32];
-    if (key < p.kv_len) {
-      load_block<CODEC, SIDE>(units_sh + (row / kUnitTokens) * UB, row % kUnitTokens, b, x);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 32; ++e) x[e] = 0.0f;
+    for (int row = warp; row < kBN; row += 8) {
+      float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      if (tile * kBN + row < p.kv_len) {  // warp-uniform
+        turbo4_row_rotated<SIDE>(units_sh + (row / kUnitTokens) * UB, row % kUnitTokens, lane, x);
+        turbo_unrotate_lane(x, lane);
+      }
+      *reinterpret_cast<uint2 *>(dst + tile_offset(row, 4 * lane)) =
+          make_uint2(pack_half2(x[0], x[1]), pack_half2(x[2], x[3]));
     }
+  } else {
+#pragma unroll 1
+    for (int item = threadIdx.x; item < kBN * 4; item += 256) {
+      const int row = item >> 2, b = item & 3;
+      const int key = tile * kBN + row;
+      float x[32];
+      if (key < p.kv_len) {
+        load_block<CODEC, SIDE>(units_sh + (row / kUnitTokens) * UB, row % kUnitTokens, b, x);
+      } else {
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      uint4 w;
-      w.x = pack_half2(x[8 * c + 0], x[8 * c + 1]);
-      w.y = pack_half2(x[8 * c + 2], x[8 * c + 3]);
-      w.z = pack_half2(x[8 * c + 4], x[8 * c + 5]);
-      w.w = pack_half2(x[8 * c + 6], x[8 * c + 7]);
-      *reinterpret_cast<uint4 *>(dst + tile_offset(row, 32 * b + 8 * c)) = w;
+        for (int e = 0; e < 32; ++e) x[e] = 0.0f;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 w;
+        w.x = pack_half2(x[8 * c + 0], x[8 * c + 1]);
+        w.y = pack_half2(x[8 * c + 2], x[8 * c + 3]);
+        w.z = pack_half2(x[8 * c + 4], x[8 * c + 5]);
+        w.w = pack_half2(x[8 * c + 6], x[8 * c + 7]);
+        *reinterpret_cast<uint4 *>(dst + tile_offset(row, 32 * b + 8 * c)) = w;
+      }
     }
   }
 }
@@ -310,11 +326,13 @@ __global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams 
   if (side == 0) {
     if (codec == KVQ_F16) dequant_tile<KVQ_F16, 0>(p, units_sh);
     else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 0>(p, units_sh);
-    else dequant_tile<KVQ_Q4_0, 0>(p, units_sh);
+    else if (codec == KVQ_Q4_0) dequant_tile<KVQ_Q4_0, 0>(p, units_sh);
+    else dequant_tile<KVQ_TURBO4, 0>(p, units_sh);
   } else {
     if (codec == KVQ_F16) dequant_tile<KVQ_F16, 1>(p, units_sh);
     else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 1>(p, units_sh);
-    else dequant_tile<KVQ_Q4_0, 1>(p, units_sh);
+    else if (codec == KVQ_Q4_0) dequant_tile<KVQ_Q4_0, 1>(p, units_sh);
+    else dequant_tile<KVQ_TURBO4, 1>(p, units_sh);
   }
   grid_launch_dependents();
 }

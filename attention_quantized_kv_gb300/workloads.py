@@ -31,6 +31,9 @@ Workloads (head_dim 128 throughout):
                          the 2048 lowest middle cells per sequence (4 sink and
                          1024 recent cells protected) and compaction of K, V,
                          scores and lengths into second buffers.
+  append_decode_turbo4_ctx32k
+                         append_decode_q4_ctx32k with K and V turbo4 (the
+                         rotated 4-bit rows, 4.125 bits per value).
   prefill_q8_32k_plus_2k 1 sequence with 32768 cached keys plus a 2048-token
                          ubatch quantize-appended, then causal attention of the
                          2048 queries over 34816 keys; 32 query / 8 KV heads,
@@ -43,7 +46,7 @@ from dataclasses import dataclass, field
 import numpy as np
 import torch
 
-F16, Q8_0, Q4_0 = 0, 1, 2
+F16, Q8_0, Q4_0, TURBO4 = 0, 1, 2, 3
 HEAD_DIM = 128
 
 
@@ -91,6 +94,11 @@ def get(name: str) -> Workload:
                         outlier_frac=0.01, outlier_scale=8.0,
                         description="1 seq, 32q/8kv heads, ctx 32768, K/V q4_0, 1% outlier "
                                     "channels x8; append 1 token then decode")
+    if name == "append_decode_turbo4_ctx32k":
+        return Workload(name, "decode", 1, 32, 8, [32768], [(TURBO4, TURBO4)], 1, append_new=1,
+                        outlier_frac=0.01, outlier_scale=8.0,
+                        description="append_decode_q4_ctx32k with K/V turbo4 (Hadamard-rotated "
+                                    "4-bit rows, 4.125 bpv) instead of q4_0")
     if name == "decode_ragged16_kf16_vq8":
         lens = [int(x) for x in np.random.default_rng(2).integers(1024, 65537, 16)]
         return Workload(name, "decode", 16, 40, 8, lens, [(F16, Q8_0)], 2,
@@ -136,7 +144,8 @@ def get(name: str) -> Workload:
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
        "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
-       "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8", "evict_ragged4_kf16_vq8"]
+       "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8", "evict_ragged4_kf16_vq8",
+       "append_decode_turbo4_ctx32k"]
 
 
 def n_evicted(w: Workload) -> list:

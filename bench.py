@@ -41,7 +41,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV attention: effective HBM GB/s, % of peak, µs per layer-step"
 DEFAULT_WORKLOAD = "append_decode_q4_ctx32k"
-ROW = {0: 256, 1: 136, 2: 72}
+ROW = {0: 256, 1: 136, 2: 72, 3: 66}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -541,7 +541,7 @@ def run_ours(args, w, rank, world, dist):
                    {"sum": sum(w.final_lens()), "min": min(w.final_lens()),
                     "max": max(w.final_lens())},
                    "layers": n_layers,
-                   "codecs": [[["f16", "q8_0", "q4_0"][c] for c in p] for p in w.codecs],
+                   "codecs": [[["f16", "q8_0", "q4_0", "turbo4"][c] for c in p] for p in w.codecs],
                    "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read)",
                    "timing": mode,
                    "parallelism": f"replicas x{world}"},

@@ -45,13 +45,28 @@
  *          u = t + 8.5 (fp32 RN); q = min(15, trunc(u));
  *          canonical byte j = q[j] | q[j+16] << 4; d16 = fp16_RN(d).
  *          x^ = d16 * (q - 8).
+ *   turbo4: a Walsh-Hadamard-rotated 4-bit row (the turbo4 row of the
+ *          "Codecs" table of the buun-llama-cpp listing, 4.125 bits per value;
+ *          the FWHT with random sign flips of its TCQ "How it works" list;
+ *          the scale and levels are this library's reading).   66 bytes / row
+ *          signs s_j = -1 where bit 63 of output j (j = 0..127) of SplitMix64
+ *          (Steele, Lea, Flood 2014) seeded with 0x4B5651 is set, else +1;
+ *          t = s * x; unnormalised FWHT of t in Sylvester order, stages
+ *          h = 1, 2, ..., 64 turning each pair (j, j + h), j & h == 0, into
+ *          (a + b, a - b) with fp32 RN additions; y = t / 8; then the q4_0
+ *          rule over all 128 values of y (one d16 per row); canonical byte
+ *          16 g + j (group g < 4, j < 16) = q[32g + j] | q[32g + j + 16] << 4.
+ *          Decoded: y^ = d16 * (q - 8) and x^ = s * H y^ / 16, exact in fp32.
+ *          Attention never forms x^: q . x^ = (H (s * q) / 16) . y^, so the
+ *          kernels rotate the query once, accumulate V in the rotated space
+ *          and rotate the output back once.
  *   The canonical row is the row's four blocks end to end (d16 little-endian
- *   before each block's quants).
+ *   before each block's quants); for turbo4 the row's d16 then its 64 bytes.
  *
  * Cache layout (one layer, one side):
  *   [n_seqs][n_kv_heads][capacity / 16 units][unit_bytes]
  *   A unit holds 16 consecutive tokens (unit_bytes = 16 * row bytes: 4096,
- *   2176, 1152).  Inside a unit, canonical byte cb of token row r (0..15) is
+ *   2176, 1152, 1056).  Inside a unit, canonical byte cb of token row r (0..15) is
  *   placed as follows (all integer arithmetic; g = r & 7, rh = r >> 3,
  *   tig = (r & 7) >> 1, par = r & 1):
  *   K side
@@ -63,6 +78,8 @@
  *     q4_0 canonical byte jc (0..15) of block b: w=jc>>2, i=jc&3
  *          -> (b>>1)*512 + (4g+w)*16 + ((b&1)*2+rh)*4 + i
  *          scale byte k of block b -> 1024 + g*16 + rh*8 + b*2 + k
+ *     turbo4 canonical byte jc of group b: as q4_0's byte jc of block b;
+ *          scale byte k -> 1024 + g*4 + rh*2 + k
  *   V side
  *     f16  value d, byte k:  mt=d>>4, gq=(d&15)>>1, s=d&1
  *          -> mt*512 + (4gq+tig)*16 + (rh*4+s*2+par)*2 + k
@@ -72,8 +89,10 @@
  *     q4_0 canonical byte jc of block b: mt=2b+(jc>>3), gq=jc&7
  *          -> (mt>>2)*512 + (4gq+tig)*16 + (mt&3)*4 + par*2 + rh
  *          scale byte k of block b -> 1024 + tig*32 + b*8 + rh*4 + par*2 + k
- *   The layout stores exactly the canonical bytes (8.5 / 4.5 / 16 bits per
- *   value); it only orders them so that each thread of the decode kernel
+ *     turbo4 canonical byte jc of group b: as q4_0's byte jc of block b;
+ *          scale byte k -> 1024 + tig*8 + rh*4 + par*2 + k
+ *   The layout stores exactly the canonical bytes (8.5 / 4.5 / 16 / 4.125
+ *   bits per value); it only orders them so that each thread of the decode kernel
  *   reads its tensor-core operand fragments with aligned 16-byte loads.
  *
  * Paged layout (kvq_layer.pages_per_seq > 0; block-level KV management as in
@@ -109,7 +128,7 @@ extern "C" {
 #endif
 
 /* Codec of one (layer, side) cache tensor. */
-typedef enum { KVQ_F16 = 0, KVQ_Q8_0 = 1, KVQ_Q4_0 = 2 } kvq_codec;
+typedef enum { KVQ_F16 = 0, KVQ_Q8_0 = 1, KVQ_Q4_0 = 2, KVQ_TURBO4 = 3 } kvq_codec;
 
 /* Host-side status returned by every entry point. */
 typedef enum {

@@ -10,7 +10,7 @@ from attention_quantized_kv_gb300 import workloads as wl
 
 import oracle
 
-ROW = {0: 256, 1: 136, 2: 72}
+ROW = {0: 256, 1: 136, 2: 72, 3: 66}
 
 
 def gpu_layer(w, layer_idx, device="cuda", chunk=4096, lens=None):

@@ -18,7 +18,7 @@ def _built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
 
 
-CODECS = [(0, 0), (1, 1), (2, 2), (0, 1), (1, 2), (2, 0)]
+CODECS = [(0, 0), (1, 1), (2, 2), (0, 1), (1, 2), (2, 0), (3, 3), (3, 0), (1, 3)]
 
 
 @pytest.mark.parametrize("ck,cv", CODECS)

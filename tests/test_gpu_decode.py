@@ -58,7 +58,7 @@ def check_against_oracle(w, layer_idx, L, q, out, lse, scale, groups=None, lens=
     return worst
 
 
-PAIRS = [(a, b) for a in (0, 1, 2) for b in (0, 1, 2)]
+PAIRS = [(a, b) for a in (0, 1, 2, 3) for b in (0, 1, 2, 3)]
 
 
 @pytest.mark.parametrize("ck,cv", PAIRS)

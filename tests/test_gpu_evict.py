@@ -105,7 +105,7 @@ def _check_scores(got, old, mass, decay, lens):
         assert np.array_equal(got[s, ln:], old[s, ln:]), "entries past the length changed"
 
 
-@pytest.mark.parametrize("ck", [0, 1, 2])
+@pytest.mark.parametrize("ck", [0, 1, 2, 3])
 @pytest.mark.parametrize("n_kv,n_q", [(2, 10), (1, 12), (3, 3)])
 def test_probe_scores_match_oracle(ck, n_kv, n_q):
     """Ragged lengths (one token, inside a unit, several pages), groups of 5,
@@ -127,7 +127,7 @@ def test_probe_scores_match_oracle(ck, n_kv, n_q):
     _check_scores(scores.cpu().numpy(), old, mass, 0.75, lens)
 
 
-@pytest.mark.parametrize("ck", [0, 2])
+@pytest.mark.parametrize("ck", [0, 2, 3])
 def test_probe_paged_identical_to_contiguous(ck):
     n_seqs, n_kv, n_q, pps, n_pages = 3, 2, 8, 4, 16
     cap = pps * 256
@@ -247,7 +247,7 @@ def _evict_lists(rng, lens, kind):
     return out
 
 
-@pytest.mark.parametrize("ck,cv", [(0, 1), (1, 2), (2, 0), (2, 2), (1, 1), (0, 0)])
+@pytest.mark.parametrize("ck,cv", [(0, 1), (1, 2), (2, 0), (2, 2), (1, 1), (0, 0), (3, 3), (3, 1)])
 @pytest.mark.parametrize("kind", ["random", "span", "sparse_keep", "none", "all"])
 def test_compact_bit_exact(ck, cv, kind):
     n_seqs, n_kv, n_q, cap = 4, 2, 4, 2048

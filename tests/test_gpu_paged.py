@@ -71,7 +71,7 @@ def _append_in_pieces(L, krows, vrows, lens, pieces):
         done = [done[s] + n[s] for s in range(n_seqs)]
 
 
-@pytest.mark.parametrize("ck,cv", [(0, 1), (1, 1), (2, 2), (2, 0), (1, 2)])
+@pytest.mark.parametrize("ck,cv", [(0, 1), (1, 1), (2, 2), (2, 0), (1, 2), (3, 3), (3, 0)])
 def test_paged_append_decode_bit_exact_pools_and_identical_outputs(ck, cv):
     n_seqs, n_kv, n_q, pps, n_pages = 4, 2, 8, 6, 40
     cap = pps * 256

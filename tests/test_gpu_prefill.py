@@ -63,6 +63,9 @@ def check_prefill(w, L, seq, q_start, q, out, lse, scale, rows=None, kv_heads=No
     (2, 2, 8, 1000, 200),
     (0, 0, 4, 37, 1),        # a single query row
     (1, 0, 5, 500, 129),     # GQA 5
+    (3, 3, 4, 300, 200),     # turbo4 on both sides (un-rotated in the pre-pass)
+    (3, 1, 2, 0, 64),
+    (2, 3, 4, 64, 100),
 ])
 def test_prefill_small(ck, cv, G, q_start, n_tok):
     n_kv = 2

@@ -29,7 +29,7 @@ def _rows(rng, n_seqs, n_tok, n_kv, scales):
 
 
 @pytest.mark.parametrize("side", [0, 1])
-@pytest.mark.parametrize("src,dst", [(a, b) for a in (0, 1, 2) for b in (0, 1, 2)])
+@pytest.mark.parametrize("src,dst", [(a, b) for a in (0, 1, 2, 3) for b in (0, 1, 2, 3)])
 def test_requantize_bit_exact(src, dst, side):
     n_seqs, n_kv, cap = 3, 2, 512
     lens = [0, 37, 300]  # empty, ragged inside a unit, several units
