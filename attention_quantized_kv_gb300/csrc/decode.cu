@@ -522,8 +522,24 @@ struct MergeArgs {
   int n_q, G;
 };
 
+// One head's merged row: o = acc / L (rotated back for turbo4 V), fp16, and
+// its natural-log lse (M is in log2 units).
 template <bool ROT>
-__device__ __forceinline__ void merge_stream(const MergeArgs p, float4 *xacc, float *xl,
+__device__ __forceinline__ void merge_write(const MergeArgs &p, int seq, int kvh, int hg, int h,
+                                            int lane, float4 acc, float M, float L) {
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
+  float ov[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
+  if (ROT) turbo_unrotate_lane(ov, lane);  // turbo4 V: back from the rotated space
+  __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
+  dst[0] = __floats2half2_rn(ov[0], ov[1]);
+  dst[1] = __floats2half2_rn(ov[2], ov[3]);
+  if (p.lse && lane == 0)
+    p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+template <bool ROT>
+__device__ __noinline__ void merge_stream(const MergeArgs p, float4 *xacc, float *xl,
                                              int stream, int seq, int kvh, int hg, int c_first,
                                              int c_last, int64_t S, int n_s, int64_t U, int P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -625,16 +641,109 @@ __device__ __forceinline__ void merge_stream(const MergeArgs p, float4 *xacc, fl
       acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
       L += xl[h + r * heads_here];
     }
-    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-    const int64_t row = static_cast<int64_t>(seq) * p.n_q + kvh * p.G + hg * 8 + h;
-    float ov[4] = {acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv};
-    if (ROT) turbo_unrotate_lane(ov, lane);  // turbo4 V: back from the rotated space
-    __half2 *dst = reinterpret_cast<__half2 *>(p.out + row * kD) + lane * 2;
-    dst[0] = __floats2half2_rn(ov[0], ov[1]);
-    dst[1] = __floats2half2_rn(ov[2], ov[3]);
-    if (p.lse && lane == 0)
-      p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+    merge_write<ROT>(p, seq, kvh, hg, h, lane, acc, M, L);
   }
+}
+
+// The merged partials of one stream when they fit the CTA's shared memory
+// and its copy ring is idle: the (max, sum) pairs of all parts and their
+// output rows (heads of the group only) arrive by bulk copies on one
+// mbarrier, issued by the 32 lanes of warp 0 and all in flight together.
+// Warp h < heads then finds head h's max M and writes the weights
+// w_j = 2^(m_j - M) over m_j (lane-parallel); after a CTA barrier the rows
+// are folded by all warps (head h, residue r: parts j = r mod reps, four
+// interleaved accumulators), and warp (h, 0) adds the reps partial sums in
+// order through xacc.  Parts are the partials of CTAs c_first ..
+// c_first + n_live - 1, whose slots are consecutive.  Returns false if the
+// copies did not land within the wait limit (error word set).
+template <bool ROT>
+__device__ __forceinline__ bool merge_stream_smem(const MergeArgs p, uint8_t *buf, uint64_t *bar,
+                                                  float4 *xacc, int stream, int seq,
+                                                  int kvh, int hg, int c_first, int n_live,
+                                                  int32_t *err) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads_here = min(8, p.G - hg * 8);
+  const uint32_t ml_bytes = static_cast<uint32_t>(n_live) * 64u;
+  const uint32_t row_bytes = static_cast<uint32_t>(heads_here) * kD * 4u;
+  const int64_t slot0 = static_cast<int64_t>(c_first) + stream;
+  if (warp == 0) {
+    if (lane == 0) {
+      // partials written through the generic proxy, read by the copy engine
+      asm volatile("fence.proxy.async.global;\n" ::: "memory");
+      fence_proxy_async_smem();
+      mbar_arrive_expect_tx(bar, ml_bytes + row_bytes * static_cast<uint32_t>(n_live));
+      bulk_copy_g2s(buf, p.part_ml + slot0 * 8, ml_bytes, bar);
+    }
+    __syncwarp();
+    for (int j = lane; j < n_live; j += 32)
+      bulk_copy_g2s(buf + ml_bytes + j * row_bytes, p.part_o + (slot0 + j) * 8 * kD, row_bytes,
+                    bar);
+  }
+  const bool ok = mbar_wait_bounded(bar, 0u);
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) set_err(err, KVQ_DEVERR_TIMEOUT);
+    mbar_wait_bounded(bar, 0u);
+    return false;
+  }
+  float2 *ml = reinterpret_cast<float2 *>(buf);
+  float M = -INFINITY, L = 0.0f;
+  if (warp < heads_here) {
+    const int h = warp;
+    for (int j = lane; j < n_live; j += 32) M = fmaxf(M, ml[j * 8 + h].x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int j = lane; j < n_live; j += 32) {
+      const float2 v = ml[j * 8 + h];
+      const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.0f : fast_exp2(v.x - M);
+      L = fmaf(w, v.y, L);
+      ml[j * 8 + h].x = w;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  }
+  __syncthreads();
+  const int reps = kWarps / heads_here;
+  const int h = warp % heads_here, r = warp / heads_here;
+  const bool active = warp < heads_here * reps;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (active) {
+    const float4 *rows = reinterpret_cast<const float4 *>(buf + ml_bytes) + h * (kD / 4) + lane;
+    const int stride = static_cast<int>(row_bytes / 16);
+    float4 a[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) a[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    int j = r;
+    for (; j + 3 * reps < n_live; j += 4 * reps) {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float w = ml[(j + u * reps) * 8 + h].x;
+        const float4 x = rows[(j + u * reps) * stride];
+        a[u].x = fmaf(w, x.x, a[u].x); a[u].y = fmaf(w, x.y, a[u].y);
+        a[u].z = fmaf(w, x.z, a[u].z); a[u].w = fmaf(w, x.w, a[u].w);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 3; ++u) {  // fewer than four parts left
+      if (j + u * reps < n_live) {
+        const float w = ml[(j + u * reps) * 8 + h].x;
+        const float4 x = rows[(j + u * reps) * stride];
+        a[u].x = fmaf(w, x.x, a[u].x); a[u].y = fmaf(w, x.y, a[u].y);
+        a[u].z = fmaf(w, x.z, a[u].z); a[u].w = fmaf(w, x.w, a[u].w);
+      }
+    }
+    acc = make_float4((a[0].x + a[1].x) + (a[2].x + a[3].x), (a[0].y + a[1].y) + (a[2].y + a[3].y),
+                      (a[0].z + a[1].z) + (a[2].z + a[3].z), (a[0].w + a[1].w) + (a[2].w + a[3].w));
+    if (r > 0) xacc[warp * 32 + lane] = acc;
+  }
+  if (reps > 1) __syncthreads();
+  if (active && r == 0) {
+    for (int q = 1; q < reps; ++q) {
+      const float4 y = xacc[(h + q * heads_here) * 32 + lane];
+      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+    }
+    merge_write<ROT>(p, seq, kvh, hg, h, lane, acc, M, L);
+  }
+  return true;
 }
 
 template <int CK, int CV>
@@ -649,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   // segment ahead; the first is requested before the ring's copies)
   __shared__ __align__(128) __half q_s[2][8 * kD];
   __shared__ uint64_t q_bar[2];
+  __shared__ uint64_t mrg_bar;  // the shared-memory merge's bulk copies (used at most once)
   // merge hand-over (read by warp part 0 of a head before the CTA's next
   // barrier, written again only after it)
   __shared__ float4 mrg_acc[kWarps * 32];
@@ -690,6 +800,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     }
     for (int s = lane; s < C::NS; s += 32) mbar_init(&full[s], 1);
     if (lane < 2) mbar_init(&q_bar[lane], 1);
+    if (lane == 2) mbar_init(&mrg_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -934,8 +1045,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     if (last_flag) {
       __threadfence();
       const MergeArgs ma = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
-      merge_stream<CV == KVQ_TURBO4>(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first, c_last,
-                                     S, seg.n_s, U, P);
+      // Shared-memory merge when this is the CTA's last segment and no warp
+      // aborted (no copy in flight into the ring or the query buffers), the
+      // parts are the consecutive slots of c_first .. c_last and they fit the
+      // ring plus the reduction slots.  Every term is the same in all warps
+      // (abort_flag is only raised inside the unit loop, before the barrier).
+      const int n_live = c_last - c_first + 1;
+      const int hh = min(8, p.G - hg * 8);
+      const bool smem_merge = seg_end == u1 && U >= P &&
+                              *reinterpret_cast<volatile int *>(&abort_flag) == 0 &&
+                              static_cast<int64_t>(n_live) * (64 + hh * kD * 4) <=
+                                  C::RING + C::RED;
+      if (smem_merge) {
+        merge_stream_smem<CV == KVQ_TURBO4>(ma, smem, &mrg_bar, mrg_acc, stream, seq, kvh, hg,
+                                            c_first, n_live, p.err);
+      } else {
+        merge_stream<CV == KVQ_TURBO4>(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first,
+                                       c_last, S, seg.n_s, U, P);
+      }
     }
 
     useg = seg_end;
