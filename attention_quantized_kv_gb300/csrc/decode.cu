@@ -68,13 +68,22 @@ struct DecodeParams {
   float scale_log2;
 };
 
+// Units per work item: nibble codecs (q4_0, turbo4) on both sides move two
+// consecutive units (32 tokens) of each side per stage, so that every bulk
+// copy carries over 2 KB (the copy engine's per-copy cost shows below a few
+// KB); wider codecs keep one unit per stage and more stages per warp.
+__host__ __device__ constexpr int items_units(int ck, int cv) {
+  return (nibble_codec(ck) && nibble_codec(cv)) ? 2 : 1;
+}
+
 template <int CK, int CV>
 struct DecodeCfg {
   static constexpr int UK = unit_bytes(CK);
   static constexpr int UV = unit_bytes(CV);
-  static constexpr int STAGE = UK + UV;
+  static constexpr int UPS = items_units(CK, CV);  // units per item (and stage)
+  static constexpr int STAGE = UPS * (UK + UV);    // [UPS K units][UPS V units]
   // Stage s always belongs to warp s % kWarps (NS is a multiple of kWarps):
-  // the warp that consumes unit k also refills its stage with unit k + NS
+  // the warp that consumes item k also refills its stage with item k + NS
   // and is the only waiter on that stage's mbarrier, so phase waits are
   // strictly sequential per barrier.
   static constexpr int NS_RAW = kRingBytes / STAGE / kWarps * kWarps;
@@ -83,8 +92,8 @@ struct DecodeCfg {
   static constexpr int RED = 4 * 32 * kRedFloats * 4;  // tree-merge slots
   static constexpr int SMEM = RING + RED;
   static_assert(NS % kWarps == 0, "stage ownership needs NS % warps == 0");
-  // Two units per warp step when each warp owns at least four stages.
-  static constexpr bool PAIR = NS / kWarps >= 4;
+  // Two one-unit items per warp step when each warp owns at least four stages.
+  static constexpr bool PAIR = UPS == 1 && NS / kWarps >= 4;
 };
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
@@ -266,15 +275,16 @@ __device__ __forceinline__ void unit_pv(const uint8_t *vu, int lane, uint32_t B0
 // sequence (kv head * n_hg + head group), unit within the stream, and the
 // unit's index in the cache (for the bulk copy).
 struct Cursor {
-  int seq, sl, j, n_s;
-  int64_t unit;   // contiguous layers: the unit's index in the cache
-  int pg0, pg1;   // paged layers: pool pages of pages j/16 and j/16 + 1 of the stream
+  int seq, sl, j, n_s;  // j, n_s: items of the stream
+  int64_t unit;   // contiguous layers: the index of the item's first unit in the cache
+  int pg0, pg1;   // paged layers: pool pages of the item's page and the next one
 };
 
 struct Geo {
-  const int32_t *pfx;
+  const int32_t *pfx;    // items per stream, prefix-summed over the sequences
   int n_seqs, n_kv, n_hg, KH;
-  int64_t ups;           // units per (seq, kv head) stream of the cache
+  int64_t upst;          // units per (seq, kv head) stream of the cache
+  int upi, ipp;          // units per item; items per page
   const int32_t *table;  // paged layers: block table; nullptr: contiguous
   int pps, n_pages;
 };
@@ -283,13 +293,14 @@ struct Geo {
 // stream (-1 past the stream or for an entry outside the pool); the next
 // page's entry is requested a whole page ahead of its first use.
 __device__ __forceinline__ void cursor_pages(const Geo &q, Cursor &c) {
-  const int pj = c.j / kPageUnits;
+  const int pj = c.j / q.ipp;
   c.pg0 = page_of(q.table, q.pps, q.n_pages, c.seq, pj);
-  c.pg1 = (pj + 1) * kPageUnits < c.n_s ? page_of(q.table, q.pps, q.n_pages, c.seq, pj + 1) : -1;
+  c.pg1 = (pj + 1) * q.ipp < c.n_s ? page_of(q.table, q.pps, q.n_pages, c.seq, pj + 1) : -1;
 }
 
 __device__ __forceinline__ int64_t cache_unit(const Geo &q, int seq, int sl, int j) {
-  return (static_cast<int64_t>(seq) * q.n_kv + sl / q.n_hg) * q.ups + j;
+  return (static_cast<int64_t>(seq) * q.n_kv + sl / q.n_hg) * q.upst +
+         static_cast<int64_t>(j) * q.upi;
 }
 
 // Largest s with pfx[s] * KH <= u (pfx non-decreasing, pfx[0] = 0).
@@ -323,17 +334,17 @@ __device__ __forceinline__ Cursor cursor_at(const Geo &q, int64_t u) {
   return c;
 }
 
-// Advance a cursor by `step` units (stops being meaningful past the end).
+// Advance a cursor by `step` items (stops being meaningful past the end).
 __device__ __forceinline__ void cursor_advance(Cursor &c, int step, const Geo &q) {
-  const int old_page = c.j / kPageUnits;
+  const int old_page = c.j / q.ipp;
   c.j += step;
   if (c.j < c.n_s) {
-    c.unit += step;
+    c.unit += static_cast<int64_t>(step) * q.upi;
     if (q.table) {
-      const int pj = c.j / kPageUnits;
+      const int pj = c.j / q.ipp;
       if (pj == old_page + 1) {  // the common crossing: shift, request the next entry
         c.pg0 = c.pg1;
-        c.pg1 = (pj + 1) * kPageUnits < c.n_s
+        c.pg1 = (pj + 1) * q.ipp < c.n_s
                     ? page_of(q.table, q.pps, q.n_pages, c.seq, pj + 1) : -1;
       } else if (pj != old_page) {
         cursor_pages(q, c);
@@ -356,12 +367,15 @@ __device__ __forceinline__ void cursor_advance(Cursor &c, int step, const Geo &q
   if (q.table) cursor_pages(q, c);
 }
 
-// Index of the cursor's unit in the cache (contiguous) or the pool (paged;
-// an entry outside the pool reads pool page 0, flagged by the caller).
+// Index of the cursor's item's first unit in the cache (contiguous) or the
+// pool (paged; an entry outside the pool reads pool page 0, flagged by the
+// caller).  An item's units are consecutive there: an item never straddles
+// a page (items per page = 16 / units per item).
 __device__ __forceinline__ int64_t cursor_unit(const Geo &q, const Cursor &c) {
   if (!q.table) return c.unit;
   const int pg = c.pg0 < 0 ? 0 : c.pg0;
-  return (static_cast<int64_t>(pg) * q.n_kv + c.sl / q.n_hg) * kPageUnits + c.j % kPageUnits;
+  return (static_cast<int64_t>(pg) * q.n_kv + c.sl / q.n_hg) * kPageUnits +
+         (c.j % q.ipp) * q.upi;
 }
 
 // Merge partial b into a (per lane; m uniform across the lanes of a head).
@@ -399,12 +413,14 @@ __device__ __forceinline__ void cta_bar() {
 }
 
 // Online softmax + PV for N units at once (N = 1 or 2): one max reduction and
-// at most one rescale per call.
+// at most one rescale per call.  A unit may have no valid token at all (the
+// second unit of a two-unit item past the length): it is fully masked.
 template <int CK, int CV, int N>
 __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
+                                              const uint8_t *const (&vus)[N],
                                               const int (&nvalid)[N], int lane,
                                               const uint32_t (&qb)[8][2], float scale_log2,
-                                              int uk_bytes, float (&o)[8][4], float (&corr)[4],
+                                              float (&o)[8][4], float (&corr)[4],
                                               float &m0, float &m1, float &l0, float &l1) {
   const int g = lane >> 2;
   float sc[N][4];
@@ -448,7 +464,7 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
     l1 += p1 + p3;
     const uint32_t B0 = movmatrix_trans(pack_half2(p0, p1));
     const uint32_t B1 = movmatrix_trans(pack_half2(p2, p3));
-    const uint8_t *vu = ku[u] + uk_bytes;
+    const uint8_t *vu = vus[u];
     if (nvalid[u] == kUnitTokens) unit_pv<CV, true>(vu, lane, B0, B1, nvalid[u], o, corr);
     else unit_pv<CV, false>(vu, lane, B0, B1, nvalid[u], o, corr);
   }
@@ -783,7 +799,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
           if (blockIdx.x == 0) set_err(p.err, KVQ_DEVERR_MAXLEN);
           len = p.max_len;
         }
-        n = len > 0 ? (len + kUnitTokens - 1) / kUnitTokens : 0;
+        n = len > 0 ? (len + C::UPS * kUnitTokens - 1) / (C::UPS * kUnitTokens) : 0;
       }
       int incl = n;
 #pragma unroll
@@ -823,7 +839,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   geo.n_kv = p.n_kv;
   geo.n_hg = p.n_hg;
   geo.KH = p.n_kv * p.n_hg;
-  geo.ups = p.capacity / kUnitTokens;
+  geo.upst = p.capacity / kUnitTokens;
+  geo.upi = C::UPS;
+  geo.ipp = kPageUnits / C::UPS;
   geo.table = p.table;
   geo.pps = p.pages_per_seq;
   geo.n_pages = p.n_pages;
@@ -844,8 +862,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     const int64_t unit = cursor_unit(geo, c);
     if (geo.table && c.pg0 < 0) set_err(p.err, KVQ_DEVERR_PAGE);
     mbar_arrive_expect_tx(&full[s], C::STAGE);
-    bulk_copy_g2s(dst, p.k_cache + unit * C::UK, C::UK, &full[s]);
-    bulk_copy_g2s(dst + C::UK, p.v_cache + unit * C::UV, C::UV, &full[s]);
+    bulk_copy_g2s(dst, p.k_cache + unit * C::UK, C::UPS * C::UK, &full[s]);
+    bulk_copy_g2s(dst + C::UPS * C::UK, p.v_cache + unit * C::UV, C::UPS * C::UV, &full[s]);
   };
 
   // Query rows of the segment at cursor c into q_s[buf] (thread 0).
@@ -947,17 +965,24 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         continue;
       }
       const int j = seg.j + (k - k0);
-      if (two) {
+      if (C::UPS == 2) {  // one item: two consecutive units of each side
+        const uint8_t *st = ring + s0 * C::STAGE;
+        const uint8_t *ku[2] = {st, st + C::UK};
+        const uint8_t *vu[2] = {st + 2 * C::UK, st + 2 * C::UK + C::UV};
+        const int nv[2] = {min(kUnitTokens, len - 2 * j * kUnitTokens),
+                           min(kUnitTokens, len - (2 * j + 1) * kUnitTokens)};
+        process_units<CK, CV, 2>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
+      } else if (two) {
         const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
+        const uint8_t *vu[2] = {ku[0] + C::UK, ku[1] + C::UK};
         const int nv[2] = {min(kUnitTokens, len - j * kUnitTokens),
                            min(kUnitTokens, len - (j + kWarps) * kUnitTokens)};
-        process_units<CK, CV, 2>(ku, nv, lane, qb, p.scale_log2, C::UK, o, corr, m0, m1, l0,
-                                 l1);
+        process_units<CK, CV, 2>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
       } else {
         const uint8_t *ku[1] = {ring + s0 * C::STAGE};
+        const uint8_t *vu[1] = {ku[0] + C::UK};
         const int nv[1] = {min(kUnitTokens, len - j * kUnitTokens)};
-        process_units<CK, CV, 1>(ku, nv, lane, qb, p.scale_log2, C::UK, o, corr, m0, m1, l0,
-                                 l1);
+        process_units<CK, CV, 1>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
       }
       // The consumed stages are free: refill them with units k + NS (+ 8).
       __syncwarp();
@@ -1114,11 +1139,13 @@ DecodePlan plan_decode(const kvq_layer &L, int max_len, int num_sms) {
   const int G = L.n_q_heads / L.n_kv_heads;
   pl.n_hgroups = (G + 7) / 8;
   const int64_t streams = static_cast<int64_t>(L.n_seqs) * L.n_kv_heads * pl.n_hgroups;
-  const int64_t max_units = streams * ((max_len + kUnitTokens - 1) / kUnitTokens);
+  const int upi = items_units(L.codec_k, L.codec_v);
+  const int64_t item_tok = static_cast<int64_t>(kUnitTokens) * upi;
+  const int64_t max_items = streams * ((max_len + item_tok - 1) / item_tok);
   // Two resident CTAs per SM, but at least ~32 units (two pairs per warp) per
   // CTA, so that short contexts do not spread into many tiny partials.
   int64_t grid = static_cast<int64_t>(num_sms > 0 ? num_sms : 148) * 2;
-  const int64_t by_work = (max_units + 31) / 32;
+  const int64_t by_work = (max_items * upi + 31) / 32;
   if (grid > by_work) grid = by_work;
   if (grid < 1) grid = 1;
   pl.grid = static_cast<int>(grid);
