@@ -72,8 +72,10 @@ struct DecodeParams {
 // consecutive units (32 tokens) of each side per stage, so that every bulk
 // copy carries over 2 KB (the copy engine's per-copy cost shows below a few
 // KB); wider codecs keep one unit per stage and more stages per warp.
+// (Four units per item measured no faster than two.)
+constexpr int kNibbleItemUnits = 2;
 __host__ __device__ constexpr int items_units(int ck, int cv) {
-  return (nibble_codec(ck) && nibble_codec(cv)) ? 2 : 1;
+  return (nibble_codec(ck) && nibble_codec(cv)) ? kNibbleItemUnits : 1;
 }
 
 template <int CK, int CV>
@@ -412,7 +414,7 @@ __device__ __forceinline__ void cta_bar() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads) : "memory");
 }
 
-// Online softmax + PV for N units at once (N = 1 or 2): one max reduction and
+// Online softmax + PV for N units at once (N = 1, 2 or 4): one max reduction and
 // at most one rescale per call.  A unit may have no valid token at all (the
 // second unit of a two-unit item past the length): it is fully masked.
 template <int CK, int CV, int N>
@@ -965,13 +967,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         continue;
       }
       const int j = seg.j + (k - k0);
-      if (C::UPS == 2) {  // one item: two consecutive units of each side
+      if (C::UPS > 1) {  // one item: UPS consecutive units of each side
         const uint8_t *st = ring + s0 * C::STAGE;
-        const uint8_t *ku[2] = {st, st + C::UK};
-        const uint8_t *vu[2] = {st + 2 * C::UK, st + 2 * C::UK + C::UV};
-        const int nv[2] = {min(kUnitTokens, len - 2 * j * kUnitTokens),
-                           min(kUnitTokens, len - (2 * j + 1) * kUnitTokens)};
-        process_units<CK, CV, 2>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
+        const uint8_t *ku[C::UPS];
+        const uint8_t *vu[C::UPS];
+        int nv[C::UPS];
+#pragma unroll
+        for (int u = 0; u < C::UPS; ++u) {
+          ku[u] = st + u * C::UK;
+          vu[u] = st + C::UPS * C::UK + u * C::UV;
+          nv[u] = min(kUnitTokens, len - (C::UPS * j + u) * kUnitTokens);
+        }
+        process_units<CK, CV, C::UPS>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0,
+                                      l1);
       } else if (two) {
         const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
         const uint8_t *vu[2] = {ku[0] + C::UK, ku[1] + C::UK};
