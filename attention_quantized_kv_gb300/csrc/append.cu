@@ -318,13 +318,16 @@ __device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, i
 }
 
 // One warp per row (grid covers all rows).
+// Every kernel here lets the next kernel of the stream launch at once (it
+// waits for this grid's completion before it reads anything this grid
+// writes), so that its prologue overlaps this one.
 __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendParams p) {
   grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
   const int64_t rows = 2ll * p.n_seqs * p.max_new * p.n_kv;
   if (row < rows) append_row(p, row, lane);
-  grid_launch_dependents();
 }
 
 // Small appends (a decode step): one CTA whose warps take all rows, then,
@@ -332,6 +335,7 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_kernel(AppendParams 
 __global__ void __launch_bounds__(kAppendWarps * 32) append_small_kernel(AppendParams p,
                                                                         int update_lens) {
   grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t rows = 2ll * p.n_seqs * p.max_new * p.n_kv;
   for (int64_t row = threadIdx.x >> 5; row < rows; row += kAppendWarps) append_row(p, row, lane);
@@ -342,18 +346,17 @@ __global__ void __launch_bounds__(kAppendWarps * 32) append_small_kernel(AppendP
       p.seq_lens[s] = v > p.capacity ? p.capacity : v;
     }
   }
-  grid_launch_dependents();
 }
 
 __global__ void update_lens_kernel(int32_t *seq_lens, const int32_t *n_new, int n_seqs,
                                    int capacity) {
   grid_dependency_wait();
+  grid_launch_dependents();
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s < n_seqs) {
     const int v = seq_lens[s] + n_new[s];
     seq_lens[s] = v > capacity ? capacity : v;
   }
-  grid_launch_dependents();
 }
 
 constexpr int64_t kSmallAppendRows = 64;  // at most 8 rows per warp
