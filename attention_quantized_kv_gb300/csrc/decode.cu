@@ -669,9 +669,8 @@ __device__ __noinline__ void merge_stream(const MergeArgs p, float4 *xacc, float
 // mbarrier, issued by the 32 lanes of warp 0 and all in flight together.
 // Warp h < heads then finds head h's max M and writes the weights
 // w_j = 2^(m_j - M) over m_j (lane-parallel); after a CTA barrier the rows
-// are folded by all warps (head h, residue r: parts j = r mod reps, four
-// interleaved accumulators), and warp (h, 0) adds the reps partial sums in
-// order through xacc.  Parts are the partials of CTAs c_first ..
+// are folded by all warps (head h, residue r: parts j = r mod reps), and
+// warp (h, 0) adds the reps partial sums in order through xacc.  Parts are the partials of CTAs c_first ..
 // c_first + n_live - 1, whose slots are consecutive.  Returns false if the
 // copies did not land within the wait limit (error word set).
 template <bool ROT>
@@ -725,32 +724,17 @@ __device__ __forceinline__ bool merge_stream_smem(const MergeArgs p, uint8_t *bu
   const bool active = warp < heads_here * reps;
   float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   if (active) {
+    // a plain loop: this code runs once per CTA, cold in the instruction
+    // cache, so its size costs more than its dependency chain
     const float4 *rows = reinterpret_cast<const float4 *>(buf + ml_bytes) + h * (kD / 4) + lane;
     const int stride = static_cast<int>(row_bytes / 16);
-    float4 a[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) a[u] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    int j = r;
-    for (; j + 3 * reps < n_live; j += 4 * reps) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const float w = ml[(j + u * reps) * 8 + h].x;
-        const float4 x = rows[(j + u * reps) * stride];
-        a[u].x = fmaf(w, x.x, a[u].x); a[u].y = fmaf(w, x.y, a[u].y);
-        a[u].z = fmaf(w, x.z, a[u].z); a[u].w = fmaf(w, x.w, a[u].w);
-      }
+#pragma unroll 1
+    for (int j = r; j < n_live; j += reps) {
+      const float w = ml[j * 8 + h].x;
+      const float4 x = rows[j * stride];
+      acc.x = fmaf(w, x.x, acc.x); acc.y = fmaf(w, x.y, acc.y);
+      acc.z = fmaf(w, x.z, acc.z); acc.w = fmaf(w, x.w, acc.w);
     }
-#pragma unroll
-    for (int u = 0; u < 3; ++u) {  // fewer than four parts left
-      if (j + u * reps < n_live) {
-        const float w = ml[(j + u * reps) * 8 + h].x;
-        const float4 x = rows[(j + u * reps) * stride];
-        a[u].x = fmaf(w, x.x, a[u].x); a[u].y = fmaf(w, x.y, a[u].y);
-        a[u].z = fmaf(w, x.z, a[u].z); a[u].w = fmaf(w, x.w, a[u].w);
-      }
-    }
-    acc = make_float4((a[0].x + a[1].x) + (a[2].x + a[3].x), (a[0].y + a[1].y) + (a[2].y + a[3].y),
-                      (a[0].z + a[1].z) + (a[2].z + a[3].z), (a[0].w + a[1].w) + (a[2].w + a[3].w));
     if (r > 0) xacc[warp * 32 + lane] = acc;
   }
   if (reps > 1) __syncthreads();
