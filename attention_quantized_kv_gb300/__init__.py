@@ -22,7 +22,7 @@ from ._abi import (KVQ_F16, KVQ_Q8_0, KVQ_Q4_0, KVQ_TURBO4, KVQ_DEVERR_CAPACITY,
                    kvq_layer)
 
 __all__ = ["KVQ_F16", "KVQ_Q8_0", "KVQ_Q4_0", "KVQ_TURBO4", "CODEC_NAMES", "KVQError", "KVLayer",
-           "kv_append_quantize", "attn_decode_workspace", "attn_decode",
+           "kv_append_quantize", "attn_decode_workspace", "attn_decode", "attn_decode_append",
            "attn_prefill_workspace", "attn_prefill_chunk", "kvq_row_bytes", "kvq_cache_bytes",
            "kvq_pool_bytes", "KVQ_DEVERR_PAGE", "kv_requantize", "degrade", "aggregate_bpv",
            "ladder_next", "default_scale", "KVQ_DEVERR_EVICT", "kv_probe_scores",
@@ -163,6 +163,22 @@ def attn_decode(layer: KVLayer, q, scale: float, out, lse, max_len: int, workspa
                                    int(max_len), _ptr(workspace), int(workspace.numel() *
                                                                       workspace.element_size()),
                                    _stream_ptr(stream)), "attn_decode")
+
+
+def attn_decode_append(layer: KVLayer, k_new, v_new, q, scale: float, out, lse, max_len: int,
+                       workspace, stream=None) -> None:
+    """One decode step in one launch: append k_new / v_new (fp16 [n_seqs, n_kv, 128], one
+    token per sequence), attend seq_lens + 1 keys, advance seq_lens.  q, out: fp16
+    [n_seqs, n_q, 128]; lse: fp32 [n_seqs, n_q] or None; workspace as attn_decode."""
+    assert k_new.dtype == torch.float16 and v_new.dtype == torch.float16
+    assert k_new.is_contiguous() and v_new.is_contiguous()
+    assert q.dtype == torch.float16 and out.dtype == torch.float16 and q.is_contiguous()
+    d = layer.desc()
+    _check(_abi.load().attn_decode_append(ctypes.byref(d), _ptr(k_new), _ptr(v_new), _ptr(q),
+                                          float(scale), _ptr(out), _ptr(lse), int(max_len),
+                                          _ptr(workspace),
+                                          int(workspace.numel() * workspace.element_size()),
+                                          _stream_ptr(stream)), "attn_decode_append")
 
 
 def attn_prefill_workspace(layer: KVLayer, q_start: int, n_q_tok: int) -> int:

@@ -20,7 +20,7 @@ KVQ_DEVERR_PAGE, KVQ_DEVERR_EVICT = 16, 32
 # Every function the header declares (checked by the tests against include/kvq.h).
 EXPORTS = ("kvq_status_str", "kvq_row_bytes", "kvq_cache_bytes", "kvq_pool_bytes",
            "kv_append_quantize",
-           "attn_decode_workspace", "attn_decode", "attn_decode_noalloc",
+           "attn_decode_workspace", "attn_decode", "attn_decode_append", "attn_decode_noalloc",
            "attn_prefill_workspace", "attn_prefill_chunk", "kv_requantize", "kvq_aggregate_bpv",
            "kvq_ladder_next", "kv_probe_scores", "kv_evict_select", "kv_compact")
 
@@ -70,6 +70,8 @@ def load(path: str | None = None):
         "kv_append_quantize": (ctypes.c_int, [L, P, P, P, i32, i32, P]),
         "attn_decode_workspace": (ctypes.c_int, [L, i32, sz]),
         "attn_decode": (ctypes.c_int, [L, P, f32, P, P, i32, P, ctypes.c_size_t, P]),
+        "attn_decode_append": (ctypes.c_int, [L, P, P, P, f32, P, P, i32, P, ctypes.c_size_t,
+                                              P]),
         "attn_decode_noalloc": (ctypes.c_int, [L, P, f32, P, P, i32, P]),
         "attn_prefill_workspace": (ctypes.c_int, [L, i32, i32, sz]),
         "attn_prefill_chunk": (ctypes.c_int, [L, i32, i32, i32, P, f32, P, P, P,

@@ -12,165 +12,11 @@
 #include <cuda_runtime.h>
 
 #include "kvq_device.cuh"
+#include "kvq_encode.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
 namespace {
-
-// q8_0: amax over the 8 lanes of the block, d = amax/127, q = round(x/d).
-__device__ __forceinline__ void encode_q8(const float (&x)[4], int (&q)[4], __half &d16) {
-  float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float d = __fdiv_rn(a, 127.0f);
-  d16 = __float2half_rn(d);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = d != 0.0f ? static_cast<int>(roundf(__fdiv_rn(x[i], d))) : 0;
-}
-
-// q4_0: signed value of largest magnitude (lowest dim wins ties), d = m/-8,
-// q = min(15, trunc(x/d + 8.5)).
-__device__ __forceinline__ void encode_q4(const float (&x)[4], int lane, int (&q)[4], __half &d16) {
-  float best = fabsf(x[0]);
-  float m = x[0];
-  int idx = 4 * lane;
-#pragma unroll
-  for (int i = 1; i < 4; ++i) {
-    const float a = fabsf(x[i]);
-    if (a > best) { best = a; m = x[i]; idx = 4 * lane + i; }
-  }
-#pragma unroll
-  for (int o = 1; o < 8; o <<= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ob > best || (ob == best && oi < idx)) { best = ob; m = om; idx = oi; }
-  }
-  const float d = __fdiv_rn(m, -8.0f);
-  d16 = __float2half_rn(d);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float t = d != 0.0f ? __fdiv_rn(x[i], d) : 0.0f;
-    const int v = static_cast<int>(__fadd_rn(t, 8.5f));  // truncation; u >= 0.5
-    q[i] = v > 15 ? 15 : v;
-  }
-}
-
-// turbo4: signs, FWHT and the factor 1/8 (the rotation of the row, exact
-// order of the definition), then the q4_0 rule over all 128 rotated values
-// (32 lanes, lowest dim wins ties).
-__device__ __forceinline__ void encode_turbo4(const float (&x)[4], int lane, int (&q)[4],
-                                              __half &d16) {
-  float y[4] = {x[0], x[1], x[2], x[3]};
-  turbo_flip_lane(y, lane);
-  fwht128_warp(y, lane);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) y[i] *= 0.125f;
-  float best = fabsf(y[0]);
-  float m = y[0];
-  int idx = 4 * lane;
-#pragma unroll
-  for (int i = 1; i < 4; ++i) {
-    const float a = fabsf(y[i]);
-    if (a > best) { best = a; m = y[i]; idx = 4 * lane + i; }
-  }
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-    const float om = __shfl_xor_sync(0xffffffffu, m, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
-    if (ob > best || (ob == best && oi < idx)) { best = ob; m = om; idx = oi; }
-  }
-  const float d = __fdiv_rn(m, -8.0f);
-  d16 = __float2half_rn(d);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float t = d != 0.0f ? __fdiv_rn(y[i], d) : 0.0f;
-    const int v = static_cast<int>(__fadd_rn(t, 8.5f));  // truncation; u >= 0.5
-    q[i] = v > 15 ? 15 : v;
-  }
-}
-
-__device__ __forceinline__ void st_u16(uint8_t *p, uint32_t v) {
-  *reinterpret_cast<uint16_t *>(p) = static_cast<uint16_t>(v);
-}
-
-// Write one row (token row r of `unit`) from lane-held data.
-template <int SIDE>
-__device__ __forceinline__ void store_row(int codec, uint8_t *unit, int r, int lane,
-                                          const uint2 raw, const int (&q)[4], __half d16) {
-  const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
-  const int b = lane >> 3, lb = lane & 7;  // block and lane-in-block
-  if (codec == KVQ_F16) {
-    if (SIDE == 0) {
-      const int h = (lane >> 2) & 1, w = lane & 3;
-      *reinterpret_cast<uint2 *>(unit + (2 * b + rh) * 512 + (4 * g + w) * 16 + h * 8) = raw;
-    } else {
-      const uint16_t v[4] = {static_cast<uint16_t>(raw.x), static_cast<uint16_t>(raw.x >> 16),
-                             static_cast<uint16_t>(raw.y), static_cast<uint16_t>(raw.y >> 16)};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int d = 4 * lane + i, mt = d >> 4, gq = (d & 15) >> 1, s = d & 1;
-        *reinterpret_cast<uint16_t *>(unit + mt * 512 + (4 * gq + tig) * 16 +
-                                      (rh * 4 + s * 2 + par) * 2) = v[i];
-      }
-    }
-    return;
-  }
-  const uint16_t dbits = __half_as_ushort(d16);
-  if (codec == KVQ_Q8_0) {
-    if (SIDE == 0) {
-      const uint32_t word = (q[0] & 0xff) | ((q[1] & 0xff) << 8) | ((q[2] & 0xff) << 16) |
-                            (static_cast<uint32_t>(q[3] & 0xff) << 24);
-      const int h = lb >> 2, w = lane & 3;
-      *reinterpret_cast<uint32_t *>(unit + b * 512 + (4 * g + w) * 16 + (2 * rh + h) * 4) = word;
-      if (lb == 0) st_u16(unit + 2048 + g * 16 + rh * 8 + b * 2, dbits);
-    } else {
-#pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int d = 4 * lane + 2 * p, mt = d >> 4, gq = (d & 15) >> 1;
-        st_u16(unit + (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2,
-               (q[2 * p] & 0xff) | ((q[2 * p + 1] & 0xff) << 8));
-      }
-      if (lb == 0) st_u16(unit + 2048 + tig * 32 + b * 8 + rh * 4 + par * 2, dbits);
-    }
-    return;
-  }
-  // q4_0 and turbo4: canonical byte jc of block (group) b = q[jc] | q[jc+16]
-  // << 4; lanes lb<4 hold jc = 4lb..4lb+3 and fetch the high nibbles from
-  // lane lb+4 of the same block.
-  int hi[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) hi[i] = __shfl_down_sync(0xffffffffu, q[i], 4);
-  if (lb < 4) {
-    uint32_t bytes[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) bytes[i] = (q[i] & 0xf) | ((hi[i] & 0xf) << 4);
-    if (SIDE == 0) {
-      const uint32_t word = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-      *reinterpret_cast<uint32_t *>(unit + (b >> 1) * 512 + (4 * g + lb) * 16 +
-                                    ((b & 1) * 2 + rh) * 4) = word;
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int jc = 4 * lb + i, mt = 2 * b + (jc >> 3), gq = jc & 7;
-        unit[(mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh] =
-            static_cast<uint8_t>(bytes[i]);
-      }
-    }
-  }
-  if (codec == KVQ_TURBO4) {  // one scale per row
-    if (lane == 0)
-      st_u16(unit + (SIDE == 0 ? 1024 + g * 4 + rh * 2 : 1024 + tig * 8 + rh * 4 + par * 2),
-             dbits);
-    return;
-  }
-  if (lb == 0) {
-    const int off = SIDE == 0 ? 1024 + g * 16 + rh * 8 + b * 2
-                              : 1024 + tig * 32 + b * 8 + rh * 4 + par * 2;
-    st_u16(unit + off, dbits);
-  }
-}
 
 // Read one row (token row r of `unit`) into the lane-held form of store_row:
 // lane l gets dims 4l..4l+3 as fp32, the decoded values x^ = d16 * q (q8_0),
@@ -284,19 +130,7 @@ __device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, i
     return;
   }
   const uint2 raw = reinterpret_cast<const uint2 *>(p.x[side] + rr * kD)[lane];
-  float x[4];
-  {
-    const __half2 h01 = *reinterpret_cast<const __half2 *>(&raw.x);
-    const __half2 h23 = *reinterpret_cast<const __half2 *>(&raw.y);
-    x[0] = __low2float(h01); x[1] = __high2float(h01);
-    x[2] = __low2float(h23); x[3] = __high2float(h23);
-  }
   const int codec = p.codec[side];
-  int q[4] = {0, 0, 0, 0};
-  __half d16 = __float2half_rn(0.0f);
-  if (codec == KVQ_Q8_0) encode_q8(x, q, d16);
-  else if (codec == KVQ_Q4_0) encode_q4(x, lane, q, d16);
-  else if (codec == KVQ_TURBO4) encode_turbo4(x, lane, q, d16);
   int64_t unit_idx;
   if (p.table) {
     const int pg =
@@ -313,8 +147,8 @@ __device__ __forceinline__ void append_row(const AppendParams &p, int64_t row, i
   }
   uint8_t *unit = p.cache[side] + unit_idx * unit_bytes(codec);
   const int r = static_cast<int>(pos % kUnitTokens);
-  if (side == 0) store_row<0>(codec, unit, r, lane, raw, q, d16);
-  else store_row<1>(codec, unit, r, lane, raw, q, d16);
+  if (side == 0) encode_row_into<0>(codec, raw, unit, r, lane);
+  else encode_row_into<1>(codec, raw, unit, r, lane);
 }
 
 // One warp per row (grid covers all rows).

@@ -41,6 +41,7 @@
 #include <math.h>
 
 #include "kvq_device.cuh"
+#include "kvq_encode.cuh"
 #include "kvq_launch.h"
 
 namespace kvq {
@@ -57,6 +58,15 @@ struct DecodeParams {
   const uint8_t *v_cache;
   const int32_t *seq_lens;
   const __half *q;
+  // Fused decode step (k_new != nullptr): one new token per sequence,
+  // fp16 rows [n_seqs][n_kv][128], encoded into the cache at position
+  // seq_lens[s] by the warp that consumes the item holding it; lens_rw
+  // (= seq_lens) is advanced by the last CTA to finish reading the lengths,
+  // counted in rd_ctr (zero between calls).
+  const __half *k_new;
+  const __half *v_new;
+  int32_t *lens_rw;
+  unsigned *rd_ctr;
   float *part_o;    // [slots][8][128]
   float2 *part_ml;  // [slots][8]: (max in log2 units, sum)
   int32_t *tickets; // [streams] arrival counters (zero between calls)
@@ -413,6 +423,9 @@ __device__ __forceinline__ void store_red(float *r, const float (&o)[8][4], floa
 __device__ __forceinline__ void cta_bar() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kThreads) : "memory");
 }
+__device__ __forceinline__ void half_bar() {  // warps 0 .. kWarps/2 - 1
+  asm volatile("bar.sync 2, %0;\n" ::"n"(kThreads / 2) : "memory");
+}
 
 // Online softmax + PV for N units at once (N = 1, 2 or 4): one max reduction and
 // at most one rescale per call.  A unit may have no valid token at all (the
@@ -748,7 +761,80 @@ __device__ __forceinline__ bool merge_stream_smem(const MergeArgs p, uint8_t *bu
   return true;
 }
 
+// Keys sequence s attends: its length, plus the token a fused decode step
+// appends when it fits the capacity.
+__device__ __forceinline__ int attended_len(const DecodeParams &p, int s) {
+  int len = p.seq_lens[s];
+  if (p.k_new && len >= 0 && len < p.capacity) ++len;
+  return len;
+}
+
+// Fused decode step, one thread per CTA after the CTA's last read of the
+// lengths: the last CTA to get here advances them (each CTA counts itself
+// only after all its reads, so no CTA sees a new length).
+__device__ __noinline__ void lengths_read(const DecodeParams &p) {
+  __threadfence();
+  const unsigned old = atomicInc(p.rd_ctr, gridDim.x - 1);
+  if (old != gridDim.x - 1) return;
+  __threadfence();
+  for (int s = 0; s < p.n_seqs; ++s) {
+    const int len = p.seq_lens[s];
+    if (len >= 0 && len < p.capacity) p.lens_rw[s] = len + 1;
+  }
+}
+
+// Fused decode step: the appended token of sequence seq exists (its length
+// is in [0, capacity)).
+__device__ __forceinline__ bool appends(const DecodeParams &p, int seq) {
+  const int len = p.seq_lens[seq];
+  return p.k_new && len >= 0 && len < p.capacity;
+}
+
+// Fused decode step: write sequence seq's new K and V rows of kv head kvh
+// (fp16 from k_new / v_new; all 32 lanes) into the cache at position
+// pos = seq_lens[seq] (the old length).
 template <int CK, int CV>
+__device__ __forceinline__ void write_new_rows(const DecodeParams &p, int seq, int kvh, int lane) {
+  const int pos = p.seq_lens[seq];
+  const int64_t row = static_cast<int64_t>(seq) * p.n_kv + kvh;
+  const uint2 rk = reinterpret_cast<const uint2 *>(p.k_new + row * kD)[lane];
+  const uint2 rv = reinterpret_cast<const uint2 *>(p.v_new + row * kD)[lane];
+  int64_t unit;
+  if (p.table) {
+    const int pg =
+        page_of(p.table, p.pages_per_seq, p.n_pages, seq, pos / (kUnitTokens * kPageUnits));
+    if (pg < 0) {
+      if (lane == 0) set_err(p.err, KVQ_DEVERR_PAGE);
+      return;
+    }
+    unit = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits + (pos / kUnitTokens) % kPageUnits;
+  } else {
+    unit = row * (p.capacity / kUnitTokens) + pos / kUnitTokens;
+  }
+  const int r = pos % kUnitTokens;
+  encode_row_into<0>(CK, rk, const_cast<uint8_t *>(p.k_cache) + unit * unit_bytes(CK), r, lane);
+  encode_row_into<1>(CV, rv, const_cast<uint8_t *>(p.v_cache) + unit * unit_bytes(CV), r, lane);
+}
+
+__device__ __forceinline__ Geo make_geo(const DecodeParams &p, const int32_t *pfx, int ups) {
+  Geo geo;
+  geo.pfx = pfx;
+  geo.n_seqs = p.n_seqs;
+  geo.n_kv = p.n_kv;
+  geo.n_hg = p.n_hg;
+  geo.KH = p.n_kv * p.n_hg;
+  geo.upst = p.capacity / kUnitTokens;
+  geo.upi = ups;
+  geo.ipp = kPageUnits / ups;
+  geo.table = p.table;
+  geo.pps = p.pages_per_seq;
+  geo.n_pages = p.n_pages;
+  return geo;
+}
+
+// FUSED: the fused decode step (p.k_new set); a separate instantiation, so
+// that the plain decode loop carries none of its state.
+template <int CK, int CV, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeParams p) {
   using C = DecodeCfg<CK, CV>;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -780,7 +866,11 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       const int s = base + lane;
       int n = 0;
       if (s < p.n_seqs) {
-        int len = p.seq_lens[s];
+        if (p.k_new && blockIdx.x == 0) {
+          const int old = p.seq_lens[s];
+          if (old < 0 || old >= p.capacity) set_err(p.err, KVQ_DEVERR_CAPACITY);
+        }
+        int len = attended_len(p, s);
         if (len > p.max_len) {
           if (blockIdx.x == 0) set_err(p.err, KVQ_DEVERR_MAXLEN);
           len = p.max_len;
@@ -819,24 +909,16 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     }
   }
 
-  Geo geo;
-  geo.pfx = pfx;
-  geo.n_seqs = p.n_seqs;
-  geo.n_kv = p.n_kv;
-  geo.n_hg = p.n_hg;
-  geo.KH = p.n_kv * p.n_hg;
-  geo.upst = p.capacity / kUnitTokens;
-  geo.upi = C::UPS;
-  geo.ipp = kPageUnits / C::UPS;
-  geo.table = p.table;
-  geo.pps = p.pages_per_seq;
-  geo.n_pages = p.n_pages;
+  const Geo geo = make_geo(p, pfx, C::UPS);
   const int64_t U = static_cast<int64_t>(pfx[p.n_seqs]) * geo.KH;
   const int P = gridDim.x;
   const int64_t u0 = U * blockIdx.x / P;
   const int64_t u1 = U * (blockIdx.x + 1) / P;
   const int R = static_cast<int>(u1 - u0);
-  if (R <= 0) return;  // whole CTA: nothing to do
+  if (R <= 0) {  // whole CTA: nothing to do
+    if (FUSED && threadIdx.x == 0) lengths_read(p);
+    return;
+  }
 
   uint8_t *ring = smem;
   float *red = reinterpret_cast<float *>(smem + C::RING);
@@ -869,6 +951,27 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     issue_q(0, seg);
     q_iss = 1;
   }
+  // Fused decode step: a stream's new token lies in its last item.  For
+  // every stream that ends inside this slice, the warp that consumes that
+  // item writes the new rows into the cache before it issues any copy, and
+  // orders those writes before its copies (with several head groups per kv
+  // head each group's stream writes the same bytes).
+  if (FUSED) {
+    bool wrote = false;
+    int64_t u = u0;
+    while (u < u1) {
+      const Cursor c = cursor_at(geo, u);
+      const int64_t send = u + (c.n_s - c.j);
+      if (send <= u1 && static_cast<int>(send - 1 - u0) % kWarps == warp && appends(p, c.seq)) {
+        write_new_rows<CK, CV>(p, c.seq, c.sl / p.n_hg, lane);
+        wrote = true;
+      }
+      u = send;
+    }
+    if (wrote) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncwarp();
+  }
+
   // Prologue: each warp issues its own first stages (k = warp, warp + 8, ...
   // below NS).  Afterwards the producer cursor pc sits at unit k + NS for the
   // warp's next unit k.
@@ -892,7 +995,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     const int64_t seg_end = min(u1, useg + (seg.n_s - seg.j));
     const int k0 = static_cast<int>(useg - u0), k1 = static_cast<int>(seg_end - u0);
     const int seq = seg.seq, kvh = seg.sl / p.n_hg, hg = seg.sl % p.n_hg;
-    int len = p.seq_lens[seq];
+    int len = attended_len(p, seq);
     len = len < p.max_len ? len : p.max_len;
 
     uint32_t qb[8][2];
@@ -1012,9 +1115,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     float *rs = red + lane * kRedFloats;
     if (warp >= 4) store_red(rs + (warp - 4) * 32 * kRedFloats, o, m0, m1, l0, l1);
     cta_bar();
-    if (warp < 4) merge_into(o, m0, m1, l0, l1, rs + warp * 32 * kRedFloats);
-    if (warp >= 1 && warp < 4) store_red(rs + warp * 32 * kRedFloats, o, m0, m1, l0, l1);
-    cta_bar();
+    // (every thread has read this segment's length: after the last segment
+    // the fused step's lengths may advance)
+    if (FUSED && seg_end == u1 && threadIdx.x == kThreads - 1) lengths_read(p);
+    if (warp < 4) {
+      merge_into(o, m0, m1, l0, l1, rs + warp * 32 * kRedFloats);
+      if (warp >= 1) store_red(rs + warp * 32 * kRedFloats, o, m0, m1, l0, l1);
+      half_bar();  // warps 0-3 only
+    }
     const int stream = seq * geo.KH + seg.sl;
     // CTAs whose slices overlap this stream: c_first..c_last; the owner of
     // unit u is floor(((u + 1) * P - 1) / U).
@@ -1105,13 +1213,20 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   }
 }
 
-template <int CK, int CV>
-cudaError_t launch_split(const DecodeParams &p, int grid, cudaStream_t stream) {
+template <int CK, int CV, bool FUSED>
+cudaError_t launch_split_f(const DecodeParams &p, int grid, cudaStream_t stream) {
   using C = DecodeCfg<CK, CV>;
   static std::atomic<uint64_t> optin{0};
-  const cudaError_t e = smem_optin(decode_split_kernel<CK, CV>, C::SMEM, optin);
+  const cudaError_t e = smem_optin(decode_split_kernel<CK, CV, FUSED>, C::SMEM, optin);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_split_kernel<CK, CV>, dim3(grid), dim3(kThreads), C::SMEM, stream, p);
+  return launch_pdl(decode_split_kernel<CK, CV, FUSED>, dim3(grid), dim3(kThreads), C::SMEM,
+                    stream, p);
+}
+
+template <int CK, int CV>
+cudaError_t launch_split(const DecodeParams &p, int grid, cudaStream_t stream) {
+  return p.k_new ? launch_split_f<CK, CV, true>(p, grid, stream)
+                 : launch_split_f<CK, CV, false>(p, grid, stream);
 }
 
 template <int CK>
@@ -1151,12 +1266,16 @@ DecodePlan plan_decode(const kvq_layer &L, int max_len, int num_sms) {
 
 cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *q, float scale,
                           void *out, float *lse, int max_len, void *workspace,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, const void *k_new, const void *v_new) {
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   DecodeParams p;
   p.k_cache = static_cast<const uint8_t *>(L.k_cache);
   p.v_cache = static_cast<const uint8_t *>(L.v_cache);
   p.seq_lens = L.seq_lens;
+  p.k_new = static_cast<const __half *>(k_new);
+  p.v_new = static_cast<const __half *>(v_new);
+  p.lens_rw = L.seq_lens;
+  p.rd_ctr = reinterpret_cast<unsigned *>(ws) + (kDecodeTicketBytes / 4 - 1);
   p.q = static_cast<const __half *>(q);
   p.tickets = reinterpret_cast<int32_t *>(ws);
   p.part_ml = reinterpret_cast<float2 *>(ws + pl.ticket_bytes);

@@ -142,6 +142,28 @@ int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, f
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
+int attn_decode_append(const kvq_layer *layer, const void *k_new, const void *v_new,
+                       const void *q, float scale, void *out, float *lse, int32_t max_len,
+                       void *workspace, size_t ws_bytes, void *stream) {
+  int st = check_layer(layer);
+  if (st != KVQ_OK) return st;
+  if (!k_new || !v_new || !q || !out || max_len <= 0) return KVQ_EINVAL;
+  if (!decode_shape_ok(layer)) return KVQ_EINVAL;
+  if (max_len > layer->capacity) return KVQ_ECAPACITY;
+  if (!aligned(k_new, 8) || !aligned(v_new, 8) || !aligned(q, 8) || !aligned(out, 8) ||
+      (lse && !aligned(lse, 4)))
+    return KVQ_EALIGN;
+  if (!workspace) return KVQ_EWORKSPACE;
+  if (!aligned(workspace, 16)) return KVQ_EALIGN;
+  const int sms = device_sms();
+  if (sms <= 0) return KVQ_ECUDA;
+  const kvq::DecodePlan pl = kvq::plan_decode(*layer, max_len, sms);
+  if (ws_bytes < static_cast<size_t>(pl.ws_bytes)) return KVQ_EWORKSPACE;
+  const cudaError_t e = kvq::launch_decode(*layer, pl, q, scale, out, lse, max_len, workspace,
+                                           static_cast<cudaStream_t>(stream), k_new, v_new);
+  return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
+}
+
 int attn_prefill_workspace(const kvq_layer *layer, int32_t q_start, int32_t n_q_tok,
                            size_t *bytes) {
   int st = check_layer(layer);

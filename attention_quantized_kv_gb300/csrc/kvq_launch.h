@@ -20,7 +20,9 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
 
 constexpr int kDecodeMaxSeqs = 1024;         // sequences per attn_decode call
 constexpr int kDecodeTicketBytes = 64 * 1024;  // per-stream counters at the workspace start
-constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4;
+// per-stream counters; the region's last word counts the CTAs of a fused
+// decode step that have read the lengths
+constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4 - 1;
 
 struct DecodePlan {
   int n_hgroups = 1;      // groups of up to 8 query heads per kv head
@@ -33,9 +35,12 @@ struct DecodePlan {
 };
 
 DecodePlan plan_decode(const kvq_layer &L, int max_len, int num_sms);
+// k_new / v_new (fused decode step, fp16 [n_seqs][n_kv][128]): append one
+// token per sequence before attending, and advance the lengths.
 cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *q, float scale,
                           void *out, float *lse, int max_len, void *workspace,
-                          cudaStream_t stream);
+                          cudaStream_t stream, const void *k_new = nullptr,
+                          const void *v_new = nullptr);
 
 struct PrefillPlan {
   int64_t kv_tokens = 0;     // keys attended by the chunk: q_start + n_q_tok

@@ -74,10 +74,17 @@ def evict_work(w, lens, n_ev, ck, cv):
     return dec, probe, sel, comp
 
 
-def step_work(w):
+def fused_decode_step(w) -> bool:
+    """A decode step that appends one token per sequence runs as one fused
+    call (attn_decode_append) per layer."""
+    return w.kind == "decode" and w.append_new == 1
+
+
+def step_work(w, fused=None):
     """(bytes, flops, roofline-kernel bytes per layer) of one step of workload
-    w; the roofline kernel is the attention call, the re-encode, or (eviction
-    steps) the compaction."""
+    w; the roofline kernel is the attention call (with the append's bytes when
+    the step is fused), the re-encode, or (eviction steps) the compaction."""
+    fused = fused_decode_step(w) if fused is None else fused
     lens = w.final_lens()
     total_b, total_f, per_layer = 0, 0, []
     for ck, cv in w.codecs:
@@ -102,7 +109,7 @@ def step_work(w):
             kv = (q0 + n_tok) * w.n_kv * (ROW[ck] + ROW[cv])
             qo = 2 * n_tok * w.n_q * 256
             fl = sum(q0 + i + 1 for i in range(n_tok)) * w.n_q * 4 * 128
-        per_layer.append(kv + qo)
+        per_layer.append(kv + qo + (app if fused else 0))
         total_b += kv + qo + app
         total_f += fl
     return total_b, total_f, per_layer
@@ -171,12 +178,13 @@ class ClockSampler:
 # ------------------------------------------------------------------ our arm
 
 class OursArm:
-    def __init__(self, w, device):
+    def __init__(self, w, device, fused=None):
         import torch
         import attention_quantized_kv_gb300 as kvq
         from attention_quantized_kv_gb300 import workloads as wl
         self.torch, self.kvq, self.wl, self.w, self.dev = torch, kvq, wl, w, device
         self.scale = 1.0 / math.sqrt(128)
+        self.fused = fused_decode_step(w) if fused is None else fused
         self.layers, self.ws, self.q, self.kn, self.vn = [], [], [], [], []
         self.max_len = max(w.final_lens())
         self.init_lens = torch.tensor(w.lens, dtype=torch.int32, device=device)
@@ -266,7 +274,7 @@ class OursArm:
         selection, compaction of both sides)."""
         w = self.w
         per_layer = {"decode": 1, "degrade": 1, "prefill": 2, "evict": 4}[w.kind]
-        if w.append_new:
+        if w.append_new and not self.fused:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
             per_layer += 1 if rows <= 64 else 2
@@ -278,15 +286,26 @@ class OursArm:
         replacements of the resident tensors."""
         kvq, w = self.kvq, self.w
         for l, L in enumerate(self.layers):
+            if self.fused:
+                self.fused_step(l, q, kn, vn, out)
+                continue
             if w.append_new:
                 kvq.kv_append_quantize(L, (kn or self.kn)[l], (vn or self.vn)[l], self.n_new)
             self.attention(l, q, out)
+
+    def fused_step(self, l, q=None, kn=None, vn=None, out=None):
+        """One layer's decode step in one call: append the token, attend."""
+        self.kvq.attn_decode_append(self.layers[l], (kn or self.kn)[l][:, 0],
+                                    (vn or self.vn)[l][:, 0], (q or self.q)[l], self.scale,
+                                    (out or self.out)[l], self.lse[l], self.max_len, self.ws[l])
 
     def roofline_calls(self, l):
         """The calls of the kernel the roofline line is about: the attention
         call, the re-encode, or (eviction steps) the compaction."""
         if self.w.kind == "evict":
             self.compact(l)
+        elif self.fused:
+            self.fused_step(l)
         else:
             self.attention(l)
 
@@ -374,8 +393,8 @@ def run_ours(args, w, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", "0"))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    arm = OursArm(w, dev)
-    bytes_step, flops_step, per_layer_bytes = step_work(w)
+    arm = OursArm(w, dev, fused=False if args.unfused else None)
+    bytes_step, flops_step, per_layer_bytes = step_work(w, arm.fused)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
     flush = (torch.empty(2 * l2, dtype=torch.uint8, device=dev),
@@ -407,6 +426,9 @@ def run_ours(args, w, rank, world, dist):
     mode = ("one CUDA graph replay per step, events outside it; "
             + ("compaction kernels" if w.kind == "evict" else "attention kernels")
             + " timed in a replay of their own")
+    if arm.fused:
+        mode = ("one CUDA graph replay per step (one fused append + attention call per "
+                "layer), events outside it")
 
     for _ in range(3):
         _flush_l2(torch, flush)
@@ -444,7 +466,7 @@ def run_ours(args, w, rank, world, dist):
         return ms
 
     step_ms = timed(g_step, arm.reset)
-    attn_ms = timed(g_attn, arm.set_final_lens)
+    attn_ms = timed(g_attn, arm.reset if arm.fused else arm.set_final_lens)
     torch.cuda.synchronize()
     clocks = clk.stop()
     if dist:
@@ -555,7 +577,8 @@ def run_ours(args, w, rank, world, dist):
         "device_errors": errs,
     }
     if w.kind in ("decode", "degrade", "evict"):
-        kname = {"decode": "attn_decode (decode_split_kernel)",
+        kname = {"decode": "attn_decode_append (decode_split_kernel, append fused)" if arm.fused
+                 else "attn_decode (decode_split_kernel)",
                  "degrade": "kv_requantize (requant_kernel)",
                  "evict": "kv_compact (compact_kernel)"}[w.kind]
         line["roofline"] = {"bound": "hbm", "kernel": kname,
@@ -744,6 +767,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="one-token decode steps as two calls (append, then attention)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -207,7 +207,7 @@ KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_
  * allocating it); every call that completes without KVQ_DEVERR_TIMEOUT
  * leaves them zero again, so one workspace serves any number of calls and
  * layers without clearing.  Calls that may run concurrently need separate
- * workspaces.  Limits: 1024 sequences and 16384 streams (sequence x kv head
+ * workspaces.  Limits: 1024 sequences and 16383 streams (sequence x kv head
  * x group of 8 query heads) per call, else KVQ_EINVAL.
  * q: fp16 [n_seqs][n_q_heads][128] (8-byte aligned); out: fp16
  * [n_seqs][n_q_heads][128]; lse: optional fp32 [n_seqs][n_q_heads] natural-log
@@ -217,6 +217,26 @@ KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_
  * lse = -inf. */
 KVQ_API int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
                 int32_t max_len, void *workspace, size_t ws_bytes, void *stream);
+
+/* One decode step of a layer in one launch: quantize-on-append of one new
+ * token per sequence (the kv_append_quantize row encoding, at position
+ * seq_lens[s]), then attn_decode over seq_lens[s] + 1 keys, then
+ * seq_lens[s] += 1.  The result (cache bytes, lengths, out, lse) is that of
+ * kv_append_quantize(n_new = 1 for every sequence, update_lens = 1)
+ * followed by attn_decode on the same stream (a new token's keys enter the
+ * typed cache before it is attended, as in the serverAppConfigs commit log,
+ * frank_small_unit.bats commit), fused so that the append costs no launch
+ * of its own.
+ * k_new, v_new: fp16 [n_seqs][n_kv_heads][128], 8-byte aligned.  A sequence
+ * whose length is already capacity (or negative) gets no new token (sets
+ * KVQ_DEVERR_CAPACITY) and attends its existing keys.  max_len must bound
+ * every new length.  The workspace is attn_decode_workspace(layer, max_len)
+ * bytes, with the same zero-between-calls contract as attn_decode; its
+ * 64 KiB counter region also counts the CTAs that have read the lengths.
+ * Other arguments and limits are those of attn_decode. */
+KVQ_API int attn_decode_append(const kvq_layer *layer, const void *k_new, const void *v_new,
+                               const void *q, float scale, void *out, float *lse,
+                               int32_t max_len, void *workspace, size_t ws_bytes, void *stream);
 
 /* attn_decode without a workspace argument, for callers that cannot allocate
  * device memory where they run attention (an interface that hands them only
