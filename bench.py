@@ -361,7 +361,7 @@ def _traffic_for(workload):
 
 
 def _kernel_source_hash(kind):
-    names = {"decode": ["decode.cu", "kvq_device.cuh"],
+    names = {"decode": ["decode.cu", "kvq_device.cuh", "kvq_encode.cuh"],
              "prefill": ["prefill.cu", "kvq_device.cuh"],
              "evict": ["evict.cu", "kvq_device.cuh"]}[kind]
     h = hashlib.sha256()
