@@ -215,8 +215,9 @@ static_assert(kPageUnits % kRqUnits == 0, "a run of units must lie inside one pa
 // rounds to fp16) into a shared copy of the destination units, which go out
 // with coalesced 16-byte stores.  The unit holding the sequence's last tokens
 // first reads its destination bytes, so that its rows past the length keep
-// them.
-template <int SIDE>
+// them.  SC / DC: source and destination codecs (compile-time, so that the
+// row decode and encode carry no codec dispatch).
+template <int SIDE, int SC, int DC>
 __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams p) {
   extern __shared__ uint4 rq_smem[];
   grid_dependency_wait();
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
     } else {
       uidx = (static_cast<int64_t>(s) * p.n_kv + kvh) * (p.capacity / kUnitTokens) + u0;
     }
-    const int sb = unit_bytes(p.src_codec), db = unit_bytes(p.dst_codec);
+    constexpr int sb = unit_bytes(SC), db = unit_bytes(DC);
     uint4 *sbuf = rq_smem;
     uint4 *dbuf = rq_smem + kRqUnits * sb / 16;
     const uint4 *su = reinterpret_cast<const uint4 *>(p.src + uidx * sb);
@@ -253,28 +254,63 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
     for (int row = warp; row < rows; row += kUnitTokens) {
       const int ul = row / kUnitTokens, r = row % kUnitTokens;
       float x[4];
-      load_row<SIDE>(p.src_codec, reinterpret_cast<const uint8_t *>(sbuf) + ul * sb, r, lane, x);
+      load_row<SIDE>(SC, reinterpret_cast<const uint8_t *>(sbuf) + ul * sb, r, lane, x);
       int q[4] = {0, 0, 0, 0};
       __half d16 = __float2half_rn(0.0f);
       uint2 raw = make_uint2(0u, 0u);
-      if (p.dst_codec == KVQ_Q8_0) {
+      if (DC == KVQ_Q8_0) {
         encode_q8(x, q, d16);
-      } else if (p.dst_codec == KVQ_Q4_0) {
+      } else if (DC == KVQ_Q4_0) {
         encode_q4(x, lane, q, d16);
-      } else if (p.dst_codec == KVQ_TURBO4) {
+      } else if (DC == KVQ_TURBO4) {
         encode_turbo4(x, lane, q, d16);
       } else {
         const __half2 h01 = __floats2half2_rn(x[0], x[1]), h23 = __floats2half2_rn(x[2], x[3]);
         raw.x = *reinterpret_cast<const uint32_t *>(&h01);
         raw.y = *reinterpret_cast<const uint32_t *>(&h23);
       }
-      store_row<SIDE>(p.dst_codec, reinterpret_cast<uint8_t *>(dbuf) + ul * db, r, lane, raw,
-                      q, d16);
+      store_row<SIDE>(DC, reinterpret_cast<uint8_t *>(dbuf) + ul * db, r, lane, raw, q, d16);
     }
     __syncthreads();
     for (int i = threadIdx.x; i < n_units * db / 16; i += blockDim.x) du[i] = dbuf[i];
   }
   grid_launch_dependents();
+}
+
+template <int SIDE, int SC, int DC>
+cudaError_t launch_requant_t(const RequantParams &p, dim3 grid, int smem, cudaStream_t stream) {
+  static std::atomic<uint64_t> optin{0};
+  const cudaError_t e = smem_optin(requant_kernel<SIDE, SC, DC>, kRqUnits * 2 * 4096, optin);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(requant_kernel<SIDE, SC, DC>, grid, dim3(kUnitTokens * 32), smem, stream, p);
+}
+
+template <int SIDE, int SC>
+cudaError_t launch_requant_d(int dc, const RequantParams &p, dim3 grid, int smem,
+                             cudaStream_t stream) {
+  switch (dc) {
+    case KVQ_F16: return launch_requant_t<SIDE, SC, KVQ_F16>(p, grid, smem, stream);
+    case KVQ_Q8_0: return launch_requant_t<SIDE, SC, KVQ_Q8_0>(p, grid, smem, stream);
+    case KVQ_Q4_0: return launch_requant_t<SIDE, SC, KVQ_Q4_0>(p, grid, smem, stream);
+    default: return launch_requant_t<SIDE, SC, KVQ_TURBO4>(p, grid, smem, stream);
+  }
+}
+
+template <int SIDE>
+cudaError_t launch_requant_c(int sc, int dc, const RequantParams &p, dim3 grid, int smem,
+                             cudaStream_t stream) {
+  switch (sc) {
+    case KVQ_F16: return launch_requant_d<SIDE, KVQ_F16>(dc, p, grid, smem, stream);
+    case KVQ_Q8_0: return launch_requant_d<SIDE, KVQ_Q8_0>(dc, p, grid, smem, stream);
+    case KVQ_Q4_0: return launch_requant_d<SIDE, KVQ_Q4_0>(dc, p, grid, smem, stream);
+    default: return launch_requant_d<SIDE, KVQ_TURBO4>(dc, p, grid, smem, stream);
+  }
+}
+
+cudaError_t launch_requant_s(int side, int sc, int dc, const RequantParams &p, dim3 grid,
+                             int smem, cudaStream_t stream) {
+  return side == 0 ? launch_requant_c<0>(sc, dc, p, grid, smem, stream)
+                   : launch_requant_c<1>(sc, dc, p, grid, smem, stream);
 }
 
 }  // namespace
@@ -296,17 +332,7 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
   const int units = L.capacity / kUnitTokens;
   const dim3 grid((units + kRqUnits - 1) / kRqUnits, L.n_kv_heads, L.n_seqs);
   const int smem = kRqUnits * (unit_bytes(p.src_codec) + unit_bytes(dst_codec));
-  cudaError_t e;
-  if (side == 0) {
-    static std::atomic<uint64_t> optin{0};
-    e = smem_optin(requant_kernel<0>, kRqUnits * 2 * 4096, optin);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(requant_kernel<0>, grid, dim3(kUnitTokens * 32), smem, stream, p);
-  }
-  static std::atomic<uint64_t> optin{0};
-  e = smem_optin(requant_kernel<1>, kRqUnits * 2 * 4096, optin);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(requant_kernel<1>, grid, dim3(kUnitTokens * 32), smem, stream, p);
+  return launch_requant_s(side, p.src_codec, dst_codec, p, grid, smem, stream);
 }
 
 cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_new,

@@ -16,6 +16,42 @@
 namespace kvq {
 namespace {
 
+// The integers the encoders take from the quotients x/d, without a division
+// or a float-to-int conversion per value.  t = RN(x * RN(1/d)) lies within
+// |x/d| * 3 * 2^-24 of RN(x/d) (two roundings of relative size 2^-24).
+// Where t is far enough from the boundary at which the encoder's integer
+// changes, t gives the same integer as RN(x/d) (tests below); elsewhere the
+// encoder divides exactly.  Integers come from the 1.5 * 2^23 addition: for
+// |y| < 2^22, RN(y + 1.5 * 2^23) holds RN-to-nearest-integer(y) in its low
+// mantissa bits.  The bytes are those of the exact division.
+constexpr float kRoundMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr int kRoundMagicBits = 0x4B400000;
+
+// q8_0: q = round-half-away(RN(x/d)) with |x/d| <= 127 (1 + 2^-23), so
+// |t - RN(x/d)| < 2^-15.4.  t more than 2^-14 away from every half-integer
+// rounds the same way, and there round-half-away equals round-to-nearest.
+__device__ __forceinline__ int q8_from_quotient(float x, float d, float rcp) {
+  const float t = __fmul_rn(x, rcp);
+  const float tm = __fadd_rn(t, kRoundMagic);
+  const float dist = fabsf(__fsub_rn(t, __fsub_rn(tm, kRoundMagic)));  // to the nearest integer
+  if (fabsf(__fsub_rn(dist, 0.5f)) > 0x1p-14f) return __float_as_int(tm) - kRoundMagicBits;
+  return static_cast<int>(roundf(__fdiv_rn(x, d)));
+}
+
+// q4_0 and turbo4: q = min(15, trunc(RN(RN(x/d) + 8.5))) with |x/d| <= 8 (1 +
+// 2^-23): u = RN(t + 8.5) lies within 2^-18.5 of the exact path's value, so
+// u more than 2^-17 away from every integer truncates the same way
+// (floor(u) = the integer nearest to u - 0.5, which is exact there).
+__device__ __forceinline__ int q4_from_quotient(float x, float d, float rcp) {
+  const float u = __fadd_rn(__fmul_rn(x, rcp), 8.5f);
+  const float fm = __fadd_rn(__fsub_rn(u, 0.5f), kRoundMagic);
+  const float fr = __fsub_rn(u, __fsub_rn(fm, kRoundMagic));  // u - floor(u)
+  const int v = (fr > 0x1p-17f && fr < 1.0f - 0x1p-17f)
+                    ? __float_as_int(fm) - kRoundMagicBits
+                    : static_cast<int>(__fadd_rn(__fdiv_rn(x, d), 8.5f));  // truncation; u >= 0.5
+  return v > 15 ? 15 : v;
+}
+
 // q8_0: amax over the 8 lanes of the block, d = amax/127, q = round(x/d).
 __device__ __forceinline__ void encode_q8(const float (&x)[4], int (&q)[4], __half &d16) {
   float a = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
@@ -23,8 +59,9 @@ __device__ __forceinline__ void encode_q8(const float (&x)[4], int (&q)[4], __ha
   for (int o = 1; o < 8; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   const float d = __fdiv_rn(a, 127.0f);
   d16 = __float2half_rn(d);
+  const float rcp = d != 0.0f ? __frcp_rn(d) : 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) q[i] = d != 0.0f ? static_cast<int>(roundf(__fdiv_rn(x[i], d))) : 0;
+  for (int i = 0; i < 4; ++i) q[i] = d != 0.0f ? q8_from_quotient(x[i], d, rcp) : 0;
 }
 
 // q4_0: signed value of largest magnitude (lowest dim wins ties), d = m/-8,
@@ -47,12 +84,9 @@ __device__ __forceinline__ void encode_q4(const float (&x)[4], int lane, int (&q
   }
   const float d = __fdiv_rn(m, -8.0f);
   d16 = __float2half_rn(d);
+  const float rcp = d != 0.0f ? __frcp_rn(d) : 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float t = d != 0.0f ? __fdiv_rn(x[i], d) : 0.0f;
-    const int v = static_cast<int>(__fadd_rn(t, 8.5f));  // truncation; u >= 0.5
-    q[i] = v > 15 ? 15 : v;
-  }
+  for (int i = 0; i < 4; ++i) q[i] = d != 0.0f ? q4_from_quotient(x[i], d, rcp) : 8;
 }
 
 // turbo4: signs, FWHT and the factor 1/8 (the rotation of the row, exact
@@ -82,12 +116,9 @@ __device__ __forceinline__ void encode_turbo4(const float (&x)[4], int lane, int
   }
   const float d = __fdiv_rn(m, -8.0f);
   d16 = __float2half_rn(d);
+  const float rcp = d != 0.0f ? __frcp_rn(d) : 0.0f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float t = d != 0.0f ? __fdiv_rn(y[i], d) : 0.0f;
-    const int v = static_cast<int>(__fadd_rn(t, 8.5f));  // truncation; u >= 0.5
-    q[i] = v > 15 ? 15 : v;
-  }
+  for (int i = 0; i < 4; ++i) q[i] = d != 0.0f ? q4_from_quotient(y[i], d, rcp) : 8;
 }
 
 __device__ __forceinline__ void st_u16(uint8_t *p, uint32_t v) {
