@@ -363,7 +363,8 @@ def _traffic_for(workload):
 def _kernel_source_hash(kind):
     names = {"decode": ["decode.cu", "kvq_device.cuh", "kvq_encode.cuh"],
              "prefill": ["prefill.cu", "kvq_device.cuh"],
-             "evict": ["evict.cu", "kvq_device.cuh"]}[kind]
+             "evict": ["evict.cu", "kvq_device.cuh"],
+             "requant": ["append.cu", "kvq_device.cuh", "kvq_encode.cuh"]}[kind]
     h = hashlib.sha256()
     for n in names:
         with open(os.path.join(ROOT, "attention_quantized_kv_gb300", "csrc", n), "rb") as f:
