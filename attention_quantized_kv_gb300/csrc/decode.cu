@@ -36,6 +36,12 @@
 //  * Online softmax in the log2 domain per head with xor-shuffle maxima; P is
 //    transposed in registers (movmatrix) into the B operand of O^T = V^T P^T
 //    (M = 16 head dims); the V block scale is folded into P.
+//
+// The fused decode step (attn_decode_append) is a second instantiation of
+// the same kernel (FUSED): each sequence's new token is encoded into the
+// cache by the warp that consumes the item holding it, before that warp
+// issues any copy (so its small loads and stores go out ahead of the copy
+// flood), and the lengths advance once every CTA has read them.
 #include <cuda_runtime.h>
 
 #include <math.h>
