@@ -126,3 +126,30 @@ def test_ladder_planner_and_aggregate_match_the_oracle():
         assert kvq.aggregate_bpv(codecs) == oracle.aggregate_bpv(codecs)
         assert kvq.ladder_next(codecs, floor, order) == oracle.ladder_next(codecs, order, floor)
         assert kvq.ladder_next(codecs, floor) == oracle.ladder_next(codecs, list(range(n)), floor)
+
+
+def test_fused_decode_step_argument_validation(lib):
+    """attn_decode_append validates on the host before any device call: layer,
+    missing rows, max_len, alignment and workspace, like attn_decode."""
+    d = _layer()
+    f = lib.attn_decode_append
+    args = dict(k=0x700000, v=0x780000, q=0x400000, out=0x500000, max_len=16, ws=0x600000,
+                ws_bytes=1 << 20)
+
+    def call(layer=ctypes.byref(d), **kw):
+        a = dict(args, **kw)
+        return f(layer, a["k"], a["v"], a["q"], 0.1, a["out"], None, a["max_len"], a["ws"],
+                 a["ws_bytes"], None)
+
+    assert call(layer=None) == 1
+    assert call(layer=ctypes.byref(_layer(head_dim=64))) == 2
+    assert call(k=None) == 1
+    assert call(v=None) == 1
+    assert call(q=None) == 1
+    assert call(max_len=0) == 1
+    assert call(max_len=5000) == 3
+    assert call(k=0x700004) == 4
+    assert call(v=0x780002) == 4
+    assert call(q=0x400002) == 4
+    assert call(ws=None) == 5
+    assert call(ws=0x600008) == 4
