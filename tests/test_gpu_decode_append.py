@@ -242,3 +242,29 @@ def test_fused_step_argument_checks():
         kvq.attn_decode_append(L, k, k, q, SCALE, torch.empty_like(q), None, 64, ws[:16])
     with pytest.raises(kvq.KVQError):
         kvq.attn_decode_append(L, k, k, q, SCALE, torch.empty_like(q), None, L.capacity + 1, ws)
+
+
+@pytest.mark.parametrize("ck,cv", [(1, 2), (2, 2), (0, 3)])
+def test_fused_step_many_short_sequences(ck, cv):
+    """1024 short sequences (the per-call maximum): every CTA holds several
+    stream ends and some warps several new-row items; two steps in a row."""
+    rng = np.random.default_rng(11 + ck)
+    lens = [int(x) for x in rng.integers(0, 90, 1024)]
+    w = wl.Workload("t", "decode", 1024, 4, 2, lens, [(ck, cv)], 500 + ck, append_new=2)
+    A = gpu_layer(w, 0, chunk=256)
+    B = clone_layer(A)
+    max_len = max(lens) + 2
+    wsa = torch.zeros(kvq.attn_decode_workspace(A, max_len), dtype=torch.uint8, device="cuda")
+    wsb = torch.zeros_like(wsa)
+    cur = list(lens)
+    for step in range(2):
+        k, v = new_rows(w, cur)
+        q = (torch.randn((1024, 4, 128), generator=torch.Generator().manual_seed(step))
+             ).to(torch.float16).cuda()
+        oa = two_call_step(A, k, v, q, max_len, wsa)
+        ob = fused_step(B, k, v, q, max_len, wsb)
+        assert_same(A, B, oa, ob)
+        cur = [n + 1 for n in cur]
+    assert B.seq_lens.tolist() == cur
+    assert not wsb[:65536].any()
+    check_oracle(w, B, q, ob[0], ob[1], cur, [(0, 0), (511, 1), (1023, 0)])
