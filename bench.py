@@ -339,7 +339,9 @@ def _flush_l2(torch, bufs):
     """Evict the step's data from L2: write one scratch buffer larger than L2,
     then read another, so that L2 ends up holding clean unrelated lines (a
     flush by writes alone leaves ~L2-size dirty data whose write-back would be
-    charged to the timed step)."""
+    charged to the timed step).  bufs None (--warm): no flush."""
+    if bufs is None:
+        return
     wbuf, rbuf = bufs
     wbuf.zero_()
     rbuf.view(torch.int32).sum()
@@ -398,7 +400,7 @@ def run_ours(args, w, rank, world, dist):
     bytes_step, flops_step, per_layer_bytes = step_work(w, arm.fused)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 128 << 20) or (128 << 20)
-    flush = (torch.empty(2 * l2, dtype=torch.uint8, device=dev),
+    flush = None if args.warm else (torch.empty(2 * l2, dtype=torch.uint8, device=dev),
              torch.zeros(2 * l2, dtype=torch.uint8, device=dev))
 
     for _ in range(args.warmup):
@@ -565,7 +567,9 @@ def run_ours(args, w, rank, world, dist):
                     "max": max(w.final_lens())},
                    "layers": n_layers,
                    "codecs": [[["f16", "q8_0", "q4_0", "turbo4"][c] for c in p] for p in w.codecs],
-                   "l2": "flushed before every timed step (2 x L2 write, then 2 x L2 read)",
+                   "l2": ("not flushed: warm L2 (the step's data left there by the previous step)"
+                          if args.warm else
+                          "flushed before every timed step (2 x L2 write, then 2 x L2 read)"),
                    "timing": mode,
                    "parallelism": f"replicas x{world}"},
         "bytes_per_step": bytes_step,
@@ -768,6 +772,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--warm", action="store_true",
+                    help="no L2 flush between steps (warm-cache numbers, reported as such)")
     ap.add_argument("--unfused", action="store_true",
                     help="one-token decode steps as two calls (append, then attention)")
     args = ap.parse_args()
