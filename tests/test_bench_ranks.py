@@ -56,3 +56,21 @@ def test_reference_arm_under_torchrun_world_size_two():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_step_work_accounts_the_fused_append():
+    """The one-token decode steps run fused: the roofline kernel then moves the
+    appended rows too (fp16 in, encoded row out, both sides); the step's bytes
+    are the same either way, and other workloads are unaffected."""
+    from attention_quantized_kv_gb300 import workloads as wl
+    w = wl.get("append_decode_q4_ctx32k")
+    assert bench.fused_decode_step(w)
+    b_f, f_f, per_f = bench.step_work(w, True)
+    b_u, f_u, per_u = bench.step_work(w, False)
+    app = w.n_seqs * w.append_new * w.n_kv * (2 * 256 + 72 + 72)
+    assert b_f == b_u and f_f == f_u
+    assert per_f[0] - per_u[0] == app
+    kv = sum(w.final_lens()) * w.n_kv * (72 + 72)
+    assert per_u[0] == kv + 2 * w.n_seqs * w.n_q * 256
+    for name in ("decode_q8_ctx4k", "prefill_q8_32k_plus_2k", "decode_16layer_ladder_2x200704"):
+        assert not bench.fused_decode_step(wl.get(name))
