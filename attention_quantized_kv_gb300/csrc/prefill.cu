@@ -167,19 +167,28 @@ __host__ __device__ __forceinline__ int tile_offset(int row, int dim) {
 // cache unit), dequantized: x^ = d * q exactly in fp32, per the cache layout.
 template <int CODEC, int SIDE>
 __device__ __forceinline__ void load_block(const uint8_t *unit, int r, int b, float (&x)[32]) {
+  // Loads are as wide as the layout keeps the block's values together: the
+  // K side holds 4 consecutive dims of a row in one 32-bit word (q8_0) or 8
+  // bytes (f16), the V side 2 consecutive dims in 16 (q8_0) or 32 (f16) bits.
   const int g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1;
   if (CODEC == KVQ_F16) {
+    if (SIDE == 0) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int d = 32 * b + e;
-      int off;
-      if (SIDE == 0) {
-        off = (2 * b + rh) * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (e >> 4) * 8 + (e & 3) * 2;
-      } else {
-        const int mt = d >> 4, gq = (d & 15) >> 1;
-        off = mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + (d & 1) * 2 + par) * 2;
+      for (int i = 0; i < 8; ++i) {  // dims 4i .. 4i + 3 of the block
+        const uint2 w = *reinterpret_cast<const uint2 *>(
+            unit + (2 * b + rh) * 512 + (4 * g + (i & 3)) * 16 + (i >> 2) * 8);
+        const __half2 h01 = *reinterpret_cast<const __half2 *>(&w.x);
+        const __half2 h23 = *reinterpret_cast<const __half2 *>(&w.y);
+        x[4 * i] = __low2float(h01); x[4 * i + 1] = __high2float(h01);
+        x[4 * i + 2] = __low2float(h23); x[4 * i + 3] = __high2float(h23);
       }
-      x[e] = __half2float(*reinterpret_cast<const __half *>(unit + off));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        const int d = 32 * b + e, mt = d >> 4, gq = (d & 15) >> 1;
+        x[e] = __half2float(*reinterpret_cast<const __half *>(
+            unit + mt * 512 + (4 * gq + tig) * 16 + (rh * 4 + (d & 1) * 2 + par) * 2));
+      }
     }
     return;
   }
@@ -190,30 +199,46 @@ __device__ __forceinline__ void load_block(const uint8_t *unit, int r, int b, fl
                                     : 1024 + tig * 32 + b * 8 + rh * 4 + par * 2);
   const float dsc = __half2float(*reinterpret_cast<const __half *>(unit + soff));
   if (CODEC == KVQ_Q8_0) {
+    if (SIDE == 0) {
 #pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      int off;
-      if (SIDE == 0) {
-        off = b * 512 + (4 * g + ((e >> 2) & 3)) * 16 + (2 * rh + (e >> 4)) * 4 + (e & 3);
-      } else {
-        const int d = 32 * b + e, mt = d >> 4, gq = (d & 15) >> 1;
-        off = (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2 + (d & 1);
+      for (int i = 0; i < 8; ++i) {  // dims 4i .. 4i + 3: one word
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(
+            unit + b * 512 + (4 * g + (i & 3)) * 16 + (2 * rh + (i >> 2)) * 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          x[4 * i + k] = dsc * static_cast<float>(static_cast<int8_t>((w >> (8 * k)) & 0xffu));
       }
-      x[e] = dsc * static_cast<float>(static_cast<int8_t>(unit[off]));
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {  // dims 2i, 2i + 1: one 16-bit pair
+        const int d = 32 * b + 2 * i, mt = d >> 4, gq = (d & 15) >> 1;
+        const uint32_t v = *reinterpret_cast<const uint16_t *>(
+            unit + (mt >> 1) * 512 + (4 * gq + tig) * 16 + ((mt & 1) * 2 + rh) * 4 + par * 2);
+        x[2 * i] = dsc * static_cast<float>(static_cast<int8_t>(v & 0xffu));
+        x[2 * i + 1] = dsc * static_cast<float>(static_cast<int8_t>(v >> 8));
+      }
     }
   } else {
+    if (SIDE == 0) {
 #pragma unroll
-    for (int jc = 0; jc < 16; ++jc) {  // canonical byte jc: dims jc (low) and jc+16 (high)
-      int off;
-      if (SIDE == 0) {
-        off = (b >> 1) * 512 + (4 * g + (jc >> 2)) * 16 + ((b & 1) * 2 + rh) * 4 + (jc & 3);
-      } else {
-        const int mt = 2 * b + (jc >> 3), gq = jc & 7;
-        off = (mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh;
+      for (int i = 0; i < 4; ++i) {  // canonical bytes 4i .. 4i + 3: one word
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(
+            unit + (b >> 1) * 512 + (4 * g + i) * 16 + ((b & 1) * 2 + rh) * 4);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int v = (w >> (8 * k)) & 0xff, jc = 4 * i + k;
+          x[jc] = dsc * static_cast<float>((v & 0xf) - 8);
+          x[jc + 16] = dsc * static_cast<float>((v >> 4) - 8);
+        }
       }
-      const int v = unit[off];
-      x[jc] = dsc * static_cast<float>((v & 0xf) - 8);
-      x[jc + 16] = dsc * static_cast<float>((v >> 4) - 8);
+    } else {
+#pragma unroll
+      for (int jc = 0; jc < 16; ++jc) {  // canonical byte jc: dims jc (low) and jc+16 (high)
+        const int mt = 2 * b + (jc >> 3), gq = jc & 7;
+        const int v = unit[(mt >> 2) * 512 + (4 * gq + tig) * 16 + (mt & 3) * 4 + par * 2 + rh];
+        x[jc] = dsc * static_cast<float>((v & 0xf) - 8);
+        x[jc + 16] = dsc * static_cast<float>((v >> 4) - 8);
+      }
     }
   }
 }
