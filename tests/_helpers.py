@@ -59,3 +59,31 @@ def gpu_stream_bytes(L, side, seq, kvh):
 
 def tol(vmax):
     return 2e-3 * vmax
+
+
+def boundary_rows(codec, n_rows, rng):
+    """fp16 rows whose quotients x/d fall at or within a few fp32 ulps of the
+    encoder's rounding boundaries (half-integers for q8_0; half-integers, so
+    that u = x/d + 8.5 is near an integer, for q4_0).  Each 32-value block
+    keeps one value of the largest magnitude and fills the rest from the fp16
+    values whose quotient lies nearest such a boundary."""
+    f16 = np.arange(1 << 16, dtype=np.uint16).view(np.float16)
+    f16 = f16[np.isfinite(f16)].astype(np.float32)
+    rows = np.zeros((n_rows, 128), np.float32)
+    for r in range(n_rows):
+        for b in range(4):
+            amax = np.float32(rng.choice([1.0, 0.3, 7.5, 1e-3, 250.0])) * np.float32(rng.uniform(0.5, 2))
+            amax = np.float32(np.float16(amax))
+            sign = np.float32(rng.choice([-1.0, 1.0]))
+            if codec == 1:
+                d = np.float32(amax / np.float32(127))
+            else:
+                d = np.float32(sign * amax / np.float32(-8))
+            cand = f16[np.abs(f16) < amax]
+            t = (cand / d).astype(np.float32).astype(np.float64)
+            dist = np.abs(np.abs(t - np.floor(t)) - 0.5)
+            pick = cand[np.argsort(dist)[:48]]
+            blk = rng.choice(pick, 32)
+            blk[rng.integers(0, 32)] = sign * amax
+            rows[r, 32 * b:32 * b + 32] = blk
+    return rows.astype(np.float16)
