@@ -106,6 +106,12 @@ def _load():
                                           ctypes.c_int, ctypes.c_int, i32p, i32p, i32p,
                                           ctypes.c_int]
         lib.kvqo_num_threads.restype = ctypes.c_int
+        lib.kvqo_set_num_threads.argtypes = [ctypes.c_int]
+        lib.kvqo_set_num_threads.restype = ctypes.c_int
+        lib.kvqo_stream_absmax.argtypes = [ctypes.c_int, ctypes.c_int, u8p, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int64]
+        lib.kvqo_stream_absmax.restype = ctypes.c_double
         u64p = ctypes.POINTER(ctypes.c_uint64)
         lib.kvqo_splitmix64_next.argtypes = [u64p]
         lib.kvqo_splitmix64_next.restype = ctypes.c_uint64
@@ -133,6 +139,21 @@ def _as_half_bits(x) -> np.ndarray:
 
 def num_threads() -> int:
     return int(_load().kvqo_num_threads())
+
+
+class threads:
+    """Context manager: run the oracle's OpenMP regions on n threads."""
+
+    def __init__(self, n: int):
+        self.n = int(n)
+
+    def __enter__(self):
+        self.old = int(_load().kvqo_set_num_threads(self.n))
+        return self
+
+    def __exit__(self, *exc):
+        _load().kvqo_set_num_threads(self.old)
+        return False
 
 
 # --------------------------------------------------------------------------- fp16
@@ -245,6 +266,17 @@ def dequant_stream(codec: int, side: int, cache: np.ndarray, n_kv: int, capacity
     if rc:
         raise ValueError("oracle dequant failed")
     return out
+
+
+def stream_absmax(codec: int, side: int, cache: np.ndarray, n_kv: int, capacity: int,
+                  seq: int, kvh: int, n_tokens: int) -> float:
+    """max |x^| over the first n_tokens decoded rows of one stream."""
+    cache = np.ascontiguousarray(cache, dtype=np.uint8)
+    m = float(_load().kvqo_stream_absmax(codec, side, _ptr(cache, ctypes.c_uint8), n_kv,
+                                         capacity, seq, kvh, n_tokens))
+    if m < 0:
+        raise ValueError("oracle absmax failed")
+    return m
 
 
 # --------------------------------------------------------------------------- attention

@@ -563,7 +563,9 @@ static void kvqo_get_row(const uint8_t *stream, int codec, int side, int64_t pos
 /* Quantize-on-append for one side of one layer.
  * x_new: fp16 [n_seqs][max_new][n_kv][128]; row i < n_new[s] of sequence s
  * goes to token position seq_lens[s] + i.  Lengths are not updated here.
- * Returns 0, -1 on bad arguments or capacity overflow, -2 on non-finite input. */
+ * Returns 0, -1 on bad arguments or capacity overflow, -2 on non-finite input.
+ * Rows are independent (each has its own token position), so OpenMP spreads
+ * the rows of a sequence over threads; each row is encoded exactly as alone. */
 int kvqo_append_side(int codec, int side, uint8_t *cache, int n_seqs, int n_kv, int capacity,
                      const int32_t *seq_lens, const int32_t *n_new, int max_new,
                      const uint16_t *x_new)
@@ -571,37 +573,72 @@ int kvqo_append_side(int codec, int side, uint8_t *cache, int n_seqs, int n_kv, 
     int rb = kvqo_row_bytes(codec);
     if (rb < 0 || capacity % KVQO_UNIT_TOKENS)
         return -1;
-    uint8_t row[256];
-    for (int s = 0; s < n_seqs; ++s) {
+    for (int s = 0; s < n_seqs; ++s)
         if (n_new[s] < 0 || n_new[s] > max_new || seq_lens[s] < 0 ||
             (int64_t)seq_lens[s] + n_new[s] > capacity)
             return -1;
-        for (int i = 0; i < n_new[s]; ++i)
-            for (int h = 0; h < n_kv; ++h) {
-                const uint16_t *x = x_new + (((int64_t)s * max_new + i) * n_kv + h) * KVQO_D;
-                if (kvqo_encode_rows(codec, 1, x, row))
-                    return -2;
-                kvqo_put_row(kvqo_stream(cache, codec, n_kv, capacity, s, h), codec, side,
-                             (int64_t)seq_lens[s] + i, row);
+    int bad = 0;
+    for (int s = 0; s < n_seqs; ++s) {
+        int64_t n_rows = (int64_t)n_new[s] * n_kv;
+#pragma omp parallel for schedule(static)
+        for (int64_t ih = 0; ih < n_rows; ++ih) {
+            int64_t i = ih / n_kv;
+            int h = (int)(ih % n_kv);
+            uint8_t row[256];
+            const uint16_t *x = x_new + (((int64_t)s * max_new + i) * n_kv + h) * KVQO_D;
+            if (kvqo_encode_rows(codec, 1, x, row)) {
+#pragma omp atomic write
+                bad = 1;
+                continue;
             }
+            kvqo_put_row(kvqo_stream(cache, codec, n_kv, capacity, s, h), codec, side,
+                         (int64_t)seq_lens[s] + i, row);
+        }
+        if (bad)
+            return -2;
     }
     return 0;
 }
 
-/* Read tokens [0, n_tokens) of one (seq, kv_head) stream back as fp64 [n][128]. */
+/* Read tokens [0, n_tokens) of one (seq, kv_head) stream back as fp64 [n][128].
+ * Tokens are decoded independently (OpenMP over tokens when not nested). */
 int kvqo_dequant_stream(int codec, int side, const uint8_t *cache, int n_kv, int capacity,
                         int seq, int kvh, int64_t n_tokens, double *out)
 {
     int rb = kvqo_row_bytes(codec);
     if (rb < 0 || n_tokens > capacity)
         return -1;
-    uint8_t row[256];
     const uint8_t *st = kvqo_stream((uint8_t *)cache, codec, n_kv, capacity, seq, kvh);
+#pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < n_tokens; ++t) {
+        uint8_t row[256];
         kvqo_get_row(st, codec, side, t, row);
         kvqo_decode_rows(codec, 1, row, out + t * KVQO_D);
     }
     return 0;
+}
+
+/* max |x^| over tokens [0, n_tokens) of one stream (0 for an empty stream):
+ * the reference magnitude of the attention tolerance. */
+double kvqo_stream_absmax(int codec, int side, const uint8_t *cache, int n_kv, int capacity,
+                          int seq, int kvh, int64_t n_tokens)
+{
+    int rb = kvqo_row_bytes(codec);
+    if (rb < 0 || n_tokens > capacity)
+        return -1.0;
+    const uint8_t *st = kvqo_stream((uint8_t *)cache, codec, n_kv, capacity, seq, kvh);
+    double m = 0.0;
+#pragma omp parallel for schedule(static) reduction(max : m)
+    for (int64_t t = 0; t < n_tokens; ++t) {
+        uint8_t row[256];
+        double x[KVQO_D];
+        kvqo_get_row(st, codec, side, t, row);
+        kvqo_decode_rows(codec, 1, row, x);
+        for (int d = 0; d < KVQO_D; ++d)
+            if (fabs(x[d]) > m)
+                m = fabs(x[d]);
+    }
+    return m;
 }
 
 /* ------------------------------------------------------------------------ */
@@ -935,7 +972,12 @@ int kvqo_attend_rows(int n_rows, const uint16_t *q, int64_t T, const double *K, 
 /* Decode attention of one layer for a subset of (seq, kv_head) groups.
  * q: fp16 [n_seqs][n_q][128]; out fp64 [n_seqs][n_q][128]; lse fp64 [n_seqs][n_q].
  * Only groups with sel[seq * n_kv + kvh] != 0 are computed (sel may be NULL
- * for all).  Query head h reads kv head h / (n_q / n_kv). */
+ * for all).  Query head h reads kv head h / (n_q / n_kv).
+ * The selected groups are taken in batches of at most ~2^28 dequantized
+ * values: each batch's K and V streams are decoded (OpenMP over group and
+ * side), then every (group, query head) row is attended on its own (OpenMP
+ * over rows), each row in the fixed order of kvqo_attend_one. */
+#define KVQO_DECODE_BATCH_VALUES ((int64_t)1 << 28)
 int kvqo_decode_layer(int codec_k, int codec_v, const uint8_t *cache_k, const uint8_t *cache_v,
                       int n_seqs, int n_kv, int n_q, int capacity, const int32_t *seq_lens,
                       const uint16_t *q, double scale, const uint8_t *sel, double *out,
@@ -944,32 +986,88 @@ int kvqo_decode_layer(int codec_k, int codec_v, const uint8_t *cache_k, const ui
     if (n_kv <= 0 || n_q % n_kv)
         return -1;
     int G = n_q / n_kv;
-    for (int s = 0; s < n_seqs; ++s)
-        for (int h = 0; h < n_kv; ++h) {
-            if (sel && !sel[s * n_kv + h])
-                continue;
-            int64_t T = seq_lens[s];
-            if (T < 0 || T > capacity)
-                return -1;
-            double *K = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
-            double *V = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
-            int64_t *lim = (int64_t *)malloc(sizeof(int64_t) * (size_t)G);
-            if (!K || !V || !lim) {
-                free(K); free(V); free(lim);
-                return -1;
-            }
-            kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, s, h, T, K);
-            kvqo_dequant_stream(codec_v, KVQO_SIDE_V, cache_v, n_kv, capacity, s, h, T, V);
-            for (int j = 0; j < G; ++j)
-                lim[j] = T;
-            int64_t row0 = (int64_t)s * n_q + (int64_t)h * G;
-            int rc = kvqo_attend_rows(G, q + row0 * KVQO_D, T, K, V, lim, scale,
-                                      out + row0 * KVQO_D, lse + row0);
-            free(K); free(V); free(lim);
-            if (rc)
-                return rc;
+    int n_groups = n_seqs * n_kv;
+    int *grp = (int *)malloc(sizeof(int) * (size_t)(n_groups > 0 ? n_groups : 1));
+    double **kv = (double **)calloc((size_t)(2 * (n_groups > 0 ? n_groups : 1)), sizeof(double *));
+    if (!grp || !kv) {
+        free(grp); free(kv);
+        return -1;
+    }
+    int n_sel = 0;
+    for (int gi = 0; gi < n_groups; ++gi) {
+        if (sel && !sel[gi])
+            continue;
+        int s = gi / n_kv;
+        if (seq_lens[s] < 0 || seq_lens[s] > capacity) {
+            free(grp); free(kv);
+            return -1;
         }
-    return 0;
+        grp[n_sel++] = gi;
+    }
+    int rc = 0;
+    for (int b0 = 0; b0 < n_sel && !rc;) {
+        /* this batch: groups b0 .. b1 - 1 */
+        int b1 = b0;
+        int64_t vals = 0;
+        while (b1 < n_sel) {
+            int64_t T = seq_lens[grp[b1] / n_kv];
+            if (b1 > b0 && vals + 2 * T * KVQO_D > KVQO_DECODE_BATCH_VALUES)
+                break;
+            vals += 2 * T * KVQO_D;
+            ++b1;
+        }
+        int nb = b1 - b0, bad = 0;
+        for (int j = 0; j < 2 * nb; ++j) {
+            int64_t T = seq_lens[grp[b0 + j / 2] / n_kv];
+            kv[j] = (double *)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1) * KVQO_D);
+            if (!kv[j])
+                bad = 1;
+        }
+        if (!bad) {
+#pragma omp parallel for schedule(dynamic, 1)
+            for (int j = 0; j < 2 * nb; ++j) {
+                int gi = grp[b0 + j / 2], s = gi / n_kv, h = gi % n_kv;
+                if (j % 2 == 0)
+                    kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, s, h,
+                                        seq_lens[s], kv[j]);
+                else
+                    kvqo_dequant_stream(codec_v, KVQO_SIDE_V, cache_v, n_kv, capacity, s, h,
+                                        seq_lens[s], kv[j]);
+            }
+#pragma omp parallel
+            {
+                int64_t Tmax = 1;
+                for (int j = 0; j < nb; ++j)
+                    if (seq_lens[grp[b0 + j] / n_kv] > Tmax)
+                        Tmax = seq_lens[grp[b0 + j] / n_kv];
+                double *s_buf = (double *)malloc(sizeof(double) * (size_t)Tmax);
+#pragma omp for schedule(dynamic, 1)
+                for (int jr = 0; jr < nb * G; ++jr) {
+                    if (!s_buf) {
+#pragma omp atomic write
+                        bad = 1;
+                        continue;
+                    }
+                    int j = jr / G, r = jr % G;
+                    int gi = grp[b0 + j], s = gi / n_kv, h = gi % n_kv;
+                    int64_t row = (int64_t)s * n_q + (int64_t)h * G + r;
+                    kvqo_attend_one(q + row * KVQO_D, kv[2 * j], kv[2 * j + 1], seq_lens[s], scale,
+                                    s_buf, out + row * KVQO_D, lse + row);
+                }
+                free(s_buf);
+            }
+        }
+        for (int j = 0; j < 2 * nb; ++j) {
+            free(kv[j]);
+            kv[j] = NULL;
+        }
+        if (bad)
+            rc = -1;
+        b0 = b1;
+    }
+    free(grp);
+    free(kv);
+    return rc;
 }
 
 /* Causal attention of one prefill chunk of sequence `seq`: query i (absolute
@@ -1036,6 +1134,21 @@ int kvqo_num_threads(void)
 #ifdef _OPENMP
     return omp_get_max_threads();
 #else
+    return 1;
+#endif
+}
+
+/* Threads of the following OpenMP regions (n >= 1); returns the previous
+ * count.  Used to time the oracle single-threaded and on all cores. */
+int kvqo_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    int old = omp_get_max_threads();
+    if (n >= 1)
+        omp_set_num_threads(n);
+    return old;
+#else
+    (void)n;
     return 1;
 #endif
 }

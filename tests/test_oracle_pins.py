@@ -747,3 +747,174 @@ def test_turbo4_attention_equals_attention_over_decoded_rows():
     for t in range(T):
         assert float(q[0, 0].astype(np.float64) @ K[t]) == pytest.approx(
             float(qr @ oracle.turbo4_rotated(rows[t])), rel=1e-12, abs=1e-12)
+
+
+# ---------------------------------------------------------------- q4_0 decoder, by hand
+
+def _q4_0_row_by_hand():
+    """One canonical q4_0 row (four 18-byte blocks) and its values worked out
+    by hand from x^ = d16 * (q - 8), low nibble = element j, high nibble =
+    element j + 16 (byte layout of the q4_0 row of the "Codecs" table's
+    4.5-bit format: fp16 scale, then 16 bytes of two nibbles each)."""
+    row, want = [], []
+    # block 0: d16 = 0x3C00 (1.0); byte j = j | (15 - j) << 4
+    row += [0x00, 0x3C] + [j | ((15 - j) << 4) for j in range(16)]
+    want += [j - 8.0 for j in range(16)] + [7.0 - j for j in range(16)]
+    # block 1: d16 = 0xB000 (-0.125); every byte 0x0F: low nibble 15, high 0
+    row += [0x00, 0xB0] + [0x0F] * 16
+    want += [-0.125 * 7] * 16 + [-0.125 * -8] * 16
+    # block 2: d16 = 0x4000 (2.0); every byte 0x88: both nibbles 8 -> 0
+    row += [0x00, 0x40] + [0x88] * 16
+    want += [0.0] * 32
+    # block 3: d16 = 0x0001 (2^-24, the smallest subnormal); bytes 0xF0, 0x1E
+    row += [0x01, 0x00] + [0xF0, 0x1E] * 8
+    lo = [0 - 8, 14 - 8] * 8
+    hi = [15 - 8, 1 - 8] * 8
+    want += [v * 2.0 ** -24 for v in lo] + [v * 2.0 ** -24 for v in hi]
+    return np.array(row, np.uint8), np.array(want, np.float64)
+
+
+def test_q4_0_decoder_hand_derived_values():
+    row, want = _q4_0_row_by_hand()
+    assert row.size == 72
+    got = oracle.decode_rows(oracle.Q4_0, row)[0]
+    assert np.array_equal(got, want)
+    # a swapped nibble order or 8 - q instead of q - 8 moves these values
+    assert got[0] == -8.0 and got[16] == 7.0 and got[32] == -0.875 and got[48] == 1.0
+
+
+@pytest.mark.parametrize("side", [0, 1])
+def test_q4_0_dequant_stream_hand_derived_values(side):
+    """The same row placed at token 21 of a stream (unit 1, row 5) by the
+    layout's offsets and read back through the stream dequantizer."""
+    row, want = _q4_0_row_by_hand()
+    cap = 256
+    cache = np.zeros(oracle.cache_bytes(oracle.Q4_0, 1, 1, cap), np.uint8)
+    unit = cache[16 * 72:32 * 72]
+    for cb in range(72):
+        unit[oracle.unit_offset(oracle.Q4_0, side, 5, cb)] = row[cb]
+    got = oracle.dequant_stream(oracle.Q4_0, side, cache, 1, cap, 0, 0, 22)
+    assert np.array_equal(got[21], want)
+    # every other row of the stream decodes from zero bytes: d16 = 0
+    assert not np.any(got[:21])
+
+
+# ---------------------------------------------------------------- unit layout, by hand
+
+# (codec, side, token row r, canonical byte cb, unit offset), each worked out
+# by hand from the placement formulas of the library's public header
+# (g = r & 7, rh = r >> 3, tig = (r & 7) >> 1, par = r & 1):
+_UNIT_OFFSETS_BY_HAND = [
+    # f16 K: d = cb >> 1, k = cb & 1; b=d>>5 h=(d>>4)&1 w=(d>>2)&3 i=d&3
+    #        -> (2b+rh)*512 + (4g+w)*16 + h*8 + i*2 + k
+    (0, 0, 0, 0, 0),
+    (0, 0, 11, 154, 2802),   # d 77: b2 h0 w3 i1; g3 rh1 -> 5*512 + 15*16 + 2
+    (0, 0, 5, 45, 349),      # d 22 k1: b0 h1 w1 i2; g5 -> 21*16 + 8 + 4 + 1
+    (0, 0, 15, 255, 4095),   # the unit's last byte
+    # f16 V: mt=d>>4 gq=(d&15)>>1 s=d&1 -> mt*512 + (4gq+tig)*16 + (rh*4+s*2+par)*2 + k
+    (0, 1, 11, 154, 2462),   # d 77: mt4 gq6 s1; tig1 par1 rh1 -> 2048 + 25*16 + 7*2
+    (0, 1, 6, 11, 181),      # d 5 k1: mt0 gq2 s1; tig3 par0 -> 11*16 + 2*2 + 1
+    (0, 1, 15, 255, 4095),
+    # q8_0 K: b = cb // 34, o = cb % 34; scale byte o < 2 -> 2048 + g*16 + rh*8 + b*2 + o;
+    #         quant e = o - 2: h=e>>4 w=(e>>2)&3 i=e&3 -> b*512 + (4g+w)*16 + (2rh+h)*4 + i
+    (1, 0, 0, 0, 2048),
+    (1, 0, 9, 35, 2075),     # block 1 scale byte 1; g1 rh1 -> 2048 + 16 + 8 + 2 + 1
+    (1, 0, 9, 91, 1117),     # block 2, e 21: h1 w1 i1 -> 1024 + 5*16 + 3*4 + 1
+    (1, 0, 15, 135, 2047),   # block 3, e 31 -> 1536 + 31*16 + 3*4 + 3
+    (1, 0, 15, 103, 2175),   # block 3 scale byte 1: the unit's last byte
+    # q8_0 V: quant of dim d = 32b + e: mt=d>>4 gq=(d&15)>>1 s=d&1
+    #         -> (mt>>1)*512 + (4gq+tig)*16 + ((mt&1)*2+rh)*4 + par*2 + s;
+    #         scale byte k -> 2048 + tig*32 + b*8 + rh*4 + par*2 + k
+    (1, 1, 0, 2, 0),
+    (1, 1, 11, 91, 1183),    # d 85: mt5 gq2 s1; tig1 par1 rh1 -> 1024 + 9*16 + 3*4 + 3
+    (1, 1, 11, 35, 2095),    # block 1 scale byte 1 -> 2048 + 32 + 8 + 4 + 2 + 1
+    (1, 1, 14, 1, 2149),     # block 0 scale byte 1; tig3 par0 rh1 -> 2048 + 96 + 4 + 1
+    (1, 1, 15, 103, 2175),
+    # q4_0 K: b = cb // 18, o = cb % 18; scale -> 1024 + g*16 + rh*8 + b*2 + o;
+    #         byte jc = o - 2: w=jc>>2 i=jc&3 -> (b>>1)*512 + (4g+w)*16 + ((b&1)*2+rh)*4 + i
+    (2, 0, 0, 2, 0),
+    (2, 0, 13, 70, 894),     # block 3 jc 14: w3 i2; g5 rh1 -> 512 + 23*16 + 3*4 + 2
+    (2, 0, 13, 19, 1115),    # block 1 scale byte 1 -> 1024 + 80 + 8 + 2 + 1
+    (2, 0, 2, 43, 657),      # block 2 jc 5: w1 i1; g2 rh0 -> 512 + 9*16 + 1
+    (2, 0, 15, 71, 1023),
+    # q4_0 V: byte jc of block b: mt=2b+(jc>>3) gq=jc&7
+    #         -> (mt>>2)*512 + (4gq+tig)*16 + (mt&3)*4 + par*2 + rh;
+    #         scale byte k -> 1024 + tig*32 + b*8 + rh*4 + par*2 + k
+    (2, 1, 0, 2, 0),
+    (2, 1, 13, 70, 943),     # block 3 jc 14: mt7 gq6; tig2 par1 rh1 -> 512 + 26*16 + 12 + 2 + 1
+    (2, 1, 13, 19, 1103),    # block 1 scale byte 1 -> 1024 + 64 + 8 + 4 + 2 + 1
+    (2, 1, 4, 29, 108),      # block 1 jc 9: mt3 gq1; tig2 par0 rh0 -> 6*16 + 3*4
+    (2, 1, 15, 71, 1023),
+    # turbo4: scale bytes cb < 2 (K: 1024 + g*4 + rh*2 + cb; V: 1024 + tig*8 + rh*4 + par*2 + cb);
+    #         group byte cb = 2 + 16b + jc sits at q4_0's place of byte jc of block b
+    (3, 0, 13, 1, 1047),     # g5 rh1 -> 1024 + 20 + 2 + 1
+    (3, 0, 13, 64, 894),     # group 3 byte 14: as the q4_0 K case above
+    (3, 0, 15, 1, 1055),     # the unit's last byte (1056 bytes)
+    (3, 1, 13, 0, 1046),     # tig2 rh1 par1 -> 1024 + 16 + 4 + 2
+    (3, 1, 13, 64, 943),     # as the q4_0 V case above
+]
+
+
+@pytest.mark.parametrize("codec,side,r,cb,want", _UNIT_OFFSETS_BY_HAND)
+def test_unit_offset_hand_worked_examples(codec, side, r, cb, want):
+    assert oracle.unit_offset(codec, side, r, cb) == want
+
+
+# ---------------------------------------------------------------- threading does not change results
+
+def test_decode_layer_is_identical_on_one_thread_and_on_all():
+    """Rows are attended independently in a fixed order, so the thread count
+    and the batching of groups change nothing, bit for bit."""
+    rng = np.random.default_rng(77)
+    n_seqs, n_kv, n_q, cap = 3, 2, 6, 512
+    lens = [300, 0, 511]
+    caches = []
+    for side, codec in ((0, oracle.Q4_0), (1, oracle.Q8_0)):
+        c = np.zeros(oracle.cache_bytes(codec, n_seqs, n_kv, cap), np.uint8)
+        x = rng.standard_normal((n_seqs, max(lens), n_kv, 128)).astype(np.float16)
+        oracle.append_side(codec, side, c, n_seqs, n_kv, cap, [0] * n_seqs, lens, x)
+        caches.append(c)
+    q = rng.standard_normal((n_seqs, n_q, 128)).astype(np.float16)
+    with oracle.threads(1):
+        o1, l1 = oracle.decode_layer(oracle.Q4_0, oracle.Q8_0, *caches, n_seqs, n_kv, n_q, cap,
+                                     lens, q, 0.088)
+    on, ln = oracle.decode_layer(oracle.Q4_0, oracle.Q8_0, *caches, n_seqs, n_kv, n_q, cap,
+                                 lens, q, 0.088)
+    assert np.array_equal(o1, on) and np.array_equal(l1, ln)
+    # one group at a time gives the same rows
+    for s in range(n_seqs):
+        for h in range(n_kv):
+            sel = np.zeros((n_seqs, n_kv), bool)
+            sel[s, h] = True
+            og, lg = oracle.decode_layer(oracle.Q4_0, oracle.Q8_0, *caches, n_seqs, n_kv, n_q,
+                                         cap, lens, q, 0.088, sel=sel)
+            rows = slice(h * 3, h * 3 + 3)
+            assert np.array_equal(og[s, rows], on[s, rows])
+            assert np.array_equal(lg[s, rows], ln[s, rows])
+    assert np.all(on[1] == 0) and np.all(ln[1] == -np.inf)
+
+
+def test_stream_absmax_is_the_largest_decoded_magnitude():
+    rng = np.random.default_rng(78)
+    cap = 256
+    for side, codec in ((0, oracle.F16), (1, oracle.Q8_0), (1, oracle.Q4_0), (0, oracle.TURBO4)):
+        c = np.zeros(oracle.cache_bytes(codec, 1, 2, cap), np.uint8)
+        x = (rng.standard_normal((1, 200, 2, 128)) * 3).astype(np.float16)
+        oracle.append_side(codec, side, c, 1, 2, cap, [0], [200], x)
+        for h in range(2):
+            want = np.abs(oracle.dequant_stream(codec, side, c, 2, cap, 0, h, 200)).max()
+            assert oracle.stream_absmax(codec, side, c, 2, cap, 0, h, 200) == want
+        assert oracle.stream_absmax(codec, side, c, 2, cap, 0, 1, 0) == 0.0
+
+
+def test_append_is_identical_on_one_thread_and_on_all():
+    rng = np.random.default_rng(79)
+    cap = 512
+    x = rng.standard_normal((2, 400, 3, 128)).astype(np.float16)
+    for codec in (0, 1, 2, 3):
+        a = np.zeros(oracle.cache_bytes(codec, 2, 3, cap), np.uint8)
+        b = np.zeros_like(a)
+        with oracle.threads(1):
+            oracle.append_side(codec, 1, a, 2, 3, cap, [5, 0], [395, 400], x)
+        oracle.append_side(codec, 1, b, 2, 3, cap, [5, 0], [395, 400], x)
+        assert np.array_equal(a, b)
