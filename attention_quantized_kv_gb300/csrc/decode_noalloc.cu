@@ -16,10 +16,10 @@
 //    cudaGetSymbolAddress (with that device current) and caches it; make that
 //    first call before any stream capture begins.
 //  * Every call shares the one array and it keeps what the previous call left
-//    there; the arrival counters are cleared (cudaMemsetAsync on the call's
-//    stream) before each launch.  Calls that may overlap on the GPU -- on
-//    different streams or from different host threads without ordering --
-//    race on the array and must not be issued.
+//    there; its counter region (the first 64 KiB) is cleared (cudaMemsetAsync
+//    on the call's stream) before each launch.  Calls that may overlap on the
+//    GPU -- on different streams or from different host threads without
+//    ordering -- race on the array and must not be issued.
 //  * A layer whose decode scratch (attn_decode_workspace) exceeds the array is
 //    refused with KVQ_EWORKSPACE before anything is launched.
 //  * Nothing here allocates: no cudaMalloc, cudaFree or allocating library call.
@@ -29,6 +29,7 @@
 #include <stdint.h>
 
 #include "../../include/kvq.h"
+#include "kvq_check.h"
 #include "kvq_launch.h"
 
 namespace {
@@ -62,39 +63,15 @@ int scratch_for_current_device(void **addr, int *sms) {
   return KVQ_OK;
 }
 
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
 }  // namespace
 
 extern "C" {
 
 int attn_decode_noalloc(const kvq_layer *L, const void *q, float scale, void *out, float *lse,
                         int32_t max_len, void *stream) {
-  // Argument checks (the same rules as attn_decode).
-  if (!L) return KVQ_EINVAL;
-  if (L->head_dim != 128) return KVQ_EUNSUPPORTED;
-  const bool codecs_ok = L->codec_k >= KVQ_F16 && L->codec_k <= KVQ_TURBO4 &&
-                         L->codec_v >= KVQ_F16 && L->codec_v <= KVQ_TURBO4;
-  if (!codecs_ok) return KVQ_EUNSUPPORTED;
-  if (L->n_seqs <= 0 || L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->capacity <= 0 ||
-      L->reserved != 0 || L->n_q_heads % L->n_kv_heads != 0)
-    return KVQ_EINVAL;
-  if (!L->k_cache || !L->v_cache || !L->seq_lens || !q || !out || max_len <= 0)
-    return KVQ_EINVAL;
-  if (L->capacity % 256 != 0) return KVQ_EALIGN;
-  if (L->pages_per_seq < 0) return KVQ_EINVAL;
-  if (L->pages_per_seq > 0 &&
-      (!L->block_table || L->n_pages <= 0 ||
-       static_cast<int64_t>(L->pages_per_seq) * 256 != L->capacity))
-    return KVQ_EINVAL;
-  if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16) || !aligned(L->seq_lens, 4) ||
-      (L->err && !aligned(L->err, 4)) || !aligned(q, 8) || !aligned(out, 8) ||
-      (lse && !aligned(lse, 4)))
-    return KVQ_EALIGN;
-  if (max_len > L->capacity) return KVQ_ECAPACITY;
-  const int64_t G = L->n_q_heads / L->n_kv_heads;
-  const int64_t streams = static_cast<int64_t>(L->n_seqs) * L->n_kv_heads * ((G + 7) / 8);
-  if (L->n_seqs > kvq::kDecodeMaxSeqs || streams > kvq::kDecodeMaxStreams) return KVQ_EINVAL;
+  // Argument checks: the same function attn_decode uses.
+  const int chk = kvq::check_decode_call(L, q, out, lse, max_len);
+  if (chk != KVQ_OK) return chk;
 
   void *scratch = nullptr;
   int sms = 0;
@@ -104,8 +81,11 @@ int attn_decode_noalloc(const kvq_layer *L, const void *q, float scale, void *ou
   if (pl.ws_bytes > static_cast<int64_t>(kNoAllocScratchBytes)) return KVQ_EWORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The per-stream arrival counters must start at zero.
-  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(streams) * 4, s) != cudaSuccess)
+  // The whole counter region at the start of the scratch (the per-stream
+  // arrival counters and the lengths-read counter of the fused step) must
+  // start at zero; the previous call may have left anything there.
+  if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(kvq::kDecodeTicketBytes), s) !=
+      cudaSuccess)
     return KVQ_ECUDA;
   const cudaError_t e = kvq::launch_decode(*L, pl, q, scale, out, lse, max_len, scratch, s);
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;

@@ -6,40 +6,16 @@
 #include <stdint.h>
 
 #include "../../include/kvq.h"
+#include "kvq_check.h"
 #include "kvq_launch.h"
 
 namespace {
 
-constexpr int kHeadDim = 128;
-
-bool valid_codec(int c) {
-  return c == KVQ_F16 || c == KVQ_Q8_0 || c == KVQ_Q4_0 || c == KVQ_TURBO4;
-}
-
-bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-int check_layer(const kvq_layer *L) {
-  if (!L) return KVQ_EINVAL;
-  if (L->head_dim != kHeadDim) return KVQ_EUNSUPPORTED;
-  if (!valid_codec(L->codec_k) || !valid_codec(L->codec_v)) return KVQ_EUNSUPPORTED;
-  if (L->n_seqs <= 0 || L->n_kv_heads <= 0 || L->n_q_heads <= 0 || L->capacity <= 0 ||
-      L->reserved != 0)
-    return KVQ_EINVAL;
-  if (L->n_q_heads % L->n_kv_heads != 0) return KVQ_EINVAL;
-  if (!L->k_cache || !L->v_cache || !L->seq_lens) return KVQ_EINVAL;
-  if (L->capacity % 256 != 0) return KVQ_EALIGN;
-  if (L->pages_per_seq < 0) return KVQ_EINVAL;
-  if (L->pages_per_seq > 0) {  // paged: a block table over pools of n_pages pages
-    if (!L->block_table || L->n_pages <= 0) return KVQ_EINVAL;
-    if (static_cast<int64_t>(L->pages_per_seq) * 256 != L->capacity) return KVQ_EINVAL;
-    if (!aligned(L->block_table, 4)) return KVQ_EALIGN;
-  }
-  if (!aligned(L->k_cache, 16) || !aligned(L->v_cache, 16) || !aligned(L->seq_lens, 4) ||
-      (L->err && !aligned(L->err, 4)))
-    return KVQ_EALIGN;
-  // every byte offset must fit in int64 (it always does for int32 geometry)
-  return KVQ_OK;
-}
+using kvq::aligned;
+using kvq::check_layer;
+using kvq::decode_shape_ok;
+using kvq::kHeadDim;
+using kvq::valid_codec;
 
 int device_sms() {
   static int cached[64] = {0};
@@ -104,13 +80,6 @@ int kv_append_quantize(const kvq_layer *layer, const void *k_new, const void *v_
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 
-// Decode streams: (sequence, kv head, group of up to 8 query heads).
-static bool decode_shape_ok(const kvq_layer *L) {
-  const int64_t G = L->n_q_heads / L->n_kv_heads;
-  const int64_t streams = static_cast<int64_t>(L->n_seqs) * L->n_kv_heads * ((G + 7) / 8);
-  return L->n_seqs <= kvq::kDecodeMaxSeqs && streams <= kvq::kDecodeMaxStreams;
-}
-
 int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes) {
   int st = check_layer(layer);
   if (st != KVQ_OK) return st;
@@ -125,12 +94,8 @@ int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes
 
 int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
                 int32_t max_len, void *workspace, size_t ws_bytes, void *stream) {
-  int st = check_layer(layer);
+  const int st = kvq::check_decode_call(layer, q, out, lse, max_len);
   if (st != KVQ_OK) return st;
-  if (!q || !out || max_len <= 0) return KVQ_EINVAL;
-  if (!decode_shape_ok(layer)) return KVQ_EINVAL;
-  if (max_len > layer->capacity) return KVQ_ECAPACITY;
-  if (!aligned(q, 8) || !aligned(out, 8) || (lse && !aligned(lse, 4))) return KVQ_EALIGN;
   if (!workspace) return KVQ_EWORKSPACE;
   if (!aligned(workspace, 16)) return KVQ_EALIGN;
   const int sms = device_sms();

@@ -14,17 +14,29 @@
 //     (two 64-dim halves of 128 rows x 128 bytes, 128-byte swizzle), so that
 //     the attention kernel moves each tile with one 32 KB bulk async copy.
 //     Each key is dequantized once per chunk, not once per query block.
-//  2. prefill_attn: one CTA per (128-query block, query head).  Warp 0 streams
-//     K and V tiles into a two-stage ring (bulk copies, mbarriers).  One
-//     thread of warp 1 issues tcgen05.mma: S = Q K^T (M=128 queries, N=128
-//     keys, K=128 dims, fp16 in, fp32 accumulate) into one of two TMEM
-//     buffers, then O += P V with P (fp16) read from TMEM and O accumulated
-//     in TMEM.  Warps 4..7 (a warpgroup, one query row per thread) run the
-//     online softmax in the log2 domain: tcgen05.ld of the S row, causal
-//     mask, row max, exp2, row sum, tcgen05.st of P over the S columns.  The
-//     running max used for P is only raised (and O, l rescaled) when a row's
-//     max grows by more than 2^8, which keeps O rescales rare and the result
-//     exact (the same max scales O and l).
+//  2. prefill_attn: persistent CTAs, one per SM.  A work item is (kv head,
+//     pair of its query heads, 128-query tile); both heads read the same K/V
+//     tiles.  An item is a run of key-tile steps (one per 128-key tile its
+//     queries attend), and each CTA takes an equal contiguous slice of all
+//     steps in (kv head, pair, query tile) order: whole items plus pieces of
+//     at most two more.  A piece writes its rows as partials (unnormalised O,
+//     max, sum); the last CTA to finish a piece of the item (an atomic
+//     ticket) merges the pieces by log-sum-exp.  Roles (12 warps): warps 0-3
+//     and 4-7 are the softmax warpgroups of the pair's two heads (one query
+//     row per thread, TMEM lane quadrant = warp % 4); warp 8 is the
+//     producer, streaming K and V tiles into a two-stage ring by bulk async
+//     copies on mbarriers; one thread of warp 9 issues tcgen05.mma: S_e =
+//     Q_e K^T (M = 128 queries, N = 128 keys, K = 128 dims, fp16 in, fp32
+//     accumulate) into head e's TMEM columns, then O_e += P_e V with P_e
+//     (fp16) read from TMEM and O_e accumulated in TMEM; warps 10-11 are
+//     idle (registers go to a CTA in groups of four warps).  MMAs are issued
+//     S0 S1 PV0 S0' PV1 S1' ..., so each head's softmax overlaps the tensor
+//     core's work for the other head.  The softmax runs in the log2 domain in
+//     two passes over the S row in TMEM (row max with the causal mask, then
+//     exp2, row sum and tcgen05.st of P over the S columns).  The running max
+//     used for P is only raised (and O, l rescaled) when a row's max grows by
+//     more than 2^8, which keeps O rescales rare and the result exact (the
+//     same max scales O and l).
 #include <cuda_runtime.h>
 
 #include <algorithm>

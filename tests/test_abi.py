@@ -153,3 +153,25 @@ def test_fused_decode_step_argument_validation(lib):
     assert call(q=0x400002) == 4
     assert call(ws=None) == 5
     assert call(ws=0x600008) == 4
+
+
+def test_paged_block_table_alignment_is_checked_by_every_decode_entry(lib):
+    """A paged layer whose block table is not 4-byte aligned is refused on the
+    host (KVQ_EALIGN) by attn_decode and attn_decode_noalloc alike: both run
+    the same validation before any device call."""
+    d = _layer(pages_per_seq=16, n_pages=40, block_table=0x700002)
+    assert lib.attn_decode(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 16, 0x600000,
+                           1 << 20, None) == 4
+    assert lib.attn_decode_noalloc(ctypes.byref(d), 0x400000, 0.1, 0x500000, None, 16,
+                                   None) == 4
+    # the no-alloc entry point rejects the other bad arguments attn_decode rejects
+    for kw, status in [(dict(head_dim=64), 2), (dict(capacity=1000), 4),
+                       (dict(pages_per_seq=16, n_pages=0, block_table=0x700000), 1),
+                       (dict(n_q_heads=7), 1)]:
+        dd = _layer(**kw)
+        assert lib.attn_decode_noalloc(ctypes.byref(dd), 0x400000, 0.1, 0x500000, None, 16,
+                                       None) == status, kw
+    assert lib.attn_decode_noalloc(ctypes.byref(_layer()), 0x400002, 0.1, 0x500000, None, 16,
+                                   None) == 4
+    assert lib.attn_decode_noalloc(ctypes.byref(_layer()), 0x400000, 0.1, 0x500000, None, 5000,
+                                   None) == 3
