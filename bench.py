@@ -2,26 +2,31 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one pass of the whole hot path over one batch of synthetic input:
-for the default workload (32 query / 8 KV heads, 32768 cached q4_0 keys with
-outlier channels) that is: quantize-append one new K/V token, then decode
-attention of all 32 query heads over the 32769 keys.  The cache is built
-(untimed) through the same append kernel.  Inputs are resident in HBM when the
-timed region starts; L2 is flushed (a 2 x L2-size write) before every timed
+A step is one pass of the whole hot path over one batch of synthetic input.
+The default workload is the 16-layer decode step: 2 sequences x 200704
+cached keys, 32 query / 4 KV heads, each layer's K and V codec drawn from
+the f16 / q8_0 / q4_0 ladder; a step is the decode attention call of every
+layer (other workloads add the append of the step's new tokens, a prefill
+chunk, a re-encode or an eviction step).  Caches are built (untimed) through
+the library's append kernel.  Inputs are resident in HBM when the timed
+region starts; L2 is flushed (2 x L2 written, then read) before every timed
 step.  Timing: CUDA events on the launching stream around each step, W
 warm-up steps, K timed steps, barrier + synchronize on both sides, max over
 ranks.  ``value`` is the whole-job effective bandwidth: algorithmic bytes
-(every attended K/V row read once, q read, out written, the appended rows
-read and written) divided by the step time.
+(every attended K/V row read once, q read, out written, appended rows read
+and written) divided by the step time; ``us_per_layer_step`` is the step
+time over the layers, and ``per_layer`` the time of each layer's call in a
+replay of its own, with the mean per (K codec, V codec) pair.
 
 Also reported: ``e2e`` (the same metric through the C ABI with pinned host
-buffers: per step the H2D copy of q and the new K/V rows, the kernels, and the
-D2H copy of the output), ``roofline`` for the decode kernels, the SM clock
+buffers: per step the H2D copy of q (and new K/V rows), the kernels, and the
+D2H copy of the output), ``roofline`` for the dominant kernel, the SM clock
 record of the timed region, and ``cpu_baseline``: the fp64 C oracle timed on
-this host's cores on a bounded sample of the same workload.
+this host's cores on a bounded sample of the same workload, on all cores and
+on one thread.
 
 ``--impl reference`` times that oracle alone (the reference arm) on the same
-workload, metric and unit.
+workload, metric and unit, without building or loading the CUDA library.
 """
 from __future__ import annotations
 
@@ -40,7 +45,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "quantized-KV attention: effective HBM GB/s, % of peak, µs per layer-step"
-DEFAULT_WORKLOAD = "append_decode_q4_ctx32k"
+DEFAULT_WORKLOAD = "decode_16layer_ladder_2x200704"
 ROW = {0: 256, 1: 136, 2: 72, 3: 66}
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
@@ -90,8 +95,7 @@ def step_work(w, fused=None):
     for ck, cv in w.codecs:
         app = w.n_seqs * w.append_new * w.n_kv * (2 * 256 + ROW[ck] + ROW[cv])
         if w.kind == "evict":
-            from attention_quantized_kv_gb300 import workloads as wl
-            dec, probe, sel, comp = evict_work(w, lens, wl.n_evicted(w), ck, cv)
+            dec, probe, sel, comp = evict_work(w, lens, _workloads().n_evicted(w), ck, cv)
             per_layer.append(comp)
             total_b += dec + probe + sel + comp + app
             total_f += sum(lens) * w.n_q * 4 * 128 + sum(lens) * w.n_q * 2 * 128
@@ -374,6 +378,18 @@ def _kernel_source_hash(kind):
     return h.hexdigest()[:16]
 
 
+def workload_config(w, world, l2, timing):
+    """The line's config: the workload's shape (the same keys on both arms)
+    plus how this arm was timed."""
+    return {"workload": w.name, "description": w.description, "n_seqs": w.n_seqs,
+            "n_q_heads": w.n_q, "n_kv_heads": w.n_kv, "head_dim": 128,
+            "context": w.final_lens() if w.n_seqs <= 2 else
+            {"sum": sum(w.final_lens()), "min": min(w.final_lens()), "max": max(w.final_lens())},
+            "layers": w.n_layers,
+            "codecs": [[["f16", "q8_0", "q4_0", "turbo4"][c] for c in p] for p in w.codecs],
+            "l2": l2, "timing": timing, "parallelism": f"replicas x{world}"}
+
+
 def reduce_max(dist, vals, device):
     """The per-rank timings reduced to their maximum over ranks (the job is as
     slow as its slowest replica); unchanged without a process group."""
@@ -425,6 +441,14 @@ def run_ours(args, w, rank, world, dist):
     with torch.cuda.graph(g_attn):
         for l in range(n_layers):
             arm.roofline_calls(l)
+    # each layer's call alone (per-layer and per-codec-pair times)
+    g_layer = []
+    if n_layers > 1:
+        for l in range(n_layers):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                arm.roofline_calls(l)
+            g_layer.append(g)
     torch.cuda.synchronize()
     mode = ("one CUDA graph replay per step, events outside it; "
             + ("compaction kernels" if w.kind == "evict" else "attention kernels")
@@ -470,6 +494,7 @@ def run_ours(args, w, rank, world, dist):
 
     step_ms = timed(g_step, arm.reset)
     attn_ms = timed(g_attn, arm.reset if arm.fused else arm.set_final_lens)
+    layer_ms = [timed(g, arm.reset if arm.fused else arm.set_final_lens) for g in g_layer]
     torch.cuda.synchronize()
     clocks = clk.stop()
     if dist:
@@ -560,18 +585,12 @@ def run_ours(args, w, rank, world, dist):
         "vs_baseline": None,
         "dtype": "f16 in / fp32 accumulate over q8_0/q4_0/f16 KV",
         "data": "synthetic (seeded N(0,1) fp16 draws, cache built by the append kernel)",
-        "config": {"workload": w.name, "description": w.description, "n_seqs": w.n_seqs,
-                   "n_q_heads": w.n_q, "n_kv_heads": w.n_kv, "head_dim": 128,
-                   "context": w.final_lens() if w.n_seqs <= 2 else
-                   {"sum": sum(w.final_lens()), "min": min(w.final_lens()),
-                    "max": max(w.final_lens())},
-                   "layers": n_layers,
-                   "codecs": [[["f16", "q8_0", "q4_0", "turbo4"][c] for c in p] for p in w.codecs],
-                   "l2": ("not flushed: warm L2 (the step's data left there by the previous step)"
-                          if args.warm else
-                          "flushed before every timed step (2 x L2 write, then 2 x L2 read)"),
-                   "timing": mode,
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(
+            w, world,
+            l2=("not flushed: warm L2 (the step's data left there by the previous step)"
+                if args.warm else
+                "flushed before every timed step (2 x L2 write, then 2 x L2 read)"),
+            timing=mode),
         "bytes_per_step": bytes_step,
         "flops_per_step": flops_step,
         "e2e": {"value": round(job_gbps(world, bytes_step, args.steps, e2e_total), 2),
@@ -581,6 +600,24 @@ def run_ours(args, w, rank, world, dist):
         "clocks": clocks,
         "device_errors": errs,
     }
+    if layer_ms:
+        names = ["f16", "q8_0", "q4_0", "turbo4"]
+        us = [float(np.mean(m)) * 1e3 for m in layer_ms]
+        pairs = {}
+        for l, (ck, cv) in enumerate(w.codecs):
+            key = f"K {names[ck]} / V {names[cv]}"
+            e = pairs.setdefault(key, {"layers": [], "us": [], "bytes": 0})
+            e["layers"].append(l)
+            e["us"].append(us[l])
+            e["bytes"] += per_layer_bytes[l]
+        line["per_layer"] = {
+            "what": "each layer's call alone: one CUDA graph replay per timed step, L2 flushed",
+            "us": [round(u, 2) for u in us],
+            "by_codec_pair": {k: {"layers": e["layers"], "us_mean": round(float(np.mean(e["us"])), 2),
+                                  "gbs": round(e["bytes"] / (sum(e["us"]) * 1e-6) / 1e9, 1),
+                                  "frac_of_hbm": round(e["bytes"] / (sum(e["us"]) * 1e-6) / 1e9
+                                                       / _peaks()[0], 4)}
+                              for k, e in sorted(pairs.items())}}
     if w.kind in ("decode", "degrade", "evict"):
         kname = {"decode": "attn_decode_append (decode_split_kernel, append fused)" if arm.fused
                  else "attn_decode (decode_split_kernel)",
@@ -603,47 +640,62 @@ def run_ours(args, w, rank, world, dist):
 # ------------------------------------------------------------------ the oracle (CPU)
 
 class OracleArm:
-    """The fp64 C oracle over a bounded sample of the workload on host cores."""
+    """The fp64 C oracle over a bounded sample of the workload on host cores.
 
-    def __init__(self, w, budget_groups=None):
+    Decode samples whole (layer, seq, kv head) groups, in order, until the
+    sample's attended (key, query head) pairs reach ``budget_rows``; one step
+    is then one oracle decode call per sampled layer over all of that layer's
+    sampled groups, so the oracle's threads spread over (group, query head)
+    rows.  Prefill samples 4 query rows of every head."""
+
+    def __init__(self, w, budget_rows=2e7):
         import torch
         import oracle
-        from attention_quantized_kv_gb300 import workloads as wl
+        wl = _workloads()
         self.w, self.oracle, self.scale = w, oracle, 1.0 / math.sqrt(128)
         dev = "cuda" if torch.cuda.is_available() else "cpu"
         if w.kind == "evict":
             self._init_evict(wl, dev)
             return
         G = w.n_q // w.n_kv
-        # sample: (layer, seq, kv head) groups, in order, until the sample's
-        # attended keys reach ~40M x rows (a few seconds of fp64 work per step)
         groups, budget = [], 0
-        cap_rows = 2e7 if w.kind == "decode" else 0
+        cap_rows = budget_rows if w.kind == "decode" else 0
         for l in range(w.n_layers):
             for s in range(w.n_seqs):
                 for h in range(w.n_kv):
-                    if groups and budget > cap_rows:
+                    if groups and budget >= cap_rows:
                         break
                     groups.append((l, s, h))
                     budget += w.final_lens()[s] * G
         self.groups = groups
-        self.caches, self.q, self.new = [], [], []
-        for l, s, h in groups:
+        # per sampled layer: the layer's caches (every group appended, the
+        # unsampled ones are simply not attended), the new rows, the query
+        self.layers = []
+        for l in sorted({g[0] for g in groups}):
+            sel = np.zeros((w.n_seqs, w.n_kv), bool)
+            for (gl, s, h) in groups:
+                if gl == l:
+                    sel[s, h] = True
+            seqs = [s for s in range(w.n_seqs) if sel[s].any()]
             ck, cv = w.codecs[l]
             cs = []
             for side, codec in ((0, ck), (1, cv)):
-                rows = wl.kv_rows(w, l, side, s, 0, w.lens[s], dev)[:, h].cpu().numpy()
-                c = np.zeros(oracle.cache_bytes(codec, 1, 1, w.capacity), np.uint8)
-                oracle.append_side(codec, side, c, 1, 1, w.capacity, [0], [w.lens[s]],
-                                   rows.reshape(1, -1, 1, 128))
-                new = (wl.kv_rows(w, l, side, s, w.lens[s], w.append_new, dev)[:, h].cpu().numpy()
-                       if w.append_new else None)
+                c = np.zeros(oracle.cache_bytes(codec, w.n_seqs, w.n_kv, w.capacity), np.uint8)
+                for s in seqs:
+                    rows = wl.kv_rows(w, l, side, s, 0, w.lens[s], dev).cpu().numpy()
+                    x = np.zeros((w.n_seqs, w.lens[s], w.n_kv, 128), np.float16)
+                    x[s] = rows
+                    n = [w.lens[s] if t == s else 0 for t in range(w.n_seqs)]
+                    oracle.append_side(codec, side, c, w.n_seqs, w.n_kv, w.capacity,
+                                       [0] * w.n_seqs, n, x)
+                new = None
+                if w.append_new:
+                    new = np.stack([wl.kv_rows(w, l, side, s, w.lens[s], w.append_new, dev)
+                                    .cpu().numpy() for s in range(w.n_seqs)])
                 cs.append((c, new))
-            self.caches.append(cs)
             n_tok = w.append_new if w.kind == "prefill" else 1
-            qq = wl.queries(w, l, n_tok, dev)[s].cpu().numpy()  # [n_tok, n_q, 128]
-            self.q.append(qq[:, h * G:(h + 1) * G])
-        # prefill: a fixed sample of query rows
+            qq = wl.queries(w, l, n_tok, dev).cpu().numpy()  # [n_seqs, n_tok, n_q, 128]
+            self.layers.append((l, sel, cs, qq))
         self.rows = None
         if w.kind == "prefill":
             self.rows = [0, 1, w.append_new // 2, w.append_new - 1]
@@ -696,9 +748,8 @@ class OracleArm:
     def sample_bytes(self):
         w = self.w
         if w.kind == "evict":
-            from attention_quantized_kv_gb300 import workloads as wl
             lens = [w.final_lens()[s] for s in self.seqs]
-            n_ev = [wl.n_evicted(w)[s] for s in self.seqs]
+            n_ev = [_workloads().n_evicted(w)[s] for s in self.seqs]
             return sum(evict_work(w, lens, n_ev, *w.codecs[0]))
         tot = 0
         G = w.n_q // w.n_kv
@@ -721,45 +772,76 @@ class OracleArm:
         if w.kind == "evict":
             self._step_evict()
             return
-        G = w.n_q // w.n_kv
-        for (l, s, h), cs, q in zip(self.groups, self.caches, self.q):
+        for l, sel, cs, qq in self.layers:
             ck, cv = w.codecs[l]
             (kc, kn), (vc, vn) = cs
-            kc, vc = kc.copy(), vc.copy()
-            if w.append_new:
-                o.append_side(ck, 0, kc, 1, 1, w.capacity, [w.lens[s]], [w.append_new],
-                              kn.reshape(1, -1, 1, 128))
-                o.append_side(cv, 1, vc, 1, 1, w.capacity, [w.lens[s]], [w.append_new],
-                              vn.reshape(1, -1, 1, 128))
+            if w.append_new:  # every step writes the same rows at the same positions
+                n = [w.append_new] * w.n_seqs
+                o.append_side(ck, 0, kc, w.n_seqs, w.n_kv, w.capacity, w.lens, n, kn)
+                o.append_side(cv, 1, vc, w.n_seqs, w.n_kv, w.capacity, w.lens, n, vn)
             if w.kind == "degrade":
                 side = w.extra["side"]
                 o.requantize_side(ck if side == 0 else cv, w.extra["dst"], side,
-                                  kc if side == 0 else vc, 1, 1, w.capacity, [w.lens[s]])
+                                  kc if side == 0 else vc, w.n_seqs, w.n_kv, w.capacity, w.lens)
             elif w.kind == "decode":
-                o.decode_layer(ck, cv, kc, vc, 1, 1, G, w.capacity, [w.final_lens()[s]],
-                               np.ascontiguousarray(q[0]), self.scale)
+                o.decode_layer(ck, cv, kc, vc, w.n_seqs, w.n_kv, w.n_q, w.capacity,
+                               w.final_lens(), np.ascontiguousarray(qq[:, 0]), self.scale,
+                               sel=sel)
             else:
-                o.prefill_chunk(ck, cv, kc, vc, 1, G, w.capacity, 0, w.lens[0],
-                                np.ascontiguousarray(q), self.scale, rows=self.rows)
+                o.prefill_chunk(ck, cv, kc, vc, w.n_kv, w.n_q, w.capacity, 0, w.lens[0],
+                                np.ascontiguousarray(qq[0]), self.scale, rows=self.rows)
 
 
-def time_oracle(w, steps, warmup, min_seconds=0.0):
+def _workloads():
+    """The workload module, loaded from its file without importing the
+    package (whose first use loads the CUDA library): the reference arm runs
+    the oracle alone."""
+    import importlib.util
+    name = "kvq_bench_workloads"
+    if name in sys.modules:
+        return sys.modules[name]
+    path = os.path.join(ROOT, "attention_quantized_kv_gb300", "workloads.py")
+    spec = importlib.util.spec_from_file_location(name, path)
+    mod = importlib.util.module_from_spec(spec)
+    sys.modules[name] = mod
+    spec.loader.exec_module(mod)
+    return mod
+
+
+def time_oracle(w, steps, warmup, min_seconds=0.0, threads=None, budget_rows=2e7):
+    """Oracle throughput on a bounded sample: bytes of the sample per second,
+    on `threads` OpenMP threads (None: all of the host's)."""
     import oracle
-    arm = OracleArm(w)
-    for _ in range(warmup):
-        arm.step()
-    t0 = time.perf_counter()
-    n = 0
-    while n < steps or (time.perf_counter() - t0) < min_seconds:
-        arm.step()
-        n += 1
-        if min_seconds and n >= steps and time.perf_counter() - t0 >= min_seconds:
-            break
-    dt = time.perf_counter() - t0
+    arm = OracleArm(w, budget_rows)
+    n_thr = oracle.num_threads() if threads is None else int(threads)
+    with oracle.threads(n_thr):
+        for _ in range(warmup):
+            arm.step()
+        t0 = time.perf_counter()
+        n = 0
+        while n < steps or (time.perf_counter() - t0) < min_seconds:
+            arm.step()
+            n += 1
+            if min_seconds and n >= steps and time.perf_counter() - t0 >= min_seconds:
+                break
+        dt = time.perf_counter() - t0
     gbs = arm.sample_bytes() * n / dt / 1e9
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": n_thr,
             "kind": "oracle", "sample": f"{arm.sample_desc}; {n} steps in {dt:.1f} s",
             "seconds": round(dt, 2)}
+
+
+def cpu_baseline(w):
+    """The oracle on all host cores (the reported value) and on one thread,
+    each on its own bounded sample (~10 s each)."""
+    import oracle
+    allc = time_oracle(w, 1, 0, min_seconds=10.0, budget_rows=2e7)
+    one = time_oracle(w, 1, 0, min_seconds=10.0, threads=1, budget_rows=2e6)
+    allc["host_cores"] = os.cpu_count()
+    allc["parallel_over"] = ("(kv head group, query head) rows of each sampled layer"
+                             if w.kind == "decode" else "query rows")
+    allc["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample", "seconds")}
+    return allc
 
 
 # ------------------------------------------------------------------ main
@@ -791,19 +873,21 @@ def main():
         tdist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
         dist = tdist
 
-    import __graft_entry__
-    __graft_entry__.build()
-    from attention_quantized_kv_gb300 import workloads as wl
-    w = wl.get(args.workload)
-
     if args.impl == "reference":
+        # the oracle alone: the CUDA library is neither built nor loaded here
+        import oracle
+        oracle.build()
+        w = _workloads().get(args.workload)
         if rank == 0:
-            r = time_oracle(w, args.steps, args.warmup)
+            r = time_oracle(w, args.steps, args.warmup, budget_rows=1e7)
+            r["host_cores"] = os.cpu_count()
             line = {"metric": METRIC, "value": r["value"], "unit": "GB/s", "n_gpus": world,
                     "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
                     "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, fp32 codec",
                     "data": "synthetic", "impl": "reference",
-                    "config": {"workload": w.name, "description": w.description},
+                    "config": workload_config(
+                        w, world, l2="not applicable (host CPU)",
+                        timing="wall clock over whole oracle steps on a bounded sample"),
                     "cpu_baseline": r,
                     "e2e": {"value": r["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
                             "d2h_bytes_per_step": 0}}
@@ -812,10 +896,14 @@ def main():
             dist.destroy_process_group()
         return
 
+    import __graft_entry__
+    __graft_entry__.build()
+    from attention_quantized_kv_gb300 import workloads as wl
+    w = wl.get(args.workload)
     line = run_ours(args, w, rank, world, dist)
     if rank == 0:
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = time_oracle(w, 1, 0, min_seconds=10.0)
+            line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()

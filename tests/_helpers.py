@@ -49,6 +49,26 @@ def oracle_stream(w, layer_idx, seq, kvh, n_tokens, device="cuda"):
     return out
 
 
+def oracle_layer(w, layer_idx, lens, device="cuda", chunk=16384):
+    """Oracle caches (K side, V side) of a whole layer: tokens [0, lens[s])
+    of every sequence appended by the oracle from the same seeded draws."""
+    ck, cv = w.codecs[layer_idx]
+    out = []
+    for side, codec in ((0, ck), (1, cv)):
+        c = np.zeros(oracle.cache_bytes(codec, w.n_seqs, w.n_kv, w.capacity), np.uint8)
+        for start in range(0, max(lens), chunk):
+            n = [max(0, min(chunk, ln - start)) for ln in lens]
+            x = np.zeros((w.n_seqs, max(n), w.n_kv, 128), np.float16)
+            for s in range(w.n_seqs):
+                if n[s]:
+                    x[s, :n[s]] = wl.kv_rows(w, layer_idx, side, s, start, n[s],
+                                             device).cpu().numpy()
+            oracle.append_side(codec, side, c, w.n_seqs, w.n_kv, w.capacity,
+                               [min(start, ln) for ln in lens], n, x)
+        out.append(c)
+    return out
+
+
 def gpu_stream_bytes(L, side, seq, kvh):
     cache = L.k_cache if side == 0 else L.v_cache
     codec = L.codec_k if side == 0 else L.codec_v
