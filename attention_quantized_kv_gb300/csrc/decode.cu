@@ -6,11 +6,12 @@
 // buun-llama-cpp listing; the K and V sides are typed independently, as in
 // its VBR section's per-(layer, side) ladder).  turbo4 is never un-rotated
 // per token: the query is rotated once (q . x^ = (H s q / 16) . y^), V is
-// accumulated in the rotated space and the merged output is rotated back.  Work is cut along the token axis; each piece produces a partial
-// (running max m, running sum l, unnormalised o) and a second kernel merges
-// the partials of each (sequence, head) with the log-sum-exp identity: the
-// last CTA to finish a stream (an atomic ticket, no waiting) merges its
-// partials and writes the output rows.
+// accumulated in the rotated space and the merged output is rotated back.
+// Work is cut along the token axis; each piece produces a partial (running
+// max m, running sum l, unnormalised o), and a second kernel, launched right
+// behind the first (programmatic dependent launch), merges the partials of
+// each (sequence, head) with the log-sum-exp identity and writes the output
+// rows: one CTA per stream, every partial requested at once.
 //
 // Work partition.  A "stream" is one (sequence, kv head, group of up to 8
 // query heads); its keys are 16-token units.  All units of all streams are
@@ -75,7 +76,6 @@ struct DecodeParams {
   unsigned *rd_ctr;
   float *part_o;    // [slots][8][128]
   float2 *part_ml;  // [slots][8]: (max in log2 units, sum)
-  int32_t *tickets; // [streams] arrival counters (zero between calls)
   __half *out;      // [n_seqs][n_q][128]
   float *lse;       // [n_seqs][n_q] or null
   int32_t *err;
@@ -549,8 +549,7 @@ __device__ __forceinline__ void load_q_frags_smem(const __half *qs, int nh, int 
   }
 }
 
-// Last-CTA merge of one stream's partials into out / lse (all 256 threads;
-// called by the CTA whose ticket completed the stream).
+// Where a merged row goes: out [n_seqs][n_q][128] fp16, lse [n_seqs][n_q].
 struct MergeArgs {
   const float2 *part_ml;
   const float *part_o;
@@ -576,199 +575,6 @@ __device__ __forceinline__ void merge_write(const MergeArgs &p, int seq, int kvh
   dst[0] = o01;
   dst[1] = o23;
   if (p.lse && lane == 0) p.lse[row] = lse;
-}
-
-template <bool ROT>
-__device__ __noinline__ void merge_stream(const MergeArgs p, float4 *xacc, float *xl,
-                                             int stream, int seq, int kvh, int hg, int c_first,
-                                             int c_last, int64_t S, int n_s, int64_t U, int P,
-                                             bool dry = false) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // Merge the stream's partials.  The heads of the group are spread over
-  // the 8 warps (reps warps per head; warp `part` of a head takes parts
-  // j = part, part + reps, ...).  Parts go in windows of 64: lanes fetch
-  // the writer CTA and the (max, sum) of parts lane and lane + 32 once, and
-  // the rows then stream through an 8-row register buffer with their CTA
-  // and weight taken from those lanes by shuffles.  With several warps per
-  // head, warps part > 0 hand their sums to warp part 0 through xacc / xl
-  // (a region no other phase writes) across one CTA barrier.
-  const int heads_here = min(8, p.G - hg * 8);
-  const int reps = kWarps / heads_here >= 4 ? 4 : (kWarps / heads_here >= 2 ? 2 : 1);
-  const int h = warp % heads_here, part = warp / heads_here;
-  const bool active = warp < heads_here * reps;
-  float M = -INFINITY, L = 0.0f;
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (active) {
-    // Part j of the stream: with at least one unit per CTA (U >= P) it is
-    // the partial of CTA c_first + j; otherwise CTAs hold at most one unit
-    // and part j is the partial of the owner of unit S + j.
-    const bool sparse = U < P;
-    const int n_live = sparse ? n_s : c_last - c_first + 1;
-    auto cta_of = [&](int j) -> int {
-      return sparse ? static_cast<int>(((S + j + 1) * P - 1) / U) : c_first + j;
-    };
-    const float2 *ml_h = p.part_ml + static_cast<int64_t>(stream) * 8 + h;
-    const float4 *o_h =
-        reinterpret_cast<const float4 *>(p.part_o + (static_cast<int64_t>(stream) * 8 + h) * kD) + lane;
-    int base = 0, ca = 0, cb = 0;
-    float2 mla, mlb;
-    float4 xa[8];
-    // Window `base`: lane data of parts base + lane, base + 32 + lane.
-    auto load_window = [&]() {
-      ca = base + lane < n_live ? cta_of(base + lane) : 0;
-      cb = base + 32 + lane < n_live ? cta_of(base + 32 + lane) : 0;
-      mla = base + lane < n_live ? __ldcg(ml_h + static_cast<int64_t>(ca) * 8)
-                                 : make_float2(-INFINITY, 0.0f);
-      mlb = base + 32 + lane < n_live ? __ldcg(ml_h + static_cast<int64_t>(cb) * 8)
-                                      : make_float2(-INFINITY, 0.0f);
-    };
-    // Rows t0 .. t0+7 of this warp in the window (window-relative part
-    // part + reps * t < 64 for every t < 64 / reps).
-    auto load_rows = [&](float4 (&x)[8], int t0) {
-#pragma unroll
-      for (int t = 0; t < 8; ++t) {
-        const int jr = part + reps * (t0 + t);
-        const int c = __shfl_sync(0xffffffffu, jr < 32 ? ca : cb, jr & 31);
-        x[t] = base + jr < n_live ? __ldcg(o_h + static_cast<int64_t>(c) * (8 * kD / 4))
-                                  : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      }
-    };
-    load_window();
-    load_rows(xa, 0);
-    M = fmaxf(mla.x, mlb.x);
-    for (int j = 64 + lane; j < n_live; j += 32)
-      M = fmaxf(M, __ldcg(ml_h + static_cast<int64_t>(cta_of(j)) * 8).x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (M != -INFINITY) {
-      const int rows_max = 64 / reps;  // rows of a warp in a full window
-      while (true) {
-        const float wa = mla.x == -INFINITY ? 0.0f : fast_exp2(mla.x - M);
-        const float wb = mlb.x == -INFINITY ? 0.0f : fast_exp2(mlb.x - M);
-        if (lane % reps == part) L += wa * mla.y + wb * mlb.y;  // 32 % reps == 0
-        auto use_rows = [&](const float4 (&x)[8], int t0) {
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            const int jr = part + reps * (t0 + t);
-            const float w = __shfl_sync(0xffffffffu, jr < 32 ? wa : wb, jr & 31);
-            acc.x = fmaf(w, x[t].x, acc.x);
-            acc.y = fmaf(w, x[t].y, acc.y);
-            acc.z = fmaf(w, x[t].z, acc.z);
-            acc.w = fmaf(w, x[t].w, acc.w);
-          }
-        };
-        const int rows = min(rows_max, (min(n_live - base, 64) - part + reps - 1) / reps);
-        for (int t0 = 0; t0 < rows; t0 += 8) {
-          use_rows(xa, t0);
-          if (t0 + 8 < rows) load_rows(xa, t0 + 8);
-        }
-        base += 64;
-        if (base >= n_live) break;
-        load_window();
-        load_rows(xa, 0);
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-    }
-    if (part > 0) {
-      xacc[warp * 32 + lane] = acc;
-      if (lane == 0) xl[warp] = L;
-    }
-  }
-  if (reps > 1) cta_bar();  // reps is the same in every warp
-  if (active && part == 0) {
-    for (int r = 1; r < reps; ++r) {
-      const float4 y = xacc[(h + r * heads_here) * 32 + lane];
-      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
-      L += xl[h + r * heads_here];
-    }
-    merge_write<ROT>(p, seq, kvh, hg, h, lane, acc, M, L, dry);
-  }
-}
-
-// The merged partials of one stream when they fit the CTA's shared memory
-// and its copy ring is idle: the (max, sum) pairs of all parts and their
-// output rows (heads of the group only) arrive by bulk copies on one
-// mbarrier, issued by the 32 lanes of warp 0 and all in flight together.
-// Warp h < heads then finds head h's max M and writes the weights
-// w_j = 2^(m_j - M) over m_j (lane-parallel); after a CTA barrier the rows
-// are folded by all warps (head h, residue r: parts j = r mod reps), and
-// warp (h, 0) adds the reps partial sums in order through xacc.  Parts are the partials of CTAs c_first ..
-// c_first + n_live - 1, whose slots are consecutive.  Returns false if the
-// copies did not land within the wait limit (error word set).
-template <bool ROT>
-__device__ __forceinline__ bool merge_stream_smem(const MergeArgs p, uint8_t *buf, uint64_t *bar,
-                                                  float4 *xacc, int stream, int seq,
-                                                  int kvh, int hg, int c_first, int n_live,
-                                                  int32_t *err, bool dry = false) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int heads_here = min(8, p.G - hg * 8);
-  const uint32_t ml_bytes = static_cast<uint32_t>(n_live) * 64u;
-  const uint32_t row_bytes = static_cast<uint32_t>(heads_here) * kD * 4u;
-  const int64_t slot0 = static_cast<int64_t>(c_first) + stream;
-  if (warp == 0 && !dry) {
-    if (lane == 0) {
-      // partials written through the generic proxy, read by the copy engine
-      asm volatile("fence.proxy.async.global;\n" ::: "memory");
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(bar, ml_bytes + row_bytes * static_cast<uint32_t>(n_live));
-      bulk_copy_g2s(buf, p.part_ml + slot0 * 8, ml_bytes, bar);
-    }
-    __syncwarp();
-    for (int j = lane; j < n_live; j += 32)
-      bulk_copy_g2s(buf + ml_bytes + j * row_bytes, p.part_o + (slot0 + j) * 8 * kD, row_bytes,
-                    bar);
-  }
-  const bool ok = dry || mbar_wait_bounded(bar, 0u);
-  if (__syncthreads_or(!ok)) {
-    if (threadIdx.x == 0) set_err(err, KVQ_DEVERR_TIMEOUT);
-    mbar_wait_bounded(bar, 0u);
-    return false;
-  }
-  float2 *ml = reinterpret_cast<float2 *>(buf);
-  float M = -INFINITY, L = 0.0f;
-  if (warp < heads_here) {
-    const int h = warp;
-    for (int j = lane; j < n_live; j += 32) M = fmaxf(M, ml[j * 8 + h].x);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    for (int j = lane; j < n_live; j += 32) {
-      const float2 v = ml[j * 8 + h];
-      const float w = (M == -INFINITY || v.x == -INFINITY) ? 0.0f : fast_exp2(v.x - M);
-      L = fmaf(w, v.y, L);
-      ml[j * 8 + h].x = w;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-  }
-  __syncthreads();
-  const int reps = kWarps / heads_here;
-  const int h = warp % heads_here, r = warp / heads_here;
-  const bool active = warp < heads_here * reps;
-  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-  if (active) {
-    // a plain loop: this code runs once per CTA, cold in the instruction
-    // cache, so its size costs more than its dependency chain
-    const float4 *rows = reinterpret_cast<const float4 *>(buf + ml_bytes) + h * (kD / 4) + lane;
-    const int stride = static_cast<int>(row_bytes / 16);
-#pragma unroll 1
-    for (int j = r; j < n_live; j += reps) {
-      const float w = ml[j * 8 + h].x;
-      const float4 x = rows[j * stride];
-      acc.x = fmaf(w, x.x, acc.x); acc.y = fmaf(w, x.y, acc.y);
-      acc.z = fmaf(w, x.z, acc.z); acc.w = fmaf(w, x.w, acc.w);
-    }
-    if (r > 0) xacc[warp * 32 + lane] = acc;
-  }
-  if (reps > 1) __syncthreads();
-  if (active && r == 0) {
-    for (int q = 1; q < reps; ++q) {
-      const float4 y = xacc[(h + q * heads_here) * 32 + lane];
-      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
-    }
-    merge_write<ROT>(p, seq, kvh, hg, h, lane, acc, M, L, dry);
-  }
-  return true;
 }
 
 // Keys sequence s attends: its length, plus the token a fused decode step
@@ -851,17 +657,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
   __shared__ uint64_t full[C::NS];
   __shared__ int32_t pfx[kMaxSeqs + 1];
   __shared__ int abort_flag;
-  __shared__ int last_flag;
   // query rows of the current and the next segment (bulk copies, one
   // segment ahead; the first is requested before the ring's copies)
   __shared__ __align__(128) __half q_s[2][8 * kD];
   __shared__ uint64_t q_bar[2];
-  __shared__ uint64_t mrg_bar;  // the shared-memory merge's bulk copies (used at most once)
-  // merge hand-over (read by warp part 0 of a head before the CTA's next
-  // barrier, written again only after it)
-  __shared__ float4 mrg_acc[kWarps * 32];
-  __shared__ float mrg_l[kWarps];
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
 
@@ -902,7 +701,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     }
     for (int s = lane; s < C::NS; s += 32) mbar_init(&full[s], 1);
     if (lane < 2) mbar_init(&q_bar[lane], 1);
-    if (lane == 2) mbar_init(&mrg_bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -1134,11 +932,6 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       half_bar();  // warps 0-3 only
     }
     const int stream = seq * geo.KH + seg.sl;
-    // CTAs whose slices overlap this stream: c_first..c_last; the owner of
-    // unit u is floor(((u + 1) * P - 1) / U).
-    const int64_t S = static_cast<int64_t>(pfx[seq]) * geo.KH + static_cast<int64_t>(seg.sl) * seg.n_s;
-    const int c_first = static_cast<int>(((S + 1) * P - 1) / U);
-    const int c_last = static_cast<int>(((S + seg.n_s) * P - 1) / U);
     if (warp == 0) {
 #pragma unroll 1
       for (int w = 1; w < 4; ++w) merge_into(o, m0, m1, l0, l1, rs + w * 32 * kRedFloats);
@@ -1147,6 +940,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         l0 += __shfl_xor_sync(0xffffffffu, l0, off);
         l1 += __shfl_xor_sync(0xffffffffu, l1, off);
       }
+      // The CTA's partial of this stream, in slot blockIdx.x + stream (a
+      // CTA's slice covers consecutive streams, so the slots of all (CTA,
+      // stream) pairs are distinct); the merge kernel reads it after this
+      // kernel has completed.
       const int64_t slot = static_cast<int64_t>(blockIdx.x) + stream;
       float *po = p.part_o + slot * 8 * kD;
       const int h0 = 2 * tig, h1 = 2 * tig + 1;
@@ -1161,60 +958,8 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         if (v0) p.part_ml[slot * 8 + h0] = make_float2(ok ? m0 : -INFINITY, ok ? l0 : 0.0f);
         if (v1) p.part_ml[slot * 8 + h1] = make_float2(ok ? m1 : -INFINITY, ok ? l1 : 0.0f);
       }
-      // Ticket: the last of the stream's CTAs to get here merges its partials.
-      __threadfence();
-      __syncwarp();
-      if (lane == 0) {
-        // Every CTA in c_first..c_last wrote a partial, except (when the grid
-        // is larger than the unit count) CTAs whose slice is empty.
-        unsigned n_parts = static_cast<unsigned>(c_last - c_first + 1);
-        if (U < P)
-          for (int c = c_first; c <= c_last; ++c)
-            if (U * (c + 1) / P == U * c / P) --n_parts;
-        const unsigned old = atomicInc(reinterpret_cast<unsigned *>(p.tickets) + stream,
-                                       n_parts - 1);
-        last_flag = (old == n_parts - 1) ? 1 : (old == 0 && n_parts > 2 ? 2 : 0);
-      }
     }
-    cta_bar();  // slots free again; last_flag visible
-    if (last_flag == 1) {
-      __threadfence();
-      const MergeArgs ma = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
-      // Shared-memory merge when this is the CTA's last segment and no warp
-      // aborted (no copy in flight into the ring or the query buffers), the
-      // parts are the consecutive slots of c_first .. c_last and they fit the
-      // ring plus the reduction slots.  Every term is the same in all warps
-      // (abort_flag is only raised inside the unit loop, before the barrier).
-      const int n_live = c_last - c_first + 1;
-      const int hh = min(8, p.G - hg * 8);
-      const bool smem_merge = seg_end == u1 && U >= P &&
-                              *reinterpret_cast<volatile int *>(&abort_flag) == 0 &&
-                              static_cast<int64_t>(n_live) * (64 + hh * kD * 4) <=
-                                  C::RING + C::RED;
-      if (smem_merge) {
-        merge_stream_smem<CV == KVQ_TURBO4>(ma, smem, &mrg_bar, mrg_acc, stream, seq, kvh, hg,
-                                            c_first, n_live, p.err);
-      } else {
-        merge_stream<CV == KVQ_TURBO4>(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first,
-                                       c_last, S, seg.n_s, U, P);
-      }
-    } else if (last_flag == 2 && seg_end == u1 &&
-               *reinterpret_cast<volatile int *>(&abort_flag) == 0) {
-      // The first CTA to finish a stream runs the stream's merge once over
-      // two parts, on its own idle shared memory and storing nothing, so
-      // that the code the stream's last CTA will run is in L2 by then (run
-      // once per stream, the merge otherwise fetches its instructions cold
-      // from device memory).
-      const MergeArgs ma = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
-      const int n_live = c_last - c_first + 1;
-      const int hh = min(8, p.G - hg * 8);
-      if (U >= P && static_cast<int64_t>(n_live) * (64 + hh * kD * 4) <= C::RING + C::RED)
-        merge_stream_smem<CV == KVQ_TURBO4>(ma, smem, &mrg_bar, mrg_acc, stream, seq, kvh, hg,
-                                            c_first, 2, p.err, true);
-      else
-        merge_stream<CV == KVQ_TURBO4>(ma, mrg_acc, mrg_l, stream, seq, kvh, hg, c_first,
-                                       c_first + 1, S, seg.n_s, U, P, true);
-    }
+    cta_bar();  // the reduction slots are free again
 
     useg = seg_end;
     ++si;
@@ -1236,6 +981,145 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     for (int k = k_fail; k < R && k < k_fail + C::NS; k += kWarps)
       mbar_wait_bounded(&full[k % C::NS], static_cast<uint32_t>(k / C::NS) & 1u, nullptr,
                         100000000ull);
+  }
+}
+
+// ------------------------------------------------------------------ merge
+
+struct MergeParams {
+  MergeArgs a;
+  const int32_t *seq_lens;  // after the decode kernel (a fused step has advanced them)
+  int n_seqs, n_kv, n_hg, max_len;
+  int ups;   // units per work item of the decode kernel's codec pair
+  int grid;  // the decode kernel's CTAs
+};
+
+// The log-sum-exp merge of every stream's partials (the second kernel of a
+// decode call), one 4-warp CTA per (stream, query head of its group):
+// o = sum_j 2^(m_j - M) o_j / L with M = max_j m_j and
+// L = sum_j 2^(m_j - M) l_j over the stream's parts j (the partials of the
+// CTAs whose slices overlap the stream, in CTA order).  Parts go in windows
+// of 64: every lane fetches the (max, sum) of parts base + lane and base +
+// 32 + lane, and warp w requests the rows of its parts j = w (mod 4) of the
+// window all at once (one round trip for up to 64 parts; the head's 512-byte
+// rows come from one SM each, so a stream's merge is spread over as many SMs
+// as the group has heads).  Every sum runs in a fixed order (warp w's parts
+// in increasing j, then warps 0..3; the sum L lane-strided in warp 0), so the
+// output does not depend on timing.  The partition is recomputed from the
+// lengths exactly as the decode kernel computed it (a fused step's lengths
+// are already advanced, which is the count it attended).
+constexpr int kMergeWarps = 4;
+constexpr int kMergeRows = 64 / kMergeWarps;  // rows of a warp per window
+
+template <bool ROT>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const MergeParams p) {
+  __shared__ int32_t pfx[kMaxSeqs + 1];
+  __shared__ float4 accs[kMergeWarps][32];
+  grid_dependency_wait();  // the partials (and a fused step's lengths) are complete
+  grid_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    const int item_tok = p.ups * kUnitTokens;
+    int carry = 0;
+    for (int base = 0; base < p.n_seqs; base += 32) {
+      const int s = base + lane;
+      int n = 0;
+      if (s < p.n_seqs) {
+        int len = p.seq_lens[s];
+        len = len < p.max_len ? len : p.max_len;
+        n = len > 0 ? (len + item_tok - 1) / item_tok : 0;
+      }
+      int incl = n;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += t;
+      }
+      if (s < p.n_seqs) pfx[s + 1] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pfx[0] = 0;
+  }
+  __syncthreads();
+  const int KH = p.n_kv * p.n_hg;
+  const int stream = blockIdx.x, seq = stream / KH, sl = stream % KH;
+  const int kvh = sl / p.n_hg, hg = sl % p.n_hg, h = blockIdx.y;
+  const int n_s = pfx[seq + 1] - pfx[seq];
+  // no keys: the decode kernel wrote the rows; heads past the group: nothing
+  if (n_s == 0 || h >= min(8, p.a.G - hg * 8)) return;
+  const int64_t U = static_cast<int64_t>(pfx[p.n_seqs]) * KH;
+  const int64_t P = p.grid;
+  const int64_t S = static_cast<int64_t>(pfx[seq]) * KH + static_cast<int64_t>(sl) * n_s;
+  // Part j: with at least one item per CTA (U >= P) the partial of CTA
+  // c_first + j; otherwise CTAs hold at most one item and part j is the
+  // partial of the owner of item S + j (the owner of item u is
+  // floor(((u + 1) P - 1) / U)).
+  const bool sparse = U < P;
+  const int64_t c_first = ((S + 1) * P - 1) / U;
+  const int n_live = sparse ? n_s : static_cast<int>(((S + n_s) * P - 1) / U - c_first + 1);
+  auto slot_of = [&](int j) -> int64_t {
+    return (sparse ? ((S + j + 1) * P - 1) / U : c_first + j) + stream;
+  };
+  const float2 *ml = p.a.part_ml + h;                                           // + slot * 8
+  const float4 *rows = reinterpret_cast<const float4 *>(p.a.part_o + h * kD) + lane;  // + slot * 256
+  // window `base`: (max, sum) of parts base + lane and base + 32 + lane, and
+  // this warp's rows of the window (parts base + warp + 4 t), all in flight
+  int64_t sa = 0, sb = 0;
+  float2 mla, mlb;
+  float4 x[kMergeRows];
+  auto load_window = [&](int base) {
+    sa = base + lane < n_live ? slot_of(base + lane) : 0;
+    sb = base + 32 + lane < n_live ? slot_of(base + 32 + lane) : 0;
+    mla = base + lane < n_live ? __ldcg(ml + sa * 8) : make_float2(-INFINITY, 0.0f);
+    mlb = base + 32 + lane < n_live ? __ldcg(ml + sb * 8) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+    for (int t = 0; t < kMergeRows; ++t) {
+      const int jr = warp + kMergeWarps * t;  // window-relative part
+      const int64_t st = __shfl_sync(0xffffffffu, jr < 32 ? sa : sb, jr & 31);
+      x[t] = base + jr < n_live ? __ldcg(rows + st * (8 * kD / 4))
+                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+  };
+  load_window(0);
+  float M = fmaxf(mla.x, mlb.x);
+  for (int j = 64 + lane; j < n_live; j += 32) M = fmaxf(M, __ldcg(ml + slot_of(j) * 8).x);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float L = 0.0f;
+  float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  if (M != -INFINITY) {
+    for (int base = 0;;) {
+      const float wa = mla.x == -INFINITY ? 0.0f : fast_exp2(mla.x - M);
+      const float wb = mlb.x == -INFINITY ? 0.0f : fast_exp2(mlb.x - M);
+      L = fmaf(wa, mla.y, L);  // lane l: parts l, l + 32, l + 64, ... in order
+      L = fmaf(wb, mlb.y, L);
+#pragma unroll
+      for (int t = 0; t < kMergeRows; ++t) {
+        const int jr = warp + kMergeWarps * t;
+        const float w = __shfl_sync(0xffffffffu, jr < 32 ? wa : wb, jr & 31);
+        if (base + jr < n_live) {
+          acc.x = fmaf(w, x[t].x, acc.x);
+          acc.y = fmaf(w, x[t].y, acc.y);
+          acc.z = fmaf(w, x[t].z, acc.z);
+          acc.w = fmaf(w, x[t].w, acc.w);
+        }
+      }
+      base += 64;
+      if (base >= n_live) break;
+      load_window(base);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+  }
+  accs[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int w = 1; w < kMergeWarps; ++w) {
+      const float4 y = accs[w][lane];
+      acc.x += y.x; acc.y += y.y; acc.z += y.z; acc.w += y.w;
+    }
+    merge_write<ROT>(p.a, seq, kvh, hg, h, lane, acc, M, L);
   }
 }
 
@@ -1305,7 +1189,6 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
   p.lens_rw = L.seq_lens;
   p.rd_ctr = reinterpret_cast<unsigned *>(ws) + (kDecodeTicketBytes / 4 - 1);
   p.q = static_cast<const __half *>(q);
-  p.tickets = reinterpret_cast<int32_t *>(ws);
   p.part_ml = reinterpret_cast<float2 *>(ws + pl.ticket_bytes);
   p.part_o = reinterpret_cast<float *>(ws + pl.ticket_bytes + pl.ml_bytes);
   p.out = static_cast<__half *>(out);
@@ -1322,12 +1205,29 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
   p.capacity = L.capacity;
   p.max_len = max_len;
   p.scale_log2 = scale * 1.4426950408889634f;
+  cudaError_t e;
   switch (L.codec_k) {
-    case KVQ_F16: return launch_split_v<KVQ_F16>(L.codec_v, p, pl.grid, stream);
-    case KVQ_Q8_0: return launch_split_v<KVQ_Q8_0>(L.codec_v, p, pl.grid, stream);
-    case KVQ_Q4_0: return launch_split_v<KVQ_Q4_0>(L.codec_v, p, pl.grid, stream);
-    default: return launch_split_v<KVQ_TURBO4>(L.codec_v, p, pl.grid, stream);
+    case KVQ_F16: e = launch_split_v<KVQ_F16>(L.codec_v, p, pl.grid, stream); break;
+    case KVQ_Q8_0: e = launch_split_v<KVQ_Q8_0>(L.codec_v, p, pl.grid, stream); break;
+    case KVQ_Q4_0: e = launch_split_v<KVQ_Q4_0>(L.codec_v, p, pl.grid, stream); break;
+    default: e = launch_split_v<KVQ_TURBO4>(L.codec_v, p, pl.grid, stream); break;
   }
+  if (e != cudaSuccess) return e;
+  MergeParams mp;
+  mp.a = {p.part_ml, p.part_o, p.out, p.lse, p.n_q, p.G};
+  mp.seq_lens = L.seq_lens;
+  mp.n_seqs = p.n_seqs;
+  mp.n_kv = p.n_kv;
+  mp.n_hg = p.n_hg;
+  mp.max_len = max_len;
+  mp.ups = items_units(L.codec_k, L.codec_v);
+  mp.grid = pl.grid;
+  const dim3 mgrid(static_cast<unsigned>(p.n_seqs * p.n_kv * p.n_hg),
+                   static_cast<unsigned>(p.G < 8 ? p.G : 8));
+  const dim3 mblock(kMergeWarps * 32);
+  return L.codec_v == KVQ_TURBO4
+             ? launch_pdl(decode_merge_kernel<true>, mgrid, mblock, 0, stream, mp)
+             : launch_pdl(decode_merge_kernel<false>, mgrid, mblock, 0, stream, mp);
 }
 
 }  // namespace kvq

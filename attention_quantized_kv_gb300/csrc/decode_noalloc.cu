@@ -6,8 +6,8 @@
 // and output buffers and has no handle to an allocator; a latency-critical
 // loop where a device allocation (which may synchronize the device) is not
 // allowed; a process whose device memory budget is fully committed up front.
-// For them the split-K partials and the per-stream arrival counters of the
-// decode kernel sit in one file-scope device array of kNoAllocScratchBytes
+// For them the split-K partials and the counter region of the decode
+// kernels sit in one file-scope device array of kNoAllocScratchBytes
 // (8 MiB), which every GPU that loads this library reserves until the
 // process exits.
 //
@@ -81,9 +81,8 @@ int attn_decode_noalloc(const kvq_layer *L, const void *q, float scale, void *ou
   if (pl.ws_bytes > static_cast<int64_t>(kNoAllocScratchBytes)) return KVQ_EWORKSPACE;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // The whole counter region at the start of the scratch (the per-stream
-  // arrival counters and the lengths-read counter of the fused step) must
-  // start at zero; the previous call may have left anything there.
+  // The counter region at the start of the scratch must start at zero; the
+  // previous call may have left anything there.
   if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(kvq::kDecodeTicketBytes), s) !=
       cudaSuccess)
     return KVQ_ECUDA;

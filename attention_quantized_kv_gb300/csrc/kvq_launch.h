@@ -19,16 +19,16 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
                            cudaStream_t stream);
 
 constexpr int kDecodeMaxSeqs = 1024;         // sequences per attn_decode call
-constexpr int kDecodeTicketBytes = 64 * 1024;  // per-stream counters at the workspace start
-// per-stream counters; the region's last word counts the CTAs of a fused
-// decode step that have read the lengths
-constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4 - 1;
+// counter region at the workspace start (zero between calls); its last word
+// counts the CTAs of a fused decode step that have read the lengths
+constexpr int kDecodeTicketBytes = 64 * 1024;
+constexpr int kDecodeMaxStreams = kDecodeTicketBytes / 4 - 1;  // streams per call
 
 struct DecodePlan {
   int n_hgroups = 1;      // groups of up to 8 query heads per kv head
   int grid = 1;           // CTAs, each an equal slice of the (stream, unit) space
   int64_t slots = 0;      // partial slots: grid + streams
-  int64_t ticket_bytes = 0;  // workspace: per-stream arrival counters (zero between calls)
+  int64_t ticket_bytes = 0;  // workspace: the counter region (zero between calls)
   int64_t ml_bytes = 0;   //            (max, sum) per slot and head
   int64_t o_bytes = 0;    //            unnormalised output per slot and head
   int64_t ws_bytes = 0;

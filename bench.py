@@ -273,11 +273,12 @@ class OursArm:
     def launches_per_step(self):
         """Kernels the library launches per step: the append is one kernel
         for at most 64 rows (it also advances the lengths), else the encode
-        kernel plus the length update; decode is one kernel, prefill two
-        (dequant pre-pass, attention), an eviction step four (decode, probe,
-        selection, compaction of both sides)."""
+        kernel plus the length update; decode is two (the split kernel, with
+        the append fused when the step appends one token, and the merge),
+        prefill two (dequant pre-pass, attention), an eviction step five
+        (decode's two, probe, selection, compaction of both sides)."""
         w = self.w
-        per_layer = {"decode": 1, "degrade": 1, "prefill": 2, "evict": 4}[w.kind]
+        per_layer = {"decode": 2, "degrade": 1, "prefill": 2, "evict": 5}[w.kind]
         if w.append_new and not self.fused:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
@@ -619,8 +620,9 @@ def run_ours(args, w, rank, world, dist):
                                                        / _peaks()[0], 4)}
                               for k, e in sorted(pairs.items())}}
     if w.kind in ("decode", "degrade", "evict"):
-        kname = {"decode": "attn_decode_append (decode_split_kernel, append fused)" if arm.fused
-                 else "attn_decode (decode_split_kernel)",
+        kname = {"decode": "attn_decode_append (decode_split_kernel with the append fused, "
+                           "decode_merge_kernel)" if arm.fused
+                 else "attn_decode (decode_split_kernel, decode_merge_kernel)",
                  "degrade": "kv_requantize (requant_kernel)",
                  "evict": "kv_compact (compact_kernel)"}[w.kind]
         line["roofline"] = {"bound": "hbm", "kernel": kname,

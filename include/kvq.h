@@ -201,11 +201,12 @@ KVQ_API int kv_append_quantize(const kvq_layer *layer, const void *k_new, const 
 KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_t *bytes);
 
 /* Decode attention: every query head of every sequence attends all
- * seq_lens[s] cached keys (split-K over the token axis, log-sum-exp merge).
- * The first 64 KiB of the workspace hold per-stream arrival counters that
+ * seq_lens[s] cached keys (split-K over the token axis; two launches: the
+ * split kernel writes partials, the merge kernel combines them by
+ * log-sum-exp).  The first 64 KiB of the workspace are a counter region that
  * must be zero before the first call (zero-fill the workspace once after
  * allocating it); every call that completes without KVQ_DEVERR_TIMEOUT
- * leaves them zero again, so one workspace serves any number of calls and
+ * leaves it zero again, so one workspace serves any number of calls and
  * layers without clearing.  Calls that may run concurrently need separate
  * workspaces.  Limits: 1024 sequences and 16383 streams (sequence x kv head
  * x group of 8 query heads) per call, else KVQ_EINVAL.
@@ -218,8 +219,8 @@ KVQ_API int attn_decode_workspace(const kvq_layer *layer, int32_t max_len, size_
 KVQ_API int attn_decode(const kvq_layer *layer, const void *q, float scale, void *out, float *lse,
                 int32_t max_len, void *workspace, size_t ws_bytes, void *stream);
 
-/* One decode step of a layer in one launch: quantize-on-append of one new
- * token per sequence (the kv_append_quantize row encoding, at position
+/* One decode step of a layer with no launch for the append: quantize-on-append
+ * of one new token per sequence (the kv_append_quantize row encoding, at position
  * seq_lens[s]), then attn_decode over seq_lens[s] + 1 keys, then
  * seq_lens[s] += 1.  The result (cache bytes, lengths, out, lse) is that of
  * kv_append_quantize(n_new = 1 for every sequence, update_lens = 1)
@@ -248,7 +249,7 @@ KVQ_API int attn_decode_append(const kvq_layer *layer, const void *k_new, const 
  * the process exits); nothing is allocated.  The first call on a device looks
  * the array up (cudaGetSymbolAddress) and must come before any stream capture.
  * The array is shared by all calls and keeps the previous call's contents:
- * the arrival counters are cleared on `stream` before each launch, and calls
+ * its counter region is cleared on `stream` before each launch, and calls
  * that can overlap on the GPU race on it, so issue them in order on one
  * stream.  A layer whose attn_decode_workspace() exceeds 8 MiB is refused
  * with KVQ_EWORKSPACE.  Arguments and results are those of attn_decode. */
