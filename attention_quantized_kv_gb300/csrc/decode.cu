@@ -131,7 +131,7 @@ __device__ __forceinline__ int v_dim(int mt, int mrow) {
 // S (16 tokens x 8 heads) of one unit, multiplied by scale*log2(e).
 template <int CK>
 __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const uint32_t (&qb)[8][2],
-                                            float scale_log2, float (&s)[4]) {
+                                            const uint2 *qlo, float scale_log2, float (&s)[4]) {
   const int g = lane >> 2;
   s[0] = s[1] = s[2] = s[3] = 0.0f;
   if (CK == KVQ_F16) {
@@ -145,7 +145,9 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
       mma16816(s, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
     }
   } else if (CK == KVQ_TURBO4) {
-    // one scale per row: the four 32-dim groups share one accumulator
+    // one scale per row: the four 32-dim groups share one accumulator; the
+    // rotated query is the fp16 pair qb + qlo (qlo[c * 32]: this lane's low
+    // halves of k-step c, in shared memory), both against the same operands
     const uint32_t sc = *reinterpret_cast<const uint32_t *>(ku + 1024 + g * 4);
     float sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -162,6 +164,9 @@ __device__ __forceinline__ void unit_scores(const uint8_t *ku, int lane, const u
                                 u4_pair_minus8_hi(X0), u4_pair_minus8_hi(X1)};
         mma16816(sb, a0, qb[2 * b][0], qb[2 * b][1]);
         mma16816(sb, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
+        const uint2 l0 = qlo[(2 * b) * 32], l1 = qlo[(2 * b + 1) * 32];
+        mma16816(sb, a0, l0.x, l0.y);
+        mma16816(sb, a1, l1.x, l1.y);
       }
     }
     const float dlo = half_bits_to_float(sc & 0xffffu), dhi = half_bits_to_float(sc >> 16);
@@ -440,14 +445,15 @@ template <int CK, int CV, int N>
 __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
                                               const uint8_t *const (&vus)[N],
                                               const int (&nvalid)[N], int lane,
-                                              const uint32_t (&qb)[8][2], float scale_log2,
+                                              const uint32_t (&qb)[8][2], const uint2 *qlo,
+                                              float scale_log2,
                                               float (&o)[8][4], float (&corr)[4],
                                               float &m0, float &m1, float &l0, float &l1) {
   const int g = lane >> 2;
   float sc[N][4];
 #pragma unroll
   for (int u = 0; u < N; ++u) {
-    unit_scores<CK>(ku[u], lane, qb, scale_log2, sc[u]);
+    unit_scores<CK>(ku[u], lane, qb, qlo, scale_log2, sc[u]);
     if (nvalid[u] < kUnitTokens) {
       if (g >= nvalid[u]) sc[u][0] = sc[u][1] = -INFINITY;
       if (g + 8 >= nvalid[u]) sc[u][2] = sc[u][3] = -INFINITY;
@@ -496,13 +502,14 @@ __device__ __forceinline__ void process_units(const uint8_t *const (&ku)[N],
 // K unit layout.
 template <int CK>
 __device__ __forceinline__ void load_q_frags(const __half *q, int64_t qrow0, int n_q, int G, int hg,
-                                             int lane, uint32_t (&qb)[8][2]) {
+                                             int lane, uint32_t (&qb)[8][2],
+                                             uint32_t (&qlo)[8][2]) {
   const int g = lane >> 2, tig = lane & 3;
   const int hq = hg * 8 + g;
   const bool hvalid = hq < G;
   const __half *qrow = q + (qrow0 + (hvalid ? hq : 0)) * kD;
   if (CK == KVQ_TURBO4) {
-    rotated_q_frags(qrow, hvalid, tig, qb, [](const __half *p) {
+    rotated_q_frags(qrow, hvalid, tig, qb, qlo, [](const __half *p) {
       return *reinterpret_cast<const uint2 *>(p);
     });
   } else {
@@ -526,12 +533,12 @@ __device__ __forceinline__ void load_q_frags(const __half *q, int64_t qrow0, int
 // (nh = rows present; row r is query head hg * 8 + r).
 template <int CK>
 __device__ __forceinline__ void load_q_frags_smem(const __half *qs, int nh, int lane,
-                                                  uint32_t (&qb)[8][2]) {
+                                                  uint32_t (&qb)[8][2], uint32_t (&qlo)[8][2]) {
   const int g = lane >> 2, tig = lane & 3;
   const bool hvalid = g < nh;
   const __half *qrow = qs + (hvalid ? g : 0) * kD;
   if (CK == KVQ_TURBO4) {
-    rotated_q_frags(qrow, hvalid, tig, qb, [](const __half *p) { return lds64(p); });
+    rotated_q_frags(qrow, hvalid, tig, qb, qlo, [](const __half *p) { return lds64(p); });
   } else {
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -730,6 +737,9 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
 
   uint8_t *ring = smem;
   float *red = reinterpret_cast<float *>(smem + C::RING);
+  // turbo4 keys: this lane's slots for the low halves of the rotated query
+  // (8 per lane, 2 KB per warp) at the start of the reduction slots
+  uint2 *const qlo = reinterpret_cast<uint2 *>(red) + warp * 8 * 32 + lane;
 
   // Issue unit k of this CTA's slice into stage k % NS (lane 0 of its owner).
   auto issue = [&](int k, const Cursor &c) {
@@ -806,7 +816,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     int len = attended_len(p, seq);
     len = len < p.max_len ? len : p.max_len;
 
-    uint32_t qb[8][2];
+    uint32_t qb[8][2], qlo_r[8][2];
     if (q_bulk) {
       const int buf = si & 1;
       bool got_q =
@@ -820,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
         ok = false;
         k_fail = k_next;
       }
-      load_q_frags_smem<CK>(q_s[buf], min(8, p.G - hg * 8), lane, qb);
+      load_q_frags_smem<CK>(q_s[buf], min(8, p.G - hg * 8), lane, qb, qlo_r);
       // The next segment's rows go out now, a whole segment ahead of their
       // use (q_s[buf ^ 1] was last read before the previous segment's
       // barriers).
@@ -831,7 +841,14 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
       }
     } else {
       load_q_frags<CK>(p.q, static_cast<int64_t>(seq) * p.n_q + kvh * p.G, p.n_q, p.G, hg, lane,
-                       qb);
+                       qb, qlo_r);
+    }
+    // turbo4 keys: the query's low halves wait in this warp's part of the
+    // reduction slots (free until the segment ends) rather than in registers
+    if (CK == KVQ_TURBO4) {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) qlo[c * 32] = make_uint2(qlo_r[c][0], qlo_r[c][1]);
+      __syncwarp();
     }
     float o[8][4];
 #pragma unroll
@@ -873,19 +890,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
           vu[u] = st + C::UPS * C::UK + u * C::UV;
           nv[u] = min(kUnitTokens, len - (C::UPS * j + u) * kUnitTokens);
         }
-        process_units<CK, CV, C::UPS>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0,
+        process_units<CK, CV, C::UPS>(ku, vu, nv, lane, qb, qlo, p.scale_log2, o, corr, m0, m1, l0,
                                       l1);
       } else if (two) {
         const uint8_t *ku[2] = {ring + s0 * C::STAGE, ring + s1 * C::STAGE};
         const uint8_t *vu[2] = {ku[0] + C::UK, ku[1] + C::UK};
         const int nv[2] = {min(kUnitTokens, len - j * kUnitTokens),
                            min(kUnitTokens, len - (j + kWarps) * kUnitTokens)};
-        process_units<CK, CV, 2>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
+        process_units<CK, CV, 2>(ku, vu, nv, lane, qb, qlo, p.scale_log2, o, corr, m0, m1, l0, l1);
       } else {
         const uint8_t *ku[1] = {ring + s0 * C::STAGE};
         const uint8_t *vu[1] = {ku[0] + C::UK};
         const int nv[1] = {min(kUnitTokens, len - j * kUnitTokens)};
-        process_units<CK, CV, 1>(ku, vu, nv, lane, qb, p.scale_log2, o, corr, m0, m1, l0, l1);
+        process_units<CK, CV, 1>(ku, vu, nv, lane, qb, qlo, p.scale_log2, o, corr, m0, m1, l0, l1);
       }
       // The consumed stages are free: refill them with units k + NS (+ 8).
       __syncwarp();
@@ -919,7 +936,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_split_kernel(const DecodeP
     }
 
     // Merge the 8 warps' partials for this segment: 8 -> 4 in pairs, then
-    // warp 0 takes in warps 1..3.  Four shared slots, three barriers.
+    // warp 0 takes in warps 1..3.  Four shared slots, three barriers (turbo4
+    // keys: one more first, as the slots hold the query's low halves until
+    // every warp has left the unit loop).
+    if (CK == KVQ_TURBO4) cta_bar();
     float *rs = red + lane * kRedFloats;
     if (warp >= 4) store_red(rs + (warp - 4) * 32 * kRedFloats, o, m0, m1, l0, l1);
     cta_bar();
@@ -990,8 +1010,9 @@ struct MergeParams {
   MergeArgs a;
   const int32_t *seq_lens;  // after the decode kernel (a fused step has advanced them)
   int n_seqs, n_kv, n_hg, max_len;
-  int ups;   // units per work item of the decode kernel's codec pair
-  int grid;  // the decode kernel's CTAs
+  int ups;    // units per work item of the decode kernel's codec pair
+  int grid;   // the decode kernel's CTAs
+  int fused;  // the decode kernel advances the lengths (a fused decode step)
 };
 
 // The log-sum-exp merge of every stream's partials (the second kernel of a
@@ -1015,9 +1036,12 @@ template <bool ROT>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const MergeParams p) {
   __shared__ int32_t pfx[kMaxSeqs + 1];
   __shared__ float4 accs[kMergeWarps][32];
-  grid_dependency_wait();  // the partials (and a fused step's lengths) are complete
-  grid_launch_dependents();
+  // The lengths are final once the decode kernel has started (this grid
+  // launches after every one of its CTAs passed its own dependency wait), and
+  // only a fused step changes them after that: a plain decode's partition is
+  // rebuilt while the decode kernel still runs, a fused step's after it.
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (p.fused) grid_dependency_wait();
   if (warp == 0) {
     const int item_tok = p.ups * kUnitTokens;
     int carry = 0;
@@ -1040,6 +1064,8 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Me
     }
     if (lane == 0) pfx[0] = 0;
   }
+  if (!p.fused) grid_dependency_wait();  // the partials are complete
+  grid_launch_dependents();
   __syncthreads();
   const int KH = p.n_kv * p.n_hg;
   const int stream = blockIdx.x, seq = stream / KH, sl = stream % KH;
@@ -1222,6 +1248,7 @@ cudaError_t launch_decode(const kvq_layer &L, const DecodePlan &pl, const void *
   mp.max_len = max_len;
   mp.ups = items_units(L.codec_k, L.codec_v);
   mp.grid = pl.grid;
+  mp.fused = k_new != nullptr;
   const dim3 mgrid(static_cast<unsigned>(p.n_seqs * p.n_kv * p.n_hg),
                    static_cast<unsigned>(p.G < 8 ? p.G : 8));
   const dim3 mblock(kMergeWarps * 32);

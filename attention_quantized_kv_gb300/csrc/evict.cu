@@ -83,7 +83,7 @@ __device__ __forceinline__ void kfrag_load(const uint8_t *ku, int lane, KFrag<CK
 // accumulator, then s += d * partial), fp32 accumulation.
 template <int CK>
 __device__ __forceinline__ void kfrag_scores(const KFrag<CK> &f, const uint32_t (&qb)[8][2],
-                                             float (&s)[4]) {
+                                             const uint32_t (&qlo)[8][2], float (&s)[4]) {
   s[0] = s[1] = s[2] = s[3] = 0.0f;
   if (CK == KVQ_F16) {
 #pragma unroll
@@ -97,6 +97,8 @@ __device__ __forceinline__ void kfrag_scores(const KFrag<CK> &f, const uint32_t 
     return;
   }
   if (CK == KVQ_TURBO4) {  // one scale per row: one accumulator for the four groups
+    // the rotated query as the fp16 pair qb + qlo: both halves multiply the
+    // same (exact) nibble operands
     float sb[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
@@ -109,6 +111,8 @@ __device__ __forceinline__ void kfrag_scores(const KFrag<CK> &f, const uint32_t 
                               u4_pair_minus8_hi(X0), u4_pair_minus8_hi(X1)};
       mma16816(sb, a0, qb[2 * b][0], qb[2 * b][1]);
       mma16816(sb, a1, qb[2 * b + 1][0], qb[2 * b + 1][1]);
+      mma16816(sb, a0, qlo[2 * b][0], qlo[2 * b][1]);
+      mma16816(sb, a1, qlo[2 * b + 1][0], qlo[2 * b + 1][1]);
     }
     const float dlo = __half2float(__ushort_as_half(static_cast<unsigned short>(f.sc.x)));
     const float dhi = __half2float(__ushort_as_half(static_cast<unsigned short>(f.sc.x >> 16)));
@@ -154,12 +158,12 @@ __device__ __forceinline__ void kfrag_scores(const KFrag<CK> &f, const uint32_t 
 // head-dim order of the codec's K unit layout.
 template <int CK>
 __device__ __forceinline__ void probe_q_frags(const __half *qrow0, int nh, int lane,
-                                              uint32_t (&qb)[8][2]) {
+                                              uint32_t (&qb)[8][2], uint32_t (&qlo)[8][2]) {
   const int g = lane >> 2, tig = lane & 3;
   const bool hvalid = g < nh;
   const __half *qrow = qrow0 + (hvalid ? g : 0) * kD;
-  if (CK == KVQ_TURBO4) {  // turbo4 keys: the rotated query
-    rotated_q_frags(qrow, hvalid, tig, qb,
+  if (CK == KVQ_TURBO4) {  // turbo4 keys: the rotated query (fp16 pair)
+    rotated_q_frags(qrow, hvalid, tig, qb, qlo,
                     [](const __half *p) { return __ldg(reinterpret_cast<const uint2 *>(p)); });
   } else {
 #pragma unroll
@@ -220,8 +224,8 @@ __global__ void __launch_bounds__(kProbeWarps * 32) probe_kernel(const ProbePara
         kfrag_load<CK>(p.k_cache + (unit0 + kvh * stride_h + warp + i * kProbeWarps) * UB, lane,
                        f[i]);
     const int nh = min(8, p.G - hg * 8);
-    uint32_t qb[8][2];
-    probe_q_frags<CK>(q_s + (static_cast<int64_t>(kvh) * p.G + hg * 8) * kD, nh, lane, qb);
+    uint32_t qb[8][2], qlo[8][2];
+    probe_q_frags<CK>(q_s + (static_cast<int64_t>(kvh) * p.G + hg * 8) * kD, nh, lane, qb, qlo);
     // log2-domain normalisers of the two heads in this lane's columns
     const int h0 = 2 * tig, h1 = 2 * tig + 1;
     const int64_t hrow = static_cast<int64_t>(kvh) * p.G + hg * 8;
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kProbeWarps * 32) probe_kernel(const ProbePara
     for (int i = 0; i < 2; ++i) {
       if (nvalid[i] <= 0) continue;  // warp-uniform
       float sc[4];
-      kfrag_scores<CK>(f[i], qb, sc);
+      kfrag_scores<CK>(f[i], qb, qlo, sc);
       const float p0 = fast_exp2(fmaf(sc[0], p.scale_log2, -n0));
       const float p1 = fast_exp2(fmaf(sc[1], p.scale_log2, -n1));
       const float p2 = fast_exp2(fmaf(sc[2], p.scale_log2, -n0));

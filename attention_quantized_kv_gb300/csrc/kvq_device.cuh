@@ -379,12 +379,15 @@ __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
-// turbo4 keys: the B fragments of the rotated query H (s * q) / 16 (fp32,
-// rounded to fp16 once), in the nibble codecs' k order; `ld` reads the 4
-// halves at a row offset (global or shared memory).
+// turbo4 keys: the B fragments of the rotated query H (s * q) / 16 in the
+// nibble codecs' k order, as an fp16 pair per value: qb = fp16(q_r) and
+// qlo = fp16(q_r - qb), so that qb + qlo carries q_r to within 2^-22 of its
+// size (two MMAs take the place of one); `ld` reads the 4 halves at a row
+// offset (global or shared memory).
 template <typename Ld>
 __device__ __forceinline__ void rotated_q_frags(const __half *qrow, bool hvalid, int tig,
-                                                uint32_t (&qb)[8][2], Ld ld) {
+                                                uint32_t (&qb)[8][2], uint32_t (&qlo)[8][2],
+                                                Ld ld) {
   float v[8][4];
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
@@ -400,6 +403,10 @@ __device__ __forceinline__ void rotated_q_frags(const __half *qrow, bool hvalid,
   for (int c = 0; c < 8; ++c) {
     qb[c][0] = pack_half2(v[c][0], v[c][2]);
     qb[c][1] = pack_half2(v[c][1], v[c][3]);
+    const float2 h0 = __half22float2(*reinterpret_cast<const __half2 *>(&qb[c][0]));
+    const float2 h1 = __half22float2(*reinterpret_cast<const __half2 *>(&qb[c][1]));
+    qlo[c][0] = pack_half2(v[c][0] - h0.x, v[c][2] - h0.y);
+    qlo[c][1] = pack_half2(v[c][1] - h1.x, v[c][3] - h1.y);
   }
 }
 

@@ -108,6 +108,15 @@ def get(name: str) -> Workload:
         return Workload(name, "decode", 2, 32, 4, [200704, 200704], _ladder(3), 3,
                         description="16 layers, 2 seqs x 200704 keys, 32q/4kv heads, "
                                     "per-(layer, side) f16/q8_0/q4_0 ladder")
+    if name in ("decode_ladder_layer0_2x200704", "decode_ladder_layer8_2x200704"):
+        # one layer of the 16-layer ladder (profiling size: ~0.5 / 0.8 GB of cache)
+        l = 0 if name.endswith("layer0_2x200704") else 8
+        w = get("decode_16layer_ladder_2x200704")
+        codecs = w.codecs[l]
+        names = ["f16", "q8_0", "q4_0"]
+        return Workload(name, "decode", 2, 32, 4, [200704, 200704], [codecs], 3,
+                        description=f"layer {l} of decode_16layer_ladder_2x200704 alone "
+                                    f"(K {names[codecs[0]]} / V {names[codecs[1]]})")
     if name == "prefill_q8_32k_plus_2k":
         return Workload(name, "prefill", 1, 32, 8, [32768], [(Q8_0, Q8_0)], 4, append_new=2048,
                         description="1 seq, 32768 cached + 2048-token ubatch appended, causal "
@@ -143,7 +152,8 @@ def get(name: str) -> Workload:
 
 
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
-       "decode_16layer_ladder_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
+       "decode_16layer_ladder_2x200704", "decode_ladder_layer0_2x200704",
+       "decode_ladder_layer8_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
        "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8", "evict_ragged4_kf16_vq8",
        "append_decode_turbo4_ctx32k"]
 
