@@ -11,6 +11,8 @@
 // row's places in the 16-token unit (see the layout in include/kvq.h).
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "kvq_device.cuh"
 #include "kvq_encode.cuh"
 #include "kvq_launch.h"
@@ -202,13 +204,15 @@ struct RequantParams {
   int32_t *err;
   const int32_t *table;  // paged layers: block table; nullptr: contiguous
   int src_codec, dst_codec, n_kv, capacity, pages_per_seq, n_pages;
+  int runs_per_stream;  // block re-encode: runs of kRbUnits units per (seq, kv head)
+  int64_t n_runs;       //                  in all
 };
 
 constexpr int kRqUnits = 8;  // units per CTA of the re-encode kernel
 static_assert(kPageUnits % kRqUnits == 0, "a run of units must lie inside one page");
 
-// One CTA per run of kRqUnits 16-token units of one (sequence, kv head)
-// stream.  The source units are copied into shared memory with coalesced
+// turbo4 on either side: one CTA per run of kRqUnits 16-token units of one
+// (sequence, kv head) stream.  The source units are copied into shared memory with coalesced
 // 16-byte loads (all of them requested before any is used); warp w then
 // re-encodes rows w, w + 16, ... below the sequence's length there (decode
 // exactly to fp32, then the append encoder of the new codec; an f16 target
@@ -277,46 +281,519 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
   grid_launch_dependents();
 }
 
+// ---------------------------------------------------------------------------
+// Re-encode between the block codecs (f16, q8_0, q4_0): one thread per
+// (unit, token row, 32-value block), so the block's amax or signed maximum is
+// a serial scan in registers and its divisions are taken once per block.
+// Persistent CTAs walk runs of kRbUnits units of a (sequence, kv head)
+// stream (run j of the flattened [seq][kv head][run] space goes to CTA
+// j % grid) through kRbStages source buffers: the source units of run
+// j + kRbStages * grid arrive by a bulk copy while the runs before it are
+// encoded.  Threads store their encoded pieces straight to the destination
+// (rows past a sequence's length are not written), so all of the shared
+// memory holds copies in flight.
+constexpr int kRbUnits = 4;
+constexpr int kRbThreads = kRbUnits * 64;
+constexpr int kRbStages = 4;  // source buffers: run i uses buffer i % kRbStages
+static_assert(kPageUnits % kRbUnits == 0, "a run of units must lie inside one page");
+
+// K side: for every codec the 32 values of block b of row r lie in four
+// pieces w = 0..3, piece w holding dims 32b + {4w..4w+3, 16+4w..16+4w+3} in
+// this order (f16: 16 bytes at (2b+rh)*512 + 64g + 16w; q8_0: 8 quants at
+// b*512 + 64g + 16w + 8rh; q4_0: canonical bytes 4w..4w+3 at
+// (b>>1)*512 + 64g + 16w + ((b&1)*2+rh)*4, low nibbles the first four
+// values, high nibbles the last four).  A thread visits its pieces in the
+// order w = (k + (g >> 1)) & 3, k = 0..3, which puts the eight threads of a
+// shared-memory phase (rows g = 0..7) on distinct banks.
+__host__ __device__ constexpr int rq_piece_dim(int w, int v) {
+  return v < 4 ? 4 * w + v : 16 + 4 * w + (v - 4);
+}
+
+// A chunk: the 8 values of one piece (K side) or of the same dims on the V
+// side, value v being dim rq_piece_dim(w, v) of the block.  V side (tig =
+// g >> 1, par = g & 1): f16 dim e at (2b + (e>>4))*512 + (4gq+tig)*16 +
+// (rh*4 + s*2 + par)*2 with gq = (e&15)>>1, s = e&1; q8_0 quant pair (e, e+1),
+// e even, at b*512 + (4gq+tig)*16 + ((e>>4)*2 + rh)*4 + par*2; q4_0 canonical
+// byte jc (dims jc and jc + 16) at (b>>1)*512 + (4(jc&7)+tig)*16 +
+// (2(b&1) + (jc>>3))*4 + par*2 + rh.
+struct RowGeo {
+  int g, rh, tig, par, b;
+};
+
+__device__ __forceinline__ int rq_v_f16_off(const RowGeo &q, int e) {
+  return (2 * q.b + (e >> 4)) * 512 + (4 * ((e & 15) >> 1) + q.tig) * 16 +
+         (q.rh * 4 + (e & 1) * 2 + q.par) * 2;
+}
+__device__ __forceinline__ int rq_v_q8_off(const RowGeo &q, int e) {  // e even
+  return q.b * 512 + (4 * ((e & 15) >> 1) + q.tig) * 16 + ((e >> 4) * 2 + q.rh) * 4 + q.par * 2;
+}
+__device__ __forceinline__ int rq_v_q4_off(const RowGeo &q, int jc) {
+  return (q.b >> 1) * 512 + (4 * (jc & 7) + q.tig) * 16 + (2 * (q.b & 1) + (jc >> 3)) * 4 +
+         q.par * 2 + q.rh;
+}
+__device__ __forceinline__ int rq_k_off(int codec, const RowGeo &q, int w) {
+  return codec == KVQ_F16    ? (2 * q.b + q.rh) * 512 + 64 * q.g + 16 * w
+         : codec == KVQ_Q8_0 ? q.b * 512 + 64 * q.g + 16 * w + 8 * q.rh
+                             : (q.b >> 1) * 512 + 64 * q.g + 16 * w + ((q.b & 1) * 2 + q.rh) * 4;
+}
+
+// The chunk's values, decoded exactly to fp32 (d: the source block's scale).
+template <int SIDE, int SC>
+__device__ __forceinline__ void rq_load_chunk(const uint8_t *u, const RowGeo &q, int w, float d,
+                                              float (&x)[8]) {
+  if (SC == KVQ_F16) {
+    uint32_t h[4];
+    if (SIDE == 0) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(u + rq_k_off(SC, q, w));
+      h[0] = raw.x; h[1] = raw.y; h[2] = raw.z; h[3] = raw.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e0 = rq_piece_dim(w, 2 * i);
+        h[i] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(u + rq_v_f16_off(q, e0))) |
+               (static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(
+                    u + rq_v_f16_off(q, e0 + 1)))
+                << 16);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h[i]));
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+    }
+  } else if (SC == KVQ_Q8_0) {
+    uint32_t lo, hi;  // quants of values 0..3 and 4..7, one per byte
+    if (SIDE == 0) {
+      const uint2 raw = *reinterpret_cast<const uint2 *>(u + rq_k_off(SC, q, w));
+      lo = raw.x;
+      hi = raw.y;
+    } else {
+      const uint32_t p0 = *reinterpret_cast<const uint16_t *>(u + rq_v_q8_off(q, 4 * w));
+      const uint32_t p1 = *reinterpret_cast<const uint16_t *>(u + rq_v_q8_off(q, 4 * w + 2));
+      const uint32_t p2 = *reinterpret_cast<const uint16_t *>(u + rq_v_q8_off(q, 16 + 4 * w));
+      const uint32_t p3 = *reinterpret_cast<const uint16_t *>(u + rq_v_q8_off(q, 18 + 4 * w));
+      lo = p0 | (p1 << 16);
+      hi = p2 | (p3 << 16);
+    }
+#pragma unroll
+    for (int v = 0; v < 8; ++v)
+      x[v] = d * static_cast<float>(
+                     static_cast<int8_t>(((v < 4 ? lo : hi) >> (8 * (v & 3))) & 0xffu));
+  } else {
+    uint32_t raw;  // canonical bytes 4w..4w+3
+    if (SIDE == 0) {
+      raw = *reinterpret_cast<const uint32_t *>(u + rq_k_off(SC, q, w));
+    } else {
+      raw = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        raw |= static_cast<uint32_t>(u[rq_v_q4_off(q, 4 * w + i)]) << (8 * i);
+    }
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const int n = static_cast<int>((raw >> (8 * (v & 3) + (v < 4 ? 0 : 4))) & 0xfu);
+      x[v] = d * static_cast<float>(n - 8);
+    }
+  }
+}
+
+// Bytes 0 of a, b, c, d as one word (a in the lowest byte).
+__device__ __forceinline__ uint32_t low_bytes4(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+// Four byte lanes holding 0..16, each clamped to 15 (16 - (16 >> 4)).
+__device__ __forceinline__ uint32_t clamp15x4(uint32_t w) { return w - ((w >> 4) & 0x01010101u); }
+
+// Store a chunk: f16 from x; else the codes k, words whose lowest byte is
+// the code (q8_0: q & 0xff; q4_0: the level 0..16 before the clamp to 15).
+template <int SIDE, int DC>
+__device__ __forceinline__ void rq_store_chunk(uint8_t *u, const RowGeo &q, int w,
+                                               const float (&x)[8], const uint32_t (&k)[8]) {
+  if (DC == KVQ_F16) {
+    uint32_t h[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 t = __floats2half2_rn(x[2 * i], x[2 * i + 1]);
+      h[i] = *reinterpret_cast<const uint32_t *>(&t);
+    }
+    if (SIDE == 0) {
+      *reinterpret_cast<uint4 *>(u + rq_k_off(DC, q, w)) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int e0 = rq_piece_dim(w, 2 * i);
+        *reinterpret_cast<uint16_t *>(u + rq_v_f16_off(q, e0)) = static_cast<uint16_t>(h[i]);
+        *reinterpret_cast<uint16_t *>(u + rq_v_f16_off(q, e0 + 1)) =
+            static_cast<uint16_t>(h[i] >> 16);
+      }
+    }
+  } else if (DC == KVQ_Q8_0) {
+    const uint32_t lo = low_bytes4(k[0], k[1], k[2], k[3]), hi = low_bytes4(k[4], k[5], k[6], k[7]);
+    if (SIDE == 0) {
+      *reinterpret_cast<uint2 *>(u + rq_k_off(DC, q, w)) = make_uint2(lo, hi);
+    } else {
+      uint16_t *const pr[4] = {reinterpret_cast<uint16_t *>(u + rq_v_q8_off(q, 4 * w)),
+                               reinterpret_cast<uint16_t *>(u + rq_v_q8_off(q, 4 * w + 2)),
+                               reinterpret_cast<uint16_t *>(u + rq_v_q8_off(q, 16 + 4 * w)),
+                               reinterpret_cast<uint16_t *>(u + rq_v_q8_off(q, 18 + 4 * w))};
+      *pr[0] = static_cast<uint16_t>(lo);
+      *pr[1] = static_cast<uint16_t>(lo >> 16);
+      *pr[2] = static_cast<uint16_t>(hi);
+      *pr[3] = static_cast<uint16_t>(hi >> 16);
+    }
+  } else {
+    const uint32_t lo = clamp15x4(low_bytes4(k[0], k[1], k[2], k[3]));
+    const uint32_t hi = clamp15x4(low_bytes4(k[4], k[5], k[6], k[7]));
+    const uint32_t word = lo | (hi << 4);  // canonical bytes 4w..4w+3
+    if (SIDE == 0) {
+      *reinterpret_cast<uint32_t *>(u + rq_k_off(DC, q, w)) = word;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        u[rq_v_q4_off(q, 4 * w + i)] = static_cast<uint8_t>(word >> (8 * i));
+    }
+  }
+}
+
+// The quotient path of q8_from_quotient / q4_from_quotient on one chunk, two
+// values per instruction: k[v] gets the fast path's code (its lowest byte;
+// q4_0: the level before the clamp), and lo / hi collect the chunk's
+// distances from the rounding boundaries (q8_0: hi = the largest distance
+// to the nearest integer; q4_0: lo, hi = the range of u - floor(u)), which
+// say whether the fast path is the exact one for every value.
+template <int DC>
+__device__ __forceinline__ void rq_codes_fast(const float (&x)[8], float rcp, uint32_t (&k)[8],
+                                              float &lo, float &hi) {
+  const float2 r2 = make_float2(rcp, rcp), m2 = make_float2(kRoundMagic, kRoundMagic);
+  const float2 nm2 = make_float2(-kRoundMagic, -kRoundMagic), n1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    if (DC == KVQ_Q8_0) {
+      const float2 t = __fmul2_rn(make_float2(x[j], x[j + 1]), r2);
+      const float2 tm = __fadd2_rn(t, m2);
+      const float2 fr = __ffma2_rn(__fadd2_rn(tm, nm2), n1, t);  // t - round(t)
+      hi = fmaxf(hi, fmaxf(fabsf(fr.x), fabsf(fr.y)));
+      k[j] = __float_as_uint(tm.x);
+      k[j + 1] = __float_as_uint(tm.y);
+    } else {
+      const float2 u =
+          __fadd2_rn(__fmul2_rn(make_float2(x[j], x[j + 1]), r2), make_float2(8.5f, 8.5f));
+      const float2 fm = __fadd2_rn(__fadd2_rn(u, make_float2(-0.5f, -0.5f)), m2);
+      const float2 fr = __ffma2_rn(__fadd2_rn(fm, nm2), n1, u);  // u - floor(u)
+      lo = fminf(lo, fminf(fr.x, fr.y));
+      hi = fmaxf(hi, fmaxf(fr.x, fr.y));
+      k[j] = __float_as_uint(fm.x);
+      k[j + 1] = __float_as_uint(fm.y);
+    }
+  }
+}
+
+// One (unit, row, block) item: decode the block exactly and encode it with
+// the append encoder of DC (q8_0: d = amax / 127; q4_0: d = m / -8 with m the
+// signed value of largest magnitude, lowest dim on ties; the quotient rule
+// of q8_from_quotient / q4_from_quotient), in two passes over the chunks
+// (the block's statistics, then the codes) so that few values are live.
+// The codes take the two-at-a-time fast path; if any value of the block
+// lies too near its rounding boundary, the block is encoded again value by
+// value with the exact path.
 template <int SIDE, int SC, int DC>
-cudaError_t launch_requant_t(const RequantParams &p, dim3 grid, int smem, cudaStream_t stream) {
+__device__ __forceinline__ void rq_encode_item(const uint8_t *su, uint8_t *du, int r, int b) {
+  RowGeo q;
+  q.g = r & 7;
+  q.rh = r >> 3;
+  q.tig = q.g >> 1;
+  q.par = q.g & 1;
+  q.b = b;
+  const int rot = SIDE == 0 ? q.g >> 1 : 0;  // K side: the piece order (c + rot) & 3
+  const int soff =
+      SIDE == 0 ? q.g * 16 + q.rh * 8 + b * 2 : q.tig * 32 + b * 8 + q.rh * 4 + q.par * 2;
+  const float ds = SC == KVQ_F16 ? 0.0f
+                                 : __half2float(*reinterpret_cast<const __half *>(
+                                       su + unit_scale_offset(SC) + soff));
+  const uint32_t zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (DC == KVQ_F16) {
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int w = (c + rot) & 3;
+      float x[8];
+      rq_load_chunk<SIDE, SC>(su, q, w, ds, x);
+      rq_store_chunk<SIDE, DC>(du, q, w, x, zero);
+    }
+    return;
+  }
+  // pass 1: amax (q8_0) or the largest and smallest value (q4_0)
+  float pmax, nmin;
+  if (SIDE == 0 && SC == KVQ_F16) {  // on the fp16 values themselves (exact)
+    __half2 hp = __float2half2_rn(-65504.0f), hn = __float2half2_rn(65504.0f);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 raw = *reinterpret_cast<const uint4 *>(su + rq_k_off(SC, q, (c + rot) & 3));
+      const uint32_t h[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 v = *reinterpret_cast<const __half2 *>(&h[i]);
+        if (DC == KVQ_Q8_0) {
+          hp = __hmax2(hp, __habs2(v));
+        } else {
+          hp = __hmax2(hp, v);
+          hn = __hmin2(hn, v);
+        }
+      }
+    }
+    pmax = fmaxf(__low2float(hp), __high2float(hp));
+    nmin = fminf(__low2float(hn), __high2float(hn));
+  } else {
+    pmax = DC == KVQ_Q8_0 ? 0.0f : -INFINITY;
+    nmin = INFINITY;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float x[8];
+      rq_load_chunk<SIDE, SC>(su, q, (c + rot) & 3, ds, x);
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        if (DC == KVQ_Q8_0) {
+          pmax = fmaxf(pmax, fabsf(x[v]));
+        } else {
+          pmax = fmaxf(pmax, x[v]);
+          nmin = fminf(nmin, x[v]);
+        }
+      }
+    }
+  }
+  float d;
+  if (DC == KVQ_Q8_0) {
+    d = __fdiv_rn(pmax, 127.0f);
+  } else {
+    float m = pmax > -nmin ? pmax : nmin;
+    if (pmax == -nmin) {  // both signs reach the largest magnitude (or all zero)
+      float best = -1.0f;
+      int idx = 32;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int w = (c + rot) & 3;
+        float x[8];
+        rq_load_chunk<SIDE, SC>(su, q, w, ds, x);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float a = fabsf(x[v]);
+          const int dim = rq_piece_dim(w, v);
+          if (a > best || (a == best && dim < idx)) { best = a; m = x[v]; idx = dim; }
+        }
+      }
+    }
+    d = __fdiv_rn(m, -8.0f);
+  }
+  *reinterpret_cast<__half *>(du + unit_scale_offset(DC) + soff) = __float2half_rn(d);
+  const float rcp = d != 0.0f ? __frcp_rn(d) : 0.0f;
+  // pass 2: the codes
+  float lo = 1.0f, hi = 0.0f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int w = (c + rot) & 3;
+    float x[8];
+    uint32_t k[8];
+    rq_load_chunk<SIDE, SC>(su, q, w, ds, x);
+    if (d != 0.0f) {
+      rq_codes_fast<DC>(x, rcp, k, lo, hi);
+    } else {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) k[v] = DC == KVQ_Q8_0 ? 0u : 8u;
+    }
+    rq_store_chunk<SIDE, DC>(du, q, w, x, k);
+  }
+  const bool exact =
+      DC == KVQ_Q8_0 ? hi < 0.5f - 0x1p-14f : (lo > 0x1p-17f && hi < 1.0f - 0x1p-17f);
+  if (d != 0.0f && !exact) {  // rare: some quotient near a boundary
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int w = (c + rot) & 3;
+      float x[8];
+      uint32_t k[8];
+      rq_load_chunk<SIDE, SC>(su, q, w, ds, x);
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        k[v] = static_cast<uint32_t>(DC == KVQ_Q8_0 ? q8_from_quotient(x[v], d, rcp)
+                                                    : q4_from_quotient(x[v], d, rcp));
+      rq_store_chunk<SIDE, DC>(du, q, w, x, k);
+    }
+  }
+}
+
+template <int SIDE, int SC, int DC>
+__global__ void __launch_bounds__(kRbThreads, DC == KVQ_Q4_0 ? 2 : 3)
+    rq_block_kernel(RequantParams p) {
+  constexpr int sb = unit_bytes(SC), db = unit_bytes(DC);
+  constexpr int SB = kRbUnits * sb;
+  extern __shared__ __align__(128) uint8_t rb_smem[];
+  __shared__ __align__(8) uint64_t full[kRbStages];
+  __shared__ int abort_flag;
+  uint8_t *const sbuf0 = rb_smem;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int q = 0; q < kRbStages; ++q) mbar_init(&full[q], 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  grid_dependency_wait();
+
+  // Thread 0 describes run j when it issues its copy (info[buf], read by
+  // every thread after the buffer's barrier): the length of its sequence,
+  // its first unit in the stream and in the cache or pool, and its number of
+  // units below the length (0: nothing to do).  The run's global reads (its
+  // length, its block-table entry) go out one run ahead (prepare), so that
+  // their latency hides behind the encoding of the current run.
+  struct RunInfo {
+    int n, u0, len, pad;
+    int64_t uidx;
+  };
+  struct RunPre {
+    int s, kvh, u0, len, pg;
+  };
+  __shared__ RunInfo info[kRbStages];
+  const uint32_t rps = static_cast<uint32_t>(p.runs_per_stream);
+  auto prepare = [&](int64_t j) {
+    const uint32_t jj = static_cast<uint32_t>(j);  // n_runs < 2^31 (checked by the host)
+    const uint32_t t = jj / rps;
+    RunPre pr;
+    pr.kvh = static_cast<int>(t % static_cast<uint32_t>(p.n_kv));
+    pr.s = static_cast<int>(t / static_cast<uint32_t>(p.n_kv));
+    pr.u0 = static_cast<int>(jj - t * rps) * kRbUnits;
+    pr.len = p.seq_lens[pr.s];
+    pr.pg = p.table ? page_of(p.table, p.pages_per_seq, p.n_pages, pr.s, pr.u0 / kPageUnits) : 0;
+    return pr;
+  };
+  auto issue = [&](const RunPre &pr, int buf) {
+    RunInfo ri;
+    ri.len = min(pr.len, p.capacity);
+    ri.u0 = pr.u0;
+    ri.n = max(0, min(kRbUnits, (ri.len + kUnitTokens - 1) / kUnitTokens - ri.u0));
+    ri.pad = 0;
+    ri.uidx = 0;
+    if (ri.n > 0) {
+      if (p.table) {
+        if (pr.pg < 0) {
+          set_err(p.err, KVQ_DEVERR_PAGE);
+          ri.n = 0;
+        } else {
+          ri.uidx = (static_cast<int64_t>(pr.pg) * p.n_kv + pr.kvh) * kPageUnits +
+                    ri.u0 % kPageUnits;
+        }
+      } else {
+        ri.uidx = (static_cast<int64_t>(pr.s) * p.n_kv + pr.kvh) * (p.capacity / kUnitTokens) +
+                  ri.u0;
+      }
+    }
+    info[buf] = ri;
+    // an empty run only completes the buffer's barrier phase
+    const uint32_t bytes = static_cast<uint32_t>(ri.n * sb);
+    mbar_arrive_expect_tx(&full[buf], bytes);
+    if (bytes) bulk_copy_g2s(sbuf0 + buf * SB, p.src + ri.uidx * sb, bytes, &full[buf]);
+  };
+
+  const int64_t G = gridDim.x;
+  int64_t issued = 0;  // thread 0: runs issued (the i-th into buffer i % kRbStages)
+  if (tid == 0) {
+    for (int64_t j = blockIdx.x; j < p.n_runs && issued < kRbStages; j += G, ++issued)
+      issue(prepare(j), static_cast<int>(issued));
+  }
+  const int ul = tid >> 6, r = tid & 15, b = (tid >> 4) & 3;
+  int i = 0;
+  for (int64_t j = blockIdx.x; j < p.n_runs; j += G, ++i) {
+    const int buf = i % kRbStages;
+    const bool got = mbar_wait_bounded(&full[buf], static_cast<uint32_t>(i / kRbStages) & 1u,
+                                       &abort_flag);
+    if (!got && tid == 0) {
+      set_err(p.err, KVQ_DEVERR_TIMEOUT);
+      atomicExch(&abort_flag, 1);
+    }
+    __syncthreads();
+    if (*reinterpret_cast<volatile int *>(&abort_flag) != 0) break;  // CTA-uniform
+    const RunInfo ri = info[buf];
+    const int64_t jn = j + kRbStages * G;  // the run that takes this buffer next
+    RunPre pre{};
+    if (tid == 0 && jn < p.n_runs) pre = prepare(jn);
+    if (ul < ri.n && (ri.u0 + ul) * kUnitTokens + r < ri.len)
+      rq_encode_item<SIDE, SC, DC>(sbuf0 + buf * SB + ul * sb, p.dst + (ri.uidx + ul) * db, r,
+                                   b);
+    __syncthreads();  // every thread is done with buffer buf
+    if (tid == 0 && jn < p.n_runs) {
+      fence_proxy_async_smem();
+      issue(pre, buf);
+      ++issued;
+    }
+  }
+  if (tid == 0) {
+    // after an abort: the copies still in flight into this CTA's buffers
+    // (runs i .. issued - 1)
+    for (int64_t q = i; q < issued; ++q)
+      mbar_wait_bounded(&full[q % kRbStages], static_cast<uint32_t>(q / kRbStages) & 1u);
+  }
+  grid_launch_dependents();
+}
+
+template <int SIDE, int SC, int DC>
+cudaError_t launch_requant_t(const RequantParams &p, dim3 grid, int smem, int num_sms,
+                             cudaStream_t stream) {
   static std::atomic<uint64_t> optin{0};
-  const cudaError_t e = smem_optin(requant_kernel<SIDE, SC, DC>, kRqUnits * 2 * 4096, optin);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(requant_kernel<SIDE, SC, DC>, grid, dim3(kUnitTokens * 32), smem, stream, p);
+  if constexpr (SC != KVQ_TURBO4 && DC != KVQ_TURBO4) {  // block codecs: a thread per block
+    constexpr int rb_smem = kRbStages * kRbUnits * unit_bytes(SC);
+    const cudaError_t e = smem_optin(rq_block_kernel<SIDE, SC, DC>, rb_smem, optin);
+    if (e != cudaSuccess) return e;
+    static std::atomic<int> per_sm{0};  // resident CTAs per SM
+    if (per_sm.load() == 0) {
+      int n = 0;
+      const cudaError_t eo = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &n, rq_block_kernel<SIDE, SC, DC>, kRbThreads, rb_smem);
+      if (eo != cudaSuccess) return eo;
+      per_sm.store(n > 0 ? n : 1);
+    }
+    const int64_t g = std::min<int64_t>(p.n_runs, static_cast<int64_t>(per_sm.load()) *
+                                                      (num_sms > 0 ? num_sms : 148));
+    if (g <= 0) return cudaSuccess;
+    return launch_pdl(rq_block_kernel<SIDE, SC, DC>, dim3(static_cast<unsigned>(g)),
+                      dim3(kRbThreads), rb_smem, stream, p);
+  } else {  // turbo4 rotates whole rows: a warp per row
+    const cudaError_t e = smem_optin(requant_kernel<SIDE, SC, DC>, kRqUnits * 2 * 4096, optin);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(requant_kernel<SIDE, SC, DC>, grid, dim3(kUnitTokens * 32), smem, stream,
+                      p);
+  }
 }
 
 template <int SIDE, int SC>
-cudaError_t launch_requant_d(int dc, const RequantParams &p, dim3 grid, int smem,
+cudaError_t launch_requant_d(int dc, const RequantParams &p, dim3 grid, int smem, int num_sms,
                              cudaStream_t stream) {
   switch (dc) {
-    case KVQ_F16: return launch_requant_t<SIDE, SC, KVQ_F16>(p, grid, smem, stream);
-    case KVQ_Q8_0: return launch_requant_t<SIDE, SC, KVQ_Q8_0>(p, grid, smem, stream);
-    case KVQ_Q4_0: return launch_requant_t<SIDE, SC, KVQ_Q4_0>(p, grid, smem, stream);
-    default: return launch_requant_t<SIDE, SC, KVQ_TURBO4>(p, grid, smem, stream);
+    case KVQ_F16: return launch_requant_t<SIDE, SC, KVQ_F16>(p, grid, smem, num_sms, stream);
+    case KVQ_Q8_0: return launch_requant_t<SIDE, SC, KVQ_Q8_0>(p, grid, smem, num_sms, stream);
+    case KVQ_Q4_0: return launch_requant_t<SIDE, SC, KVQ_Q4_0>(p, grid, smem, num_sms, stream);
+    default: return launch_requant_t<SIDE, SC, KVQ_TURBO4>(p, grid, smem, num_sms, stream);
   }
 }
 
 template <int SIDE>
 cudaError_t launch_requant_c(int sc, int dc, const RequantParams &p, dim3 grid, int smem,
-                             cudaStream_t stream) {
+                             int num_sms, cudaStream_t stream) {
   switch (sc) {
-    case KVQ_F16: return launch_requant_d<SIDE, KVQ_F16>(dc, p, grid, smem, stream);
-    case KVQ_Q8_0: return launch_requant_d<SIDE, KVQ_Q8_0>(dc, p, grid, smem, stream);
-    case KVQ_Q4_0: return launch_requant_d<SIDE, KVQ_Q4_0>(dc, p, grid, smem, stream);
-    default: return launch_requant_d<SIDE, KVQ_TURBO4>(dc, p, grid, smem, stream);
+    case KVQ_F16: return launch_requant_d<SIDE, KVQ_F16>(dc, p, grid, smem, num_sms, stream);
+    case KVQ_Q8_0: return launch_requant_d<SIDE, KVQ_Q8_0>(dc, p, grid, smem, num_sms, stream);
+    case KVQ_Q4_0: return launch_requant_d<SIDE, KVQ_Q4_0>(dc, p, grid, smem, num_sms, stream);
+    default: return launch_requant_d<SIDE, KVQ_TURBO4>(dc, p, grid, smem, num_sms, stream);
   }
 }
 
 cudaError_t launch_requant_s(int side, int sc, int dc, const RequantParams &p, dim3 grid,
-                             int smem, cudaStream_t stream) {
-  return side == 0 ? launch_requant_c<0>(sc, dc, p, grid, smem, stream)
-                   : launch_requant_c<1>(sc, dc, p, grid, smem, stream);
+                             int smem, int num_sms, cudaStream_t stream) {
+  return side == 0 ? launch_requant_c<0>(sc, dc, p, grid, smem, num_sms, stream)
+                   : launch_requant_c<1>(sc, dc, p, grid, smem, num_sms, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *dst_cache,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int num_sms) {
   RequantParams p;
   p.src = static_cast<const uint8_t *>(side == 0 ? L.k_cache : L.v_cache);
   p.dst = static_cast<uint8_t *>(dst_cache);
@@ -330,9 +807,12 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
   p.n_kv = L.n_kv_heads;
   p.capacity = L.capacity;
   const int units = L.capacity / kUnitTokens;
-  const dim3 grid((units + kRqUnits - 1) / kRqUnits, L.n_kv_heads, L.n_seqs);
+  p.runs_per_stream = (units + kRbUnits - 1) / kRbUnits;
+  p.n_runs = static_cast<int64_t>(p.runs_per_stream) * L.n_kv_heads * L.n_seqs;
+  if (p.n_runs >= (int64_t{1} << 31)) return cudaErrorInvalidValue;  // 32-bit run indices
+  const dim3 grid((units + kRqUnits - 1) / kRqUnits, L.n_kv_heads, L.n_seqs);  // turbo4 kernel
   const int smem = kRqUnits * (unit_bytes(p.src_codec) + unit_bytes(dst_codec));
-  return launch_requant_s(side, p.src_codec, dst_codec, p, grid, smem, stream);
+  return launch_requant_s(side, p.src_codec, dst_codec, p, grid, smem, num_sms, stream);
 }
 
 cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_new,

@@ -183,7 +183,8 @@ int kv_requantize(const kvq_layer *layer, int32_t side, int32_t dst_codec, void 
                                              layer->capacity, kHeadDim);
   if (d0 < s0 + sb && s0 < d0 + db) return KVQ_EINVAL;
   const cudaError_t e =
-      kvq::launch_requant(*layer, side, dst_codec, dst_cache, static_cast<cudaStream_t>(stream));
+      kvq::launch_requant(*layer, side, dst_codec, dst_cache, static_cast<cudaStream_t>(stream),
+                          device_sms());
   return e == cudaSuccess ? KVQ_OK : KVQ_ECUDA;
 }
 

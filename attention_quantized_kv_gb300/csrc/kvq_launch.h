@@ -16,7 +16,7 @@ cudaError_t launch_append(const kvq_layer &L, const void *k_new, const void *v_n
 // Re-encode one side of the layer into dst_cache (dst_codec): tokens below
 // each sequence's length (append.cu).
 cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *dst_cache,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int num_sms);
 
 constexpr int kDecodeMaxSeqs = 1024;         // sequences per attn_decode call
 // counter region at the workspace start (zero between calls); its last word

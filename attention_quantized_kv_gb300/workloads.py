@@ -43,6 +43,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass, field
 
+import re
+
 import numpy as np
 import torch
 
@@ -108,9 +110,11 @@ def get(name: str) -> Workload:
         return Workload(name, "decode", 2, 32, 4, [200704, 200704], _ladder(3), 3,
                         description="16 layers, 2 seqs x 200704 keys, 32q/4kv heads, "
                                     "per-(layer, side) f16/q8_0/q4_0 ladder")
-    if name in ("decode_ladder_layer0_2x200704", "decode_ladder_layer8_2x200704"):
-        # one layer of the 16-layer ladder (profiling size: ~0.5 / 0.8 GB of cache)
-        l = 0 if name.endswith("layer0_2x200704") else 8
+    m = re.fullmatch(r"decode_ladder_layer(\d+)_2x200704", name)
+    if m and int(m.group(1)) < 16:
+        # one layer of the 16-layer ladder alone (a profiling size: 0.23 to
+        # 0.82 GB of cache)
+        l = int(m.group(1))
         w = get("decode_16layer_ladder_2x200704")
         codecs = w.codecs[l]
         names = ["f16", "q8_0", "q4_0"]
@@ -133,6 +137,13 @@ def get(name: str) -> Workload:
                         extra={"side": 0, "dst": Q8_0},
                         description="one degrade-ladder step: re-encode the K side of a "
                                     "2 x 200704-key layer (4 kv heads) from f16 to q8_0")
+    if name == "degrade_v_f16_q8_2x200704":
+        w = get("degrade_f16_q8_2x200704")
+        w.name = name
+        w.extra = {"side": 1, "dst": Q8_0}
+        w.description = ("one degrade-ladder step on the V side: re-encode the V side of a "
+                         "2 x 200704-key layer (4 kv heads) from f16 to q8_0")
+        return w
     if name == "evict_ragged16_kf16_vq8":
         w = get("decode_ragged16_kf16_vq8")
         w.name, w.kind = name, "evict"
@@ -154,6 +165,7 @@ def get(name: str) -> Workload:
 ALL = ["decode_q8_ctx4k", "append_decode_q4_ctx32k", "decode_ragged16_kf16_vq8",
        "decode_16layer_ladder_2x200704", "decode_ladder_layer0_2x200704",
        "decode_ladder_layer8_2x200704", "prefill_q8_32k_plus_2k", "degrade_f16_q8_2x200704",
+       "degrade_v_f16_q8_2x200704",
        "decode_ragged16_kf16_vq8_paged", "evict_ragged16_kf16_vq8", "evict_ragged4_kf16_vq8",
        "append_decode_turbo4_ctx32k"]
 

@@ -623,7 +623,7 @@ def run_ours(args, w, rank, world, dist):
         kname = {"decode": "attn_decode_append (decode_split_kernel with the append fused, "
                            "decode_merge_kernel)" if arm.fused
                  else "attn_decode (decode_split_kernel, decode_merge_kernel)",
-                 "degrade": "kv_requantize (requant_kernel)",
+                 "degrade": "kv_requantize (rq_block_kernel; requant_kernel for turbo4)",
                  "evict": "kv_compact (compact_kernel)"}[w.kind]
         line["roofline"] = {"bound": "hbm", "kernel": kname,
                             "achieved": round(achieved_attn, 2), "peak": hbm,

@@ -58,6 +58,53 @@ def test_requantize_bit_exact(src, dst, side):
     assert np.array_equal(dst_gpu.cpu().numpy(), o_dst)
 
 
+@pytest.mark.parametrize("side", [0, 1])
+@pytest.mark.parametrize("src,dst", [(0, 1), (0, 2), (1, 2), (2, 0), (1, 1)])
+def test_requantize_many_runs_per_cta(src, dst, side):
+    """Thousands of 64-token runs, more than the persistent grid holds at
+    once, mostly empty ones (a whole empty sequence, a short one) between
+    long streams with a partial last unit: every CTA walks several runs
+    through both buffers each way."""
+    n_seqs, n_kv, cap = 3, 2, 40960
+    lens = [0, 37, 40001]
+    rng = np.random.default_rng(70 + 3 * src + dst + 9 * side)
+    rows = _rows(rng, n_seqs, max(lens), n_kv, [1.0, 1e-3, 40.0])
+    o_src = np.zeros(oracle.cache_bytes(src, n_seqs, n_kv, cap), np.uint8)
+    oracle.append_side(src, side, o_src, n_seqs, n_kv, cap, [0] * n_seqs, lens, rows)
+    o_dst = oracle.requantize_side(src, dst, side, o_src, n_seqs, n_kv, cap, lens)
+    ck, cv = (src, 1) if side == 0 else (1, src)
+    L = kvq.KVLayer(n_seqs, n_kv, 2 * n_kv, cap, ck, cv,
+                    k_cache=torch.zeros(kvq.kvq_cache_bytes(ck, n_seqs, n_kv, cap),
+                                        dtype=torch.uint8, device="cuda"),
+                    v_cache=torch.zeros(kvq.kvq_cache_bytes(cv, n_seqs, n_kv, cap),
+                                        dtype=torch.uint8, device="cuda"))
+    x = torch.from_numpy(rows).cuda()
+    kvq.kv_append_quantize(L, x, x, torch.tensor(lens, dtype=torch.int32, device="cuda"))
+    assert np.array_equal((L.k_cache if side == 0 else L.v_cache).cpu().numpy(), o_src)
+    # bytes past the lengths must survive: start the destination from a pattern
+    dst_gpu = torch.full((kvq.kvq_cache_bytes(dst, n_seqs, n_kv, cap),), 0xA5, dtype=torch.uint8,
+                         device="cuda")
+    kvq.kv_requantize(L, side, dst, dst_gpu)
+    torch.cuda.synchronize()
+    assert L.err.item() == 0
+    # expected: the oracle's bytes for rows below the length, the pattern for
+    # every other byte (the row of each unit byte from the oracle's layout)
+    ub = oracle.cache_bytes(dst, 1, 1, 16)
+    row_of = np.empty(ub, np.int32)
+    table = oracle.unit_offset_table(dst, side)
+    for r in range(16):
+        row_of[table[r]] = r
+    tok = (np.arange(cap // 16)[:, None] * 16 + row_of[None, :]).reshape(-1)  # per stream byte
+    want = np.full(o_dst.shape, 0xA5, np.uint8)
+    per_stream = (cap // 16) * ub
+    for s_ in range(n_seqs):
+        for h in range(n_kv):
+            base = (s_ * n_kv + h) * per_stream
+            keep = tok < lens[s_]
+            want[base:base + per_stream][keep] = o_dst[base:base + per_stream][keep]
+    np.testing.assert_array_equal(dst_gpu.cpu().numpy(), want)
+
+
 def test_requantize_rejects_overlap_and_bad_arguments():
     L = kvq.KVLayer(1, 1, 1, 256, 0, 0)
     with pytest.raises(kvq.KVQError):
