@@ -240,6 +240,8 @@ def _evict_lists(rng, lens, kind):
         elif kind == "random":
             k = rng.integers(0, ln + 1) // 3
             out.append(np.sort(rng.choice(ln, k, replace=False)).astype(np.int32))
+        elif kind == "light":  # ~5%: a run's sources fit the stage (the pipelined path)
+            out.append(np.sort(rng.choice(ln, ln // 20, replace=False)).astype(np.int32))
         elif kind == "span":  # one long run: sources jump across many units
             a = ln // 5
             out.append(np.arange(a, a + ln // 2, dtype=np.int32))
@@ -251,7 +253,7 @@ def _evict_lists(rng, lens, kind):
 
 
 @pytest.mark.parametrize("ck,cv", [(0, 1), (1, 2), (2, 0), (2, 2), (1, 1), (0, 0), (3, 3), (3, 1)])
-@pytest.mark.parametrize("kind", ["random", "span", "sparse_keep", "none", "all"])
+@pytest.mark.parametrize("kind", ["random", "light", "span", "sparse_keep", "none", "all"])
 def test_compact_bit_exact(ck, cv, kind):
     n_seqs, n_kv, n_q, cap = 4, 2, 4, 2048
     lens = [0, 37, 1500, 2048]
@@ -282,6 +284,34 @@ def test_compact_bit_exact(ck, cv, kind):
     for s in range(n_seqs):
         kept = np.delete(sc[s, :lens[s]], evl[s])
         assert np.array_equal(got_s[s, :new_lens[s]], kept)
+
+
+@pytest.mark.parametrize("ck,cv", [(0, 1), (2, 3)])
+def test_compact_many_kv_heads(ck, cv):
+    """8 kv heads: each run's 16 (kv head, side) pairs cycle through the two
+    stage buffers several times; light and heavy eviction mixed over the
+    sequences (pipelined and round-by-round runs in one launch)."""
+    n_seqs, n_kv, n_q, cap = 3, 8, 16, 2048
+    lens = [2048, 1999, 700]
+    rng = np.random.default_rng(400 + 3 * ck + cv)
+    kr, vr = _rows(rng, n_seqs, cap, n_kv), _rows(rng, n_seqs, cap, n_kv)
+    L, ok, ov = _caches(ck, cv, n_seqs, n_kv, n_q, cap, lens, kr, vr)
+    evl = [np.sort(rng.choice(2048, 90, replace=False)).astype(np.int32),
+           np.sort(rng.choice(1999, 700, replace=False)).astype(np.int32),
+           np.arange(100, 400, dtype=np.int32)]
+    me = max(len(e) for e in evl)
+    ev = np.zeros((n_seqs, me), np.int32)
+    for s, e in enumerate(evl):
+        ev[s, :len(e)] = e
+    nev = np.array([len(e) for e in evl], np.int32)
+    k_dst, v_dst = torch.zeros_like(L.k_cache), torch.zeros_like(L.v_cache)
+    kvq.kv_compact(L, torch.from_numpy(ev).cuda(), torch.from_numpy(nev).cuda(), k_dst, v_dst)
+    torch.cuda.synchronize()
+    assert L.err.item() == 0
+    want_k = oracle.compact_side(ck, 0, ok, n_seqs, n_kv, cap, lens, evl)
+    want_v = oracle.compact_side(cv, 1, ov, n_seqs, n_kv, cap, lens, evl)
+    assert np.array_equal(k_dst.cpu().numpy(), want_k)
+    assert np.array_equal(v_dst.cpu().numpy(), want_v)
 
 
 def test_compact_paged_pools_bit_exact():
