@@ -204,8 +204,8 @@ struct RequantParams {
   int32_t *err;
   const int32_t *table;  // paged layers: block table; nullptr: contiguous
   int src_codec, dst_codec, n_kv, capacity, pages_per_seq, n_pages;
-  int runs_per_stream;  // block re-encode: runs of kRbUnits units per (seq, kv head)
-  int64_t n_runs;       //                  in all
+  int units_per_stream;  // block re-encode: units per (seq, kv head) stream
+  int64_t n_units;       //                  in all
 };
 
 constexpr int kRqUnits = 8;  // units per CTA of the re-encode kernel
@@ -285,17 +285,17 @@ __global__ void __launch_bounds__(kUnitTokens * 32) requant_kernel(RequantParams
 // Re-encode between the block codecs (f16, q8_0, q4_0): one thread per
 // (unit, token row, 32-value block), so the block's amax or signed maximum is
 // a serial scan in registers and its divisions are taken once per block.
-// Persistent CTAs walk runs of kRbUnits units of a (sequence, kv head)
-// stream (run j of the flattened [seq][kv head][run] space goes to CTA
-// j % grid) through kRbStages source buffers: the source units of run
-// j + kRbStages * grid arrive by a bulk copy while the runs before it are
-// encoded.  Threads store their encoded pieces straight to the destination
-// (rows past a sequence's length are not written), so all of the shared
-// memory holds copies in flight.
-constexpr int kRbUnits = 4;
-constexpr int kRbThreads = kRbUnits * 64;
-constexpr int kRbStages = 4;  // source buffers: run i uses buffer i % kRbStages
-static_assert(kPageUnits % kRbUnits == 0, "a run of units must lie inside one page");
+// Every warp of the persistent grid works alone, with no CTA-wide barrier:
+// it walks 16-token units of the flattened [seq][kv head][unit] space (unit
+// j goes to warp j % (all warps)) through kRbStages shared-memory stages of
+// its own.  Lane 0 bulk-copies the source unit j + kRbStages * (all warps)
+// into a stage as soon as the warp is done with it, so kRbStages - 1 units
+// per warp are in flight while one is encoded; each lane encodes two of the
+// unit's 64 (row, block) items and stores the encoded pieces straight to the
+// destination (rows past a sequence's length are not written).
+constexpr int kRbWarps = 8;
+constexpr int kRbThreads = kRbWarps * 32;
+constexpr int kRbStages = 2;  // source stages per warp: a warp's unit i uses stage i % kRbStages
 
 // K side: for every codec the 32 values of block b of row r lie in four
 // pieces w = 0..3, piece w holding dims 32b + {4w..4w+3, 16+4w..16+4w+3} in
@@ -624,111 +624,108 @@ template <int SIDE, int SC, int DC>
 __global__ void __launch_bounds__(kRbThreads, DC == KVQ_Q4_0 ? 2 : 3)
     rq_block_kernel(RequantParams p) {
   constexpr int sb = unit_bytes(SC), db = unit_bytes(DC);
-  constexpr int SB = kRbUnits * sb;
   extern __shared__ __align__(128) uint8_t rb_smem[];
-  __shared__ __align__(8) uint64_t full[kRbStages];
-  __shared__ int abort_flag;
-  uint8_t *const sbuf0 = rb_smem;
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int q = 0; q < kRbStages; ++q) mbar_init(&full[q], 1);
-    abort_flag = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-  grid_dependency_wait();
-
-  // Thread 0 describes run j when it issues its copy (info[buf], read by
-  // every thread after the buffer's barrier): the length of its sequence,
-  // its first unit in the stream and in the cache or pool, and its number of
-  // units below the length (0: nothing to do).  The run's global reads (its
-  // length, its block-table entry) go out one run ahead (prepare), so that
-  // their latency hides behind the encoding of the current run.
-  struct RunInfo {
-    int n, u0, len, pad;
+  __shared__ __align__(8) uint64_t full[kRbWarps][kRbStages];
+  // lane 0 describes each unit when it issues its copy: the rows below the
+  // length (0: nothing to do) and the unit's index in the cache or pool
+  struct UnitInfo {
+    int rows, pad;
     int64_t uidx;
   };
-  struct RunPre {
-    int s, kvh, u0, len, pg;
+  __shared__ UnitInfo info[kRbWarps][kRbStages];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t *const stage0 = rb_smem + warp * kRbStages * sb;
+  if (lane == 0) {
+    for (int q = 0; q < kRbStages; ++q) mbar_init(&full[warp][q], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  grid_dependency_wait();
+
+  // The unit's global reads (its sequence's length, its block-table entry)
+  // go out one unit ahead (prepare), so that their latency hides behind the
+  // encoding of the current unit.
+  struct UnitPre {
+    int s, kvh, u, len, pg;
   };
-  __shared__ RunInfo info[kRbStages];
-  const uint32_t rps = static_cast<uint32_t>(p.runs_per_stream);
+  const uint32_t ups = static_cast<uint32_t>(p.units_per_stream);
   auto prepare = [&](int64_t j) {
-    const uint32_t jj = static_cast<uint32_t>(j);  // n_runs < 2^31 (checked by the host)
-    const uint32_t t = jj / rps;
-    RunPre pr;
+    const uint32_t jj = static_cast<uint32_t>(j);  // n_units < 2^31 (checked by the host)
+    const uint32_t t = jj / ups;
+    UnitPre pr;
     pr.kvh = static_cast<int>(t % static_cast<uint32_t>(p.n_kv));
     pr.s = static_cast<int>(t / static_cast<uint32_t>(p.n_kv));
-    pr.u0 = static_cast<int>(jj - t * rps) * kRbUnits;
+    pr.u = static_cast<int>(jj - t * ups);
     pr.len = p.seq_lens[pr.s];
-    pr.pg = p.table ? page_of(p.table, p.pages_per_seq, p.n_pages, pr.s, pr.u0 / kPageUnits) : 0;
+    pr.pg = p.table ? page_of(p.table, p.pages_per_seq, p.n_pages, pr.s, pr.u / kPageUnits) : 0;
     return pr;
   };
-  auto issue = [&](const RunPre &pr, int buf) {
-    RunInfo ri;
-    ri.len = min(pr.len, p.capacity);
-    ri.u0 = pr.u0;
-    ri.n = max(0, min(kRbUnits, (ri.len + kUnitTokens - 1) / kUnitTokens - ri.u0));
-    ri.pad = 0;
-    ri.uidx = 0;
-    if (ri.n > 0) {
+  auto issue = [&](const UnitPre &pr, int st) {  // lane 0
+    UnitInfo ui;
+    ui.rows = max(0, min(kUnitTokens, min(pr.len, p.capacity) - pr.u * kUnitTokens));
+    ui.pad = 0;
+    ui.uidx = 0;
+    if (ui.rows > 0) {
       if (p.table) {
         if (pr.pg < 0) {
           set_err(p.err, KVQ_DEVERR_PAGE);
-          ri.n = 0;
+          ui.rows = 0;
         } else {
-          ri.uidx = (static_cast<int64_t>(pr.pg) * p.n_kv + pr.kvh) * kPageUnits +
-                    ri.u0 % kPageUnits;
+          ui.uidx = (static_cast<int64_t>(pr.pg) * p.n_kv + pr.kvh) * kPageUnits +
+                    pr.u % kPageUnits;
         }
       } else {
-        ri.uidx = (static_cast<int64_t>(pr.s) * p.n_kv + pr.kvh) * (p.capacity / kUnitTokens) +
-                  ri.u0;
+        ui.uidx = static_cast<int64_t>(pr.s * p.n_kv + pr.kvh) * ups + pr.u;
       }
     }
-    info[buf] = ri;
-    // an empty run only completes the buffer's barrier phase
-    const uint32_t bytes = static_cast<uint32_t>(ri.n * sb);
-    mbar_arrive_expect_tx(&full[buf], bytes);
-    if (bytes) bulk_copy_g2s(sbuf0 + buf * SB, p.src + ri.uidx * sb, bytes, &full[buf]);
+    info[warp][st] = ui;
+    // an empty unit only completes the stage's barrier phase
+    const uint32_t bytes = ui.rows > 0 ? static_cast<uint32_t>(sb) : 0u;
+    mbar_arrive_expect_tx(&full[warp][st], bytes);
+    if (bytes) bulk_copy_g2s(stage0 + st * sb, p.src + ui.uidx * sb, bytes, &full[warp][st]);
   };
 
-  const int64_t G = gridDim.x;
-  int64_t issued = 0;  // thread 0: runs issued (the i-th into buffer i % kRbStages)
-  if (tid == 0) {
-    for (int64_t j = blockIdx.x; j < p.n_runs && issued < kRbStages; j += G, ++issued)
+  const int64_t W = static_cast<int64_t>(gridDim.x) * kRbWarps;
+  const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kRbWarps + warp;
+  int64_t issued = 0;  // lane 0: units issued (the i-th into stage i % kRbStages)
+  if (lane == 0) {
+    for (int64_t j = j0; j < p.n_units && issued < kRbStages; j += W, ++issued)
       issue(prepare(j), static_cast<int>(issued));
   }
-  const int ul = tid >> 6, r = tid & 15, b = (tid >> 4) & 3;
+  __syncwarp();
   int i = 0;
-  for (int64_t j = blockIdx.x; j < p.n_runs; j += G, ++i) {
-    const int buf = i % kRbStages;
-    const bool got = mbar_wait_bounded(&full[buf], static_cast<uint32_t>(i / kRbStages) & 1u,
-                                       &abort_flag);
-    if (!got && tid == 0) {
-      set_err(p.err, KVQ_DEVERR_TIMEOUT);
-      atomicExch(&abort_flag, 1);
+  for (int64_t j = j0; j < p.n_units; j += W, ++i) {
+    const int st = i % kRbStages;
+    const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(
+                                                  &full[warp][st],
+                                                  static_cast<uint32_t>(i / kRbStages) & 1u));
+    if (!got) {
+      if (lane == 0) set_err(p.err, KVQ_DEVERR_TIMEOUT);
+      break;
     }
-    __syncthreads();
-    if (*reinterpret_cast<volatile int *>(&abort_flag) != 0) break;  // CTA-uniform
-    const RunInfo ri = info[buf];
-    const int64_t jn = j + kRbStages * G;  // the run that takes this buffer next
-    RunPre pre{};
-    if (tid == 0 && jn < p.n_runs) pre = prepare(jn);
-    if (ul < ri.n && (ri.u0 + ul) * kUnitTokens + r < ri.len)
-      rq_encode_item<SIDE, SC, DC>(sbuf0 + buf * SB + ul * sb, p.dst + (ri.uidx + ul) * db, r,
-                                   b);
-    __syncthreads();  // every thread is done with buffer buf
-    if (tid == 0 && jn < p.n_runs) {
+    const UnitInfo ui = info[warp][st];
+    const int64_t jn = j + kRbStages * W;  // the unit that takes this stage next
+    UnitPre pre{};
+    if (lane == 0 && jn < p.n_units) pre = prepare(jn);
+#pragma unroll 1
+    for (int t = 0; t < 2; ++t) {  // items lane and lane + 32: row item & 15, block item >> 4
+      const int item = lane + 32 * t, r = item & 15, b = item >> 4;
+      if (r < ui.rows)
+        rq_encode_item<SIDE, SC, DC>(stage0 + st * sb, p.dst + ui.uidx * db, r, b);
+    }
+    __syncwarp();  // every lane is done with the stage
+    if (lane == 0 && jn < p.n_units) {
       fence_proxy_async_smem();
-      issue(pre, buf);
+      issue(pre, st);
       ++issued;
     }
+    __syncwarp();
   }
-  if (tid == 0) {
-    // after an abort: the copies still in flight into this CTA's buffers
-    // (runs i .. issued - 1)
+  if (lane == 0) {
+    // after a timeout: the copies still in flight into this warp's stages
+    // (units i .. issued - 1)
     for (int64_t q = i; q < issued; ++q)
-      mbar_wait_bounded(&full[q % kRbStages], static_cast<uint32_t>(q / kRbStages) & 1u);
+      mbar_wait_bounded(&full[warp][q % kRbStages], static_cast<uint32_t>(q / kRbStages) & 1u);
   }
   grid_launch_dependents();
 }
@@ -738,7 +735,7 @@ cudaError_t launch_requant_t(const RequantParams &p, dim3 grid, int smem, int nu
                              cudaStream_t stream) {
   static std::atomic<uint64_t> optin{0};
   if constexpr (SC != KVQ_TURBO4 && DC != KVQ_TURBO4) {  // block codecs: a thread per block
-    constexpr int rb_smem = kRbStages * kRbUnits * unit_bytes(SC);
+    constexpr int rb_smem = kRbWarps * kRbStages * unit_bytes(SC);
     const cudaError_t e = smem_optin(rq_block_kernel<SIDE, SC, DC>, rb_smem, optin);
     if (e != cudaSuccess) return e;
     static std::atomic<int> per_sm{0};  // resident CTAs per SM
@@ -749,8 +746,9 @@ cudaError_t launch_requant_t(const RequantParams &p, dim3 grid, int smem, int nu
       if (eo != cudaSuccess) return eo;
       per_sm.store(n > 0 ? n : 1);
     }
-    const int64_t g = std::min<int64_t>(p.n_runs, static_cast<int64_t>(per_sm.load()) *
-                                                      (num_sms > 0 ? num_sms : 148));
+    const int64_t g =
+        std::min<int64_t>((p.n_units + kRbWarps - 1) / kRbWarps,
+                          static_cast<int64_t>(per_sm.load()) * (num_sms > 0 ? num_sms : 148));
     if (g <= 0) return cudaSuccess;
     return launch_pdl(rq_block_kernel<SIDE, SC, DC>, dim3(static_cast<unsigned>(g)),
                       dim3(kRbThreads), rb_smem, stream, p);
@@ -807,9 +805,9 @@ cudaError_t launch_requant(const kvq_layer &L, int side, int dst_codec, void *ds
   p.n_kv = L.n_kv_heads;
   p.capacity = L.capacity;
   const int units = L.capacity / kUnitTokens;
-  p.runs_per_stream = (units + kRbUnits - 1) / kRbUnits;
-  p.n_runs = static_cast<int64_t>(p.runs_per_stream) * L.n_kv_heads * L.n_seqs;
-  if (p.n_runs >= (int64_t{1} << 31)) return cudaErrorInvalidValue;  // 32-bit run indices
+  p.units_per_stream = units;
+  p.n_units = static_cast<int64_t>(units) * L.n_kv_heads * L.n_seqs;
+  if (p.n_units >= (int64_t{1} << 31)) return cudaErrorInvalidValue;  // 32-bit unit indices
   const dim3 grid((units + kRqUnits - 1) / kRqUnits, L.n_kv_heads, L.n_seqs);  // turbo4 kernel
   const int smem = kRqUnits * (unit_bytes(p.src_codec) + unit_bytes(dst_codec));
   return launch_requant_s(side, p.src_codec, dst_codec, p, grid, smem, num_sms, stream);
