@@ -392,9 +392,20 @@ __device__ __forceinline__ int qt_tiles(const AttnParams &p, int qt) {
 // query tile qt), item index g * n_qt + qt, each item a run of qt_tiles(qt)
 // key-tile steps.  CTA c takes the steps [W c / P, W (c + 1) / P): whole
 // items, plus pieces of the first and last ones.  A segment is one item's
-// piece [j_lo, j_hi) of key tiles.
+// piece [j_lo, j_hi) of steps.
+//
+// Step j of an item reads key tile (j + rot) % nt rather than tile j.  The
+// item's rotation puts its tiles in step with every CTA's own clock: the
+// owner of the item's last step starts the item (or its piece of it) at the
+// point of its slice where it reads tile 0 + (its slice position) mod nt, so
+// that at any moment the CTAs working on one kv head read about the same
+// tile.  The ~19 CTAs of a kv head then share each tile through L2 instead of
+// each reading the whole kv head from HBM at its own pace.  (Softmax over
+// the tiles in any order gives the same result up to rounding; the causal
+// mask follows the tile, not the step.)
 struct Segment {
   int g, qt, j_lo, j_hi, nt;  // nt: the item's key tiles
+  int rot;                    // step j reads key tile (j + rot) % nt
   int64_t start;              // the item's first step
 };
 struct SegIter {
@@ -420,6 +431,15 @@ struct SegIter {
     seg.qt = qt;
     seg.nt = nt;
     seg.start = item_start;
+    {
+      // the owner of the item's last step and the first step of its slice
+      const int64_t P = gridDim.x;
+      const int64_t last = item_start + nt - 1;
+      const int64_t c_last = ((last + 1) * P - 1) / p.W;
+      const int64_t slice0 = p.W * c_last / P;
+      const int64_t r = (item_start - slice0) % nt;
+      seg.rot = static_cast<int>(r < 0 ? r + nt : r);
+    }
     seg.j_lo = static_cast<int>(s - item_start);
     const int64_t end = min(s1, item_start + nt);
     seg.j_hi = static_cast<int>(end - item_start);
@@ -515,11 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
         const uint8_t *vt = p.vtiles + static_cast<int64_t>(kvh) * p.n_tiles * kTileBytes;
         for (int j = sg.j_lo; j < sg.j_hi; ++j, ++t) {
           const int s = t % kStages;
+          const int64_t tile = (j + sg.rot) % sg.nt;
           const uint32_t ph = static_cast<uint32_t>(t / kStages - 1) & 1u;
           if (t >= kStages && !mbar_wait_bounded(&bars.kempty[s], ph, &abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars.kfull[s], kTileBytes);
-          bulk_copy_g2s(sk + s * kTileBytes, kt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
-                        &bars.kfull[s]);
+          bulk_copy_g2s(sk + s * kTileBytes, kt + tile * kTileBytes, kTileBytes, &bars.kfull[s]);
           if (t >= kStages && !mbar_wait_bounded(&bars.vempty[s], ph, &abort_flag)) {
             // the V copy of this tile was not started: drain below counts t + 1 K copies
             mbar_wait_bounded(&bars.kfull[s], static_cast<uint32_t>(t / kStages) & 1u, nullptr,
@@ -528,8 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
             break;
           }
           mbar_arrive_expect_tx(&bars.vfull[s], kTileBytes);
-          bulk_copy_g2s(sv + s * kTileBytes, vt + static_cast<int64_t>(j) * kTileBytes, kTileBytes,
-                        &bars.vfull[s]);
+          bulk_copy_g2s(sv + s * kTileBytes, vt + tile * kTileBytes, kTileBytes, &bars.vfull[s]);
         }
       }
       // After an abort, wait (bounded) for the copies still landing in the ring.
@@ -697,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
           break;
         }
         tc_fence_after();
-        const int kbase = j * kBN;
+        const int kbase = ((j + sg.rot) % sg.nt) * kBN;
         // Tiles crossing some row's position (warp-uniform test): the scores of
         // keys past the row's position are overwritten with -inf in TMEM, so
         // that pass 2 needs no mask.
