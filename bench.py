@@ -840,8 +840,13 @@ def cpu_baseline(w):
     allc = time_oracle(w, 1, 0, min_seconds=10.0, budget_rows=2e7)
     one = time_oracle(w, 1, 0, min_seconds=10.0, threads=1, budget_rows=2e6)
     allc["host_cores"] = os.cpu_count()
-    allc["parallel_over"] = ("(kv head group, query head) rows of each sampled layer"
-                             if w.kind == "decode" else "query rows")
+    allc["parallel_over"] = {
+        "decode": "(kv head group, query head) rows of each sampled layer",
+        "prefill": "query rows",
+        "degrade": "tokens of each sampled stream",
+        "evict": "decode: query rows; probe: tokens; compaction: (seq, kv head) streams; "
+                 "selection: one thread",
+    }[w.kind]
     allc["single_thread"] = {k: one[k] for k in ("value", "unit", "cores", "sample", "seconds")}
     return allc
 

@@ -703,16 +703,21 @@ int kvqo_requantize_side(int src_codec, int dst_codec, int side, const uint8_t *
     if (kvqo_row_bytes(src_codec) < 0 || kvqo_row_bytes(dst_codec) < 0 ||
         capacity % KVQO_UNIT_TOKENS)
         return -1;
-    uint8_t row[256], out[256];
-    double xd[KVQO_D];
-    float x[KVQO_D];
-    for (int s = 0; s < n_seqs; ++s) {
+    for (int s = 0; s < n_seqs; ++s)
         if (seq_lens[s] < 0 || seq_lens[s] > capacity)
             return -1;
+    int bad = 0;
+    for (int s = 0; s < n_seqs; ++s) {
         for (int h = 0; h < n_kv; ++h) {
             const uint8_t *ss = kvqo_stream((uint8_t *)src, src_codec, n_kv, capacity, s, h);
             uint8_t *ds = kvqo_stream(dst, dst_codec, n_kv, capacity, s, h);
+            /* rows are independent: OpenMP over tokens, same bytes on any
+             * thread count */
+#pragma omp parallel for schedule(static)
             for (int64_t t = 0; t < seq_lens[s]; ++t) {
+                uint8_t row[256], out[256];
+                double xd[KVQO_D];
+                float x[KVQO_D];
                 kvqo_get_row(ss, src_codec, side, t, row);
                 kvqo_decode_rows(src_codec, 1, row, xd);
                 for (int d = 0; d < KVQO_D; ++d)
@@ -724,22 +729,28 @@ int kvqo_requantize_side(int src_codec, int dst_codec, int side, const uint8_t *
                         out[2 * d + 1] = (uint8_t)(hb >> 8);
                     }
                 } else if (dst_codec == KVQO_TURBO4) {
-                    if (kvqo_turbo4_encode_row_f32(x, out))
-                        return -1;
+                    if (kvqo_turbo4_encode_row_f32(x, out)) {
+#pragma omp atomic write
+                        bad = 1;
+                        continue;
+                    }
                 } else {
-                    for (int b = 0; b < 4; ++b) {
-                        int rc = dst_codec == KVQO_Q8_0
-                                     ? kvqo_q8_0_encode_block_f32(x + 32 * b, out + 34 * b)
-                                     : kvqo_q4_0_encode_block_f32(x + 32 * b, out + 18 * b);
-                        if (rc)
-                            return -1;
+                    int rc = 0;
+                    for (int b = 0; b < 4; ++b)
+                        rc |= dst_codec == KVQO_Q8_0
+                                  ? kvqo_q8_0_encode_block_f32(x + 32 * b, out + 34 * b)
+                                  : kvqo_q4_0_encode_block_f32(x + 32 * b, out + 18 * b);
+                    if (rc) {
+#pragma omp atomic write
+                        bad = 1;
+                        continue;
                     }
                 }
                 kvqo_put_row(ds, dst_codec, side, t, out);
             }
         }
     }
-    return 0;
+    return bad ? -1 : 0;
 }
 
 /* Bits per value of a codec: row bytes * 8 / head_dim (16, 8.5, 4.5). */
@@ -818,7 +829,12 @@ int kvqo_probe_mass(int codec_k, const uint8_t *cache_k, int n_seqs, int n_kv, i
             kvqo_dequant_stream(codec_k, KVQO_SIDE_K, cache_k, n_kv, capacity, s, h, T, K);
             for (int j = 0; j < G; ++j) {
                 const uint16_t *qh = q + ((int64_t)s * n_q + (int64_t)h * G + j) * KVQO_D;
+                /* the scores and the per-token additions are independent per
+                 * token (OpenMP over tokens); the normaliser is summed on one
+                 * thread in token order, so the bits do not depend on the
+                 * thread count */
                 double mx = -INFINITY;
+#pragma omp parallel for schedule(static) reduction(max : mx)
                 for (int64_t t = 0; t < T; ++t) {
                     double d = 0.0;
                     for (int c = 0; c < KVQO_D; ++c)
@@ -830,6 +846,7 @@ int kvqo_probe_mass(int codec_k, const uint8_t *cache_k, int n_seqs, int n_kv, i
                 double sum = 0.0;
                 for (int64_t t = 0; t < T; ++t)
                     sum += exp(sc[t] - mx);
+#pragma omp parallel for schedule(static)
                 for (int64_t t = 0; t < T; ++t)
                     m[t] += exp(sc[t] - mx) / sum;
             }
@@ -881,10 +898,13 @@ int kvqo_compact_side(int codec, int side, const uint8_t *src, uint8_t *dst, int
 {
     if (kvqo_row_bytes(codec) < 0)
         return -1;
-    uint8_t row[256];
+    /* streams are independent: OpenMP over (seq, kv head), same bytes on any
+     * thread count */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
     for (int s = 0; s < n_seqs; ++s) {
-        const int32_t *ev = evict + (int64_t)s * max_evict;
         for (int h = 0; h < n_kv; ++h) {
+            uint8_t row[256];
+            const int32_t *ev = evict + (int64_t)s * max_evict;
             const uint8_t *ss = kvqo_stream((uint8_t *)src, codec, n_kv, capacity, s, h);
             uint8_t *ds = kvqo_stream(dst, codec, n_kv, capacity, s, h);
             int e = 0;

@@ -918,3 +918,31 @@ def test_append_is_identical_on_one_thread_and_on_all():
             oracle.append_side(codec, 1, a, 2, 3, cap, [5, 0], [395, 400], x)
         oracle.append_side(codec, 1, b, 2, 3, cap, [5, 0], [395, 400], x)
         assert np.array_equal(a, b)
+
+
+def test_requantize_compact_and_probe_are_identical_on_one_thread_and_on_all():
+    """Rows, streams and tokens are independent in these three: the bytes (and
+    the probe mass, whose normaliser is summed on one thread in token order)
+    must not depend on the thread count."""
+    rng = np.random.default_rng(83)
+    cap, n_kv, n_seqs = 512, 2, 2
+    lens = [400, 137]
+    x = rng.standard_normal((n_seqs, 400, n_kv, 128)).astype(np.float16)
+    for src, dst in ((0, 1), (1, 2), (2, 3), (3, 0)):
+        c = np.zeros(oracle.cache_bytes(src, n_seqs, n_kv, cap), np.uint8)
+        oracle.append_side(src, 0, c, n_seqs, n_kv, cap, [0, 0], lens, x)
+        with oracle.threads(1):
+            a = oracle.requantize_side(src, dst, 0, c, n_seqs, n_kv, cap, lens)
+        b = oracle.requantize_side(src, dst, 0, c, n_seqs, n_kv, cap, lens)
+        assert np.array_equal(a, b)
+        ev = [np.sort(rng.choice(lens[s], lens[s] // 4, replace=False)).astype(np.int32)
+              for s in range(n_seqs)]
+        with oracle.threads(1):
+            ca = oracle.compact_side(src, 0, c, n_seqs, n_kv, cap, lens, ev)
+        cb = oracle.compact_side(src, 0, c, n_seqs, n_kv, cap, lens, ev)
+        assert np.array_equal(ca, cb)
+        q = rng.standard_normal((n_seqs, 8, 128)).astype(np.float16)
+        with oracle.threads(1):
+            ma = oracle.probe_mass(src, c, n_seqs, n_kv, 8, cap, lens, q, 0.088)
+        mb = oracle.probe_mass(src, c, n_seqs, n_kv, 8, cap, lens, q, 0.088)
+        assert np.array_equal(ma, mb)
