@@ -146,6 +146,38 @@ def test_paged_prefill_matches_contiguous_and_requantize_bit_exact():
     assert np.array_equal(paged.v_cache.cpu().numpy(), want)
 
 
+@pytest.mark.parametrize("side", [0, 1])
+@pytest.mark.parametrize("src,dst", [(0, 1), (1, 2), (2, 0), (0, 3)])
+def test_paged_requantize_many_pages_bit_exact(src, dst, side):
+    """Re-encode one side of a shuffled pool of 64 pages (three ragged
+    sequences, one of them empty): every warp walks many pool units, each
+    looked up in the block table, and the bytes equal the oracle's re-encode
+    moved into the same pages; the other side is untouched."""
+    n_seqs, n_kv, n_q, pps, n_pages = 3, 2, 4, 24, 64
+    cap = pps * 256
+    lens = [6000, 0, 4097]
+    rng = np.random.default_rng(90 + 3 * src + dst + 11 * side)
+    table = _table(rng, n_seqs, pps, n_pages, lens)
+    ck, cv = (src, 1) if side == 0 else (1, src)
+    kr, vr = _rows(rng, n_seqs, max(lens), n_kv), _rows(rng, n_seqs, max(lens), n_kv)
+    paged, _ = _layers(ck, cv, n_seqs, n_kv, n_q, cap, n_pages, table)
+    _append_in_pieces(paged, kr, vr, lens, 3)
+    torch.cuda.synchronize()
+    codec = ck if side == 0 else cv
+    cache = paged.k_cache if side == 0 else paged.v_cache
+    other = (paged.v_cache if side == 0 else paged.k_cache).clone()
+    o = oracle.from_pool(codec, cache.cpu().numpy(), n_seqs, n_kv, cap, table, n_pages)
+    re = oracle.requantize_side(codec, dst, side, o, n_seqs, n_kv, cap, lens)
+    want = oracle.to_pool(dst, re, n_seqs, n_kv, cap, table, n_pages)
+    got = torch.zeros(kvq.kvq_pool_bytes(dst, n_pages, n_kv), dtype=torch.uint8, device="cuda")
+    kvq.kv_requantize(paged, side, dst, got)
+    torch.cuda.synchronize()
+    assert paged.err.item() == 0
+    # pool units no sequence uses were not written (the oracle's pool is zero there)
+    assert np.array_equal(got.cpu().numpy(), want)
+    assert torch.equal(other, paged.v_cache if side == 0 else paged.k_cache)
+
+
 def test_out_of_pool_entries_are_flagged_not_faulted():
     n_seqs, n_kv, n_q, pps, n_pages = 1, 1, 2, 2, 2
     cap = pps * 256
