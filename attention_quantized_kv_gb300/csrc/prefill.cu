@@ -7,7 +7,7 @@
 // buffers are sized by the ubatch alone; the chunk's K/V are quantize-appended
 // first, then attended in their quantized form).
 //
-// Two kernels:
+// Three kernels:
 //  1. dequant_tiles: the attended keys of both sides, dequantized (x^ = d * q,
 //     rounded once to fp16; f16 is copied), written to the workspace as
 //     128-key tiles already in the tensor core's shared-memory operand layout
@@ -20,8 +20,7 @@
 //     queries attend), and each CTA takes an equal contiguous slice of all
 //     steps in (kv head, pair, query tile) order: whole items plus pieces of
 //     at most two more.  A piece writes its rows as partials (unnormalised O,
-//     max, sum); the last CTA to finish a piece of the item (an atomic
-//     ticket) merges the pieces by log-sum-exp.  Roles (12 warps): warps 0-3
+//     max, sum) and the CTA moves on.  Roles (12 warps): warps 0-3
 //     and 4-7 are the softmax warpgroups of the pair's two heads (one query
 //     row per thread, TMEM lane quadrant = warp % 4); warp 8 is the
 //     producer, streaming K and V tiles into a two-stage ring by bulk async
@@ -37,6 +36,9 @@
 //     used for P is only raised (and O, l rescaled) when a row's max grows by
 //     more than 2^8, which keeps O rescales rare and the result exact (the
 //     same max scales O and l).
+//  3. piece_merge: the items split over several CTAs, merged by log-sum-exp
+//     once the attention kernel has completed (a CTA per item and head, a
+//     thread per query row), so that no CTA waits at its end for the merge.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -261,9 +263,8 @@ struct DequantParams {
   uint8_t *tiles[2];   // [n_kv][n_tiles][32 KB]
   const int32_t *seq_lens;
   int32_t *err;
-  unsigned *tickets;  // the attention kernel's arrival counters, zeroed here
   const int32_t *table;  // paged layers: block table; nullptr: contiguous
-  int seq, n_kv, capacity, kv_len, n_tiles, n_items, pages_per_seq, n_pages;
+  int seq, n_kv, capacity, kv_len, n_tiles, pages_per_seq, n_pages;
 };
 
 // grid: (n_tiles, n_kv, 2 sides); 256 threads.  The tile's eight 16-token
@@ -338,10 +339,9 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
 __global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams p) {
   __shared__ __align__(16) uint8_t units_sh[kBN / kUnitTokens * 4096];
   grid_dependency_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
-    if (threadIdx.x == 0 && p.seq_lens[p.seq] < p.kv_len) set_err(p.err, KVQ_DEVERR_SEQLEN);
-    for (int i = threadIdx.x; i < p.n_items; i += blockDim.x) p.tickets[i] = 0u;
-  }
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
+      p.seq_lens[p.seq] < p.kv_len)
+    set_err(p.err, KVQ_DEVERR_SEQLEN);
   const int side = blockIdx.z, codec = p.codec[side];
   if (side == 0) {
     if (codec == KVQ_F16) dequant_tile<KVQ_F16, 0>(p, units_sh);
@@ -367,7 +367,6 @@ struct AttnParams {
   float *lse;
   int32_t *err;
   float *part;            // partial slots [slot][2][128][kPartStride]: O (unnormalised), m, l
-  unsigned *tickets;      // [n_items] arrival counters (zeroed by the dequant kernel)
   int n_q, G, n_tok, q_start, kv_len, n_tiles;
   int npairs, n_qt, n_items;
   int64_t Tq;             // key-tile steps of one (kv head, head pair) group: sum over q tiles
@@ -383,9 +382,12 @@ struct __align__(8) AttnBars {
 };
 
 // Key tiles attended by query tile qt (128 rows; the last may be short).
+__device__ __forceinline__ int qt_tiles_of(int q_start, int n_tok, int qt) {
+  const int rows_end = min(kBM * (qt + 1), n_tok);
+  return (q_start + rows_end + kBN - 1) / kBN;
+}
 __device__ __forceinline__ int qt_tiles(const AttnParams &p, int qt) {
-  const int rows_end = min(kBM * (qt + 1), p.n_tok);
-  return (p.q_start + rows_end + kBN - 1) / kBN;
+  return qt_tiles_of(p.q_start, p.n_tok, qt);
 }
 
 // The work is the list of items (group g = kv head * npairs + head pair,
@@ -466,8 +468,7 @@ struct SegIter {
 // for the other head.  An S buffer is rewritten only after the PV that read
 // its P, in issue order (tcgen05.mma from one thread executes in order).
 // A segment that covers a whole item writes its rows; the pieces of a split
-// item are written as partials (unnormalised O, m, l), and the last CTA to
-// finish a piece of the item (a ticket) merges them (log-sum-exp).
+// item are written as partials (unnormalised O, m, l) for piece_merge_kernel.
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnParams p) {
   const int64_t P = gridDim.x;
   const int64_t s0 = p.W * blockIdx.x / P, s1 = p.W * (blockIdx.x + 1) / P;
@@ -483,7 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ int last_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t idesc_qk = idesc_f16(0), idesc_pv = idesc_f16(1);
@@ -699,7 +699,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
     bool have_seg = next_mine(it, sg);
     if (have_seg) load_q(sg);
     while (have_seg) {
-      const bool two = seg_two(sg);
       const int kvh = sg.g / p.npairs, hp = sg.g % p.npairs;
       const int head = kvh * p.G + 2 * hp + e;
       const int q0 = sg.qt * kBM;
@@ -858,7 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
         continue;
       }
       // A piece of a split item: write the partial row (O as accumulated, in
-      // the scale of m; m in log2 units; l), then take a ticket.
+      // the scale of m; m in log2 units; l) into slot blockIdx.x + item; the
+      // merge kernel behind this one combines the item's pieces.
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
@@ -873,69 +873,6 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.ofree[e]);
       reinterpret_cast<float2 *>(prow + kD)[0] = make_float2(m, l);
-      __threadfence();
-      // every row of both heads written before the ticket (named barrier 1
-      // for a pair of heads, 2 for a single head: warpgroup 1 never meets 2)
-      const int bar_id = two ? 1 : 2, nthr = two ? 256 : 128;
-      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
-      // CTAs holding a piece of the item: owners of its first and last step
-      // (the owner of step s is floor(((s + 1) P - 1) / W); with W >= P every
-      // CTA owns at least one step)
-      const int64_t c_first = ((sg.start + 1) * P - 1) / p.W;
-      const int64_t c_last = ((sg.start + sg.nt) * P - 1) / p.W;
-      if (threadIdx.x == 0) {
-        const unsigned n_parts = static_cast<unsigned>(c_last - c_first + 1);
-        const unsigned old = atomicInc(p.tickets + item, n_parts - 1);
-        last_flag = old == n_parts - 1 ? 1 : 0;
-      }
-      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
-      if (last_flag) {
-        __threadfence();
-        // merge this row over the item's pieces (slots c + item), 32 dims at a time
-        float M = -INFINITY, L = 0.0f;
-        for (int64_t c = c_first; c <= c_last; ++c)
-          M = fmaxf(M, __ldcg(p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride + kD));
-        for (int64_t c = c_first; c <= c_last; ++c) {
-          const float2 ml = __ldcg(reinterpret_cast<const float2 *>(
-              p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride + kD));
-          if (ml.x != -INFINITY) L = fmaf(fast_exp2(ml.x - M), ml.y, L);
-        }
-        const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-        __half *dst = p.out + row * kD;
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          float4 acc[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-          for (int64_t c = c_first; c <= c_last; ++c) {
-            const float *pr = p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride;
-            const float mk = __ldcg(pr + kD);
-            const float w = mk == -INFINITY ? 0.0f : fast_exp2(mk - M);
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 x = __ldcg(reinterpret_cast<const float4 *>(pr + cc * 32) + i);
-              acc[i].x = fmaf(w, x.x, acc[i].x);
-              acc[i].y = fmaf(w, x.y, acc[i].y);
-              acc[i].z = fmaf(w, x.z, acc[i].z);
-              acc[i].w = fmaf(w, x.w, acc[i].w);
-            }
-          }
-          if (r < rows) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const uint32_t w0 = pack_half2(acc[2 * i].x * inv, acc[2 * i].y * inv);
-              const uint32_t w1 = pack_half2(acc[2 * i].z * inv, acc[2 * i].w * inv);
-              const uint32_t w2 = pack_half2(acc[2 * i + 1].x * inv, acc[2 * i + 1].y * inv);
-              const uint32_t w3 = pack_half2(acc[2 * i + 1].z * inv, acc[2 * i + 1].w * inv);
-              reinterpret_cast<uint4 *>(dst + cc * 32)[i] = make_uint4(w0, w1, w2, w3);
-            }
-          }
-        }
-        if (p.lse && r < rows)
-          p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-      }
-      // the flag is read by every thread before anyone takes the next ticket
-      asm volatile("bar.sync %0, %1;\n" ::"r"(bar_id), "r"(nthr) : "memory");
       sg = nsg;
       have_seg = have_next;
     }
@@ -953,6 +890,112 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const AttnPar
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// ------------------------------------------------------------------ piece merge
+
+struct PieceMergeParams {
+  const float *part;  // the attention kernel's partial slots
+  __half *out;
+  float *lse;
+  int n_q, G, n_tok, q_start, npairs, n_qt;
+  int64_t Tq, W;
+  int grid;           // the attention kernel's CTAs
+};
+
+// The items that the attention kernel split over several CTAs, merged by
+// log-sum-exp after it has completed: one CTA per (item, head of its pair),
+// four threads per query row (32 dims each), o = sum_c 2^(m_c - M) o_c / L
+// with M = max_c m_c and L = sum_c 2^(m_c - M) l_c over the item's pieces
+// c = c_first..c_last (the CTAs owning its first and last step), summed in
+// that order.  Each thread requests the (m, l) of up to four pieces at once,
+// then its 32 dims of two pieces at a time, so that the usual two-piece item
+// takes two round trips to memory.  Items that one CTA took whole were
+// written by the attention kernel; their CTAs return.
+constexpr int kMergeThreads = 4 * kBM;
+
+__global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceMergeParams p) {
+  grid_dependency_wait();  // the partials are complete
+  const int item = blockIdx.x, e = blockIdx.y;
+  const int g = item / p.n_qt, qt = item % p.n_qt;
+  if (e == 1 && 2 * (g % p.npairs) + 1 >= p.G) return;  // a pair with one head
+  int64_t start = static_cast<int64_t>(g) * p.Tq;
+  for (int q = 0; q < qt; ++q) start += qt_tiles_of(p.q_start, p.n_tok, q);
+  const int nt = qt_tiles_of(p.q_start, p.n_tok, qt);
+  const int64_t P = p.grid;
+  const int64_t c_first = ((start + 1) * P - 1) / p.W;  // owner of step s: ((s + 1) P - 1) / W
+  const int64_t c_last = ((start + nt) * P - 1) / p.W;
+  if (c_first == c_last) return;
+  const int r = threadIdx.x >> 2, cc = threadIdx.x & 3;
+  const int q0 = qt * kBM;
+  if (r >= min(kBM, p.n_tok - q0)) return;
+  const int head = (g / p.npairs) * p.G + 2 * (g % p.npairs) + e;
+  const int64_t row = static_cast<int64_t>(q0 + r) * p.n_q + head;
+  auto part_row = [&](int64_t c) {
+    return p.part + ((c + item) * 2 * kBM + e * kBM + r) * kPartStride;
+  };
+  auto ml_of = [&](int64_t c) {
+    return c <= c_last ? __ldcg(reinterpret_cast<const float2 *>(part_row(c) + kD))
+                       : make_float2(-INFINITY, 0.0f);
+  };
+  float M = -INFINITY;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    float2 ml[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ml[i] = ml_of(c0 + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) M = fmaxf(M, ml[i].x);
+  }
+  float L = 0.0f;
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
+    float2 ml[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ml[i] = ml_of(c0 + i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (ml[i].x != -INFINITY) L = fmaf(fast_exp2(ml[i].x - M), ml[i].y, L);
+  }
+  float4 acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (int64_t c0 = c_first; c0 <= c_last; c0 += 2) {
+    float4 x[2][8];
+    float w[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const bool have = c0 + k <= c_last;
+      const float *pr = part_row(have ? c0 + k : c0);
+      const float mk = have ? __ldcg(pr + kD) : -INFINITY;
+      w[k] = mk == -INFINITY ? 0.0f : fast_exp2(mk - M);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        x[k][i] = have ? __ldcg(reinterpret_cast<const float4 *>(pr + cc * 32) + i)
+                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (c0 + k > c_last) break;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        acc[i].x = fmaf(w[k], x[k][i].x, acc[i].x);
+        acc[i].y = fmaf(w[k], x[k][i].y, acc[i].y);
+        acc[i].z = fmaf(w[k], x[k][i].z, acc[i].z);
+        acc[i].w = fmaf(w[k], x[k][i].w, acc[i].w);
+      }
+    }
+  }
+  const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+  __half *dst = p.out + row * kD + cc * 32;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w0 = pack_half2(acc[2 * i].x * inv, acc[2 * i].y * inv);
+    const uint32_t w1 = pack_half2(acc[2 * i].z * inv, acc[2 * i].w * inv);
+    const uint32_t w2 = pack_half2(acc[2 * i + 1].x * inv, acc[2 * i + 1].y * inv);
+    const uint32_t w3 = pack_half2(acc[2 * i + 1].z * inv, acc[2 * i + 1].w * inv);
+    reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w0, w1, w2, w3);
+  }
+  if (p.lse && cc == 0) p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  grid_launch_dependents();
 }
 
 }  // namespace
@@ -977,9 +1020,8 @@ PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok, int num_s
   for (int qt = 0; qt < pl.n_qt; ++qt) pl.Tq += host_qt_tiles(q_start, n_q_tok, qt);
   pl.W = static_cast<int64_t>(L.n_kv_heads) * pl.npairs * pl.Tq;
   pl.grid = std::max<int64_t>(1, std::min<int64_t>(num_sms > 0 ? num_sms : 148, pl.W));
-  // tickets after the K and V tiles (256-byte aligned), then the partial slots
-  pl.ticket_off = 2 * pl.ws_k_bytes;
-  pl.part_off = pl.ticket_off + (pl.n_items * 4 + 255) / 256 * 256;
+  // the partial slots after the K and V tiles
+  pl.part_off = 2 * pl.ws_k_bytes;
   pl.part_bytes = (pl.grid + pl.n_items) * 2 * kBM * kPartStride * 4;
   pl.ws_bytes = pl.part_off + pl.part_bytes;
   return pl;
@@ -999,7 +1041,6 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   dp.tiles[1] = ws + pl.ws_k_bytes;
   dp.seq_lens = L.seq_lens;
   dp.err = L.err;
-  dp.tickets = reinterpret_cast<unsigned *>(ws + pl.ticket_off);
   dp.table = L.pages_per_seq > 0 ? L.block_table : nullptr;
   dp.pages_per_seq = L.pages_per_seq;
   dp.n_pages = L.n_pages;
@@ -1008,7 +1049,6 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   dp.capacity = L.capacity;
   dp.kv_len = static_cast<int>(pl.kv_tokens);
   dp.n_tiles = n_tiles;
-  dp.n_items = static_cast<int>(pl.n_items);
   cudaError_t e = launch_pdl(dequant_tiles_kernel, dim3(n_tiles, L.n_kv_heads, 2), dim3(256), 0,
                              stream, dp);
   if (e != cudaSuccess) return e;
@@ -1021,7 +1061,6 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   ap.lse = lse;
   ap.err = L.err;
   ap.part = reinterpret_cast<float *>(ws + pl.part_off);
-  ap.tickets = reinterpret_cast<unsigned *>(ws + pl.ticket_off);
   ap.n_q = L.n_q_heads;
   ap.G = L.n_q_heads / L.n_kv_heads;
   ap.n_tok = n_q_tok;
@@ -1038,8 +1077,24 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   static std::atomic<uint64_t> optin{0};
   e = smem_optin(prefill_attn_kernel, smem, optin);
   if (e != cudaSuccess) return e;
-  return launch_pdl(prefill_attn_kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(kThreads),
-                    smem, stream, ap);
+  e = launch_pdl(prefill_attn_kernel, dim3(static_cast<unsigned>(pl.grid)), dim3(kThreads), smem,
+                 stream, ap);
+  if (e != cudaSuccess) return e;
+  PieceMergeParams mp;
+  mp.part = ap.part;
+  mp.out = ap.out;
+  mp.lse = lse;
+  mp.n_q = ap.n_q;
+  mp.G = ap.G;
+  mp.n_tok = n_q_tok;
+  mp.q_start = q_start;
+  mp.npairs = pl.npairs;
+  mp.n_qt = pl.n_qt;
+  mp.Tq = pl.Tq;
+  mp.W = pl.W;
+  mp.grid = static_cast<int>(pl.grid);
+  return launch_pdl(piece_merge_kernel, dim3(static_cast<unsigned>(pl.n_items), 2),
+                    dim3(kMergeThreads), 0, stream, mp);
 }
 
 }  // namespace kvq

@@ -275,10 +275,11 @@ class OursArm:
         for at most 64 rows (it also advances the lengths), else the encode
         kernel plus the length update; decode is two (the split kernel, with
         the append fused when the step appends one token, and the merge),
-        prefill two (dequant pre-pass, attention), an eviction step five
-        (decode's two, probe, selection, compaction of both sides)."""
+        prefill three (dequant pre-pass, attention, merge of the split
+        items), an eviction step five (decode's two, probe, selection,
+        compaction of both sides)."""
         w = self.w
-        per_layer = {"decode": 2, "degrade": 1, "prefill": 2, "evict": 5}[w.kind]
+        per_layer = {"decode": 2, "degrade": 1, "prefill": 3, "evict": 5}[w.kind]
         if w.append_new and not self.fused:
             n_tok = w.append_new if w.kind == "prefill" else 1
             rows = 2 * w.n_seqs * n_tok * w.n_kv
