@@ -49,6 +49,7 @@ struct PrefillPlan {
   int npairs = 0, n_qt = 0;  // query-head pairs per kv head, 128-query tiles
   int64_t n_items = 0;       // (kv head, head pair, query tile) work items
   int64_t Tq = 0, W = 0;     // key-tile steps per (kv head, pair); in all
+  int64_t sms = 0;           // the device's SMs
   int64_t grid = 0;          // persistent CTAs (at most one per SM)
   int64_t part_off = 0, part_bytes = 0;
   int64_t ws_bytes = 0;

@@ -265,44 +265,30 @@ struct DequantParams {
   int32_t *err;
   const int32_t *table;  // paged layers: block table; nullptr: contiguous
   int seq, n_kv, capacity, kv_len, n_tiles, pages_per_seq, n_pages;
+  int buf_bytes;         // one shared buffer: a tile's units of the wider side's codec
 };
 
-// grid: (n_tiles, n_kv, 2 sides); 256 threads.  The tile's eight 16-token
-// units are first copied into shared memory with coalesced 16-byte loads;
-// then each thread takes (key row, 32-value block) items, dequantizes the
-// block there and writes four 16-byte chunks of the swizzled fp16 tile.
+// Persistent CTAs of 256 threads over the work items (side, kv head, tile),
+// item w = (side * n_kv + kv head) * n_tiles + tile; CTA c takes w = c,
+// c + grid, ...  An item's units (at most eight, inside one page) arrive by
+// one bulk copy into one of two shared buffers, the next item's while the
+// current one is dequantized: each thread takes (key row, 32-value block)
+// items, dequantizes the block there and writes four 16-byte chunks of the
+// swizzled fp16 tile.
+constexpr int kDqThreads = 256;
+constexpr int kDqUnits = kBN / kUnitTokens;  // units per tile
+
 template <int CODEC, int SIDE>
-__device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *units_sh) {
-  const int tile = blockIdx.x, kvh = blockIdx.y;
+__device__ __forceinline__ void dequant_tile(const DequantParams &p, const uint8_t *units_sh,
+                                             int tile, int kvh) {
   constexpr int UB = unit_bytes(CODEC);
-  const int64_t units = p.capacity / kUnitTokens;
-  const int u_first = tile * (kBN / kUnitTokens);
-  const int u_end = min(u_first + kBN / kUnitTokens,
-                        static_cast<int>((p.kv_len + kUnitTokens - 1) / kUnitTokens));
-  // the tile's units (a tile lies inside one page: kPageUnits % (kBN / 16) == 0)
-  int64_t uidx;
-  if (p.table) {
-    int pg = page_of(p.table, p.pages_per_seq, p.n_pages, p.seq, u_first / kPageUnits);
-    if (pg < 0) {
-      if (threadIdx.x == 0) set_err(p.err, KVQ_DEVERR_PAGE);
-      pg = 0;  // read pool page 0 in its place
-    }
-    uidx = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits + u_first % kPageUnits;
-  } else {
-    uidx = (static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + u_first;
-  }
-  const uint8_t *src = p.cache[SIDE] + uidx * UB;
-  const int n16 = (u_end - u_first) * UB / 16;
-  for (int i = threadIdx.x; i < n16; i += 256)
-    reinterpret_cast<uint4 *>(units_sh)[i] = reinterpret_cast<const uint4 *>(src)[i];
-  __syncthreads();
   uint8_t *dst = p.tiles[SIDE] + (static_cast<int64_t>(kvh) * p.n_tiles + tile) * kTileBytes;
   if (CODEC == KVQ_TURBO4) {
     // a warp per key row: y^ from the nibbles, then x^ = s * H y^ / 16 across
     // the warp (exact), rounded to fp16 once like every other codec
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll 1
-    for (int row = warp; row < kBN; row += 8) {
+    for (int row = warp; row < kBN; row += kDqThreads / 32) {
       float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
       if (tile * kBN + row < p.kv_len) {  // warp-uniform
         turbo4_row_rotated<SIDE>(units_sh + (row / kUnitTokens) * UB, row % kUnitTokens, lane, x);
@@ -313,7 +299,7 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
     }
   } else {
 #pragma unroll 1
-    for (int item = threadIdx.x; item < kBN * 4; item += 256) {
+    for (int item = threadIdx.x; item < kBN * 4; item += kDqThreads) {
       const int row = item >> 2, b = item & 3;
       const int key = tile * kBN + row;
       float x[32];
@@ -336,23 +322,86 @@ __device__ __forceinline__ void dequant_tile(const DequantParams &p, uint8_t *un
   }
 }
 
-__global__ void __launch_bounds__(256) dequant_tiles_kernel(const DequantParams p) {
-  __shared__ __align__(16) uint8_t units_sh[kBN / kUnitTokens * 4096];
+template <int SIDE>
+__device__ __forceinline__ void dequant_tile_c(const DequantParams &p, const uint8_t *units_sh,
+                                               int tile, int kvh) {
+  const int codec = p.codec[SIDE];
+  if (codec == KVQ_F16) dequant_tile<KVQ_F16, SIDE>(p, units_sh, tile, kvh);
+  else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, SIDE>(p, units_sh, tile, kvh);
+  else if (codec == KVQ_Q4_0) dequant_tile<KVQ_Q4_0, SIDE>(p, units_sh, tile, kvh);
+  else dequant_tile<KVQ_TURBO4, SIDE>(p, units_sh, tile, kvh);
+}
+
+__global__ void __launch_bounds__(kDqThreads, 4) dequant_tiles_kernel(const DequantParams p) {
+  extern __shared__ __align__(128) uint8_t dq_sh[];  // two buffers of p.buf_bytes
+  __shared__ uint64_t full[2];
+  if (threadIdx.x == 0) {
+    mbar_init(&full[0], 1);
+    mbar_init(&full[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
   grid_dependency_wait();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0 &&
-      p.seq_lens[p.seq] < p.kv_len)
+  if (blockIdx.x == 0 && threadIdx.x == 0 && p.seq_lens[p.seq] < p.kv_len)
     set_err(p.err, KVQ_DEVERR_SEQLEN);
-  const int side = blockIdx.z, codec = p.codec[side];
-  if (side == 0) {
-    if (codec == KVQ_F16) dequant_tile<KVQ_F16, 0>(p, units_sh);
-    else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 0>(p, units_sh);
-    else if (codec == KVQ_Q4_0) dequant_tile<KVQ_Q4_0, 0>(p, units_sh);
-    else dequant_tile<KVQ_TURBO4, 0>(p, units_sh);
-  } else {
-    if (codec == KVQ_F16) dequant_tile<KVQ_F16, 1>(p, units_sh);
-    else if (codec == KVQ_Q8_0) dequant_tile<KVQ_Q8_0, 1>(p, units_sh);
-    else if (codec == KVQ_Q4_0) dequant_tile<KVQ_Q4_0, 1>(p, units_sh);
-    else dequant_tile<KVQ_TURBO4, 1>(p, units_sh);
+  const int n_work = 2 * p.n_kv * p.n_tiles;
+  const int64_t units = p.capacity / kUnitTokens;
+  const int units_kv = (p.kv_len + kUnitTokens - 1) / kUnitTokens;
+  // thread 0: bulk-copy item w's units into buffer `buf`
+  auto issue = [&](int w, int buf) {
+    const int side = w / (p.n_kv * p.n_tiles);
+    const int kvh = (w / p.n_tiles) % p.n_kv, tile = w % p.n_tiles;
+    const int ub = unit_bytes(side ? p.codec[1] : p.codec[0]);
+    const int u_first = tile * kDqUnits;
+    const int n_u = min(kDqUnits, units_kv - u_first);
+    int64_t uidx;
+    if (p.table) {  // a tile lies inside one page (kPageUnits % kDqUnits == 0)
+      int pg = page_of(p.table, p.pages_per_seq, p.n_pages, p.seq, u_first / kPageUnits);
+      if (pg < 0) {
+        set_err(p.err, KVQ_DEVERR_PAGE);
+        pg = 0;  // read pool page 0 in its place
+      }
+      uidx = (static_cast<int64_t>(pg) * p.n_kv + kvh) * kPageUnits + u_first % kPageUnits;
+    } else {
+      uidx = (static_cast<int64_t>(p.seq) * p.n_kv + kvh) * units + u_first;
+    }
+    const uint32_t bytes = n_u > 0 ? static_cast<uint32_t>(n_u * ub) : 0u;
+    mbar_arrive_expect_tx(&full[buf], bytes);
+    const uint8_t *src = (side ? p.cache[1] : p.cache[0]) + uidx * ub;
+    if (bytes) bulk_copy_g2s(dq_sh + buf * p.buf_bytes, src, bytes, &full[buf]);
+  };
+  int issued = 0;  // thread 0: items issued (the k-th into buffer k & 1)
+  if (threadIdx.x == 0 && static_cast<int>(blockIdx.x) < n_work) {
+    issue(blockIdx.x, 0);
+    issued = 1;
+  }
+  int i = 0;
+  bool ok = true;
+  for (int w = blockIdx.x; w < n_work; w += gridDim.x, ++i) {
+    const int buf = i & 1;
+    // the other buffer was last read in item i - 1 (the barrier below ended it)
+    if (threadIdx.x == 0 && w + static_cast<int>(gridDim.x) < n_work) {
+      fence_proxy_async_smem();
+      issue(w + gridDim.x, buf ^ 1);
+      ++issued;
+    }
+    const bool got = __syncthreads_and(
+        mbar_wait_bounded(&full[buf], static_cast<uint32_t>(i >> 1) & 1u) ? 1 : 0);
+    if (!got) {
+      if (threadIdx.x == 0) set_err(p.err, KVQ_DEVERR_TIMEOUT);
+      ok = false;
+      break;
+    }
+    const int side = w / (p.n_kv * p.n_tiles);
+    const int kvh = (w / p.n_tiles) % p.n_kv, tile = w % p.n_tiles;
+    const uint8_t *units_sh = dq_sh + buf * p.buf_bytes;
+    if (side == 0) dequant_tile_c<0>(p, units_sh, tile, kvh);
+    else dequant_tile_c<1>(p, units_sh, tile, kvh);
+    __syncthreads();  // every thread is done with this buffer
+  }
+  if (!ok && threadIdx.x == 0) {  // after a timeout: the copies still in flight
+    for (int k = i; k < issued; ++k)
+      mbar_wait_bounded(&full[k & 1], static_cast<uint32_t>(k >> 1) & 1u, nullptr, 100000000ull);
   }
   grid_launch_dependents();
 }
@@ -1019,7 +1068,8 @@ PrefillPlan plan_prefill(const kvq_layer &L, int q_start, int n_q_tok, int num_s
   pl.Tq = 0;
   for (int qt = 0; qt < pl.n_qt; ++qt) pl.Tq += host_qt_tiles(q_start, n_q_tok, qt);
   pl.W = static_cast<int64_t>(L.n_kv_heads) * pl.npairs * pl.Tq;
-  pl.grid = std::max<int64_t>(1, std::min<int64_t>(num_sms > 0 ? num_sms : 148, pl.W));
+  pl.sms = num_sms > 0 ? num_sms : 148;
+  pl.grid = std::max<int64_t>(1, std::min<int64_t>(pl.sms, pl.W));
   // the partial slots after the K and V tiles
   pl.part_off = 2 * pl.ws_k_bytes;
   pl.part_bytes = (pl.grid + pl.n_items) * 2 * kBM * kPartStride * 4;
@@ -1049,8 +1099,22 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   dp.capacity = L.capacity;
   dp.kv_len = static_cast<int>(pl.kv_tokens);
   dp.n_tiles = n_tiles;
-  cudaError_t e = launch_pdl(dequant_tiles_kernel, dim3(n_tiles, L.n_kv_heads, 2), dim3(256), 0,
-                             stream, dp);
+  dp.buf_bytes = kBN / kUnitTokens * std::max(unit_bytes(L.codec_k), unit_bytes(L.codec_v));
+  const int dq_smem = 2 * dp.buf_bytes;
+  // opted in once per device for the widest codec (f16 units), whatever this
+  // layer's codecs are
+  static std::atomic<uint64_t> dq_optin{0};
+  cudaError_t e = smem_optin(dequant_tiles_kernel, 2 * kDqUnits * unit_bytes(KVQ_F16), dq_optin);
+  if (e != cudaSuccess) return e;
+  int dq_per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&dq_per_sm, dequant_tiles_kernel, kDqThreads,
+                                                    dq_smem);
+  if (e != cudaSuccess) return e;
+  const int64_t dq_work = 2 * static_cast<int64_t>(L.n_kv_heads) * n_tiles;
+  const int64_t dq_grid =
+      std::max<int64_t>(1, std::min<int64_t>(dq_work, static_cast<int64_t>(std::max(dq_per_sm, 1)) * pl.sms));
+  e = launch_pdl(dequant_tiles_kernel, dim3(static_cast<unsigned>(dq_grid)), dim3(kDqThreads),
+                 dq_smem, stream, dp);
   if (e != cudaSuccess) return e;
 
   AttnParams ap;
