@@ -953,15 +953,16 @@ struct PieceMergeParams {
 };
 
 // The items that the attention kernel split over several CTAs, merged by
-// log-sum-exp after it has completed: one CTA per (item, head of its pair),
-// four threads per query row (32 dims each), o = sum_c 2^(m_c - M) o_c / L
-// with M = max_c m_c and L = sum_c 2^(m_c - M) l_c over the item's pieces
+// log-sum-exp after it has completed: o = sum_c 2^(m_c - M) o_c / L with
+// M = max_c m_c and L = sum_c 2^(m_c - M) l_c over the item's pieces
 // c = c_first..c_last (the CTAs owning its first and last step), summed in
-// that order.  Each thread requests the (m, l) of up to four pieces at once,
-// then its 32 dims of two pieces at a time, so that the usual two-piece item
-// takes two round trips to memory.  Items that one CTA took whole were
-// written by the attention kernel; their CTAs return.
-constexpr int kMergeThreads = 4 * kBM;
+// that order.  Grid (item, head of its pair, quarter of the 128 rows); a
+// thread per (query row, 8 dims), so that many small threads keep the reads
+// of the partial rows in flight: each requests the (m, l) of up to four
+// pieces at once, then its 8 dims of two pieces at a time.  Items that one
+// CTA took whole were written by the attention kernel; their CTAs return.
+constexpr int kMergeRowsPerCta = 32;
+constexpr int kMergeThreads = kMergeRowsPerCta * (kD / 8);
 
 __global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceMergeParams p) {
   grid_dependency_wait();  // the partials are complete
@@ -975,7 +976,7 @@ __global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceM
   const int64_t c_first = ((start + 1) * P - 1) / p.W;  // owner of step s: ((s + 1) P - 1) / W
   const int64_t c_last = ((start + nt) * P - 1) / p.W;
   if (c_first == c_last) return;
-  const int r = threadIdx.x >> 2, cc = threadIdx.x & 3;
+  const int r = blockIdx.z * kMergeRowsPerCta + (threadIdx.x >> 4), cc = threadIdx.x & 15;
   const int q0 = qt * kBM;
   if (r >= min(kBM, p.n_tok - q0)) return;
   const int head = (g / p.npairs) * p.G + 2 * (g % p.npairs) + e;
@@ -987,45 +988,49 @@ __global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceM
     return c <= c_last ? __ldcg(reinterpret_cast<const float2 *>(part_row(c) + kD))
                        : make_float2(-INFINITY, 0.0f);
   };
-  float M = -INFINITY;
-  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-    float2 ml[4];
+  // (m, l) of the first four pieces in one round trip (an item rarely has
+  // more), the rest four at a time
+  float2 ml[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ml[i] = ml_of(c0 + i);
+  for (int i = 0; i < 4; ++i) ml[i] = ml_of(c_first + i);
+  float M = fmaxf(fmaxf(ml[0].x, ml[1].x), fmaxf(ml[2].x, ml[3].x));
+  for (int64_t c0 = c_first + 4; c0 <= c_last; c0 += 4) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) M = fmaxf(M, ml[i].x);
+    for (int i = 0; i < 4; ++i) M = fmaxf(M, ml_of(c0 + i).x);
   }
   float L = 0.0f;
-  for (int64_t c0 = c_first; c0 <= c_last; c0 += 4) {
-    float2 ml[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ml[i] = ml_of(c0 + i);
+  for (int i = 0; i < 4; ++i)
+    if (ml[i].x != -INFINITY) L = fmaf(fast_exp2(ml[i].x - M), ml[i].y, L);
+  for (int64_t c0 = c_first + 4; c0 <= c_last; c0 += 4) {
+    float2 mr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mr[i] = ml_of(c0 + i);
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      if (ml[i].x != -INFINITY) L = fmaf(fast_exp2(ml[i].x - M), ml[i].y, L);
+      if (mr[i].x != -INFINITY) L = fmaf(fast_exp2(mr[i].x - M), mr[i].y, L);
   }
-  float4 acc[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  float4 acc[2] = {make_float4(0.0f, 0.0f, 0.0f, 0.0f), make_float4(0.0f, 0.0f, 0.0f, 0.0f)};
   for (int64_t c0 = c_first; c0 <= c_last; c0 += 2) {
-    float4 x[2][8];
+    float4 x[2][2];
     float w[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const bool have = c0 + k <= c_last;
       const float *pr = part_row(have ? c0 + k : c0);
-      const float mk = have ? __ldcg(pr + kD) : -INFINITY;
+      const int64_t j = c0 + k - c_first;  // ml[] holds pieces 0..3 (selected, not indexed)
+      const float mk = !have ? -INFINITY
+                       : j == 0 ? ml[0].x : j == 1 ? ml[1].x : j == 2 ? ml[2].x
+                       : j == 3 ? ml[3].x : __ldcg(pr + kD);
       w[k] = mk == -INFINITY ? 0.0f : fast_exp2(mk - M);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        x[k][i] = have ? __ldcg(reinterpret_cast<const float4 *>(pr + cc * 32) + i)
-                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      x[k][0] = have ? __ldcg(reinterpret_cast<const float4 *>(pr + cc * 8)) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      x[k][1] = have ? __ldcg(reinterpret_cast<const float4 *>(pr + cc * 8) + 1) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     }
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       if (c0 + k > c_last) break;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 2; ++i) {
         acc[i].x = fmaf(w[k], x[k][i].x, acc[i].x);
         acc[i].y = fmaf(w[k], x[k][i].y, acc[i].y);
         acc[i].z = fmaf(w[k], x[k][i].z, acc[i].z);
@@ -1034,15 +1039,9 @@ __global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceM
     }
   }
   const float inv = L > 0.0f ? 1.0f / L : 0.0f;
-  __half *dst = p.out + row * kD + cc * 32;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t w0 = pack_half2(acc[2 * i].x * inv, acc[2 * i].y * inv);
-    const uint32_t w1 = pack_half2(acc[2 * i].z * inv, acc[2 * i].w * inv);
-    const uint32_t w2 = pack_half2(acc[2 * i + 1].x * inv, acc[2 * i + 1].y * inv);
-    const uint32_t w3 = pack_half2(acc[2 * i + 1].z * inv, acc[2 * i + 1].w * inv);
-    reinterpret_cast<uint4 *>(dst)[i] = make_uint4(w0, w1, w2, w3);
-  }
+  *reinterpret_cast<uint4 *>(p.out + row * kD + cc * 8) =
+      make_uint4(pack_half2(acc[0].x * inv, acc[0].y * inv), pack_half2(acc[0].z * inv, acc[0].w * inv),
+                 pack_half2(acc[1].x * inv, acc[1].y * inv), pack_half2(acc[1].z * inv, acc[1].w * inv));
   if (p.lse && cc == 0) p.lse[row] = L > 0.0f ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
   grid_launch_dependents();
 }
@@ -1157,7 +1156,8 @@ cudaError_t launch_prefill(const kvq_layer &L, const PrefillPlan &pl, int seq, i
   mp.Tq = pl.Tq;
   mp.W = pl.W;
   mp.grid = static_cast<int>(pl.grid);
-  return launch_pdl(piece_merge_kernel, dim3(static_cast<unsigned>(pl.n_items), 2),
+  return launch_pdl(piece_merge_kernel,
+                    dim3(static_cast<unsigned>(pl.n_items), 2, kBM / kMergeRowsPerCta),
                     dim3(kMergeThreads), 0, stream, mp);
 }
 
