@@ -965,16 +965,21 @@ constexpr int kMergeRowsPerCta = 32;
 constexpr int kMergeThreads = kMergeRowsPerCta * (kD / 8);
 
 __global__ void __launch_bounds__(kMergeThreads) piece_merge_kernel(const PieceMergeParams p) {
+  __shared__ int64_t owners[2];
   grid_dependency_wait();  // the partials are complete
   const int item = blockIdx.x, e = blockIdx.y;
   const int g = item / p.n_qt, qt = item % p.n_qt;
   if (e == 1 && 2 * (g % p.npairs) + 1 >= p.G) return;  // a pair with one head
-  int64_t start = static_cast<int64_t>(g) * p.Tq;
-  for (int q = 0; q < qt; ++q) start += qt_tiles_of(p.q_start, p.n_tok, q);
-  const int nt = qt_tiles_of(p.q_start, p.n_tok, qt);
-  const int64_t P = p.grid;
-  const int64_t c_first = ((start + 1) * P - 1) / p.W;  // owner of step s: ((s + 1) P - 1) / W
-  const int64_t c_last = ((start + nt) * P - 1) / p.W;
+  if (threadIdx.x == 0) {  // the owners of the item's first and last step, once per CTA
+    int64_t start = static_cast<int64_t>(g) * p.Tq;
+    for (int q = 0; q < qt; ++q) start += qt_tiles_of(p.q_start, p.n_tok, q);
+    const int nt = qt_tiles_of(p.q_start, p.n_tok, qt);
+    const int64_t P = p.grid;
+    owners[0] = ((start + 1) * P - 1) / p.W;  // owner of step s: ((s + 1) P - 1) / W
+    owners[1] = ((start + nt) * P - 1) / p.W;
+  }
+  __syncthreads();
+  const int64_t c_first = owners[0], c_last = owners[1];
   if (c_first == c_last) return;
   const int r = blockIdx.z * kMergeRowsPerCta + (threadIdx.x >> 4), cc = threadIdx.x & 15;
   const int q0 = qt * kBM;
